@@ -1,0 +1,353 @@
+"""Independent pins for the fp64 oracle (CPU only).
+
+Each ``pin_*`` function checks the oracle loaded as ``lib`` against something
+other than itself: exhaustive comparison with torch's float8/bfloat16
+decoders, a known-answer table of the e2m1 format, hand-made byte fixtures,
+closed forms, invariants, and a brute-force dense evaluation of tiny layers
+written here with numpy, scipy and torch (no oracle code).  They raise
+AssertionError on a mismatch.  ``tests/test_oracle_pins.py`` runs them on the
+real oracle; ``tests/test_oracle_mutants.py`` runs them on builds of the
+oracle with a planted mistake and requires that each mistake is caught.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+import scipy.special
+import torch
+
+import oracle
+from nvfp4_moe_decode_gb300 import synth
+
+# The 16 values of the FP4 E2M1 element format (OCP Microscaling Formats
+# specification v1.0, FP4 E2M1: exponent bias 1, largest normal 6.0, smallest
+# normal 1.0, subnormal 0.5); codes 8..15 are the negatives of 0..7.
+E2M1_KNOWN = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+              -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+# ---------------------------------------------------------------------------
+# independent helpers (numpy / torch / scipy only)
+# ---------------------------------------------------------------------------
+
+def np_e4m3(u8: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(u8, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def np_bf16(u16: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def np_dequant(codes: np.ndarray, scales: np.ndarray, tscale: float) -> np.ndarray:
+    lo = codes & 0x0F
+    hi = codes >> 4
+    nib = np.stack([lo, hi], axis=-1).reshape(codes.shape[0], -1)   # (n, 2j), (n, 2j+1)
+    vals = np.array(E2M1_KNOWN)[nib]
+    sc = np.repeat(np_e4m3(scales), 16, axis=1)
+    return vals * sc * float(tscale)
+
+
+def brute_topk(logits_row: np.ndarray, k: int):
+    """The unique k-subset whose members all rank before every non-member
+    (rank: larger fp32-rounded logit first, then lower index)."""
+    E = len(logits_row)
+    f = logits_row.astype(np.float32)
+
+    def before(a, b):
+        return (f[a] > f[b]) or (f[a] == f[b] and a < b)
+
+    found = []
+    for S in itertools.combinations(range(E), k):
+        rest = [e for e in range(E) if e not in S]
+        if all(before(a, b) for a in S for b in rest):
+            found.append(S)
+    assert len(found) == 1
+    S = sorted(found[0], key=lambda e: (-float(f[e]), e))
+    return np.array(S, dtype=np.int32)
+
+
+def host_inputs(li: synth.LayerInputs):
+    """torch CPU LayerInputs -> numpy bit patterns + oracle ExpertWeights."""
+    x = li.x.view(torch.int16).numpy().view(np.uint16)
+    wr = li.router_w.view(torch.int16).numpy().view(np.uint16)
+    E, S = li.n_routed, li.n_shared
+    ex = []
+    for e in range(E + S):
+        if li.wtype == synth.NVFP4:
+            ex.append(oracle.ExpertWeights(0, li.codes13[e].numpy(), li.scales13[e].numpy(),
+                                           float(li.tscale13[e]), li.codes2[e].numpy(),
+                                           li.scales2[e].numpy(), float(li.tscale2[e])))
+        else:
+            ex.append(oracle.ExpertWeights(1, li.w13[e].view(torch.int16).numpy().view(np.uint16),
+                                           None, 1.0,
+                                           li.w2[e].view(torch.int16).numpy().view(np.uint16),
+                                           None, 1.0))
+    return x, wr, ex[:E], (ex[E] if S else None)
+
+
+def dense_expert_outputs(W13: np.ndarray, W2: np.ndarray, X: np.ndarray, I: int) -> np.ndarray:
+    g = X @ W13[:I].T
+    u = X @ W13[I:].T
+    h = g * scipy.special.expit(g) * u
+    return h @ W2.T
+
+
+def brute_layer(li: synth.LayerInputs, top_k: int):
+    """Dense masked evaluation over every expert (no sparsity, no oracle code)."""
+    x = np_bf16(li.x.view(torch.int16).numpy())
+    wr = np_bf16(li.router_w.view(torch.int16).numpy())
+    E, S, I = li.n_routed, li.n_shared, li.inter
+    logits = x @ wr.T
+    T = x.shape[0]
+    gate = np.zeros((T, E))
+    idx = np.zeros((T, top_k), dtype=np.int32)
+    for t in range(T):
+        sel = brute_topk(logits[t], top_k)
+        idx[t] = sel
+        s = scipy.special.expit(logits[t, sel])
+        gate[t, sel] = s / s.sum()
+
+    def weights(e):
+        if li.wtype == synth.NVFP4:
+            W13 = np_dequant(li.codes13[e].numpy(), li.scales13[e].numpy(), float(li.tscale13[e]))
+            W2 = np_dequant(li.codes2[e].numpy(), li.scales2[e].numpy(), float(li.tscale2[e]))
+        else:
+            W13 = np_bf16(li.w13[e].view(torch.int16).numpy())
+            W2 = np_bf16(li.w2[e].view(torch.int16).numpy())
+        return W13, W2
+
+    out = np.zeros_like(x)
+    for e in range(E):
+        W13, W2 = weights(e)
+        out += gate[:, e:e + 1] * dense_expert_outputs(W13, W2, x, I)
+    for s_ in range(S):
+        W13, W2 = weights(E + s_)
+        out += dense_expert_outputs(W13, W2, x, I)
+    return out, idx, gate, logits
+
+
+def run_oracle(li: synth.LayerInputs, top_k: int, lib):
+    x, wr, routed, shared = host_inputs(li)
+    return oracle.moe_forward(x, wr, routed, top_k, li.inter, shared, lib=lib)
+
+
+# ---------------------------------------------------------------------------
+# pins
+# ---------------------------------------------------------------------------
+
+def pin_e2m1_known_values(lib):
+    for c in range(16):
+        v = oracle.e2m1_value(c, lib)
+        assert v == E2M1_KNOWN[c] and math.copysign(1, v) == math.copysign(1, E2M1_KNOWN[c]), \
+            (c, v, E2M1_KNOWN[c])
+
+
+def pin_e4m3_matches_torch(lib):
+    ref = np_e4m3(np.arange(256, dtype=np.uint8))
+    for c in range(256):
+        v = oracle.e4m3_value(c, lib)
+        if np.isnan(ref[c]):
+            assert math.isnan(v), c
+        else:
+            assert v == ref[c], (c, v, ref[c])
+
+
+def pin_bf16_matches_torch(lib):
+    codes = np.arange(65536, dtype=np.uint32)
+    ref = np_bf16(codes.astype(np.uint16))
+    step = 97  # a stride through all exponents and signs (plus the specials)
+    picks = list(range(0, 65536, step)) + [0x0000, 0x8000, 0x0001, 0x7F7F, 0xFF7F, 0x7F80,
+                                           0x3F80, 0xBF80, 0x0080]
+    for c in picks:
+        v = oracle.bf16_value(c, lib)
+        if np.isnan(ref[c]):
+            assert math.isnan(v)
+        else:
+            assert v == ref[c], (hex(c), v, ref[c])
+
+
+def pin_dequant_byte_fixture(lib):
+    """Hand-made bytes: row 0 = 0x21 0x8F ..., scale 0x38 (= 1.0), 0x40 (= 2.0)."""
+    K = 32
+    codes = np.zeros((2, K // 2), dtype=np.uint8)
+    scales = np.zeros((2, K // 16), dtype=np.uint8)
+    codes[0, 0] = 0x21   # k=0: code 1 (0.5); k=1: code 2 (1.0)
+    codes[0, 1] = 0x8F   # k=2: code 15 (-6.0); k=3: code 8 (-0.0)
+    codes[0, 8] = 0x07   # k=16: code 7 (6.0); k=17: code 0
+    codes[1, 15] = 0xA3  # row 1, k=30: code 3 (1.5); k=31: code 10 (-1.0)
+    scales[0, 0] = 0x38  # 1.0 for row 0, k in [0, 16)
+    scales[0, 1] = 0x40  # 2.0 for row 0, k in [16, 32)
+    scales[1, 1] = 0x30  # 0.5 for row 1, k in [16, 32)
+    W = oracle.dequant_nvfp4(codes, scales, 1.0, lib)
+    expect = np.zeros((2, K))
+    expect[0, 0], expect[0, 1], expect[0, 2], expect[0, 3] = 0.5, 1.0, -6.0, -0.0
+    expect[0, 16] = 12.0
+    expect[1, 30], expect[1, 31] = 0.75, -0.5
+    assert np.array_equal(W, expect), np.argwhere(W != expect)
+    W3 = oracle.dequant_nvfp4(codes, scales, 3.0, lib)
+    assert np.array_equal(W3, 3.0 * expect)
+
+
+def pin_dequant_matches_numpy(lib):
+    rng = np.random.default_rng(7)
+    codes = rng.integers(0, 256, size=(16, 64), dtype=np.uint8)
+    codes[0, :] = np.arange(64, dtype=np.uint8) * 4 + 1   # many code pairs
+    scales = rng.integers(0, 0x7E, size=(16, 8), dtype=np.uint8)  # finite e4m3
+    W = oracle.dequant_nvfp4(codes, scales, 0.75, lib)
+    assert np.array_equal(W, np_dequant(codes, scales, 0.75))
+
+
+def pin_router_logits_numpy(lib):
+    li = synth.make_layer(3, 5, hidden=64, n_routed=8, inter=16, weights=False)
+    x = li.x.view(torch.int16).numpy().view(np.uint16)
+    wr = li.router_w.view(torch.int16).numpy().view(np.uint16)
+    lg = oracle.router_logits(x, wr, lib)
+    ref = np_bf16(x) @ np_bf16(wr).T
+    assert np.allclose(lg, ref, rtol=1e-13, atol=1e-15)
+
+
+def pin_topk_bruteforce(lib):
+    rng = np.random.default_rng(11)
+    for E, k in [(4, 2), (6, 3), (8, 6), (7, 1), (5, 5)]:
+        lg = rng.normal(size=(20, E))
+        lg[0, :] = 0.0                          # all equal: lowest indices win
+        lg[1, :] = np.round(lg[1, :] * 2) / 2   # many exact ties
+        idx, w = oracle.select_topk(lg, k, lib)
+        for t in range(lg.shape[0]):
+            assert np.array_equal(idx[t], brute_topk(lg[t], k)), (E, k, t, idx[t])
+            s = scipy.special.expit(lg[t, idx[t]])
+            assert np.allclose(w[t], s / s.sum(), rtol=1e-14, atol=0)
+        assert np.array_equal(idx[0], np.arange(k))
+
+
+def pin_topk_invariants(lib):
+    rng = np.random.default_rng(5)
+    lg = rng.normal(scale=0.9, size=(64, 256))
+    idx, w = oracle.select_topk(lg, 6, lib)
+    for t in range(64):
+        sel = idx[t]
+        assert len(set(sel.tolist())) == 6 and sel.min() >= 0 and sel.max() < 256
+        assert np.all(w[t] > 0) and abs(w[t].sum() - 1.0) <= 1e-12
+        rest = np.setdiff1d(np.arange(256), sel)
+        assert lg[t, sel].astype(np.float32).min() >= lg[t, rest].astype(np.float32).max()
+
+
+def pin_layer_bruteforce_nvfp4(lib):
+    li = synth.make_layer(1, 5, hidden=32, n_routed=6, inter=16, n_shared=1)
+    out, idx, w, _ = run_oracle(li, 2, lib)
+    ref, ridx, _, _ = brute_layer(li, 2)
+    assert np.array_equal(idx, ridx)
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def pin_layer_bruteforce_bf16(lib):
+    li = synth.make_layer(2, 4, hidden=32, n_routed=5, inter=16, n_shared=1, wtype=synth.BF16)
+    out, idx, w, _ = run_oracle(li, 3, lib)
+    ref, ridx, _, _ = brute_layer(li, 3)
+    assert np.array_equal(idx, ridx)
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def pin_layer_bruteforce_larger_k(lib):
+    li = synth.make_layer(4, 3, hidden=48, n_routed=8, inter=32, n_shared=1)
+    out, idx, w, _ = run_oracle(li, 6, lib)
+    ref, ridx, _, _ = brute_layer(li, 6)
+    assert np.array_equal(idx, ridx)
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def pin_zero_input(lib):
+    """x = 0: every logit is 0, experts 0..k-1 are chosen with weight 1/k, and
+    every expert output is 0 (g = u = 0)."""
+    li = synth.make_layer(5, 3, hidden=32, n_routed=6, inter=16)
+    li.x.zero_()
+    out, idx, w, _ = run_oracle(li, 3, lib)
+    assert np.all(out == 0.0)
+    assert np.array_equal(idx, np.tile(np.arange(3, dtype=np.int32), (3, 1)))
+    assert np.allclose(w, 1.0 / 3.0, rtol=0, atol=1e-15)
+
+
+def pin_zero_scales(lib):
+    li = synth.make_layer(6, 2, hidden=32, n_routed=4, inter=16)
+    li.scales13.zero_()
+    out, _, _, _ = run_oracle(li, 2, lib)
+    assert np.all(out == 0.0)
+
+
+def pin_routed_off_leaves_shared(lib):
+    """Routed tensor scales 0: the output is the shared expert alone, which
+    for a one-hot x reduces to a closed form."""
+    li = synth.make_layer(8, 1, hidden=32, n_routed=4, inter=16)
+    li.tscale13[:4] = 0.0
+    H, I = 32, 16
+    # Shared expert: every gate/up code 2 (1.0) in column 0 only; x = e_0 * 1.5.
+    li.x.zero_()
+    li.x[0, 0] = 1.5
+    sh = 4
+    li.codes13[sh].zero_()
+    li.codes13[sh][:, 0] = 0x02          # element (n, 0) = code 2 = 1.0, (n, 1) = 0
+    li.scales13[sh].fill_(0x38)          # 1.0
+    li.codes2[sh].zero_()
+    li.codes2[sh][:, 0] = 0x02 | (0x0A << 4)   # element (n,0) = 1.0, (n,1) = -1.0
+    li.scales2[sh].fill_(0x40)           # 2.0
+    out, _, _, _ = run_oracle(li, 2, lib)
+    g = 1.5
+    h0 = g * (1.0 / (1.0 + math.exp(-g))) * 1.5     # every row i: g_i = u_i = 1.5
+    # y_n = sum_i W2[n][i] h_i = 2.0 * (1.0 * h0 - 1.0 * h0) = 0 for column pair;
+    # rows n: only columns 0 and 1 are nonzero -> y_n = 2*h0 - 2*h0 = 0.
+    assert np.allclose(out, 0.0, atol=1e-15)
+    li.codes2[sh][:, 0] = 0x02           # now only element (n, 0) = 1.0
+    out, _, _, _ = run_oracle(li, 2, lib)
+    assert np.allclose(out, 2.0 * h0, rtol=1e-15, atol=0), (out[0, :4], 2 * h0)
+
+
+def pin_combine_linear_in_down_scale(lib):
+    """Doubling every routed down tensor scale doubles the routed part."""
+    li = synth.make_layer(9, 3, hidden=32, n_routed=5, inter=16)
+    base, _, _, _ = run_oracle(li, 2, lib)
+    li.tscale2[:5] = 0.0
+    shared_only, _, _, _ = run_oracle(li, 2, lib)
+    li.tscale2[:5] = 2.0
+    doubled, _, _, _ = run_oracle(li, 2, lib)
+    routed = base - shared_only
+    assert np.allclose(doubled - shared_only, 2.0 * routed, rtol=1e-12,
+                       atol=1e-12 * np.abs(routed).max())
+
+
+def pin_expert_permutation_invariance(lib):
+    """Relabelling the routed experts (router rows permuted with them) leaves
+    the output unchanged when no two logits tie."""
+    li = synth.make_layer(10, 4, hidden=32, n_routed=6, inter=16)
+    base, idx, _, _ = run_oracle(li, 2, lib)
+    perm = torch.tensor([3, 0, 5, 1, 4, 2])
+    li.router_w = li.router_w[perm].contiguous()
+    full = torch.cat([perm, torch.tensor([6])])
+    for name in ("codes13", "scales13", "codes2", "scales2", "tscale13", "tscale2"):
+        setattr(li, name, getattr(li, name)[full].contiguous())
+    out, idx2, _, _ = run_oracle(li, 2, lib)
+    assert np.allclose(out, base, rtol=1e-12, atol=1e-12 * np.abs(base).max())
+    assert np.array_equal(perm.numpy()[idx2], idx)
+
+
+ALL_PINS = [
+    pin_e2m1_known_values,
+    pin_e4m3_matches_torch,
+    pin_bf16_matches_torch,
+    pin_dequant_byte_fixture,
+    pin_dequant_matches_numpy,
+    pin_router_logits_numpy,
+    pin_topk_bruteforce,
+    pin_topk_invariants,
+    pin_layer_bruteforce_nvfp4,
+    pin_layer_bruteforce_bf16,
+    pin_layer_bruteforce_larger_k,
+    pin_zero_input,
+    pin_zero_scales,
+    pin_routed_off_leaves_shared,
+    pin_combine_linear_in_down_scale,
+    pin_expert_permutation_invariance,
+]
