@@ -1,0 +1,383 @@
+"""Benchmark of the small-batch NVFP4 MoE layer on GB300.
+
+Default workload: one NVFP4 MoE layer at T = 8 tokens (H = 2048, 256 routed
+experts of I = 512, sigmoid top-6, one shared expert), the configuration the
+headline metric is quoted on.  A step is one full layer forward (router +
+top-6 + gate/up + SiLU*up + down + combine).  L2 is kept cold by rotating the
+steps over L distinct resident layers (the selected-expert bytes of one
+rotation are far larger than the 126 MB L2): step k runs layer k mod L.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--tokens T] [--layers L]
+
+Prints one JSON line (rank 0).  value = algorithmic bytes of all steps / time
+(GB/s); the bytes of a step are the router weights + the selected and shared
+experts' packed weights + x + out.  N > 1 (torchrun) runs independent
+replicas, one per GPU; value sums their bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+EXPERT_BYTES = 1_179_648 + 589_824       # packed gate/up + down of one expert
+ROUTER_BYTES = 256 * 2048 * 2
+METRIC = "MoE layer µs and weight-read GB/s (% of HBM peak) at T=1/8, NVFP4 and BF16"
+
+
+def layer_bytes(T: int, n_distinct: int, n_shared: int = 1) -> int:
+    return ROUTER_BYTES + (n_distinct + n_shared) * EXPERT_BYTES + 2 * T * 2048 * 2
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.gpu)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def reduce_max(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(layers_host, x_bits, T: int, budget_s: float):
+    """Run the fp64 oracle layer over the resident layers until budget_s.
+    Returns (seconds, algorithmic bytes, layers done, threads)."""
+    import oracle
+
+    done, nbytes, t0 = 0, 0, time.perf_counter()
+    while True:
+        for (wr, experts, shared, nd) in layers_host:
+            oracle.moe_forward(x_bits, wr, experts, 6, 512, shared)
+            done += 1
+            nbytes += layer_bytes(T, nd)
+            if time.perf_counter() - t0 >= budget_s:
+                return time.perf_counter() - t0, nbytes, done, oracle.num_threads()
+
+
+def host_layers_for_oracle(lis, x, n: int):
+    """Host copies of the experts the oracle will select in the first n layers."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)  # noqa: E731
+    xb = bits(x)
+    out = []
+    for li in lis[:n]:
+        wr = bits(li.router_w)
+        idx, _ = oracle.select_topk(oracle.router_logits(xb, wr), 6)
+        experts = [None] * 256
+        sel = sorted(set(idx.reshape(-1).tolist()))
+        for e in sel:
+            experts[e] = oracle.ExpertWeights(0, li.codes13[e].cpu().numpy(), li.scales13[e].cpu().numpy(),
+                                              float(li.tscale13[e]), li.codes2[e].cpu().numpy(),
+                                              li.scales2[e].cpu().numpy(), float(li.tscale2[e]))
+        shared = oracle.ExpertWeights(0, li.codes13[256].cpu().numpy(), li.scales13[256].cpu().numpy(),
+                                      float(li.tscale13[256]), li.codes2[256].cpu().numpy(),
+                                      li.scales2[256].cpu().numpy(), float(li.tscale2[256]))
+        out.append((wr, experts, shared, len(sel)))
+    return xb, out
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--tokens", type=int, default=8)
+    ap.add_argument("--layers", type=int, default=16)
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3
+
+    import torch
+
+    world, rank, local = dist_setup()
+    T, L = args.tokens, args.layers
+    workload = (f"one NVFP4 MoE layer, T={T} tokens (H=2048, 256 routed experts I=512, sigmoid top-6, "
+                f"1 shared expert), synthetic seeded weights")
+    config = {"workload": workload, "tokens": T, "hidden": 2048, "experts": 256, "top_k": 6, "inter": 512,
+              "layers_rotated": L,
+              "l2": f"cold: steps rotate over {L} distinct resident layers (selected bytes per rotation >> L2)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from nvfp4_moe_decode_gb300 import synth
+
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        import oracle
+
+        oracle.build()
+        nl = min(L, 4)
+        lis = [synth.make_layer(s, T, device=dev) for s in range(nl)]
+        x = lis[0].x
+        xb, hl = host_layers_for_oracle(lis, x, nl)
+        for _ in range(args.warmup if args.warmup < 4 else 3):
+            oracle.moe_forward(xb, hl[0][0], hl[0][1], 6, 512, hl[0][2])
+        t_tot, b_tot, n_tot = 0.0, 0, 0
+        for _ in range(args.steps if args.steps <= 20 else 20):
+            s, b, n, threads = oracle_sample(hl, xb, T, 0.0)
+            t_tot += s
+            b_tot += b
+            n_tot += n
+        v = b_tot / t_tot / 1e9
+        line = {"metric": METRIC, "value": v, "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
+                "steps": n_tot, "warmup": args.warmup, "ms_per_step": 1e3 * t_tot / n_tot,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"kind": "oracle", "value": v, "unit": "GB/s", "cores": threads,
+                                 "sample": f"{n_tot} layer forwards of the fp64 C oracle, one per step"},
+                "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import nvfp4_moe_decode_gb300 as m
+    from nvfp4_moe_decode_gb300 import synth
+    from nvfp4_moe_decode_gb300.layer import PackedLayer, new_workspace
+
+    m.load()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+
+    # ---- resident layers (seeds 0..L-1), x fixed (seed 0) ----
+    lis, packed = [], []
+    x = synth.make_x(0, T, device=dev)
+    with torch.cuda.stream(stream):
+        for s in range(L):
+            li = synth.make_layer(s, T, device=dev)
+            pl = PackedLayer.from_inputs(li, stream)
+            lis.append(li)
+            packed.append(pl)
+    stream.synchronize()
+    # distinct routed experts per layer (from our router, outside the timed region)
+    ws = new_workspace(T, dev, stream)
+    nd = []
+    with torch.cuda.stream(stream):
+        idx = torch.empty(T, 6, dtype=torch.int32, device=dev)
+        w = torch.empty(T, 6, dtype=torch.float32, device=dev)
+        for pl in packed:
+            m.moe_route(x, pl.router_w, T, idx, w, None, ws, stream)
+            stream.synchronize()
+            nd.append(len(set(idx.cpu().reshape(-1).tolist())))
+    m.moe_workspace_init(ws, stream)
+    out = torch.empty(T, 2048, dtype=torch.bfloat16, device=dev)
+
+    def run_steps(k0: int, n: int):
+        for k in range(k0, k0 + n):
+            packed[k % L].forward(x, out, ws, stream)
+
+    # ---- graphs: one rotation of L steps, plus the remainder ----
+    def capture(n: int):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            run_steps(0, n)
+        return g
+
+    run_steps(0, L)   # eager warm-up before capture
+    stream.synchronize()
+    g_full = capture(L)
+    K, W = args.steps, args.warmup
+
+    with torch.cuda.stream(stream):
+        for _ in range(W // L):
+            g_full.replay()
+        run_steps(0, W % L)
+    stream.synchronize()
+    rem_graph = capture(K % L) if K % L else None
+    steps_bytes = sum(layer_bytes(T, nd[k % L]) for k in range(K))
+
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.2)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K // L):
+            g_full.replay()
+        if rem_graph is not None:
+            rem_graph.replay()
+        e1.record(stream)
+    e1.synchronize()
+    clk = clocks.stop()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    ms_max = reduce_max(ms, world)
+    total_bytes = reduce_sum(float(steps_bytes), world)
+    value = total_bytes / (ms_max * 1e-3) / 1e9
+    us_per_layer = 1e3 * ms_max / K
+
+    flag = m.moe_read_device_flag(ws, stream)
+
+    # ---- e2e: host x in, host out back, through the public C-ABI ----
+    xh = x.cpu().pin_memory()
+    oh = torch.empty(T, 2048, dtype=torch.bfloat16).pin_memory()
+    ne = args.e2e_steps
+    xd = torch.empty_like(x)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for k in range(ne):
+            xd.copy_(xh, non_blocking=True)
+            packed[k % L].forward(xd, out, ws, stream)
+            oh.copy_(out, non_blocking=True)
+            stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_bytes = sum(layer_bytes(T, nd[k % L]) for k in range(ne))
+    e2e_v = reduce_sum(e2e_bytes, world) / reduce_max(e2e_s, world) / 1e9
+
+    peak, peak_src = peaks()
+    layer_alg = steps_bytes / K
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4 weights x bf16 activations, f32 accumulate", "data": "synthetic",
+        "config": {**config, "us_per_layer": us_per_layer, "tokens_per_s": T * K / (ms_max * 1e-3),
+                   "distinct_experts_per_layer": nd, "algorithmic_bytes_per_layer": layer_alg,
+                   "hbm_frac": value / world / peak, "device_flag": flag},
+        "roofline": {"bound": "hbm", "achieved": layer_alg / (us_per_layer * 1e-6) / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": layer_alg / (us_per_layer * 1e-6) / 1e9 / peak,
+                     "traffic": None, "peak_source": peak_src,
+                     "kernel": "moe_layer_forward (router + gate/up + down, PDL-chained)"},
+        "e2e": {"value": e2e_v, "unit": "GB/s", "steps": ne, "h2d_bytes_per_step": T * 2048 * 2,
+                "d2h_bytes_per_step": T * 2048 * 2},
+        "gpu_launches": 3 * K,
+        "clocks": clk,
+    }
+
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        xb, hl = host_layers_for_oracle(lis, x, min(L, 4))
+        s, b, n, threads = oracle_sample(hl, xb, T, args.cpu_budget)
+        line["cpu_baseline"] = {"value": b / s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{n} layer forwards (T={T}) of the fp64 C oracle over "
+                                          f"{len(hl)} of the rotated layers, {s:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,231 @@
+/*
+ * nvfp4moe.h -- C ABI of libnvfp4moe.so, the GB300 (sm_103a) small-batch
+ * weight-only NVFP4 (W4A16) mixture-of-experts layer.
+ *
+ * The operation (sources are web pages, cited by title and section):
+ *
+ *  [FLINT]  "vLLM adds day-0 support for Recursive's Flint, hitting about 485
+ *           tokens/s on one GB200", section "A 40B MoE that activates 2.5B
+ *           parameters": hidden size 2048, 256 routed experts, sigmoid top-6
+ *           routing plus one shared expert; the NVFP4 checkpoint is repacked
+ *           losslessly at load time and runs weight-only (W4A16) with BF16
+ *           activations.  Section "From 1,096 kernels to 346": router and
+ *           expert GEMVs read only the selected experts' weights; routing and
+ *           the expert combine are fused into the neighbouring GEMVs; each
+ *           kernel uses programmatic dependent launch.
+ *  [MOET]   "Frontier MoE on consumer Blackwell (SM120)", section
+ *           "GLM-5.2 (753B) - the headline model": NVFP4 = e2m1 code x e4m3
+ *           scale per block of 16 x per-tensor fp32 scale.
+ *
+ * For T tokens x[T][H] (bf16) the layer computes
+ *     logit[t][e] = sum_k x[t][k] * router_w[e][k]
+ *     sel[t]      = the top_k experts by logit (lower index wins a tie)
+ *     w[t][i]     = sigmoid(logit[t][sel_i]) / sum_j sigmoid(logit[t][sel_j])
+ *     FFN_e(v)    = W2_e ( silu(W1_e v) * (W3_e v) )      (W13 = [W1; W3])
+ *     out[t]      = sum_i w[t][i] * FFN_{sel_i}(x[t]) + FFN_shared(x[t])
+ * with NVFP4 weights dequantised exactly (e2m1 * e4m3 * tensor scale), fp32
+ * accumulation, the SiLU*up activation rounded to bf16 (the activations are
+ * BF16), and out rounded once to bf16.
+ *
+ * Shapes this build supports: H = 2048, I = 512 (W13 is [2I][H], W2 is
+ * [H][I]), E = 256 routed experts, top_k = 6, 0 or 1 shared expert, and
+ * 1 <= T <= MOE_MAX_DECODE_T tokens per call.
+ *
+ * Conventions for every entry point:
+ *  - All data pointers are DEVICE pointers (cudaMalloc / torch memory) on the
+ *    current device, 16-byte aligned, unless a comment says "host".
+ *  - The caller owns every buffer; the library allocates and frees nothing.
+ *  - Calls enqueue work on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and return without synchronising, except where stated.
+ *  - Argument errors are detected on the host before anything is enqueued
+ *    and return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED; launch failures
+ *    return MOE_ERR_CUDA.  Conditions found on the device (a non-finite
+ *    router logit, an expired bounded wait) set bits of a flag word in the
+ *    workspace, read back by moe_read_device_flag.  Kernels never trap.
+ *  - The library keeps no mutable global state; calls on different streams
+ *    with different workspaces may run concurrently.
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size */
+    MOE_ERR_UNSUPPORTED = 2, /* shape or mode this build does not implement */
+    MOE_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    MOE_ERR_DEVICE_FLAG = 4, /* moe_read_device_flag found a device-side error */
+    MOE_ERR_WORKSPACE = 5    /* workspace too small */
+} moe_status;
+
+/* Weight storage of an expert bank. */
+enum { MOE_W_NVFP4 = 0, MOE_W_BF16 = 1 };
+
+/* Row order of a packed NVFP4 matrix.  GATE_UP interleaves the gate rows
+ * [0, N/2) and up rows [N/2, N) of a W13 matrix so that one 16-row band
+ * holds gate rows 8b..8b+7 and the matching up rows. */
+enum { MOE_PACK_PLAIN = 0, MOE_PACK_GATE_UP = 1 };
+
+/* Device-side error bits reported by moe_read_device_flag. */
+enum {
+    MOE_FLAG_NONFINITE_LOGIT = 1, /* a router logit was NaN/Inf; routing used index order */
+    MOE_FLAG_WAIT_TIMEOUT = 2,    /* a bounded wait on a barrier expired; output invalid */
+    MOE_FLAG_BAD_INDEX = 4        /* an expert index out of range was seen; skipped */
+};
+
+#define MOE_HIDDEN 2048
+#define MOE_INTER 512
+#define MOE_EXPERTS 256
+#define MOE_TOPK 6
+#define MOE_MAX_DECODE_T 8
+
+/*
+ * A bank of experts with identical shapes, stored back to back.
+ *  wtype == MOE_W_NVFP4: w13 holds n_experts packed W13 matrices (gate/up,
+ *     [2I][H], packed with MOE_PACK_GATE_UP), each moe_packed_bytes(2I, H)
+ *     bytes; w2 holds n_experts packed W2 matrices ([H][I], MOE_PACK_PLAIN),
+ *     each moe_packed_bytes(H, I) bytes; tscale13/tscale2 are device float
+ *     arrays [n_experts] of per-tensor scales.
+ *  wtype == MOE_W_BF16: w13 is bf16 [n_experts][2I][H] row-major, w2 is bf16
+ *     [n_experts][H][I]; tscale13/tscale2 are ignored (may be NULL).
+ * The struct itself is host memory; the pointers in it are device pointers.
+ */
+typedef struct {
+    int32_t wtype;
+    int32_t n_experts;
+    const void *w13;
+    const void *w2;
+    const float *tscale13;
+    const float *tscale2;
+} moe_expert_bank;
+
+/* ABI version of this header (bumped on any incompatible change). */
+int moe_abi_version(void);
+
+/* Human-readable name of a status (static storage; never NULL). */
+const char *moe_status_string(moe_status s);
+
+/* ----------------------------------------------------------------------- */
+/* Packing (load time).  [FLINT, "A 40B MoE ...": the NVFP4 blocks are     */
+/* repacked losslessly at load time.]                                      */
+/* ----------------------------------------------------------------------- */
+
+/* Bytes of one packed NVFP4 matrix [N][K]: N*K/2 code bytes + N*K/16 scale
+ * bytes (the same as the canonical form; packing permutes bytes and nibbles
+ * only).  Returns 0 when N is not a multiple of 16 or K not a multiple of
+ * 128. */
+size_t moe_packed_bytes(int N, int K);
+
+/*
+ * Pack `count` canonical NVFP4 matrices [N][K] into the kernel layout.
+ *  codes:  device u8 [count][N][K/2]; byte (n, j) holds element (n, 2j) in
+ *          its low nibble and (n, 2j+1) in its high nibble (e2m1 codes).
+ *  scales: device u8 [count][N][K/16]; e4m3 (E4M3FN) scale of elements
+ *          (n, 16b .. 16b+15) at (n, b).
+ *  kind:   MOE_PACK_PLAIN or MOE_PACK_GATE_UP (needs N % 32 == 0).
+ *  packed: device, count * moe_packed_bytes(N, K) bytes, 16-byte aligned.
+ * The result is a pure permutation of the input nibbles and scale bytes.
+ * Errors: MOE_ERR_INVALID_ARG for null pointers, count < 1 or unsupported
+ * N/K; nothing is enqueued then.
+ */
+moe_status moe_pack_nvfp4(const uint8_t *codes, const uint8_t *scales, int N, int K, int kind,
+                          int count, void *packed, moe_stream_t stream);
+
+/* Exact inverse of moe_pack_nvfp4 (same arguments, opposite direction). */
+moe_status moe_unpack_nvfp4(const void *packed, int N, int K, int kind, int count,
+                            uint8_t *codes, uint8_t *scales, moe_stream_t stream);
+
+/*
+ * Dequantise one packed NVFP4 matrix to fp32 in canonical row order:
+ * out[n][k] = fp32(e2m1 * e4m3 * tscale) (the e2m1*e4m3 product is exact;
+ * one rounding when tscale is applied).  out: device float [N][K].
+ * Used to check the packed layout and the in-register decode.
+ * [MOET, "GLM-5.2": e2m1 x e4m3 block-16 x per-tensor scale_2]
+ */
+moe_status moe_dequant_nvfp4(const void *packed, int N, int K, int kind, float tscale,
+                             float *out, moe_stream_t stream);
+
+/* ----------------------------------------------------------------------- */
+/* Workspace.                                                              */
+/* ----------------------------------------------------------------------- */
+
+/* Workspace bytes for moe_route / moe_layer_forward with T tokens (0 if T
+ * is unsupported).  The workspace holds routing results, the SiLU*up
+ * activations, combine partials, arrival counters and the device flag. */
+size_t moe_workspace_bytes(int T);
+
+/* Zero a workspace (enqueued memset).  Required once before the first use of
+ * a workspace; the kernels leave the counters zeroed after every call. */
+moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Read and clear the device flag word of a workspace.  SYNCHRONISES the
+ * stream.  *flag_out (host) receives the MOE_FLAG_* bits.  Returns MOE_OK when
+ * no bit was set, MOE_ERR_DEVICE_FLAG when one was, MOE_ERR_CUDA on a CUDA
+ * error.
+ */
+moe_status moe_read_device_flag(void *workspace, moe_stream_t stream, uint32_t *flag_out);
+
+/* ----------------------------------------------------------------------- */
+/* Routing.  [FLINT, "A 40B MoE ...": sigmoid top-6 routing]               */
+/* ----------------------------------------------------------------------- */
+
+/*
+ * Router GEMV + sigmoid + top-k + renormalisation for T tokens.
+ *  x:        device bf16 [T][H];  router_w: device bf16 [E][H].
+ *  idx:      device int32 [T][top_k] (selection order: best first).
+ *  w:        device float [T][top_k], renormalised to sum to 1 per token.
+ *  logits:   device float [T][E] fp32 logits, or NULL.
+ * Logits are fp32 sums of exact bf16*bf16 products (fixed summation tree of
+ * depth <= 24); the selection is taken on them, a tie going to the lower
+ * index.  A non-finite logit sets MOE_FLAG_NONFINITE_LOGIT.
+ * Errors: MOE_ERR_UNSUPPORTED unless H, E, top_k match this build and
+ * 1 <= T <= MOE_MAX_DECODE_T; MOE_ERR_WORKSPACE if workspace_bytes is below
+ * moe_workspace_bytes(T).
+ */
+moe_status moe_route(const void *x, const void *router_w, int T, int n_experts, int top_k,
+                     int32_t *idx, float *w, float *logits, void *workspace,
+                     size_t workspace_bytes, moe_stream_t stream);
+
+/* ----------------------------------------------------------------------- */
+/* The layer.  [FLINT, "From 1,096 kernels to 346": router and expert GEMVs */
+/* that read only the selected experts' weights, routing and the combine   */
+/* fused into the neighbouring kernels, chained by programmatic dependent  */
+/* launch.]                                                                */
+/* ----------------------------------------------------------------------- */
+
+/*
+ * out = MoE(x) for 1 <= T <= MOE_MAX_DECODE_T tokens (see the top of this
+ * header).  Three kernels, chained with programmatic dependent launch:
+ * the router (+top-k, the expert union and per-slot token weights), the
+ * gate/up GEMV fused with SiLU*up over the distinct selected experts (each
+ * read once for all tokens) plus the shared expert, and the down GEMV fused
+ * with the routing-weighted combine and the shared expert.
+ *  x:        device bf16 [T][H]; must not alias out.
+ *  router_w: device bf16 [E][H].
+ *  routed:   host struct describing E = 256 routed experts.
+ *  shared:   host struct with n_experts 0 or 1 (NULL = no shared expert).
+ *  out:      device bf16 [T][H].
+ *  workspace: device, >= moe_workspace_bytes(T), initialised once with
+ *            moe_workspace_init; one workspace per concurrently running call.
+ * The routed and shared banks must have the same wtype in this build.
+ * Activations must satisfy |x| < 2^32 (they are scaled by 2^96 inside the
+ * tensor-core products).
+ */
+moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expert_bank *routed,
+                             const moe_expert_bank *shared, void *out, int T, void *workspace,
+                             size_t workspace_bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4MOE_H */

@@ -1,0 +1,250 @@
+// api.cu -- the extern "C" entry points of libnvfp4moe.so: argument checks,
+// workspace handling and the launch sequence (declared in nvfp4moe.h).
+#include <cstring>
+
+#include "kernels.cuh"
+
+using namespace moe;
+
+namespace {
+
+constexpr int ABI_VERSION = 1;
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0)
+        return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    if (dev >= 0 && dev < 64)
+        cached[dev] = n;
+    return n;
+}
+
+// Slot-group and band-group sizes of the down kernel for T tokens.
+void down_tiling(int T, int &BG, int &SG)
+{
+    if (T <= 2) { BG = 1; SG = 2; }
+    else { BG = 4; SG = 2; }
+}
+
+int max_slots(int T, int n_shared)
+{
+    int routed = T * TOPK < E ? T * TOPK : E;
+    return n_shared + routed;
+}
+
+moe_status check_bank(const moe_expert_bank *b, int expect_n, bool allow_empty)
+{
+    if (b == nullptr)
+        return allow_empty ? MOE_OK : MOE_ERR_INVALID_ARG;
+    if (allow_empty && b->n_experts == 0)
+        return MOE_OK;
+    if (b->n_experts != expect_n)
+        return MOE_ERR_UNSUPPORTED;
+    if (b->wtype != MOE_W_NVFP4)
+        return MOE_ERR_UNSUPPORTED;
+    if (!b->w13 || !b->w2 || !b->tscale13 || !b->tscale2)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(b->w13) || !aligned16(b->w2))
+        return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_abi_version(void) { return ABI_VERSION; }
+
+const char *moe_status_string(moe_status s)
+{
+    switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_FLAG: return "MOE_ERR_DEVICE_FLAG";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    }
+    return "MOE_UNKNOWN_STATUS";
+}
+
+size_t moe_packed_bytes(int N, int K)
+{
+    if (N <= 0 || K <= 0 || N % 16 != 0 || K % 128 != 0)
+        return 0;
+    return (size_t)N * K / 2 + (size_t)N * K / 16;
+}
+
+static moe_status check_pack_args(const void *a, const void *b, const void *c, int N, int K, int kind,
+                                  int count)
+{
+    if (!a || !b || !c || count < 1 || moe_packed_bytes(N, K) == 0)
+        return MOE_ERR_INVALID_ARG;
+    if (kind != MOE_PACK_PLAIN && kind != MOE_PACK_GATE_UP)
+        return MOE_ERR_INVALID_ARG;
+    if (kind == MOE_PACK_GATE_UP && N % 32 != 0)
+        return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status moe_pack_nvfp4(const uint8_t *codes, const uint8_t *scales, int N, int K, int kind,
+                          int count, void *packed, moe_stream_t stream)
+{
+    moe_status s = check_pack_args(codes, scales, packed, N, K, kind, count);
+    if (s != MOE_OK)
+        return s;
+    PackArgs a{codes, scales, static_cast<uint8_t *>(packed), N, K, kind, count};
+    return cuda_status(launch_pack(a, (cudaStream_t)stream));
+}
+
+moe_status moe_unpack_nvfp4(const void *packed, int N, int K, int kind, int count, uint8_t *codes,
+                            uint8_t *scales, moe_stream_t stream)
+{
+    moe_status s = check_pack_args(packed, codes, scales, N, K, kind, count);
+    if (s != MOE_OK)
+        return s;
+    UnpackArgs a{static_cast<const uint8_t *>(packed), codes, scales, N, K, kind, count};
+    return cuda_status(launch_unpack(a, (cudaStream_t)stream));
+}
+
+moe_status moe_dequant_nvfp4(const void *packed, int N, int K, int kind, float tscale, float *out,
+                             moe_stream_t stream)
+{
+    moe_status s = check_pack_args(packed, out, out, N, K, kind, 1);
+    if (s != MOE_OK)
+        return s;
+    if (!aligned16(packed))
+        return MOE_ERR_INVALID_ARG;
+    DequantArgs a{static_cast<const uint8_t *>(packed), out, N, K, kind, tscale};
+    return cuda_status(launch_dequant(a, (cudaStream_t)stream));
+}
+
+size_t moe_workspace_bytes(int T)
+{
+    if (T < 1 || T > MAXT)
+        return 0;
+    return ws_layout().total;
+}
+
+moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, moe_stream_t stream)
+{
+    if (!workspace || !aligned16(workspace))
+        return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < ws_layout().total)
+        return MOE_ERR_WORKSPACE;
+    return cuda_status(cudaMemsetAsync(workspace, 0, ws_layout().total, (cudaStream_t)stream));
+}
+
+moe_status moe_read_device_flag(void *workspace, moe_stream_t stream, uint32_t *flag_out)
+{
+    if (!workspace || !flag_out)
+        return MOE_ERR_INVALID_ARG;
+    uint32_t v = 0;
+    uint8_t *flag = static_cast<uint8_t *>(workspace) + ws_layout().ctrl;
+    cudaError_t e = cudaMemcpyAsync(&v, flag, sizeof v, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(flag, 0, sizeof v, (cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return MOE_ERR_CUDA;
+    *flag_out = v;
+    return v ? MOE_ERR_DEVICE_FLAG : MOE_OK;
+}
+
+static moe_status check_route_args(const void *x, const void *router_w, int T, void *workspace,
+                                   size_t workspace_bytes)
+{
+    if (!x || !router_w || !workspace)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(router_w) || !aligned16(workspace))
+        return MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > MAXT)
+        return MOE_ERR_UNSUPPORTED;
+    if (workspace_bytes < ws_layout().total)
+        return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+moe_status moe_route(const void *x, const void *router_w, int T, int n_experts, int top_k,
+                     int32_t *idx, float *w, float *logits, void *workspace, size_t workspace_bytes,
+                     moe_stream_t stream)
+{
+    moe_status s = check_route_args(x, router_w, T, workspace, workspace_bytes);
+    if (s != MOE_OK)
+        return s;
+    if (n_experts != E || top_k != TOPK)
+        return MOE_ERR_UNSUPPORTED;
+    if (!idx || !w)
+        return MOE_ERR_INVALID_ARG;
+    RouterArgs a{static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(router_w),
+                 T, 0, static_cast<uint8_t *>(workspace), idx, w, logits};
+    return cuda_status(launch_router(a, (cudaStream_t)stream, true));
+}
+
+moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expert_bank *routed,
+                             const moe_expert_bank *shared, void *out, int T, void *workspace,
+                             size_t workspace_bytes, moe_stream_t stream)
+{
+    moe_status s = check_route_args(x, router_w, T, workspace, workspace_bytes);
+    if (s != MOE_OK)
+        return s;
+    if (!out || !aligned16(out) || out == x)
+        return MOE_ERR_INVALID_ARG;
+    if ((s = check_bank(routed, E, false)) != MOE_OK)
+        return s;
+    if ((s = check_bank(shared, 1, true)) != MOE_OK)
+        return s;
+    const int n_shared = (shared && shared->n_experts > 0) ? 1 : 0;
+    const int nsm = sm_count();
+    if (nsm <= 0)
+        return MOE_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+
+    RouterArgs ra{static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(router_w),
+                  T, n_shared, ws, nullptr, nullptr, nullptr};
+    cudaError_t e = launch_router(ra, st, true);
+    if (e != cudaSuccess)
+        return MOE_ERR_CUDA;
+
+    GateUpArgs ga{};
+    ga.x = static_cast<const __nv_bfloat16 *>(x);
+    ga.T = T;
+    ga.routed_w13 = static_cast<const uint8_t *>(routed->w13);
+    ga.routed_ts13 = routed->tscale13;
+    ga.shared_w13 = n_shared ? static_cast<const uint8_t *>(shared->w13) : nullptr;
+    ga.shared_ts13 = n_shared ? shared->tscale13 : nullptr;
+    ga.n_shared = n_shared;
+    ga.ws = ws;
+    e = launch_gate_up(ga, nsm, st, true);
+    if (e != cudaSuccess)
+        return MOE_ERR_CUDA;
+
+    DownArgs da{};
+    da.T = T;
+    da.routed_w2 = static_cast<const uint8_t *>(routed->w2);
+    da.routed_ts2 = routed->tscale2;
+    da.shared_w2 = n_shared ? static_cast<const uint8_t *>(shared->w2) : nullptr;
+    da.shared_ts2 = n_shared ? shared->tscale2 : nullptr;
+    da.n_shared = n_shared;
+    down_tiling(T, da.BG, da.SG);
+    da.ws = ws;
+    da.out = static_cast<__nv_bfloat16 *>(out);
+    const int qmax = (max_slots(T, n_shared) + da.SG - 1) / da.SG;
+    e = launch_down(da, qmax, st, true);
+    return cuda_status(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,264 @@
+// router.cu -- K1: router GEMV + sigmoid top-k + renormalise + expert union.
+//
+// Flint page ("vLLM adds day-0 support for Recursive's Flint"), section
+// "A 40B MoE that activates 2.5B parameters": 256 experts, sigmoid top-6
+// routing plus a shared expert.  Section "From 1,096 kernels to 346": the
+// routing is fused into the router GEMV, and every kernel uses programmatic
+// dependent launch so that it loads its weights while its predecessor runs.
+//
+// Grid: E/2 CTAs of 256 threads.  CTA c computes the logits of experts 2c and
+// 2c+1 for all T tokens: warps 0-3 take expert 2c, warps 4-7 expert 2c+1, one
+// quarter of the hidden dimension each.  A lane multiplies 16 bf16 pairs
+// (exact products in fp32) in k order, the warp adds its 32 lane sums by a
+// 5-level butterfly, and warp 0/4 adds the four quarter sums in order: every
+// logit is an fp32 sum of exact products of depth 16 + 5 + 3 = 24.
+//
+// The CTA that arrives last (arrival counter in the workspace) selects the
+// top-k of each token on the fp32 logits (one warp per token), computes the
+// renormalised sigmoid weights, and builds the slot table that the expert
+// kernels read: the shared expert(s) first, then the distinct selected
+// experts in ascending order, each with the routing weight of every token
+// (0 where the token did not select it).
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+// Order-preserving key: larger logit first, then smaller expert index.
+// -0.0 is folded into +0.0 (they compare equal as values); NaN sorts last.
+__device__ __forceinline__ unsigned long long rank_key(float v, int e)
+{
+    uint32_t u;
+    if (v != v) {
+        u = 0u;
+    } else {
+        v = v + 0.0f;
+        u = __float_as_uint(v);
+        u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    }
+    return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFu - (uint32_t)e);
+}
+
+__device__ __forceinline__ int key_expert(unsigned long long k) { return 0xFFFF - (int)(k & 0xFFFFu); }
+
+__device__ __forceinline__ void cas_desc(unsigned long long &a, unsigned long long &b)
+{
+    unsigned long long hi = a > b ? a : b;
+    unsigned long long lo = a > b ? b : a;
+    a = hi;
+    b = lo;
+}
+
+// Sort 8 keys in descending order (Batcher's odd-even merge network, 19 CAS).
+__device__ __forceinline__ void sort8_desc(unsigned long long k[8])
+{
+    cas_desc(k[0], k[1]); cas_desc(k[2], k[3]); cas_desc(k[4], k[5]); cas_desc(k[6], k[7]);
+    cas_desc(k[0], k[2]); cas_desc(k[1], k[3]); cas_desc(k[4], k[6]); cas_desc(k[5], k[7]);
+    cas_desc(k[1], k[2]); cas_desc(k[5], k[6]);
+    cas_desc(k[0], k[4]); cas_desc(k[1], k[5]); cas_desc(k[2], k[6]); cas_desc(k[3], k[7]);
+    cas_desc(k[2], k[4]); cas_desc(k[3], k[5]);
+    cas_desc(k[1], k[2]); cas_desc(k[3], k[4]); cas_desc(k[5], k[6]);
+}
+
+// Sort a bitonic sequence of 8 keys into descending order (12 CAS).
+__device__ __forceinline__ void bitonic8_desc(unsigned long long k[8])
+{
+    cas_desc(k[0], k[4]); cas_desc(k[1], k[5]); cas_desc(k[2], k[6]); cas_desc(k[3], k[7]);
+    cas_desc(k[0], k[2]); cas_desc(k[1], k[3]); cas_desc(k[4], k[6]); cas_desc(k[5], k[7]);
+    cas_desc(k[0], k[1]); cas_desc(k[2], k[3]); cas_desc(k[4], k[5]); cas_desc(k[6], k[7]);
+}
+
+// Top-8 of E = 256 keys held 8 per lane; every lane ends with the sorted top 8.
+__device__ __forceinline__ void warp_top8(unsigned long long k[8])
+{
+    sort8_desc(k);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        unsigned long long p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            p[i] = __shfl_xor_sync(0xFFFFFFFFu, k[i], off);
+        // top 8 of two descending lists = elementwise max against the reversed
+        // partner list, which is bitonic
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            k[i] = k[i] > p[7 - i] ? k[i] : p[7 - i];
+        bitonic8_desc(k);
+    }
+}
+
+}  // namespace
+
+
+__global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a)
+{
+    const WsLayout L = ws_layout();
+    uint32_t *ctrl = reinterpret_cast<uint32_t *>(a.ws + L.ctrl);
+    float *logits = reinterpret_cast<float *>(a.ws + L.logits);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 2 + (warp >> 2);
+    const int kq = warp & 3;
+
+    // Router weights do not depend on the preceding kernel: load them first.
+    uint4 wv[2];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+        wv[m] = ldg_nc_v4(a.wr + (size_t)e * H + 512 * kq + 256 * m + 8 * lane);
+
+    griddep_wait();      // x may be written by the preceding kernel
+    griddep_launch();    // the expert kernel may start its prologue now
+
+    __shared__ float part[8][MAXT];
+    __shared__ int is_last;
+
+    for (int t = 0; t < a.T; ++t) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            uint4 xv = ldg_nc_v4(a.x + (size_t)t * H + 512 * kq + 256 * m + 8 * lane);
+            const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+            const uint32_t ws[4] = {wv[m].x, wv[m].y, wv[m].z, wv[m].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc = fmaf(bf16_bits_to_float(xs[q] & 0xFFFFu), bf16_bits_to_float(ws[q] & 0xFFFFu), acc);
+                acc = fmaf(bf16_bits_to_float(xs[q] >> 16), bf16_bits_to_float(ws[q] >> 16), acc);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+        if (lane == 0)
+            part[warp][t] = acc;
+    }
+    __syncthreads();
+    if ((warp & 3) == 0 && lane < a.T) {
+        const int t = lane;
+        float v = ((part[warp][t] + part[warp + 1][t]) + part[warp + 2][t]) + part[warp + 3][t];
+        logits[t * E + e] = v;
+        if (a.user_logits)
+            a.user_logits[(size_t)t * E + e] = v;
+        __threadfence();   // publish before this CTA's arrival is counted
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t prev = atomicAdd(&ctrl[1], 1u);
+        is_last = (prev == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!is_last)
+        return;
+    __threadfence();
+
+    // ---- last CTA: top-k per token, weights, slot table ----
+    __shared__ int32_t sel[MAXT][TOPK];
+    __shared__ float selw[MAXT][TOPK];
+    int32_t *topk_idx = reinterpret_cast<int32_t *>(a.ws + L.topk_idx);
+    float *topk_w = reinterpret_cast<float *>(a.ws + L.topk_w);
+    SlotTable *st = reinterpret_cast<SlotTable *>(a.ws + L.slots);
+
+    if (warp < a.T) {
+        const int t = warp;
+        unsigned long long k[8];
+        bool bad = false;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int ee = lane + 32 * m;
+            float v = __ldcg(logits + t * E + ee);
+            bad |= !isfinite(v);
+            k[m] = rank_key(v, ee);
+        }
+        if (__any_sync(0xFFFFFFFFu, bad) && lane == 0)
+            atomicOr(&ctrl[0], FLAG_NONFINITE);
+        warp_top8(k);
+        // weights: sigmoid of the selected logits, renormalised (fp32)
+        float s = 0.0f, sum = 0.0f;
+        int ex = 0;
+#pragma unroll
+        for (int i = 0; i < TOPK; ++i) {
+            const int ei = key_expert(k[i]);
+            const float v = __ldcg(logits + t * E + ei);
+            const float si = 1.0f / (1.0f + expf(-v));
+            sum += si;
+            if (lane == i) { s = si; ex = ei; }
+        }
+        if (lane < TOPK) {
+            const float wi = s / sum;
+            sel[t][lane] = ex;
+            selw[t][lane] = wi;
+            topk_idx[t * TOPK + lane] = ex;
+            topk_w[t * TOPK + lane] = wi;
+            if (a.user_idx) a.user_idx[t * TOPK + lane] = ex;
+            if (a.user_w) a.user_w[t * TOPK + lane] = wi;
+        }
+    }
+    __syncthreads();
+
+    // Slot table: shared expert(s), then the sorted union of selected experts.
+    __shared__ uint32_t bitmap[E / 32];
+    __shared__ int32_t prefix[E / 32];
+    if (threadIdx.x < E / 32)
+        bitmap[threadIdx.x] = 0u;
+    __syncthreads();
+    if (threadIdx.x < a.T * TOPK) {
+        const int ei = sel[threadIdx.x / TOPK][threadIdx.x % TOPK];
+        atomicOr(&bitmap[ei >> 5], 1u << (ei & 31));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int i = 0; i < E / 32; ++i) {
+            prefix[i] = run;
+            run += __popc(bitmap[i]);
+        }
+        st->n_shared = a.n_shared;
+        st->n_slots = a.n_shared + run;
+    }
+    __syncthreads();
+    // expert ids of the routed slots
+    if (threadIdx.x < E) {
+        const int ei = threadIdx.x;
+        const uint32_t bits = bitmap[ei >> 5];
+        if (bits & (1u << (ei & 31))) {
+            const int slot = a.n_shared + prefix[ei >> 5] + __popc(bits & ((1u << (ei & 31)) - 1u));
+            st->expert[slot] = ei;
+        }
+    }
+    // per-slot token weights: clear every slot, then fill
+    for (int i = threadIdx.x; i < MAX_SLOTS * MAXT; i += blockDim.x)
+        st->wts[i / MAXT][i % MAXT] = 0.0f;
+    if (threadIdx.x < a.n_shared)
+        st->expert[threadIdx.x] = -1 - (int)threadIdx.x;
+    __syncthreads();
+    if (threadIdx.x < a.n_shared * MAXT) {
+        const int s = threadIdx.x / MAXT, t = threadIdx.x % MAXT;
+        st->wts[s][t] = (t < a.T) ? 1.0f : 0.0f;
+    }
+    if (threadIdx.x < a.T * TOPK) {
+        const int t = threadIdx.x / TOPK, i = threadIdx.x % TOPK;
+        const int ei = sel[t][i];
+        const uint32_t bits = bitmap[ei >> 5];
+        const int slot = a.n_shared + prefix[ei >> 5] + __popc(bits & ((1u << (ei & 31)) - 1u));
+        st->wts[slot][t] = selw[t][i];
+    }
+    if (threadIdx.x == 0)
+        ctrl[1] = 0u;   // re-arm the arrival counter for the next call
+}
+
+cudaError_t launch_router(const RouterArgs &a, cudaStream_t stream, bool pdl)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(E / 2);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, router_topk_kernel, a);
+}
+
+}  // namespace moe

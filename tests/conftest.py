@@ -18,3 +18,23 @@ def oracle_lib():
     import oracle
 
     return oracle.load()
+
+
+@pytest.fixture(scope="session")
+def moe_lib():
+    """Build (if needed) and load libnvfp4moe.so; no GPU is touched."""
+    from nvfp4_moe_decode_gb300 import _build
+    import nvfp4_moe_decode_gb300 as m
+
+    _build.build()
+    return m.load()
+
+
+@pytest.fixture(scope="session")
+def cuda_dev(moe_lib):
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    return torch.device("cuda:0")

@@ -1,0 +1,95 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import nvfp4_moe_decode_gb300 as m
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for mt in re.finditer(r"\b(moe_[a-z0-9_]+)\s*\(", text):
+            names.add(mt.group(1))
+    return names
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == set(m.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(moe_lib):
+    for name in declared_functions():
+        assert hasattr(moe_lib, name), name
+        assert ctypes.cast(getattr(moe_lib, name), ctypes.c_void_p).value
+
+
+def test_abi_version_and_status_strings(moe_lib):
+    assert m.moe_abi_version() == 1
+    assert m.moe_status_string(m.MOE_OK) == "MOE_OK"
+    assert m.moe_status_string(m.MOE_ERR_WORKSPACE) == "MOE_ERR_WORKSPACE"
+    assert m.moe_status_string(99) == "MOE_UNKNOWN_STATUS"
+
+
+def test_packed_bytes(moe_lib):
+    assert m.moe_packed_bytes(1024, 2048) == 1_179_648
+    assert m.moe_packed_bytes(2048, 512) == 589_824
+    assert m.moe_packed_bytes(15, 2048) == 0
+    assert m.moe_packed_bytes(16, 64) == 0
+    assert m.moe_packed_bytes(0, 128) == 0
+
+
+def test_workspace_bytes(moe_lib):
+    for T in range(1, 9):
+        assert m.moe_workspace_bytes(T) > 0
+    assert m.moe_workspace_bytes(0) == 0
+    assert m.moe_workspace_bytes(9) == 0
+
+
+def test_host_argument_errors_enqueue_nothing(moe_lib):
+    lib = moe_lib
+    dummy = 1 << 20  # an aligned non-null value; never dereferenced on these paths
+    # pack: null pointers, count 0, bad kind, bad shape
+    assert lib.moe_pack_nvfp4(None, dummy, 16, 128, 0, 1, dummy, None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_pack_nvfp4(dummy, dummy, 16, 128, 0, 0, dummy, None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_pack_nvfp4(dummy, dummy, 16, 128, 7, 1, dummy, None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_pack_nvfp4(dummy, dummy, 16, 128, 1, 1, dummy, None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_unpack_nvfp4(dummy, 16, 100, 0, 1, dummy, dummy, None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_dequant_nvfp4(dummy + 4, 16, 128, 0, 1.0, dummy, None) == m.MOE_ERR_INVALID_ARG
+    # route / forward: null, misaligned, unsupported T, small workspace
+    ws = m.moe_workspace_bytes(1)
+    assert lib.moe_route(None, dummy, 1, 256, 6, dummy, dummy, None, dummy, ws, None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(dummy + 2, dummy, 1, 256, 6, dummy, dummy, None, dummy, ws, None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(dummy, dummy, 9, 256, 6, dummy, dummy, None, dummy, ws, None) == m.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route(dummy, dummy, 1, 128, 6, dummy, dummy, None, dummy, ws, None) == m.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route(dummy, dummy, 1, 256, 6, dummy, dummy, None, dummy, 16, None) == m.MOE_ERR_WORKSPACE
+    bank = m.moe_expert_bank(m.MOE_W_NVFP4, 256, dummy, dummy, dummy, dummy)
+    bad_n = m.moe_expert_bank(m.MOE_W_NVFP4, 255, dummy, dummy, dummy, dummy)
+    bad_w = m.moe_expert_bank(7, 256, dummy, dummy, dummy, dummy)
+    null_w = m.moe_expert_bank(m.MOE_W_NVFP4, 256, None, dummy, dummy, dummy)
+    fwd = lib.moe_layer_forward
+    B = ctypes.byref
+    assert fwd(dummy, dummy, B(bank), None, dummy, 0, dummy, ws, None) == m.MOE_ERR_UNSUPPORTED
+    assert fwd(dummy, dummy, B(bank), None, dummy, 1, dummy, 8, None) == m.MOE_ERR_WORKSPACE
+    assert fwd(dummy, dummy, B(bank), None, dummy, 1, dummy, ws, None) == m.MOE_ERR_INVALID_ARG  # out aliases x
+    assert fwd(dummy, dummy, B(bad_n), None, dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_UNSUPPORTED
+    assert fwd(dummy, dummy, B(bad_w), None, dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_UNSUPPORTED
+    assert fwd(dummy, dummy, B(null_w), None, dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_INVALID_ARG
+    assert fwd(dummy, dummy, None, None, dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_init(None, ws, None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_init(dummy, 8, None) == m.MOE_ERR_WORKSPACE
+    assert lib.moe_read_device_flag(None, None, None) == m.MOE_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(OSError):
+        m.load(str(tmp_path / "missing.so"))
