@@ -358,7 +358,7 @@ def main():
                      "kernel": "moe_layer_forward (router + gate/up + down, PDL-chained)"},
         "e2e": {"value": e2e_v, "unit": "GB/s", "steps": ne, "h2d_bytes_per_step": T * 2048 * 2,
                 "d2h_bytes_per_step": T * 2048 * 2},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 4 * K,
         "clocks": clk,
     }
 

@@ -30,18 +30,9 @@ int sm_count()
     return n;
 }
 
-// Slot-group and band-group sizes of the down kernel for T tokens.
-void down_tiling(int T, int &BG, int &SG)
-{
-    if (T <= 2) { BG = 1; SG = 2; }
-    else { BG = 4; SG = 2; }
-}
-
-int max_slots(int T, int n_shared)
-{
-    int routed = T * TOPK < E ? T * TOPK : E;
-    return n_shared + routed;
-}
+// K split of the gate/up kernel and band-group size of the down kernel.
+int gate_up_ks(int T) { return T <= 4 ? 2 : 1; }
+int down_bg(int T) { return T <= 2 ? 2 : (T <= 6 ? 4 : 8); }
 
 moe_status check_bank(const moe_expert_bank *b, int expect_n, bool allow_empty)
 {
@@ -222,6 +213,7 @@ moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expe
     GateUpArgs ga{};
     ga.x = static_cast<const __nv_bfloat16 *>(x);
     ga.T = T;
+    ga.KS = gate_up_ks(T);
     ga.routed_w13 = static_cast<const uint8_t *>(routed->w13);
     ga.routed_ts13 = routed->tscale13;
     ga.shared_w13 = n_shared ? static_cast<const uint8_t *>(shared->w13) : nullptr;
@@ -234,17 +226,19 @@ moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expe
 
     DownArgs da{};
     da.T = T;
+    da.BG = down_bg(T);
     da.routed_w2 = static_cast<const uint8_t *>(routed->w2);
     da.routed_ts2 = routed->tscale2;
     da.shared_w2 = n_shared ? static_cast<const uint8_t *>(shared->w2) : nullptr;
     da.shared_ts2 = n_shared ? shared->tscale2 : nullptr;
     da.n_shared = n_shared;
-    down_tiling(T, da.BG, da.SG);
     da.ws = ws;
-    da.out = static_cast<__nv_bfloat16 *>(out);
-    const int qmax = (max_slots(T, n_shared) + da.SG - 1) / da.SG;
-    e = launch_down(da, qmax, st, true);
-    return cuda_status(e);
+    e = launch_down(da, nsm, st, true);
+    if (e != cudaSuccess)
+        return MOE_ERR_CUDA;
+
+    CombineArgs ca{T, ws, static_cast<__nv_bfloat16 *>(out)};
+    return cuda_status(launch_combine(ca, st, true));
 }
 
 }  // extern "C"

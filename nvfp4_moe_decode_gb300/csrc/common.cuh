@@ -5,30 +5,36 @@
 // repacked at load time as the Flint page, "A 40B MoE that activates 2.5B
 // parameters", describes for its checkpoint):
 //
-//   A matrix W[N][K] is cut into N/16 bands of 16 rows.  Band b is 9*K bytes:
-//   first 8*K bytes of e2m1 codes, then K bytes of e4m3 scales.
-//   Codes: K/64 chunks of 512 bytes.  In chunk j, lane l = 4*g + c (g = l/4,
-//   c = l%4) owns 16 bytes = four 32-bit words, word s for the k16 step s of
-//   the chunk (k0 = 64*j + 16*s).  Nibble p of a word (bits 4p..4p+3) holds
-//   the element of register r = p & 3, half hi = p >> 2 of the mma.m16n8k16
-//   A fragment:  band row  g + 8*(r & 1),  column  k0 + 2*c + 8*(r >> 1) + hi.
-//   Scales: K/128 super-chunks of 128 bytes; in super-chunk q, the 16 bytes
-//   at 16*g hold, at byte 2*sb + h, the scale of band row g + 8*h for the
-//   16-element block 8*q + sb.
+//   A matrix W[N][K] is cut into N/16 bands of 16 rows.  Band b is 9*K bytes
+//   made of K/128 super-chunks of 1152 bytes; super-chunk q covers columns
+//   [128q, 128q+128): 1024 bytes of e2m1 codes followed by 128 bytes of e4m3
+//   scales, so any run of whole super-chunks is one contiguous copy.
+//   Codes: the two 512-byte chunks j = 2q, 2q+1 (64 columns each).  In a
+//   chunk, lane l = 4*g + c (g = l/4, c = l%4) owns 16 bytes = four 32-bit
+//   words, word s for the k16 step s of the chunk (k0 = 64*j + 16*s).  Byte r
+//   of a word is register r of the mma.m16n8k16 A fragment: band row
+//   g + 8*(r & 1), columns k0 + 2*c + 8*(r >> 1) + {0 (low nibble),
+//   1 (high nibble)}.
+//   Scales: the 16 bytes at 1024 + 16*g hold, at byte 2*sb + h, the scale of
+//   band row g + 8*h for the 16-column block 8*q + sb.
 //   Band rows: PLAIN band b row i = matrix row 16*b + i.  GATE_UP (a W13
 //   matrix, N = 2*I): row i < 8 is gate row 8*b + i, row i >= 8 is up row
 //   N/2 + 8*b + (i - 8), so that one mma accumulator tile holds matching gate
 //   and up rows for the SiLU*up epilogue.
 //
-// In-register decode: with nibble code (s, mag) the bf16 bit pattern
-// (s << 15) | (mag << 6) is exactly e2m1(code) * 2^-126 (mag = 1 lands on
-// the bf16 subnormal 2^-127 = 0.5 * 2^-126).  The activations are scaled by
-// 2^96 (exact for |x| < 2^32) so the tensor-core products stay in the normal
-// fp32 range; the product e2m1 * x * 2^-30 is rescaled by 2^30 together with
-// the e4m3 block scale and the tensor scale.
+// In-register decode: cvt.rn.f16x2.e2m1x2 turns one code byte into the two
+// exact e2m1 values of an A register.  The activations (bf16) enter the
+// tensor cores as fp16 after an exact per-token power-of-two rescale that puts
+// the token's largest magnitude in [2^14, 2^15): bf16's 8-bit significand
+// fits fp16's 11 bits, so every element within 2^31 of the largest is exact
+// and only smaller ones (whose products lie below the fp32 rounding of the
+// sum) are rounded.  Products are exact and accumulate in fp32; the e4m3
+// block scale is applied to each k16 step's fp32 partial, the tensor scale
+// and the power of two at the end.
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -52,8 +58,8 @@ constexpr size_t W2_BAND_BYTES = band_bytes(I);             // 4608
 constexpr size_t W13_BYTES = W13_BANDS * W13_BAND_BYTES;    // 1179648
 constexpr size_t W2_BYTES = W2_BANDS * W2_BAND_BYTES;       // 589824
 
-constexpr float X_SCALE = 79228162514264337593543950336.0f;   // 2^96
-constexpr float OUT_RESCALE = 1073741824.0f;                  // 2^30 = 2^126 / 2^96
+constexpr int SC_BYTES = 1152;            // one 128-column super-chunk of a band
+constexpr int ACT_EXP = 14;               // activations scaled so max|v| is in [2^14, 2^15)
 
 // Device flag bits (mirrors of the public MOE_FLAG_*).
 constexpr uint32_t FLAG_NONFINITE = MOE_FLAG_NONFINITE_LOGIT;
@@ -68,14 +74,17 @@ constexpr uint32_t SPIN_LIMIT = 1u << 20;
 // Workspace layout (bytes from the workspace base; 256-byte aligned regions).
 // ---------------------------------------------------------------------------
 struct WsLayout {
-    size_t ctrl;       // u32[64]: [0] flag, [1] router arrival counter
-    size_t counters;   // u32[W2_BANDS] down-combine arrival counters
+    size_t ctrl;       // u32[64]: [0] flag, [1] router arrivals, [2] down work counter,
+                       //          [3] down CTAs finished
+    size_t slot_cnt;   // u32[MAX_SLOTS] gate/up bands finished per slot
     size_t logits;     // f32[MAXT][E]
     size_t topk_idx;   // i32[MAXT][TOPK]
     size_t topk_w;     // f32[MAXT][TOPK]
     size_t slots;      // SlotTable
-    size_t h;          // bf16[MAX_SLOTS][MAXT][I]
-    size_t partials;   // f32[MAX_SLOTS][H][MAXT]
+    size_t h;          // bf16[MAX_SLOTS][MAXT][I]   SiLU*up activations
+    size_t hfrag;      // u32x2[MAX_SLOTS][I/16][32] the same as f16 mma B fragments
+    size_t hexp;       // i32[MAX_SLOTS][MAXT]       their power-of-two exponents
+    size_t partials;   // f32[MAX_SLOTS][H][MAXT]    per-slot down outputs (weighted)
     size_t total;
 };
 
@@ -93,12 +102,14 @@ __host__ __device__ inline WsLayout ws_layout()
     WsLayout L;
     size_t o = 0;
     L.ctrl = o;      o = align256(o + 64 * 4);
-    L.counters = o;  o = align256(o + W2_BANDS * 4);
+    L.slot_cnt = o;  o = align256(o + MAX_SLOTS * 4);
     L.logits = o;    o = align256(o + (size_t)MAXT * E * 4);
     L.topk_idx = o;  o = align256(o + (size_t)MAXT * TOPK * 4);
     L.topk_w = o;    o = align256(o + (size_t)MAXT * TOPK * 4);
     L.slots = o;     o = align256(o + sizeof(SlotTable));
     L.h = o;         o = align256(o + (size_t)MAX_SLOTS * MAXT * I * 2);
+    L.hfrag = o;     o = align256(o + (size_t)MAX_SLOTS * (I / 16) * 32 * 8);
+    L.hexp = o;      o = align256(o + (size_t)MAX_SLOTS * MAXT * 4);
     L.partials = o;  o = align256(o + (size_t)MAX_SLOTS * H * MAXT * 4);
     L.total = o;
     return L;
@@ -135,37 +146,37 @@ __host__ __device__ inline void code_position(int i, int k, int &byte_off, int &
     int hi = kk & 1, c = (kk & 7) >> 1, rhi = kk >> 3;
     int g = i & 7, rlo = i >> 3;
     int r = rlo + 2 * rhi;
-    int p = r + 4 * hi;
     int lane = 4 * g + c;
-    byte_off = j * 512 + lane * 16 + s * 4 + p / 2;
-    nib = p & 1;
+    byte_off = (j >> 1) * SC_BYTES + (j & 1) * 512 + lane * 16 + s * 4 + r;
+    nib = hi;
 }
 
-// Inverse of code_position for one nibble: (byte offset within the code
-// region, nibble) -> (band row, column).
+// Inverse of code_position: (byte offset of a code byte within the band,
+// nibble) -> (band row, column).  The byte must be a code byte.
 __host__ __device__ inline void code_element(int byte_off, int nib, int &i, int &k)
 {
-    int j = byte_off / 512, rem = byte_off % 512;
+    int q = byte_off / SC_BYTES, rem0 = byte_off % SC_BYTES;
+    int j = 2 * q + rem0 / 512, rem = rem0 % 512;
     int lane = rem / 16, w = rem % 16;
-    int s = w / 4, p = (w % 4) * 2 + nib;
+    int s = w / 4, r = w % 4;
     int g = lane >> 2, c = lane & 3;
-    int r = p & 3, hi = p >> 2;
     i = g + 8 * (r & 1);
-    k = 64 * j + 16 * s + 2 * c + 8 * (r >> 1) + hi;
+    k = 64 * j + 16 * s + 2 * c + 8 * (r >> 1) + nib;
 }
 
-// Packed scale byte of (band row i, block bk) within the band (K = row length).
-__host__ __device__ inline int scale_position(int K, int i, int bk)
+__host__ __device__ inline bool is_scale_byte(int byte_off) { return byte_off % SC_BYTES >= 1024; }
+
+// Packed scale byte of (band row i, block bk) within the band.
+__host__ __device__ inline int scale_position(int i, int bk)
 {
     int q = bk / 8, sb = bk % 8;
     int g = i & 7, h = i >> 3;
-    return 8 * K + q * 128 + g * 16 + 2 * sb + h;
+    return q * SC_BYTES + 1024 + g * 16 + 2 * sb + h;
 }
 
-__host__ __device__ inline void scale_element(int K, int off, int &i, int &bk)
+__host__ __device__ inline void scale_element(int off, int &i, int &bk)
 {
-    int o = off - 8 * K;
-    int q = o / 128, rem = o % 128;
+    int q = off / SC_BYTES, rem = off % SC_BYTES - 1024;
     int g = rem / 16, w = rem % 16;
     int sb = w / 2, h = w % 2;
     i = g + 8 * h;
@@ -175,19 +186,15 @@ __host__ __device__ inline void scale_element(int K, int off, int &i, int &bk)
 #ifdef __CUDACC__
 
 // ---------------------------------------------------------------------------
-// Decode: one packed code word -> the four bf16x2 A-fragment registers.
+// Decode: byte r of a packed code word -> the f16x2 A-fragment register r.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t decode_reg(uint32_t w, int r)
 {
-    // register r takes nibble r (low half) and nibble r + 4 (high half):
-    // magnitude bits -> 6..8 / 22..24, sign bit -> 15 / 31.
-    const uint32_t MAG = 0x01C001C0u, SGN = 0x80008000u;
-    switch (r) {
-    case 0: return ((w << 6) & MAG) | ((w << 12) & SGN);
-    case 1: return ((w << 2) & MAG) | ((w << 8) & SGN);
-    case 2: return ((w >> 2) & MAG) | ((w << 4) & SGN);
-    default: return ((w >> 6) & MAG) | (w & SGN);
-    }
+    uint32_t h2;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
+        : "=r"(h2) : "r"(w >> (8 * r)));
+    return h2;
 }
 
 // Two e4m3 scale bytes (low byte -> .x) to fp32 (exact).
@@ -201,13 +208,13 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_bytes)
 }
 
 // ---------------------------------------------------------------------------
-// Tensor core: D = A(16x16 bf16, row) * B(16x8 bf16, col), fp32, C = 0.
+// Tensor core: D = A(16x16 f16, row) * B(16x8 f16, col), fp32, C = 0.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void mma_bf16_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1)
+__device__ __forceinline__ void mma_f16_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1)
 {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%10,%10,%10,%10};\n"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
@@ -291,13 +298,27 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void *p)
     return v;
 }
 
-// bf16 pair (low = first) scaled by 2^96 (exact for |v| < 2^32).
-__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v)
+// Exponent e such that 2^e <= v < 2^(e+1) for a finite v > 0 (0 for v = 0).
+__device__ __forceinline__ int exponent_of(float v)
 {
-    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&v);
-    __nv_bfloat162 s = __float2bfloat162_rn(X_SCALE);
-    __nv_bfloat162 r = __hmul2(b, s);
-    return *reinterpret_cast<uint32_t *>(&r);
+    if (!(v > 0.0f) || !isfinite(v))
+        return 0;
+    return ((int)((__float_as_uint(v) >> 23) & 0xFF)) - 127;
+}
+
+// Two bf16 values (low first) times 2^sh, as an f16x2 (exact in the range
+// described at the top of this file).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t v, float pow2)
+{
+    const float lo = __uint_as_float(v << 16) * pow2;
+    const float hi = __uint_as_float(v & 0xFFFF0000u) * pow2;
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16)

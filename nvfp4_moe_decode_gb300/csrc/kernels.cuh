@@ -1,25 +1,23 @@
-// kernels.cuh -- argument blocks and host launchers of the kernels behind
-// libnvfp4moe.so (internal; not part of the public C ABI).
+// kernels.cuh -- argument blocks, tiling constants and host launchers of the
+// kernels behind libnvfp4moe.so (internal; not part of the public C ABI).
 #pragma once
 
 #include "common.cuh"
 
 namespace moe {
 
-constexpr int CONSUMER_WARPS = 8;
-constexpr int EXPERT_THREADS = (CONSUMER_WARPS + 1) * 32;   // 288
-constexpr int CONSUMER_THREADS = CONSUMER_WARPS * 32;       // 256
+// K2 gate/up: one CTA per SM, 8 warps, each with a private ring of stages.
+constexpr int GU_WARPS = 8;
+constexpr int GU_RING = 4;                                   // stages per warp
+constexpr int GU_SC_PER_STAGE = 2;                           // super-chunks per stage
+constexpr int GU_STAGE_BYTES = GU_SC_PER_STAGE * SC_BYTES;   // 2304
+constexpr int GU_STEPS = H / 16;                             // 128 k16 steps
 
-constexpr int GU_STAGES = 4;
-constexpr int GU_STEPS = H / 16;                                  // 128 k16 steps
-constexpr int GU_CHUNKS_PER_WARP = (H / 64) / CONSUMER_WARPS;     // 4
-constexpr size_t GU_SMEM_STAGES = GU_STAGES * W13_BAND_BYTES;     // 73728
-constexpr size_t GU_SMEM_XFRAG = (size_t)GU_STEPS * 32 * 8;       // 32768
-constexpr size_t GU_SMEM_RED = CONSUMER_WARPS * 32 * 4 * 4;       // 4096
-constexpr size_t GU_SMEM_BARS = 2 * GU_STAGES * 8;
-constexpr size_t GU_SMEM = GU_SMEM_STAGES + GU_SMEM_XFRAG + GU_SMEM_RED + GU_SMEM_BARS;
-constexpr int DN_STEPS = I / 16;                 // 32 k16 steps
-constexpr int DN_MAX_SG = 4;
+// K3 down: one CTA per SM, 8 warps in groups of BG warps (one band each).
+constexpr int DN_WARPS = 8;
+constexpr int DN_RING = 2;                                   // W2 bands per warp in flight
+constexpr int DN_STEPS = I / 16;                             // 32 k16 steps
+constexpr int DN_HBUF_ENTRIES = 4096;                        // 32 KB of h fragments per CTA
 
 struct RouterArgs {
     const __nv_bfloat16 *x;        // [T][H]
@@ -33,8 +31,9 @@ struct RouterArgs {
 };
 
 struct GateUpArgs {
-    const __nv_bfloat16 *x;   // [T][H]
+    const __nv_bfloat16 *x;        // [T][H]
     int T;
+    int KS;                        // warps that split one band's K (1, 2 or 4)
     const uint8_t *routed_w13;
     const float *routed_ts13;
     const uint8_t *shared_w13;
@@ -45,22 +44,20 @@ struct GateUpArgs {
 
 struct DownArgs {
     int T;
+    int BG;                        // bands (warps) per unit: 2, 4 or 8
     const uint8_t *routed_w2;
     const float *routed_ts2;
     const uint8_t *shared_w2;
     const float *shared_ts2;
     int n_shared;
-    int BG;   // bands per CTA (1, 2, 4 or 8)
-    int SG;   // slots per CTA (1..DN_MAX_SG)
     uint8_t *ws;
-    __nv_bfloat16 *out;   // [T][H]
 };
 
-__host__ __device__ inline size_t down_smem_bytes(int BG, int SG)
-{
-    return (size_t)SG * BG * W2_BAND_BYTES + (size_t)SG * DN_STEPS * 32 * 8 +
-           (size_t)CONSUMER_WARPS * 32 * 4 * 4 + (size_t)DN_MAX_SG * 8;
-}
+struct CombineArgs {
+    int T;
+    uint8_t *ws;
+    __nv_bfloat16 *out;            // [T][H]
+};
 
 struct PackArgs {
     const uint8_t *codes;    // [count][N][K/2]
@@ -83,9 +80,13 @@ struct DequantArgs {
     float tscale;
 };
 
+size_t gate_up_smem_bytes();
+size_t down_smem_bytes();
+
 cudaError_t launch_router(const RouterArgs &a, cudaStream_t stream, bool pdl);
 cudaError_t launch_gate_up(const GateUpArgs &a, int grid, cudaStream_t stream, bool pdl);
-cudaError_t launch_down(const DownArgs &a, int qmax, cudaStream_t stream, bool pdl);
+cudaError_t launch_down(const DownArgs &a, int grid, cudaStream_t stream, bool pdl);
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream, bool pdl);
 cudaError_t launch_pack(const PackArgs &a, cudaStream_t s);
 cudaError_t launch_unpack(const UnpackArgs &a, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs &a, cudaStream_t s);

@@ -25,7 +25,7 @@ __global__ void pack_kernel(PackArgs a)
         const uint8_t *codes = a.codes + m * (size_t)a.N * (a.K / 2);
         const uint8_t *scales = a.scales + m * (size_t)a.N * (a.K / 16);
         uint8_t v;
-        if (off < 8 * a.K) {
+        if (!is_scale_byte(off)) {
             v = 0;
             for (int nib = 0; nib < 2; ++nib) {
                 int i, k;
@@ -37,7 +37,7 @@ __global__ void pack_kernel(PackArgs a)
             }
         } else {
             int i, bk;
-            scale_element(a.K, off, i, bk);
+            scale_element(off, i, bk);
             const int n = band_row_to_matrix_row(a.kind, a.N, b, i);
             v = scales[(size_t)n * (a.K / 16) + bk];
         }
@@ -75,14 +75,14 @@ __global__ void unpack_kernel(UnpackArgs a)
             const int n = (int)(r / (a.K / 16)), bk = (int)(r % (a.K / 16));
             int b, i;
             matrix_row_to_band(a.kind, a.N, n, b, i);
-            a.scales[o2] = a.packed[m * per_mat + (size_t)b * bb + scale_position(a.K, i, bk)];
+            a.scales[o2] = a.packed[m * per_mat + (size_t)b * bb + scale_position(i, bk)];
         }
     }
 }
 
 
-// out[n][k] = e2m1 * e4m3 * tscale, decoding the code word exactly as the
-// GEMV kernels do (bf16 bit placement = e2m1 * 2^-126).
+// out[n][k] = e2m1 * e4m3 * tscale, decoding the code byte exactly as the
+// GEMV kernels do (cvt.rn.f16x2.e2m1x2 on the byte that holds the element).
 __global__ void dequant_kernel(DequantArgs a)
 {
     const size_t total = (size_t)a.N * a.K;
@@ -95,12 +95,10 @@ __global__ void dequant_kernel(DequantArgs a)
         code_position(i, k, off, nib);
         const uint8_t *band = a.packed + (size_t)b * bb;
         const uint32_t word = *reinterpret_cast<const uint32_t *>(band + (off & ~3));
-        const int p = (off & 3) * 2 + nib;
-        const uint32_t reg = decode_reg(word, p & 3);
-        const uint32_t bits = (p >> 2) ? (reg >> 16) : (reg & 0xFFFFu);
-        const float code_val = bf16_bits_to_float(bits) * __int_as_float(0x7E800000);  // x 2^126
-        const int soff = scale_position(a.K, i, k / 16);
-        const uint32_t sb = band[soff];
+        const uint32_t reg = decode_reg(word, off & 3);
+        const __half2 hh = *reinterpret_cast<const __half2 *>(&reg);
+        const float code_val = nib ? __high2float(hh) : __low2float(hh);
+        const uint32_t sb = band[scale_position(i, k / 16)];
         const float sc = e4m3x2_to_float2(sb).x;
         a.out[o] = code_val * sc * a.tscale;
     }

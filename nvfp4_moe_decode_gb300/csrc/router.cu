@@ -113,24 +113,44 @@ __global__ void __launch_bounds__(256) router_topk_kernel(RouterArgs a)
     __shared__ float part[8][MAXT];
     __shared__ int is_last;
 
-    for (int t = 0; t < a.T; ++t) {
-        float acc = 0.0f;
+    // all tokens at once: the x loads are independent, so they are issued
+    // together; each token keeps its own sequential chain of 16 products
+    uint4 xv[MAXT][2];
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            uint4 xv = ldg_nc_v4(a.x + (size_t)t * H + 512 * kq + 256 * m + 8 * lane);
-            const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-            const uint32_t ws[4] = {wv[m].x, wv[m].y, wv[m].z, wv[m].w};
+    for (int t = 0; t < MAXT; ++t)
+        if (t < a.T) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                acc = fmaf(bf16_bits_to_float(xs[q] & 0xFFFFu), bf16_bits_to_float(ws[q] & 0xFFFFu), acc);
-                acc = fmaf(bf16_bits_to_float(xs[q] >> 16), bf16_bits_to_float(ws[q] >> 16), acc);
+            for (int m = 0; m < 2; ++m)
+                xv[t][m] = ldg_nc_v4(a.x + (size_t)t * H + 512 * kq + 256 * m + 8 * lane);
+        }
+    float acc[MAXT];
+#pragma unroll
+    for (int t = 0; t < MAXT; ++t) {
+        acc[t] = 0.0f;
+        if (t < a.T) {
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const uint32_t xs[4] = {xv[t][m].x, xv[t][m].y, xv[t][m].z, xv[t][m].w};
+                const uint32_t ws[4] = {wv[m].x, wv[m].y, wv[m].z, wv[m].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[t] = fmaf(bf16_bits_to_float(xs[q] & 0xFFFFu), bf16_bits_to_float(ws[q] & 0xFFFFu), acc[t]);
+                    acc[t] = fmaf(bf16_bits_to_float(xs[q] >> 16), bf16_bits_to_float(ws[q] >> 16), acc[t]);
+                }
             }
         }
+    }
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-            acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-        if (lane == 0)
-            part[warp][t] = acc;
+    for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+        for (int t = 0; t < MAXT; ++t)
+            if (t < a.T)
+                acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], off);
+    if (lane == 0) {
+#pragma unroll
+        for (int t = 0; t < MAXT; ++t)
+            if (t < a.T)
+                part[warp][t] = acc[t];
     }
     __syncthreads();
     if ((warp & 3) == 0 && lane < a.T) {
