@@ -355,10 +355,10 @@ def main():
         "roofline": {"bound": "hbm", "achieved": layer_alg / (us_per_layer * 1e-6) / 1e9, "peak": peak,
                      "unit": "GB/s", "frac": layer_alg / (us_per_layer * 1e-6) / 1e9 / peak,
                      "traffic": None, "peak_source": peak_src,
-                     "kernel": "moe_layer_forward (router + gate/up + down, PDL-chained)"},
+                     "kernel": "moe_layer_kernel (router, top-6, gate/up, down, combine fused; one launch per layer)"},
         "e2e": {"value": e2e_v, "unit": "GB/s", "steps": ne, "h2d_bytes_per_step": T * 2048 * 2,
                 "d2h_bytes_per_step": T * 2048 * 2},
-        "gpu_launches": 4 * K,
+        "gpu_launches": K,
         "clocks": clk,
     }
 

@@ -30,10 +30,6 @@ int sm_count()
     return n;
 }
 
-// K split of the gate/up kernel and band-group size of the down kernel.
-int gate_up_ks(int T) { return T <= 4 ? 2 : 1; }
-int down_bg(int T) { return T <= 2 ? 2 : (T <= 6 ? 4 : 8); }
-
 moe_status check_bank(const moe_expert_bank *b, int expect_n, bool allow_empty)
 {
     if (b == nullptr)
@@ -204,41 +200,25 @@ moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expe
     cudaStream_t st = (cudaStream_t)stream;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
 
-    RouterArgs ra{static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(router_w),
-                  T, n_shared, ws, nullptr, nullptr, nullptr};
-    cudaError_t e = launch_router(ra, st, true);
-    if (e != cudaSuccess)
-        return MOE_ERR_CUDA;
-
-    GateUpArgs ga{};
-    ga.x = static_cast<const __nv_bfloat16 *>(x);
-    ga.T = T;
-    ga.KS = gate_up_ks(T);
-    ga.routed_w13 = static_cast<const uint8_t *>(routed->w13);
-    ga.routed_ts13 = routed->tscale13;
-    ga.shared_w13 = n_shared ? static_cast<const uint8_t *>(shared->w13) : nullptr;
-    ga.shared_ts13 = n_shared ? shared->tscale13 : nullptr;
-    ga.n_shared = n_shared;
-    ga.ws = ws;
-    e = launch_gate_up(ga, nsm, st, true);
-    if (e != cudaSuccess)
-        return MOE_ERR_CUDA;
-
-    DownArgs da{};
-    da.T = T;
-    da.BG = down_bg(T);
-    da.routed_w2 = static_cast<const uint8_t *>(routed->w2);
-    da.routed_ts2 = routed->tscale2;
-    da.shared_w2 = n_shared ? static_cast<const uint8_t *>(shared->w2) : nullptr;
-    da.shared_ts2 = n_shared ? shared->tscale2 : nullptr;
-    da.n_shared = n_shared;
-    da.ws = ws;
-    e = launch_down(da, nsm, st, true);
-    if (e != cudaSuccess)
-        return MOE_ERR_CUDA;
-
-    CombineArgs ca{T, ws, static_cast<__nv_bfloat16 *>(out)};
-    return cuda_status(launch_combine(ca, st, true));
+    LayerArgs la{};
+    la.x = static_cast<const __nv_bfloat16 *>(x);
+    la.wr = static_cast<const __nv_bfloat16 *>(router_w);
+    la.T = T;
+    la.r_w13 = static_cast<const uint8_t *>(routed->w13);
+    la.r_w2 = static_cast<const uint8_t *>(routed->w2);
+    la.r_ts13 = routed->tscale13;
+    la.r_ts2 = routed->tscale2;
+    if (n_shared) {
+        la.s_w13 = static_cast<const uint8_t *>(shared->w13);
+        la.s_w2 = static_cast<const uint8_t *>(shared->w2);
+        la.s_ts13 = shared->tscale13;
+        la.s_ts2 = shared->tscale2;
+    }
+    la.n_shared = n_shared;
+    la.ws = ws;
+    la.out = static_cast<__nv_bfloat16 *>(out);
+    // one CTA per SM; at least 128 for the router phase
+    return cuda_status(launch_layer(la, nsm >= 128 ? nsm : 128, st, true));
 }
 
 }  // extern "C"

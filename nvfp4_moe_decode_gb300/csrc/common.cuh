@@ -74,16 +74,16 @@ constexpr uint32_t SPIN_LIMIT = 1u << 20;
 // Workspace layout (bytes from the workspace base; 256-byte aligned regions).
 // ---------------------------------------------------------------------------
 struct WsLayout {
-    size_t ctrl;       // u32[64]: [0] flag, [1] router arrivals, [2] down work counter,
-                       //          [3] down CTAs finished
+    size_t ctrl;       // u32[64]: [0] device flag, [1] routing-kernel arrivals,
+                       //   [2] layer-kernel router arrivals, [3] unit queue, [4] CTAs done
     size_t slot_cnt;   // u32[MAX_SLOTS] gate/up bands finished per slot
+    size_t hmax;       // u32[MAX_SLOTS][MAXT] running max |h| (float bits) per slot, token
+    size_t band_cnt;   // u32[W2_BANDS] down partials arrived per 16-row band
     size_t logits;     // f32[MAXT][E]
     size_t topk_idx;   // i32[MAXT][TOPK]
     size_t topk_w;     // f32[MAXT][TOPK]
     size_t slots;      // SlotTable
     size_t h;          // bf16[MAX_SLOTS][MAXT][I]   SiLU*up activations
-    size_t hfrag;      // u32x2[MAX_SLOTS][I/16][32] the same as f16 mma B fragments
-    size_t hexp;       // i32[MAX_SLOTS][MAXT]       their power-of-two exponents
     size_t partials;   // f32[MAX_SLOTS][H][MAXT]    per-slot down outputs (weighted)
     size_t total;
 };
@@ -103,13 +103,13 @@ __host__ __device__ inline WsLayout ws_layout()
     size_t o = 0;
     L.ctrl = o;      o = align256(o + 64 * 4);
     L.slot_cnt = o;  o = align256(o + MAX_SLOTS * 4);
+    L.hmax = o;      o = align256(o + (size_t)MAX_SLOTS * MAXT * 4);
+    L.band_cnt = o;  o = align256(o + W2_BANDS * 4);
     L.logits = o;    o = align256(o + (size_t)MAXT * E * 4);
     L.topk_idx = o;  o = align256(o + (size_t)MAXT * TOPK * 4);
     L.topk_w = o;    o = align256(o + (size_t)MAXT * TOPK * 4);
     L.slots = o;     o = align256(o + sizeof(SlotTable));
     L.h = o;         o = align256(o + (size_t)MAX_SLOTS * MAXT * I * 2);
-    L.hfrag = o;     o = align256(o + (size_t)MAX_SLOTS * (I / 16) * 32 * 8);
-    L.hexp = o;      o = align256(o + (size_t)MAX_SLOTS * MAXT * 4);
     L.partials = o;  o = align256(o + (size_t)MAX_SLOTS * H * MAXT * 4);
     L.total = o;
     return L;

@@ -6,19 +6,6 @@
 
 namespace moe {
 
-// K2 gate/up: one CTA per SM, 8 warps, each with a private ring of stages.
-constexpr int GU_WARPS = 8;
-constexpr int GU_RING = 4;                                   // stages per warp
-constexpr int GU_SC_PER_STAGE = 2;                           // super-chunks per stage
-constexpr int GU_STAGE_BYTES = GU_SC_PER_STAGE * SC_BYTES;   // 2304
-constexpr int GU_STEPS = H / 16;                             // 128 k16 steps
-
-// K3 down: one CTA per SM, 8 warps in groups of BG warps (one band each).
-constexpr int DN_WARPS = 8;
-constexpr int DN_RING = 2;                                   // W2 bands per warp in flight
-constexpr int DN_STEPS = I / 16;                             // 32 k16 steps
-constexpr int DN_HBUF_ENTRIES = 4096;                        // 32 KB of h fragments per CTA
-
 struct RouterArgs {
     const __nv_bfloat16 *x;        // [T][H]
     const __nv_bfloat16 *wr;       // [E][H]
@@ -30,31 +17,15 @@ struct RouterArgs {
     float *user_logits;            // optional [T][E]
 };
 
-struct GateUpArgs {
+struct LayerArgs {
     const __nv_bfloat16 *x;        // [T][H]
+    const __nv_bfloat16 *wr;       // [E][H]
     int T;
-    int KS;                        // warps that split one band's K (1, 2 or 4)
-    const uint8_t *routed_w13;
-    const float *routed_ts13;
-    const uint8_t *shared_w13;
-    const float *shared_ts13;
+    const uint8_t *r_w13, *r_w2;   // routed bank (packed NVFP4)
+    const float *r_ts13, *r_ts2;
+    const uint8_t *s_w13, *s_w2;   // shared expert (packed NVFP4), if n_shared
+    const float *s_ts13, *s_ts2;
     int n_shared;
-    uint8_t *ws;
-};
-
-struct DownArgs {
-    int T;
-    int BG;                        // bands (warps) per unit: 2, 4 or 8
-    const uint8_t *routed_w2;
-    const float *routed_ts2;
-    const uint8_t *shared_w2;
-    const float *shared_ts2;
-    int n_shared;
-    uint8_t *ws;
-};
-
-struct CombineArgs {
-    int T;
     uint8_t *ws;
     __nv_bfloat16 *out;            // [T][H]
 };
@@ -80,13 +51,10 @@ struct DequantArgs {
     float tscale;
 };
 
-size_t gate_up_smem_bytes();
-size_t down_smem_bytes();
+size_t layer_smem_bytes();
 
 cudaError_t launch_router(const RouterArgs &a, cudaStream_t stream, bool pdl);
-cudaError_t launch_gate_up(const GateUpArgs &a, int grid, cudaStream_t stream, bool pdl);
-cudaError_t launch_down(const DownArgs &a, int grid, cudaStream_t stream, bool pdl);
-cudaError_t launch_combine(const CombineArgs &a, cudaStream_t stream, bool pdl);
+cudaError_t launch_layer(const LayerArgs &a, int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_pack(const PackArgs &a, cudaStream_t s);
 cudaError_t launch_unpack(const UnpackArgs &a, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs &a, cudaStream_t s);
