@@ -12,26 +12,33 @@
 //  1. before waiting on the preceding kernel: router CTAs load their slice of
 //     the router weights; group 0 of the first 64 CTAs starts the bulk copies
 //     of one band of the shared expert (it needs no routing);
-//  2. router: CTAs 0..127 (warps 8..15) compute the fp32 logits of two experts
-//     each and publish them; warps 0..7 turn x into f16 mma fragments;
-//  3. every CTA waits for all logits, takes the top-6 of each token (one warp
+//  2. x arrives in shared memory by one bulk copy; CTAs 0..127 (warps 8..15)
+//     compute the fp32 logits of two experts each and publish them with a
+//     release-add; warps 0..7 turn x into f16 mma fragments;
+//  3. every CTA acquires the logits, takes the top-6 of each token (one warp
 //     per token, identical in every CTA) and builds the slot table: the shared
 //     expert, then the distinct selected experts in ascending order, each with
 //     its per-token routing weight;
-//  4. a work queue (one atomic counter) hands each group units:
-//       gate/up unit (slot, band):  the 4 warps take one K quarter each of a
-//         16-row band of W13 (8 gate + 8 up rows); SiLU*up -> h (bf16) with a
+//  4. units are dealt round-robin to the 4 x #CTA groups (group id
+//     grp * #CTA + cta; a group takes ids gid, gid + G, gid + 2G, ...):
+//       gate/up unit (slot, band): the 4 warps take one K quarter each of a
+//         16-row band of W13 (8 gate + 8 up rows); SiLU*up -> h (bf16) and a
 //         per-(slot, token) running max of |h|;
-//       down unit (slot, 4 bands):  waits until the slot's 64 gate/up bands are
-//         done, loads the slot's h, rescales it to f16 fragments, and each warp
-//         computes one 16-row band of W2 h, times the routing weight;
-//     gate/up units come first in the queue, so a down unit only ever waits
-//     on units that running warps already hold;
+//       down unit (slot, 4 bands): once the slot's 64 gate/up bands are done,
+//         the slot's h arrives by bulk copy and is rescaled in place to f16
+//         fragments; each warp computes one 16-row band of W2 h, times the
+//         routing weight;
+//     gate/up ids precede down ids and every group walks its ids in
+//     increasing order, so a down unit only waits on gate/up units that other
+//     groups reach without waiting themselves.  Completion (a release-add
+//     after a warp barrier) is posted one unit late, when the stores it covers
+//     have landed, by a lane that issues no bulk copies, and always before the
+//     warp waits on anything;
 //  5. the last down partial of each band adds all partials in slot order
 //     (deterministic) and writes out (bf16).
 // Every warp streams its units' weights through a private 3-stage ring of
-// shared-memory buffers filled by cp.async.bulk; waits are bounded and report
-// MOE_FLAG_WAIT_TIMEOUT instead of hanging.
+// shared-memory buffers filled by cp.async.bulk; every wait is bounded and
+// reports MOE_FLAG_WAIT_TIMEOUT instead of hanging.
 #include "kernels.cuh"
 #include "topk.cuh"
 
@@ -46,28 +53,31 @@ constexpr int GW = 4;                  // warps per group
 constexpr int RING = 3;                // stages per warp
 constexpr int STG = 2 * SC_BYTES;      // 2304 bytes: two super-chunks
 constexpr int ROUTER_CTAS = E / 2;     // 128 CTAs x 2 experts
-constexpr int UNITS_AHEAD = 3;         // unit-id ring per group
-constexpr int H_BYTES = MAXT * I * 2;  // one slot's h (bf16), 8 KB at T = 8
+constexpr int HROW = I * 2 + 16;       // padded bytes of one token's h row in shared memory
+constexpr int HBUF = MAXT * HROW;      // one slot's h, 8.1 KB at T = 8
+constexpr uint32_t SLOT_DONE = W13_BANDS; // gate/up bands that complete a slot
+constexpr int GU_UNITS = W13_BANDS / GW;  // 16 gate/up units of 4 bands per slot
+constexpr int DN_UNITS = W2_BANDS / GW;   // 32 down units of 4 bands per slot
+constexpr int GU_PARTS = (H / 128) / 2;   // 8 stages per W13 band
+constexpr int DN_PARTS = (I / 128) / 2;   // 2 stages per W2 band
 
 struct FSmem {
     uint8_t ring[FW][RING][STG];
     uint2 xfrag[(H / 16) * 32];        // compact: entry (step, l) at step * 4T + l
-    uint8_t hbuf[NG][2][H_BYTES];      // raw h, rescaled in place into fragments
-    float4 red[2][NG][GW - 1][32];     // gate/up K-part partials (double-buffered)
+    uint8_t hbuf[NG][2][HBUF];         // raw h rows, rescaled in place into fragments;
+                                       // before the unit loop: x (T x 4 KB)
     uint64_t full[FW][RING];
     uint64_t hbar[NG][2];
-    int unit[NG][UNITS_AHEAD];
-    int hissued[NG][2];
+    uint64_t xbar;
     float rpart[8][MAXT];
     int32_t sel[MAXT][TOPK];
     float selw[MAXT][TOPK];
     uint32_t bitmap[E / 32];
-    int32_t prefix[E / 32];
     int n_slots;
     int32_t slot_expert[MAX_SLOTS];
     float wts[MAX_SLOTS][MAXT];
     int xshift[MAXT];
-    int route_ok;
+    int hshift[NG][2][MAXT];           // power-of-two exponents of the h in hbuf[grp][b]
 };
 
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }
@@ -85,13 +95,35 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acquire.gpu;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Bounded spin until *p >= target.  Returns false (and flags) on timeout.
 __device__ __forceinline__ bool spin_until(const uint32_t *p, uint32_t target, uint32_t *flag)
 {
     for (uint32_t it = 0; it < SPIN_LIMIT; ++it) {
         if (ld_acquire(p) >= target)
             return true;
-        __nanosleep(64);
+        __nanosleep(128);
     }
     atomicOr(flag, FLAG_TIMEOUT);
     return false;
@@ -148,7 +180,7 @@ __device__ __forceinline__ void mma_stage(const uint8_t *stage, const uint2 *bfr
 struct Unit {
     bool down;   // down unit (else gate/up)
     int slot;
-    int idx;     // band (gate/up) or band group (down)
+    int band;    // this warp's 16-row band (W13 band for gate/up, W2 band for down)
 };
 
 }  // namespace
@@ -171,6 +203,7 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = warp / GW, wq = warp % GW;
     const bool leader = (wq == 0);
+    const bool lead_thread = leader && lane == 0;
     const int T = a.T;
     const int blanes = 4 * T;
 
@@ -181,12 +214,12 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             mbar_init(&sm.hbar[grp][0], 1);
             mbar_init(&sm.hbar[grp][1], 1);
         }
+        if (threadIdx.x == 0)
+            mbar_init(&sm.xbar, 1);
         fence_barrier_init();
     }
     __syncthreads();
 
-    // ---- unit decoding (valid once the slot table is known, or for the
-    // shared expert, whose slot 0 needs no routing) ----
     auto w13_src = [&](int slot, int band) -> const uint8_t * {
         const uint8_t *base = (slot < a.n_shared) ? a.s_w13 + (size_t)slot * W13_BYTES
                                                   : a.r_w13 + (size_t)sm.slot_expert[slot] * W13_BYTES;
@@ -197,26 +230,26 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
                                                   : a.r_w2 + (size_t)sm.slot_expert[slot] * W2_BYTES;
         return base + (size_t)band * W2_BAND_BYTES;
     };
-    // stage i of this warp's stream: unit i/2, part i%2
-    auto issue_stage = [&](int i, const Unit &u) {
+    // one stage = two super-chunks (2304 bytes) of this warp's band: part p
+    auto issue_stage = [&](int ring_slot, const Unit &u, int p) {
         if (lane != 0)
             return;
-        const uint8_t *src;
-        if (!u.down)
-            src = w13_src(u.slot, u.idx) + (size_t)(4 * wq + 2 * (i & 1)) * SC_BYTES;
-        else
-            src = w2_src(u.slot, 4 * u.idx + wq) + (size_t)(2 * (i & 1)) * SC_BYTES;
-        uint64_t *bar = &sm.full[warp][i % RING];
+        const uint8_t *src = (u.down ? w2_src(u.slot, u.band) : w13_src(u.slot, u.band)) + (size_t)(2 * p) * SC_BYTES;
+        uint64_t *bar = &sm.full[warp][ring_slot];
         mbar_arrive_expect_tx(bar, STG);
-        bulk_g2s(sm.ring[warp][i % RING], src, STG, bar);
+        bulk_g2s(sm.ring[warp][ring_slot], src, STG, bar);
     };
 
     // ---- phase 1: work that needs nothing from the preceding kernel ----
-    const bool static_shared = (a.n_shared > 0) && grp == 0 && blockIdx.x < W13_BANDS;
+    // units are dealt round-robin: group gid takes ids gid, gid + G, ...; the
+    // shared expert's 16 gate/up units (ids 0..15) go to group 0 of CTAs 0..15
+    const int n_groups = NG * (int)gridDim.x;
+    const int gid = grp * (int)gridDim.x + (int)blockIdx.x;
+    const bool static_shared = (a.n_shared > 0) && gid < GU_UNITS;
     if (static_shared) {
-        const Unit u0{false, 0, (int)blockIdx.x};
-        issue_stage(0, u0);
-        issue_stage(1, u0);
+        const Unit u0{false, 0, 4 * gid + wq};
+        for (int p = 0; p < RING; ++p)
+            issue_stage(p, u0, p);
     }
     const bool router_warp = blockIdx.x < ROUTER_CTAS && warp >= 8;
     const int r_e = blockIdx.x * 2 + ((warp - 8) >> 2);
@@ -228,19 +261,19 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             wv[m] = ldg_nc_v4(a.wr + (size_t)r_e * H + 512 * r_kq + 256 * m + 8 * lane);
     }
 
-    griddep_wait();      // x is written by the preceding kernel
+    griddep_wait();      // x is written by the preceding kernel; the counters are re-armed
     griddep_launch();    // the next kernel may start its own phase 1
 
-    // ---- phase 2: router logits (warps 8..15) | activation fragments (0..7) ----
+    // ---- phase 2: x -> shared memory; router logits | activation fragments ----
+    uint8_t *xs = &sm.hbuf[0][0][0];   // T x 4 KB, free until the unit loop
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&sm.xbar, (uint32_t)(T * H * 2));
+        bulk_g2s(xs, a.x, (uint32_t)(T * H * 2), &sm.xbar);
+    }
+    mbar_wait_bounded(&sm.xbar, 0, flag);
+    const __nv_bfloat16 *xsh = reinterpret_cast<const __nv_bfloat16 *>(xs);
+
     if (router_warp) {
-        uint4 xv[MAXT][2];
-#pragma unroll
-        for (int t = 0; t < MAXT; ++t)
-            if (t < T) {
-#pragma unroll
-                for (int m = 0; m < 2; ++m)
-                    xv[t][m] = ldg_nc_v4(a.x + (size_t)t * H + 512 * r_kq + 256 * m + 8 * lane);
-            }
         float acc[MAXT];
 #pragma unroll
         for (int t = 0; t < MAXT; ++t) {
@@ -248,12 +281,13 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             if (t < T) {
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
-                    const uint32_t xs[4] = {xv[t][m].x, xv[t][m].y, xv[t][m].z, xv[t][m].w};
-                    const uint32_t ws[4] = {wv[m].x, wv[m].y, wv[m].z, wv[m].w};
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(xsh + (size_t)t * H + 512 * r_kq + 256 * m + 8 * lane);
+                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                    const uint32_t ww[4] = {wv[m].x, wv[m].y, wv[m].z, wv[m].w};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        acc[t] = fmaf(bf16_bits_to_float(xs[q] & 0xFFFFu), bf16_bits_to_float(ws[q] & 0xFFFFu), acc[t]);
-                        acc[t] = fmaf(bf16_bits_to_float(xs[q] >> 16), bf16_bits_to_float(ws[q] >> 16), acc[t]);
+                        acc[t] = fmaf(bf16_bits_to_float(xw[q] & 0xFFFFu), bf16_bits_to_float(ww[q] & 0xFFFFu), acc[t]);
+                        acc[t] = fmaf(bf16_bits_to_float(xw[q] >> 16), bf16_bits_to_float(ww[q] >> 16), acc[t]);
                     }
                 }
             }
@@ -273,20 +307,18 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
         named_barrier_sync(5, 256);
         if ((warp == 8 || warp == 12) && lane < T) {
             const int t = lane, w0 = warp - 8;
-            const float v = ((sm.rpart[w0][t] + sm.rpart[w0 + 1][t]) + sm.rpart[w0 + 2][t]) + sm.rpart[w0 + 3][t];
-            logits[t * E + r_e] = v;
-            __threadfence();
+            logits[t * E + r_e] = ((sm.rpart[w0][t] + sm.rpart[w0 + 1][t]) + sm.rpart[w0 + 2][t]) + sm.rpart[w0 + 3][t];
         }
         named_barrier_sync(5, 256);
         if (warp == 8 && lane == 0)
-            atomicAdd(&ctrl[2], 1u);   // after the fence above: the logits are published
+            red_release_add(&ctrl[2], 1u);   // publishes this CTA's logits
     } else if (warp < 8) {
         if (warp < T) {
-            const uint4 *row = reinterpret_cast<const uint4 *>(a.x + (size_t)warp * H);
+            const uint4 *row = reinterpret_cast<const uint4 *>(xsh + (size_t)warp * H);
             float m = 0.f;
 #pragma unroll
             for (int i = 0; i < H / 256; ++i) {
-                const uint4 v = __ldg(row + lane + 32 * i);
+                const uint4 v = row[lane + 32 * i];
                 const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
@@ -298,21 +330,19 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             if (lane == 0)
                 sm.xshift[warp] = act_shift(m);
         }
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < (H / 16) * blanes; idx += FT) {
-        const int step = idx / blanes, l = idx % blanes, g = l >> 2, c = l & 3;
-        const float p = pow2i(sm.xshift[g]);
-        const uint32_t *xr = reinterpret_cast<const uint32_t *>(a.x + (size_t)g * H + 16 * step);
-        uint2 v;
-        v.x = bf16x2_to_f16x2_scaled(__ldg(xr + c), p);
-        v.y = bf16x2_to_f16x2_scaled(__ldg(xr + 4 + c), p);
-        sm.xfrag[idx] = v;
+        named_barrier_sync(6, 256);
+        const uint32_t *xw = reinterpret_cast<const uint32_t *>(xs);
+        for (int idx = threadIdx.x; idx < (H / 16) * blanes; idx += 256) {
+            const int step = idx / blanes, l = idx % blanes, g = l >> 2, c = l & 3;
+            const float p = pow2i(sm.xshift[g]);
+            const int w0 = (g * H + 16 * step) / 2 + c;
+            sm.xfrag[idx] = make_uint2(bf16x2_to_f16x2_scaled(xw[w0], p), bf16x2_to_f16x2_scaled(xw[w0 + 4], p));
+        }
     }
 
     // ---- phase 3: routing (every CTA, identically) ----
     if (threadIdx.x == 0)
-        sm.route_ok = spin_until(&ctrl[2], (uint32_t)ROUTER_CTAS, flag) ? 1 : 0;
+        spin_until(&ctrl[2], (uint32_t)ROUTER_CTAS, flag);
     __syncthreads();
     if (warp < T) {
         int ex;
@@ -332,42 +362,56 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             }
         }
     }
-    if (threadIdx.x < E / 32)
-        sm.bitmap[threadIdx.x] = 0u;
-    for (int i = threadIdx.x; i < MAX_SLOTS * MAXT; i += FT)
-        sm.wts[i / MAXT][i % MAXT] = 0.0f;
     __syncthreads();
-    if (threadIdx.x < T * TOPK) {
-        const int ei = sm.sel[threadIdx.x / TOPK][threadIdx.x % TOPK];
-        atomicOr(&sm.bitmap[ei >> 5], 1u << (ei & 31));
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int i = 0; i < E / 32; ++i) {
-            sm.prefix[i] = run;
-            run += __popc(sm.bitmap[i]);
+    if (warp == 0) {
+        // slot table by one warp: bitmap of the selected experts, ranks, weights
+        if (lane < E / 32)
+            sm.bitmap[lane] = 0u;
+        for (int i = lane; i < MAX_SLOTS * MAXT; i += 32)
+            sm.wts[i / MAXT][i % MAXT] = 0.0f;
+        __syncwarp();
+        for (int i = lane; i < T * TOPK; i += 32) {
+            const int ei = sm.sel[i / TOPK][i % TOPK];
+            atomicOr(&sm.bitmap[ei >> 5], 1u << (ei & 31));
         }
-        sm.n_slots = a.n_shared + run;
-    }
-    __syncthreads();
-    if (threadIdx.x < E) {
-        const int ei = threadIdx.x;
-        const uint32_t bits = sm.bitmap[ei >> 5];
-        if (bits & (1u << (ei & 31)))
-            sm.slot_expert[a.n_shared + sm.prefix[ei >> 5] + __popc(bits & ((1u << (ei & 31)) - 1u))] = ei;
-    }
-    if (threadIdx.x < a.n_shared) {
-        sm.slot_expert[threadIdx.x] = -1 - (int)threadIdx.x;
-        for (int t = 0; t < T; ++t)
-            sm.wts[threadIdx.x][t] = 1.0f;
-    }
-    __syncthreads();
-    if (threadIdx.x < T * TOPK) {
-        const int t = threadIdx.x / TOPK, i = threadIdx.x % TOPK;
-        const int ei = sm.sel[t][i];
-        const uint32_t bits = sm.bitmap[ei >> 5];
-        sm.wts[a.n_shared + sm.prefix[ei >> 5] + __popc(bits & ((1u << (ei & 31)) - 1u))][t] = sm.selw[t][i];
+        __syncwarp();
+        const uint32_t bits = lane < E / 32 ? sm.bitmap[lane] : 0u;
+        int cnt = __popc(bits), incl = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off)
+                incl += v;
+        }
+        const int base = a.n_shared + incl - cnt;
+        const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        {
+            uint32_t b = bits;
+            int r = 0;
+            while (b) {
+                const int bit = __ffs(b) - 1;
+                sm.slot_expert[base + r] = lane * 32 + bit;
+                ++r;
+                b &= b - 1;
+            }
+        }
+        if (lane < a.n_shared) {
+            sm.slot_expert[lane] = -1 - lane;
+            for (int t = 0; t < T; ++t)
+                sm.wts[lane][t] = 1.0f;
+        }
+        if (lane == 0)
+            sm.n_slots = a.n_shared + total;
+        __syncwarp();
+        for (int i = lane; i < T * TOPK; i += 32) {
+            const int t = i / TOPK, ei = sm.sel[t][i % TOPK];
+            const uint32_t wbits = sm.bitmap[ei >> 5];
+            const int before = __popc(wbits & ((1u << (ei & 31)) - 1u));
+            int prefix = 0;
+            for (int w = 0; w < (ei >> 5); ++w)
+                prefix += __popc(sm.bitmap[w]);
+            sm.wts[a.n_shared + prefix + before][t] = sm.selw[t][i % TOPK];
+        }
     }
     __syncthreads();
     const int n_slots = sm.n_slots;
@@ -383,100 +427,167 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             st->wts[i / MAXT][i % MAXT] = sm.wts[i / MAXT][i % MAXT];
     }
 
-    // ---- phase 4: the unit queue ----
-    const int n_routed_slots = n_slots - a.n_shared;
-    const int gu_total = n_slots * W13_BANDS;                       // unit ids [0, gu_total): gate/up
-    const int q_gu = n_routed_slots * W13_BANDS;                    // routed gate/up units in the queue
-    const int q_total = q_gu + n_slots * (W2_BANDS / GW);           // + down units
-    const int end_id = gu_total + n_slots * (W2_BANDS / GW);
-    auto fetch = [&]() -> int {
-        const uint32_t q = atomicAdd(&ctrl[3], 1u);
-        if ((int)q < q_gu)
-            return a.n_shared * W13_BANDS + (int)q;
-        if ((int)q < q_total)
-            return gu_total + ((int)q - q_gu);
-        return end_id;
-    };
+    // ---- phase 4: the units ----
+    const int gu_total = n_slots * GU_UNITS;                        // unit ids [0, gu_total): gate/up
+    const int end_id = gu_total + n_slots * DN_UNITS;               // then down units
+    auto unit_id = [&](int k) { return gid + k * n_groups; };
     auto decode = [&](int id) -> Unit {
         if (id < gu_total)
-            return Unit{false, id / W13_BANDS, id % W13_BANDS};
+            return Unit{false, id / GU_UNITS, 4 * (id % GU_UNITS) + wq};
         const int d = id - gu_total;
-        return Unit{true, d / (W2_BANDS / GW), d % (W2_BANDS / GW)};
+        return Unit{true, d / DN_UNITS, 4 * (d % DN_UNITS) + wq};
     };
-    // h of a down unit: raw bf16 [T][I] of the slot into hbuf[grp][b]
+    auto nparts = [&](const Unit &u) { return u.down ? DN_PARTS : GU_PARTS; };
+    // first down unit of this group, and the down-unit index of unit k
+    const int k_down0 = gid >= gu_total ? 0 : (gu_total - gid + n_groups - 1) / n_groups;
+    // h of down unit dk: the slot's T rows into padded rows of hbuf[grp][dk & 1]
+    // (leader lane only; the slot counter has been acquired)
     auto issue_h = [&](int slot, int b) {
+#pragma unroll
+        for (int t = 0; t < MAXT; ++t)
+            if (t < T)
+                sm.hshift[grp][b][t] = act_shift(__uint_as_float(__ldcg(&hmax[slot * MAXT + t])));
+        fence_proxy_async_global();   // h was published to the generic proxy by releases
         uint64_t *bar = &sm.hbar[grp][b];
-        const uint32_t bytes = (uint32_t)(T * I * 2);
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(sm.hbuf[grp][b], hglob + (size_t)slot * MAXT * I, bytes, bar);
+        mbar_arrive_expect_tx(bar, (uint32_t)(T * I * 2));
+        for (int t = 0; t < T; ++t)
+            bulk_g2s(sm.hbuf[grp][b] + t * HROW, hglob + ((size_t)slot * MAXT + t) * I, (uint32_t)(I * 2), bar);
     };
-    auto slot_ready = [&](int slot) { return ld_acquire(&slot_cnt[slot]) >= (uint32_t)W13_BANDS; };
 
-    if (leader && lane == 0) {
-        sm.unit[grp][0] = static_shared ? (int)blockIdx.x : fetch();
-        sm.unit[grp][1] = fetch();
-        sm.unit[grp][2] = fetch();
-        sm.hissued[grp][0] = sm.hissued[grp][1] = 0;
-        for (int k = 0; k < 2; ++k) {
-            const int id = sm.unit[grp][k];
-            if (id < end_id) {
-                const Unit u = decode(id);
-                if (u.down && slot_ready(u.slot)) {
-                    issue_h(u.slot, k);
-                    sm.hissued[grp][k] = 1;
-                }
+    // ---- stage stream of this warp: (unit k, part p) in order, RING in flight ----
+    int ik = 0, ip = 0, icount = 0;      // next stage to issue
+    if (static_shared) {
+        ip = RING;                       // parts 0..RING-1 of unit 0 were issued before the wait
+        icount = RING;
+    }
+    auto issue_ahead = [&](int limit) {
+        while (icount < limit) {
+            const int id = unit_id(ik);
+            if (id >= end_id)
+                break;
+            const Unit u = decode(id);
+            issue_stage(icount % RING, u, ip);
+            ++icount;
+            if (++ip == nparts(u)) {
+                ip = 0;
+                ++ik;
             }
         }
-    }
-    named_barrier_sync(1 + grp, GW * 32);
-    {
-        const int id0 = sm.unit[grp][0];
-        if (!static_shared && id0 < end_id) {
-            issue_stage(0, decode(id0));
-            issue_stage(1, decode(id0));
-        }
-    }
+    };
+    issue_ahead(RING);
 
-    int hcnt[2] = {0, 0};
+    // ---- leader: h of the group's down units, issued as their slots complete ----
+    int h_next = 0;                  // next down unit whose h is not yet requested
+    int h_done = 0;                  // down units whose buffer has been released
+    int probe_for = -1;              // down unit the pending probe is for
+    uint32_t probe_val = 0u;
+    auto try_issue_h = [&]() {
+        if (!lead_thread)
+            return;
+        while (h_next < h_done + 2) {
+            const int id = unit_id(k_down0 + h_next);
+            if (id >= end_id)
+                return;
+            const int slot = decode(id).slot;
+            if (probe_for == h_next && probe_val >= SLOT_DONE) {
+                fence_acquire_gpu();     // pairs with the releases that counted the slot done
+                issue_h(slot, h_next & 1);
+                ++h_next;
+                probe_for = -1;
+                continue;
+            }
+            probe_val = ld_relaxed(&slot_cnt[slot]);   // looked at on the next call
+            probe_for = h_next;
+            return;
+        }
+    };
+
+    // The last down partial of a band adds every slot's partial in slot order.
+    auto combine_band = [&](int band) {
+        const int r = lane >> 1, th = lane & 1;      // row r, tokens 4*th .. 4*th+3
+        const float4 *src = reinterpret_cast<const float4 *>(partials + ((size_t)16 * band + r) * MAXT) + th;
+        float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        constexpr int BATCH = 16;
+        for (int s0 = 0; s0 < n_slots; s0 += BATCH) {
+            float4 v[BATCH];
+#pragma unroll
+            for (int j = 0; j < BATCH; ++j)
+                v[j] = (s0 + j < n_slots) ? __ldcg(src + (size_t)(s0 + j) * H * MAXT / 4)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < BATCH; ++j) {
+                s4.x += v[j].x; s4.y += v[j].y; s4.z += v[j].z; s4.w += v[j].w;
+            }
+        }
+        const float vals[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int t = 4 * th + j;
+            if (t < T)
+                a.out[(size_t)t * H + 16 * band + r] = __float2bfloat16_rn(vals[j]);
+        }
+        if (lane == 0)
+            band_cnt[band] = 0u;
+    };
+
+    // Completion signals of the previous unit, posted one unit late by lane 31
+    // (it issues no bulk copies, so the release only waits for stores).
+    int pend_slot = -1;              // gate/up: slot whose band this warp finished
+    int pend_band = -1;              // down: band whose partial this warp wrote
+    auto post_signals = [&]() {
+        if (pend_slot >= 0) {
+            __syncwarp();
+            if (lane == 31)
+                red_release_add(&slot_cnt[pend_slot], 1u);
+            pend_slot = -1;
+        }
+        if (pend_band >= 0) {
+            __syncwarp();
+            uint32_t prev = 0;
+            if (lane == 31)
+                prev = atom_add_acq_rel(&band_cnt[pend_band], 1u);
+            prev = __shfl_sync(0xFFFFFFFFu, prev, 31);
+            if (prev == (uint32_t)(n_slots - 1))
+                combine_band(pend_band);
+            pend_band = -1;
+        }
+    };
+
+    int ccount = 0;                  // stages consumed
     float acc[4];
     for (int k = 0;; ++k) {
-        const int id = sm.unit[grp][k % UNITS_AHEAD];
+        const int id = unit_id(k);
         if (id >= end_id)
             break;
         const Unit u = decode(id);
-        const int id_next = sm.unit[grp][(k + 1) % UNITS_AHEAD];
-        const bool has_next = id_next < end_id;
-        const Unit un = has_next ? decode(id_next) : Unit{false, 0, 0};
-        if (has_next)
-            issue_stage(2 * k + 2, un);
+        try_issue_h();
 
         const uint2 *bfrag = sm.xfrag;
-        int step0 = 32 * wq;   // gate/up: this warp's K quarter
+        int b = 0;
         if (u.down) {
-            const int b = k & 1;
-            if (leader && lane == 0 && !sm.hissued[grp][b]) {
-                spin_until(&slot_cnt[u.slot], (uint32_t)W13_BANDS, flag);
+            const int dk = k - k_down0;
+            b = dk & 1;
+            post_signals();    // never wait while holding a completion signal
+            if (lead_thread && h_next == dk) {
+                spin_until(&slot_cnt[u.slot], SLOT_DONE, flag);
                 issue_h(u.slot, b);
-                sm.hissued[grp][b] = 1;
+                ++h_next;
+                probe_for = -1;
             }
-            mbar_wait_bounded(&sm.hbar[grp][b], hcnt[b] & 1, flag);
-            hcnt[b]++;
-            // rescale h (bf16 [T][I]) in place into f16 fragments [step][4T]
-            uint32_t *hb = reinterpret_cast<uint32_t *>(sm.hbuf[grp][b]);
+            mbar_wait_bounded(&sm.hbar[grp][b], (dk >> 1) & 1, flag);
+            // rescale h (padded bf16 rows) in place into f16 fragments [step][4T]
+            const uint32_t *hw = reinterpret_cast<const uint32_t *>(sm.hbuf[grp][b]);
             const int nent = (I / 16) * blanes;            // <= 1024
-            uint32_t src[2][8];
-            int shv[MAXT];
-#pragma unroll
-            for (int t = 0; t < MAXT; ++t)
-                shv[t] = (t < T) ? act_shift(__uint_as_float(__ldcg(&hmax[u.slot * MAXT + t]))) : 0;
+            uint32_t src0[8], src1[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int e = (wq * 32 + lane) + j * (GW * 32);
-                src[0][j] = src[1][j] = 0u;
+                src0[j] = src1[j] = 0u;
                 if (e < nent) {
                     const int step = e / blanes, l = e % blanes, g = l >> 2, c = l & 3;
-                    src[0][j] = hb[(g * I + 16 * step) / 2 + c];
-                    src[1][j] = hb[(g * I + 16 * step + 8) / 2 + c];
+                    const int w0 = (g * HROW) / 4 + 8 * step + c;
+                    src0[j] = hw[w0];
+                    src1[j] = hw[w0 + 4];
                 }
             }
             named_barrier_sync(1 + grp, GW * 32);
@@ -485,144 +596,78 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             for (int j = 0; j < 8; ++j) {
                 const int e = (wq * 32 + lane) + j * (GW * 32);
                 if (e < nent) {
-                    const int g = (e % blanes) >> 2;
-                    int sh = 0;
-#pragma unroll
-                    for (int t = 0; t < MAXT; ++t)
-                        if (t == g) sh = shv[t];
-                    const float p = pow2i(sh);
-                    hf[e] = make_uint2(bf16x2_to_f16x2_scaled(src[0][j], p), bf16x2_to_f16x2_scaled(src[1][j], p));
+                    const float p = pow2i(sm.hshift[grp][b][(e % blanes) >> 2]);
+                    hf[e] = make_uint2(bf16x2_to_f16x2_scaled(src0[j], p), bf16x2_to_f16x2_scaled(src1[j], p));
                 }
             }
             named_barrier_sync(1 + grp, GW * 32);
             bfrag = hf;
-            step0 = 0;
         }
 
         acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-        // stage 2k
-        mbar_wait_bounded(&sm.full[warp][(2 * k) % RING], ((2 * k) / RING) & 1, flag);
-        mma_stage(sm.ring[warp][(2 * k) % RING], bfrag, blanes, step0, lane, acc);
-        __syncwarp();
-        if (has_next)
-            issue_stage(2 * k + 3, un);
-        // stage 2k + 1
-        mbar_wait_bounded(&sm.full[warp][(2 * k + 1) % RING], ((2 * k + 1) / RING) & 1, flag);
-        mma_stage(sm.ring[warp][(2 * k + 1) % RING], bfrag, blanes, step0 + 16, lane, acc);
-        __syncwarp();
+        const int np = nparts(u);
+        for (int p = 0; p < np; ++p) {
+            const int rs = ccount % RING;
+            mbar_wait_bounded(&sm.full[warp][rs], (ccount / RING) & 1, flag);
+            mma_stage(sm.ring[warp][rs], bfrag, blanes, 16 * p, lane, acc);
+            __syncwarp();
+            ++ccount;
+            issue_ahead(ccount + RING);
+        }
+
+        post_signals();    // the previous unit's stores have landed by now
 
         const int g = lane >> 2, c = lane & 3;
         if (!u.down) {
-            // K parts -> warp 0 of the group; SiLU*up; h; running max of |h|
-            if (wq != 0)
-                sm.red[k & 1][grp][wq - 1][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            named_barrier_sync(1 + grp, GW * 32);
-            if (wq == 0) {
+            // SiLU*up for h rows 8 * band + g; running max of |h|
+            const float ts = (u.slot < a.n_shared) ? __ldg(a.s_ts13 + u.slot)
+                                                   : __ldg(a.r_ts13 + sm.slot_expert[u.slot]);
+            float hm[2];
 #pragma unroll
-                for (int j = 0; j < GW - 1; ++j) {
-                    const float4 r = sm.red[k & 1][grp][j][lane];
-                    acc[0] += r.x; acc[1] += r.y; acc[2] += r.z; acc[3] += r.w;
+            for (int tt = 0; tt < 2; ++tt) {
+                const int t = 2 * c + tt;
+                hm[tt] = 0.f;
+                if (t < T) {
+                    const float f = ts * pow2i(-sm.xshift[t]);
+                    const float gv = acc[tt] * f, uv = acc[2 + tt] * f;
+                    const __nv_bfloat16 hv = __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
+                    hglob[((size_t)u.slot * MAXT + t) * I + u.band * 8 + g] = hv;
+                    hm[tt] = fabsf(__bfloat162float(hv));
                 }
-                const float ts = (u.slot < a.n_shared) ? __ldg(a.s_ts13 + u.slot)
-                                                       : __ldg(a.r_ts13 + sm.slot_expert[u.slot]);
-                float hm[2];
-#pragma unroll
-                for (int tt = 0; tt < 2; ++tt) {
-                    const int t = 2 * c + tt;
-                    hm[tt] = 0.f;
-                    if (t < T) {
-                        const float f = ts * pow2i(-sm.xshift[t]);
-                        const float gv = acc[tt] * f, uv = acc[2 + tt] * f;
-                        const __nv_bfloat16 hv = __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
-                        hglob[((size_t)u.slot * MAXT + t) * I + u.idx * 8 + g] = hv;
-                        hm[tt] = fabsf(__bfloat162float(hv));
-                    }
-                }
-#pragma unroll
-                for (int off = 4; off <= 16; off <<= 1) {
-                    hm[0] = fmaxf(hm[0], __shfl_xor_sync(0xFFFFFFFFu, hm[0], off));
-                    hm[1] = fmaxf(hm[1], __shfl_xor_sync(0xFFFFFFFFu, hm[1], off));
-                }
-                if (g == 0) {
-#pragma unroll
-                    for (int tt = 0; tt < 2; ++tt)
-                        if (2 * c + tt < T)
-                            atomicMax(&hmax[u.slot * MAXT + 2 * c + tt], __float_as_uint(hm[tt]));
-                }
-                __threadfence();
-                __syncwarp();
-                if (lane == 0)
-                    atomicAdd(&slot_cnt[u.slot], 1u);
             }
+#pragma unroll
+            for (int off = 4; off <= 16; off <<= 1) {
+                hm[0] = fmaxf(hm[0], __shfl_xor_sync(0xFFFFFFFFu, hm[0], off));
+                hm[1] = fmaxf(hm[1], __shfl_xor_sync(0xFFFFFFFFu, hm[1], off));
+            }
+            if (g == 0) {
+#pragma unroll
+                for (int tt = 0; tt < 2; ++tt)
+                    if (2 * c + tt < T)
+                        atomicMax(&hmax[u.slot * MAXT + 2 * c + tt], __float_as_uint(hm[tt]));
+            }
+            pend_slot = u.slot;
         } else {
             // down: one band per warp, x routing weight x tensor scale x 2^-shift
-            const int band = 4 * u.idx + wq;
             const float ts = (u.slot < a.n_shared) ? __ldg(a.s_ts2 + u.slot)
                                                    : __ldg(a.r_ts2 + sm.slot_expert[u.slot]);
-            float *P = partials + ((size_t)u.slot * H + 16 * band) * MAXT;
+            float *P = partials + ((size_t)u.slot * H + 16 * u.band) * MAXT;
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt) {
                 const int t = 2 * c + tt;
                 if (t < T) {
-                    const int sh = act_shift(__uint_as_float(__ldcg(&hmax[u.slot * MAXT + t])));
-                    const float f = sm.wts[u.slot][t] * ts * pow2i(-sh);
+                    const float f = sm.wts[u.slot][t] * ts * pow2i(-sm.hshift[grp][b][t]);
                     P[g * MAXT + t] = acc[tt] * f;
                     P[(g + 8) * MAXT + t] = acc[2 + tt] * f;
                 }
             }
-            __threadfence();
-            __syncwarp();
-            uint32_t prev = 0;
-            if (lane == 0)
-                prev = atomicAdd(&band_cnt[band], 1u);
-            prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
-            if (prev == (uint32_t)(n_slots - 1)) {
-                // last partial of this band: add all slots in slot order
-                __threadfence();
-                const int r = lane >> 1, th = lane & 1;      // row r, tokens 4*th .. 4*th+3
-                const float4 *src = reinterpret_cast<const float4 *>(partials + ((size_t)16 * band + r) * MAXT) + th;
-                float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                constexpr int BATCH = 16;
-                for (int s0 = 0; s0 < n_slots; s0 += BATCH) {
-                    float4 v[BATCH];
-#pragma unroll
-                    for (int j = 0; j < BATCH; ++j)
-                        v[j] = (s0 + j < n_slots) ? __ldcg(src + (size_t)(s0 + j) * H * MAXT / 4)
-                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int j = 0; j < BATCH; ++j) {
-                        s4.x += v[j].x; s4.y += v[j].y; s4.z += v[j].z; s4.w += v[j].w;
-                    }
-                }
-                const float vals[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int t = 4 * th + j;
-                    if (t < T)
-                        a.out[(size_t)t * H + 16 * band + r] = __float2bfloat16_rn(vals[j]);
-                }
-                if (lane == 0)
-                    band_cnt[band] = 0u;
-            }
+            pend_band = u.band;
+            // the group's hbuf[b] is free once all four warps are done with it
+            named_barrier_sync(1 + grp, GW * 32);
+            ++h_done;
         }
-
-        // end of unit: the group's red / hbuf / unit slot are free
-        named_barrier_sync(1 + grp, GW * 32);
-        if (leader && lane == 0) {
-            sm.unit[grp][k % UNITS_AHEAD] = fetch();     // unit k + 3
-            const int b = k & 1;                          // h buffer of unit k + 2
-            sm.hissued[grp][b] = 0;
-            const int id2 = sm.unit[grp][(k + 2) % UNITS_AHEAD];
-            if (id2 < end_id) {
-                const Unit u2 = decode(id2);
-                if (u2.down && slot_ready(u2.slot)) {
-                    issue_h(u2.slot, b);
-                    sm.hissued[grp][b] = 1;
-                }
-            }
-        }
-        named_barrier_sync(1 + grp, GW * 32);
     }
+    post_signals();
 
     // ---- the last CTA to finish re-arms the counters for the next call ----
     __syncthreads();
@@ -632,7 +677,6 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
         if (prev == gridDim.x - 1) {
             __threadfence();
             ctrl[2] = 0u;
-            ctrl[3] = 0u;
             for (int s = 0; s < MAX_SLOTS; ++s)
                 slot_cnt[s] = 0u;
             for (int i = 0; i < MAX_SLOTS * MAXT; ++i)

@@ -28,50 +28,11 @@ __device__ __forceinline__ unsigned long long rank_key(float v, int e)
 
 __device__ __forceinline__ int key_expert(unsigned long long k) { return 0xFFFF - (int)(k & 0xFFFFu); }
 
-__device__ __forceinline__ void cas_desc(unsigned long long &a, unsigned long long &b)
+// The logit a key was built from (exact; NaN keys give a NaN).
+__device__ __forceinline__ float key_logit(unsigned long long key)
 {
-    unsigned long long hi = a > b ? a : b;
-    unsigned long long lo = a > b ? b : a;
-    a = hi;
-    b = lo;
-}
-
-// Sort 8 keys in descending order (Batcher's odd-even merge network, 19 CAS).
-__device__ __forceinline__ void sort8_desc(unsigned long long k[8])
-{
-    cas_desc(k[0], k[1]); cas_desc(k[2], k[3]); cas_desc(k[4], k[5]); cas_desc(k[6], k[7]);
-    cas_desc(k[0], k[2]); cas_desc(k[1], k[3]); cas_desc(k[4], k[6]); cas_desc(k[5], k[7]);
-    cas_desc(k[1], k[2]); cas_desc(k[5], k[6]);
-    cas_desc(k[0], k[4]); cas_desc(k[1], k[5]); cas_desc(k[2], k[6]); cas_desc(k[3], k[7]);
-    cas_desc(k[2], k[4]); cas_desc(k[3], k[5]);
-    cas_desc(k[1], k[2]); cas_desc(k[3], k[4]); cas_desc(k[5], k[6]);
-}
-
-// Sort a bitonic sequence of 8 keys into descending order (12 CAS).
-__device__ __forceinline__ void bitonic8_desc(unsigned long long k[8])
-{
-    cas_desc(k[0], k[4]); cas_desc(k[1], k[5]); cas_desc(k[2], k[6]); cas_desc(k[3], k[7]);
-    cas_desc(k[0], k[2]); cas_desc(k[1], k[3]); cas_desc(k[4], k[6]); cas_desc(k[5], k[7]);
-    cas_desc(k[0], k[1]); cas_desc(k[2], k[3]); cas_desc(k[4], k[5]); cas_desc(k[6], k[7]);
-}
-
-// Top-8 of E = 256 keys held 8 per lane; every lane ends with the sorted top 8.
-__device__ __forceinline__ void warp_top8(unsigned long long k[8])
-{
-    sort8_desc(k);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        unsigned long long p[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            p[i] = __shfl_xor_sync(0xFFFFFFFFu, k[i], off);
-        // top 8 of two descending lists = elementwise max against the reversed
-        // partner list, which is bitonic
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            k[i] = k[i] > p[7 - i] ? k[i] : p[7 - i];
-        bitonic8_desc(k);
-    }
+    const uint32_t u = (uint32_t)(key >> 32);
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
 }
 
 // Top-k of one token's E = 256 fp32 logits by one warp: returns in lanes
@@ -90,16 +51,30 @@ __device__ __forceinline__ void warp_route_token(const float *logits_row, int la
         k[m] = rank_key(v, ee);
     }
     nonfinite = __any_sync(0xFFFFFFFFu, bad);
-    warp_top8(k);
+    // TOPK rounds of a warp-wide argmax (keys are unique: index in the low bits)
     float s = 0.0f, sum = 0.0f;
     ex = 0;
-#pragma unroll
+#pragma unroll 1
     for (int i = 0; i < TOPK; ++i) {
-        const int ei = key_expert(k[i]);
-        const float v = __ldcg(logits_row + ei);
-        const float si = 1.0f / (1.0f + expf(-v));
+        unsigned long long best = k[0];
+#pragma unroll
+        for (int m = 1; m < 8; ++m)
+            best = k[m] > best ? k[m] : best;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+            best = o > best ? o : best;
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+            if (k[m] == best)
+                k[m] = 0ull;
+        const float si = 1.0f / (1.0f + expf(-key_logit(best)));
         sum += si;
-        if (lane == i) { s = si; ex = ei; }
+        if (lane == i) {
+            s = si;
+            ex = key_expert(best);
+        }
     }
     wt = s / sum;
 }
