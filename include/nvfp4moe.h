@@ -204,11 +204,14 @@ moe_status moe_route(const void *x, const void *router_w, int T, int n_experts, 
 
 /*
  * out = MoE(x) for 1 <= T <= MOE_MAX_DECODE_T tokens (see the top of this
- * header).  Three kernels, chained with programmatic dependent launch:
- * the router (+top-k, the expert union and per-slot token weights), the
- * gate/up GEMV fused with SiLU*up over the distinct selected experts (each
- * read once for all tokens) plus the shared expert, and the down GEMV fused
- * with the routing-weighted combine and the shared expert.
+ * header).  One persistent kernel (one CTA per SM, launched with
+ * programmatic dependent launch so that its weight prefetch overlaps the
+ * preceding kernel) runs the router GEMV and the top-k of every token, builds
+ * the union of the selected experts with per-token weights, streams each
+ * selected expert's W13 once for all tokens (SiLU*up fused into the epilogue),
+ * then its W2 (routing weight fused), and adds the per-expert partials of
+ * every output row in a fixed order (deterministic, bit-identical between
+ * calls).  The routing results stay readable in the workspace.
  *  x:        device bf16 [T][H]; must not alias out.
  *  router_w: device bf16 [E][H].
  *  routed:   host struct describing E = 256 routed experts.
@@ -216,9 +219,12 @@ moe_status moe_route(const void *x, const void *router_w, int T, int n_experts, 
  *  out:      device bf16 [T][H].
  *  workspace: device, >= moe_workspace_bytes(T), initialised once with
  *            moe_workspace_init; one workspace per concurrently running call.
- * The routed and shared banks must have the same wtype in this build.
- * Activations must satisfy |x| < 2^32 (they are scaled by 2^96 inside the
- * tensor-core products).
+ * Both banks must be NVFP4 in this build (BF16 banks: MOE_ERR_UNSUPPORTED).
+ * Activations must be finite with max|x[t]| < 2^114 per token: each token is
+ * scaled by a power of two into f16 for the tensor cores (see csrc/common.cuh).
+ * Every SM must be able to host one CTA at the same time (the kernel's CTAs
+ * wait on each other's counters, with bounded waits that set
+ * MOE_FLAG_WAIT_TIMEOUT if that ever fails).
  */
 moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expert_bank *routed,
                              const moe_expert_bank *shared, void *out, int T, void *workspace,
