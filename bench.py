@@ -18,6 +18,7 @@ replicas, one per GPU; value sums their bytes over the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -36,6 +37,24 @@ METRIC = "MoE layer µs and weight-read GB/s (% of HBM peak) at T=1/8, NVFP4 and
 
 def layer_bytes(T: int, n_distinct: int, n_shared: int = 1) -> int:
     return ROUTER_BYTES + (n_distinct + n_shared) * EXPERT_BYTES + 2 * T * 2048 * 2
+
+
+# DRAM traffic of moe_layer_kernel per algorithmic byte, from an ncu capture
+# (profiles/moe_layer_kernel_t8.md).  It holds only for the kernel sources it
+# was measured on; any change to them makes the bench report traffic as null.
+NCU_TRAFFIC = {
+    "sources_sha256": "3ac48e2a6a2ddba51dd3ee3a1663fd6a037adf549c30524c0e674fbc3d881a5f",
+    "per_algorithmic_byte": 165_376_512 / 161_480_704,
+}
+KERNEL_SOURCES = ("layer.cu", "common.cuh", "kernels.cuh", "topk.cuh")
+
+
+def kernel_sources_sha256() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "nvfp4_moe_decode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def peaks():
@@ -345,6 +364,9 @@ def main():
 
     peak, peak_src = peaks()
     layer_alg = steps_bytes / K
+    traffic = None
+    if kernel_sources_sha256() == NCU_TRAFFIC["sources_sha256"]:
+        traffic = layer_alg * NCU_TRAFFIC["per_algorithmic_byte"]
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -354,7 +376,7 @@ def main():
                    "hbm_frac": value / world / peak, "device_flag": flag},
         "roofline": {"bound": "hbm", "achieved": layer_alg / (us_per_layer * 1e-6) / 1e9, "peak": peak,
                      "unit": "GB/s", "frac": layer_alg / (us_per_layer * 1e-6) / 1e9 / peak,
-                     "traffic": None, "peak_source": peak_src,
+                     "traffic": traffic, "peak_source": peak_src,
                      "kernel": "moe_layer_kernel (router, top-6, gate/up, down, combine fused; one launch per layer)"},
         "e2e": {"value": e2e_v, "unit": "GB/s", "steps": ne, "h2d_bytes_per_step": T * 2048 * 2,
                 "d2h_bytes_per_step": T * 2048 * 2},
