@@ -42,8 +42,9 @@
  *    return MOE_ERR_CUDA.  Conditions found on the device (a non-finite
  *    router logit, an expired bounded wait) set bits of a flag word in the
  *    workspace, read back by moe_read_device_flag.  Kernels never trap.
- *  - The library keeps no mutable global state; calls on different streams
- *    with different workspaces may run concurrently.
+ *  - Apart from the fixed scratch of moe_layer_forward_static, the library
+ *    keeps no mutable global state; calls on different streams with
+ *    different workspaces may run concurrently.
  */
 #ifndef NVFP4MOE_H
 #define NVFP4MOE_H
@@ -229,6 +230,44 @@ moe_status moe_route(const void *x, const void *router_w, int T, int n_experts, 
 moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expert_bank *routed,
                              const moe_expert_bank *shared, void *out, int T, void *workspace,
                              size_t workspace_bytes, moe_stream_t stream);
+
+/* ----------------------------------------------------------------------- */
+/* The layer without a caller-provided workspace.  The pages describe no   */
+/* such entry point; it exists for callers that cannot allocate.           */
+/* ----------------------------------------------------------------------- */
+
+/* Bytes of the library's fixed per-device scratch: the workspace of
+ * moe_layer_forward at T = MOE_MAX_DECODE_T. */
+#define MOE_STATIC_SCRATCH_BYTES 3625984u
+
+/*
+ * moe_layer_forward with the workspace replaced by a fixed device array of
+ * MOE_STATIC_SCRATCH_BYTES inside the library, for callers that cannot own or
+ * allocate device memory (a plugin interface that passes only inputs and
+ * outputs, a process whose device memory is fixed at start-up).  Computes
+ * exactly what moe_layer_forward computes (same kernel, same results).
+ *  Arguments: as moe_layer_forward, without workspace / workspace_bytes.
+ *  Allocation: none; no cudaMalloc / cudaFree and no allocating library call.
+ *  First call on each device: looks up the array's device address with
+ *    cudaGetSymbolAddress (that device current) and zeroes the array on
+ *    `stream`; make that first call before any stream capture.  Later calls
+ *    only launch the layer.
+ *  Zero state: the control words of the scratch (arrival counters, running
+ *    maxima, device flag) must be zero when a call starts; the setup zeroes
+ *    them and every call leaves them zero when it completes.  The device flag
+ *    of this scratch is not reported; a caller that needs the flags uses
+ *    moe_layer_forward with its own workspace.
+ *  Concurrency: one scratch per device.  Calls on the same device must not
+ *    overlap (serialise them on one stream or with events); overlapping calls
+ *    race on the scratch and give wrong results.
+ *  Errors: MOE_ERR_UNSUPPORTED for T outside 1..MOE_MAX_DECODE_T (the
+ *    scratch's maximum), before any CUDA call; MOE_ERR_CUDA if the setup
+ *    fails; otherwise the statuses of moe_layer_forward.
+ */
+moe_status moe_layer_forward_static(const void *x, const void *router_w,
+                                    const moe_expert_bank *routed,
+                                    const moe_expert_bank *shared, void *out, int T,
+                                    moe_stream_t stream);
 
 #ifdef __cplusplus
 }

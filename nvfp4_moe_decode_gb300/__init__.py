@@ -44,8 +44,10 @@ MAX_DECODE_T = 8
 EXPORTS = (
     "moe_abi_version", "moe_status_string", "moe_packed_bytes", "moe_pack_nvfp4",
     "moe_unpack_nvfp4", "moe_dequant_nvfp4", "moe_workspace_bytes", "moe_workspace_init",
-    "moe_read_device_flag", "moe_route", "moe_layer_forward",
+    "moe_read_device_flag", "moe_route", "moe_layer_forward", "moe_layer_forward_static",
 )
+
+MOE_STATIC_SCRATCH_BYTES = 3_625_984
 
 
 class MoeError(RuntimeError):
@@ -94,6 +96,8 @@ def _declare(lib):
     bank_p = ctypes.POINTER(moe_expert_bank)
     lib.moe_layer_forward.argtypes = [vp, vp, bank_p, bank_p, vp, i32, vp, sz, vp]
     lib.moe_layer_forward.restype = i32
+    lib.moe_layer_forward_static.argtypes = [vp, vp, bank_p, bank_p, vp, i32, vp]
+    lib.moe_layer_forward_static.restype = i32
     return lib
 
 
@@ -206,3 +210,12 @@ def moe_layer_forward(x, router_w, routed: moe_expert_bank, shared: Optional[moe
                                _ptr(workspace), workspace.numel() * workspace.element_size(),
                                _stream(stream))
     _check("moe_layer_forward", st)
+
+
+def moe_layer_forward_static(x, router_w, routed: moe_expert_bank, shared: Optional[moe_expert_bank], out,
+                             T: int, stream=None):
+    lib = load()
+    st = lib.moe_layer_forward_static(_ptr(x), _ptr(router_w), ctypes.byref(routed),
+                                      ctypes.byref(shared) if shared is not None else None, _ptr(out),
+                                      int(T), _stream(stream))
+    _check("moe_layer_forward_static", st)

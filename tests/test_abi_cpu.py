@@ -53,6 +53,8 @@ def test_workspace_bytes(moe_lib):
         assert m.moe_workspace_bytes(T) > 0
     assert m.moe_workspace_bytes(0) == 0
     assert m.moe_workspace_bytes(9) == 0
+    # the fixed scratch of moe_layer_forward_static covers the largest batch
+    assert m.moe_workspace_bytes(m.MAX_DECODE_T) == m.MOE_STATIC_SCRATCH_BYTES
 
 
 def test_host_argument_errors_enqueue_nothing(moe_lib):
@@ -88,6 +90,10 @@ def test_host_argument_errors_enqueue_nothing(moe_lib):
     assert lib.moe_workspace_init(None, ws, None) == m.MOE_ERR_INVALID_ARG
     assert lib.moe_workspace_init(dummy, 8, None) == m.MOE_ERR_WORKSPACE
     assert lib.moe_read_device_flag(None, None, None) == m.MOE_ERR_INVALID_ARG
+    # the no-allocation variant rejects T beyond its scratch before any CUDA call
+    fs = lib.moe_layer_forward_static
+    assert fs(dummy, dummy, B(bank), None, dummy * 2, 9, None) == m.MOE_ERR_UNSUPPORTED
+    assert fs(dummy, dummy, B(bank), None, dummy * 2, 0, None) == m.MOE_ERR_UNSUPPORTED
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
