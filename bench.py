@@ -30,13 +30,14 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-EXPERT_BYTES = 1_179_648 + 589_824       # packed gate/up + down of one expert
+EXPERT_BYTES = {"nvfp4": 1_179_648 + 589_824,      # packed gate/up + down of one expert
+                "bf16": (2 * 512 * 2048 + 2048 * 512) * 2}
 ROUTER_BYTES = 256 * 2048 * 2
 METRIC = "MoE layer µs and weight-read GB/s (% of HBM peak) at T=1/8, NVFP4 and BF16"
 
 
-def layer_bytes(T: int, n_distinct: int, n_shared: int = 1) -> int:
-    return ROUTER_BYTES + (n_distinct + n_shared) * EXPERT_BYTES + 2 * T * 2048 * 2
+def layer_bytes(T: int, n_distinct: int, n_shared: int = 1, wtype: str = "nvfp4") -> int:
+    return ROUTER_BYTES + (n_distinct + n_shared) * EXPERT_BYTES[wtype] + 2 * T * 2048 * 2
 
 
 # DRAM traffic of moe_layer_kernel per algorithmic byte, from an ncu capture
@@ -164,7 +165,7 @@ def barrier(world: int):
 # CPU oracle timing (the reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(layers_host, x_bits, T: int, budget_s: float):
+def oracle_sample(layers_host, x_bits, T: int, budget_s: float, wtype: str = "nvfp4"):
     """Run the fp64 oracle layer over the resident layers until budget_s.
     Returns (seconds, algorithmic bytes, layers done, threads)."""
     import oracle
@@ -174,9 +175,24 @@ def oracle_sample(layers_host, x_bits, T: int, budget_s: float):
         for (wr, experts, shared, nd) in layers_host:
             oracle.moe_forward(x_bits, wr, experts, 6, 512, shared)
             done += 1
-            nbytes += layer_bytes(T, nd)
+            nbytes += layer_bytes(T, nd, 1, wtype)
             if time.perf_counter() - t0 >= budget_s:
                 return time.perf_counter() - t0, nbytes, done, oracle.num_threads()
+
+
+def host_expert(li, e: int):
+    """Host copy of expert e of a synthetic layer, in the oracle's form."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    if li.wtype == 0:
+        return oracle.ExpertWeights(0, li.codes13[e].cpu().numpy(), li.scales13[e].cpu().numpy(),
+                                    float(li.tscale13[e]), li.codes2[e].cpu().numpy(),
+                                    li.scales2[e].cpu().numpy(), float(li.tscale2[e]))
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)  # noqa: E731
+    return oracle.ExpertWeights(1, bits(li.w13[e]), None, 1.0, bits(li.w2[e]), None, 1.0)
 
 
 def host_layers_for_oracle(lis, x, n: int):
@@ -195,13 +211,8 @@ def host_layers_for_oracle(lis, x, n: int):
         experts = [None] * 256
         sel = sorted(set(idx.reshape(-1).tolist()))
         for e in sel:
-            experts[e] = oracle.ExpertWeights(0, li.codes13[e].cpu().numpy(), li.scales13[e].cpu().numpy(),
-                                              float(li.tscale13[e]), li.codes2[e].cpu().numpy(),
-                                              li.scales2[e].cpu().numpy(), float(li.tscale2[e]))
-        shared = oracle.ExpertWeights(0, li.codes13[256].cpu().numpy(), li.scales13[256].cpu().numpy(),
-                                      float(li.tscale13[256]), li.codes2[256].cpu().numpy(),
-                                      li.scales2[256].cpu().numpy(), float(li.tscale2[256]))
-        out.append((wr, experts, shared, len(sel)))
+            experts[e] = host_expert(li, e)
+        out.append((wr, experts, host_expert(li, 256), len(sel)))
     return xb, out
 
 
@@ -215,6 +226,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--tokens", type=int, default=8)
     ap.add_argument("--layers", type=int, default=16)
+    ap.add_argument("--wtype", choices=["nvfp4", "bf16"], default="nvfp4")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -224,10 +236,11 @@ def main():
     import torch
 
     world, rank, local = dist_setup()
-    T, L = args.tokens, args.layers
-    workload = (f"one NVFP4 MoE layer, T={T} tokens (H=2048, 256 routed experts I=512, sigmoid top-6, "
+    T, L, WT = args.tokens, args.layers, args.wtype
+    WTI = 0 if WT == "nvfp4" else 1
+    workload = (f"one {WT.upper()} MoE layer, T={T} tokens (H=2048, 256 routed experts I=512, sigmoid top-6, "
                 f"1 shared expert), synthetic seeded weights")
-    config = {"workload": workload, "tokens": T, "hidden": 2048, "experts": 256, "top_k": 6, "inter": 512,
+    config = {"workload": workload, "weights": WT, "tokens": T, "hidden": 2048, "experts": 256, "top_k": 6, "inter": 512,
               "layers_rotated": L,
               "l2": f"cold: steps rotate over {L} distinct resident layers (selected bytes per rotation >> L2)"}
 
@@ -241,14 +254,14 @@ def main():
 
         oracle.build()
         nl = min(L, 4)
-        lis = [synth.make_layer(s, T, device=dev) for s in range(nl)]
+        lis = [synth.make_layer(s, T, wtype=WTI, device=dev) for s in range(nl)]
         x = lis[0].x
         xb, hl = host_layers_for_oracle(lis, x, nl)
         for _ in range(args.warmup if args.warmup < 4 else 3):
             oracle.moe_forward(xb, hl[0][0], hl[0][1], 6, 512, hl[0][2])
         t_tot, b_tot, n_tot = 0.0, 0, 0
         for _ in range(args.steps if args.steps <= 20 else 20):
-            s, b, n, threads = oracle_sample(hl, xb, T, 0.0)
+            s, b, n, threads = oracle_sample(hl, xb, T, 0.0, WT)
             t_tot += s
             b_tot += b
             n_tot += n
@@ -265,7 +278,7 @@ def main():
 
     import nvfp4_moe_decode_gb300 as m
     from nvfp4_moe_decode_gb300 import synth
-    from nvfp4_moe_decode_gb300.layer import PackedLayer, new_workspace
+    from nvfp4_moe_decode_gb300.layer import Bf16Layer, PackedLayer, new_workspace
 
     m.load()
     dev = torch.device(f"cuda:{local}")
@@ -277,8 +290,8 @@ def main():
     x = synth.make_x(0, T, device=dev)
     with torch.cuda.stream(stream):
         for s in range(L):
-            li = synth.make_layer(s, T, device=dev)
-            pl = PackedLayer.from_inputs(li, stream)
+            li = synth.make_layer(s, T, wtype=WTI, device=dev)
+            pl = PackedLayer.from_inputs(li, stream) if WTI == 0 else Bf16Layer.from_inputs(li)
             lis.append(li)
             packed.append(pl)
     stream.synchronize()
@@ -317,7 +330,7 @@ def main():
         run_steps(0, W % L)
     stream.synchronize()
     rem_graph = capture(K % L) if K % L else None
-    steps_bytes = sum(layer_bytes(T, nd[k % L]) for k in range(K))
+    steps_bytes = sum(layer_bytes(T, nd[k % L], 1, WT) for k in range(K))
 
     clocks = ClockSampler(local)
     barrier(world)
@@ -359,18 +372,18 @@ def main():
             oh.copy_(out, non_blocking=True)
             stream.synchronize()
     e2e_s = time.perf_counter() - t0
-    e2e_bytes = sum(layer_bytes(T, nd[k % L]) for k in range(ne))
+    e2e_bytes = sum(layer_bytes(T, nd[k % L], 1, WT) for k in range(ne))
     e2e_v = reduce_sum(e2e_bytes, world) / reduce_max(e2e_s, world) / 1e9
 
     peak, peak_src = peaks()
     layer_alg = steps_bytes / K
     traffic = None
-    if kernel_sources_sha256() == NCU_TRAFFIC["sources_sha256"]:
+    if WT == "nvfp4" and kernel_sources_sha256() == NCU_TRAFFIC["sources_sha256"]:
         traffic = layer_alg * NCU_TRAFFIC["per_algorithmic_byte"]
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "nvfp4 weights x bf16 activations, f32 accumulate", "data": "synthetic",
+        "dtype": f"{WT} weights x bf16 activations, f32 accumulate", "data": "synthetic",
         "config": {**config, "us_per_layer": us_per_layer, "tokens_per_s": T * K / (ms_max * 1e-3),
                    "distinct_experts_per_layer": nd, "algorithmic_bytes_per_layer": layer_alg,
                    "hbm_frac": value / world / peak, "device_flag": flag},
@@ -389,7 +402,7 @@ def main():
 
         oracle.build()
         xb, hl = host_layers_for_oracle(lis, x, min(L, 4))
-        s, b, n, threads = oracle_sample(hl, xb, T, args.cpu_budget)
+        s, b, n, threads = oracle_sample(hl, xb, T, args.cpu_budget, WT)
         line["cpu_baseline"] = {"value": b / s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                                 "sample": f"{n} layer forwards (T={T}) of the fp64 C oracle over "
                                           f"{len(hl)} of the rotated layers, {s:.1f} s"}

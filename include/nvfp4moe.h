@@ -220,9 +220,14 @@ moe_status moe_route(const void *x, const void *router_w, int T, int n_experts, 
  *  out:      device bf16 [T][H].
  *  workspace: device, >= moe_workspace_bytes(T), initialised once with
  *            moe_workspace_init; one workspace per concurrently running call.
- * Both banks must be NVFP4 in this build (BF16 banks: MOE_ERR_UNSUPPORTED).
- * Activations must be finite with max|x[t]| < 2^114 per token: each token is
- * scaled by a power of two into f16 for the tensor cores (see csrc/common.cuh).
+ * Weight types: both banks NVFP4 (W4A16), or both BF16 (the W16A16 variant
+ * [FLINT, "From 1,096 kernels to 346": BF16 decode]: same routing, same
+ * combine, bf16 weights read row-major); a shared bank of the other type than
+ * the routed one gives MOE_ERR_UNSUPPORTED.
+ * Activations must be finite; with NVFP4 weights also max|x[t]| < 2^114 per
+ * token: each token is scaled by a power of two into f16 for the tensor cores
+ * (see csrc/common.cuh).  With BF16 weights the activations and h enter the
+ * tensor cores as bf16 unchanged.
  * Every SM must be able to host one CTA at the same time (the kernel's CTAs
  * wait on each other's counters, with bounded waits that set
  * MOE_FLAG_WAIT_TIMEOUT if that ever fails).

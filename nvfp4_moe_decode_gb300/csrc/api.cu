@@ -38,9 +38,11 @@ moe_status check_bank(const moe_expert_bank *b, int expect_n, bool allow_empty)
         return MOE_OK;
     if (b->n_experts != expect_n)
         return MOE_ERR_UNSUPPORTED;
-    if (b->wtype != MOE_W_NVFP4)
+    if (b->wtype != MOE_W_NVFP4 && b->wtype != MOE_W_BF16)
         return MOE_ERR_UNSUPPORTED;
-    if (!b->w13 || !b->w2 || !b->tscale13 || !b->tscale2)
+    if (!b->w13 || !b->w2)
+        return MOE_ERR_INVALID_ARG;
+    if (b->wtype == MOE_W_NVFP4 && (!b->tscale13 || !b->tscale2))
         return MOE_ERR_INVALID_ARG;
     if (!aligned16(b->w13) || !aligned16(b->w2))
         return MOE_ERR_INVALID_ARG;
@@ -194,6 +196,8 @@ moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expe
     if ((s = check_bank(shared, 1, true)) != MOE_OK)
         return s;
     const int n_shared = (shared && shared->n_experts > 0) ? 1 : 0;
+    if (n_shared && shared->wtype != routed->wtype)
+        return MOE_ERR_UNSUPPORTED;   // one weight type per layer
     const int nsm = sm_count();
     if (nsm <= 0)
         return MOE_ERR_CUDA;
@@ -215,6 +219,7 @@ moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expe
         la.s_ts2 = shared->tscale2;
     }
     la.n_shared = n_shared;
+    la.bf16w = routed->wtype == MOE_W_BF16 ? 1 : 0;
     la.ws = ws;
     la.out = static_cast<__nv_bfloat16 *>(out);
     // one CTA per SM; at least 128 for the router phase

@@ -57,6 +57,8 @@ constexpr size_t W13_BAND_BYTES = band_bytes(H);            // 18432
 constexpr size_t W2_BAND_BYTES = band_bytes(I);             // 4608
 constexpr size_t W13_BYTES = W13_BANDS * W13_BAND_BYTES;    // 1179648
 constexpr size_t W2_BYTES = W2_BANDS * W2_BAND_BYTES;       // 589824
+constexpr size_t W13_BYTES_BF = (size_t)2 * I * H * 2;     // 4194304: bf16 W13 of one expert
+constexpr size_t W2_BYTES_BF = (size_t)H * I * 2;          // 2097152: bf16 W2 of one expert
 
 constexpr int SC_BYTES = 1152;            // one 128-column super-chunk of a band
 constexpr int ACT_EXP = 14;               // activations scaled so max|v| is in [2^14, 2^15)

@@ -21,11 +21,12 @@ struct LayerArgs {
     const __nv_bfloat16 *x;        // [T][H]
     const __nv_bfloat16 *wr;       // [E][H]
     int T;
-    const uint8_t *r_w13, *r_w2;   // routed bank (packed NVFP4)
-    const float *r_ts13, *r_ts2;
-    const uint8_t *s_w13, *s_w2;   // shared expert (packed NVFP4), if n_shared
-    const float *s_ts13, *s_ts2;
+    const uint8_t *r_w13, *r_w2;   // routed bank (packed NVFP4, or bf16 row-major if bf16w)
+    const float *r_ts13, *r_ts2;   // NVFP4 only
+    const uint8_t *s_w13, *s_w2;   // shared expert (same weight type), if n_shared
+    const float *s_ts13, *s_ts2;   // NVFP4 only
     int n_shared;
+    int bf16w;                     // 1: both banks hold bf16 weights
     uint8_t *ws;
     __nv_bfloat16 *out;            // [T][H]
 };

@@ -21,9 +21,12 @@
 //     its per-token routing weight;
 //  4. units are dealt round-robin to the 4 x #CTA groups (group id
 //     grp * #CTA + cta; a group takes ids gid, gid + G, gid + 2G, ...):
-//       gate/up unit (slot, band): the 4 warps take one K quarter each of a
-//         16-row band of W13 (8 gate + 8 up rows); SiLU*up -> h (bf16) and a
-//         per-(slot, token) running max of |h|;
+//       gate/up unit, NVFP4 weights (slot, 4 bands): each warp streams one
+//         whole 16-row band of W13 (8 gate + 8 up rows); SiLU*up -> h (bf16)
+//         and a per-(slot, token) running max of |h|;
+//       gate/up unit, BF16 weights (slot, band): the 4 warps take one K
+//         quarter each of the band; warp 0 adds the four partials in warp
+//         order and applies SiLU*up;
 //       down unit (slot, 4 bands): once the slot's 64 gate/up bands are done,
 //         the slot's h arrives by bulk copy and is rescaled in place to f16
 //         fragments; each warp computes one 16-row band of W2 h, times the
@@ -36,9 +39,12 @@
 //     warp waits on anything;
 //  5. the last down partial of each band adds all partials in slot order
 //     (deterministic) and writes out (bf16).
-// Every warp streams its units' weights through a private 3-stage ring of
-// shared-memory buffers filled by cp.async.bulk; every wait is bounded and
-// reports MOE_FLAG_WAIT_TIMEOUT instead of hanging.
+// NVFP4: every warp streams its units' weights through a private 3-stage ring
+// of shared-memory buffers filled by cp.async.bulk and decodes them in
+// registers.  BF16 (the W16A16 variant of the Flint page, section "From 1,096
+// kernels to 346": BF16 decode): the rows are row-major in HBM, and each warp
+// loads its 16 rows straight into registers, four 64-column chunks ahead.
+// Every wait is bounded and reports MOE_FLAG_WAIT_TIMEOUT instead of hanging.
 #include "kernels.cuh"
 #include "topk.cuh"
 
@@ -56,13 +62,14 @@ constexpr int ROUTER_CTAS = E / 2;     // 128 CTAs x 2 experts
 constexpr int HROW = I * 2 + 16;       // padded bytes of one token's h row in shared memory
 constexpr int HBUF = MAXT * HROW;      // one slot's h, 8.1 KB at T = 8
 constexpr uint32_t SLOT_DONE = W13_BANDS; // gate/up bands that complete a slot
-constexpr int GU_UNITS = W13_BANDS / GW;  // 16 gate/up units of 4 bands per slot
+constexpr int GU_UNITS = W13_BANDS / GW;  // NVFP4: 16 gate/up units of 4 bands per slot
+constexpr int GU_UNITS_BF = W13_BANDS;    // BF16: 64 gate/up units of one band per slot
 constexpr int DN_UNITS = W2_BANDS / GW;   // 32 down units of 4 bands per slot
 constexpr int GU_PARTS = (H / 128) / 2;   // 8 stages per W13 band
 constexpr int DN_PARTS = (I / 128) / 2;   // 2 stages per W2 band
 
 struct FSmem {
-    uint8_t ring[FW][RING][STG];
+    uint8_t ring[FW][RING][STG];       // BF16 weights: the K-split partials (BfRed) instead
     uint2 xfrag[(H / 16) * 32];        // compact: entry (step, l) at step * 4T + l
     uint8_t hbuf[NG][2][HBUF];         // raw h rows, rescaled in place into fragments;
                                        // before the unit loop: x (T x 4 KB)
@@ -144,6 +151,80 @@ __device__ __forceinline__ void decode4(uint32_t w, uint32_t &a0, uint32_t &a1, 
         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(w));
 }
 
+// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32.
+__device__ __forceinline__ void mma_bf16_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// BF16 rows are consumed in a k order chosen so that each lane's A registers
+// come from two coalesced 16-byte loads per row and 64-column chunk: lane
+// (g, c) loads columns 8c..8c+7 and 32+8c..32+8c+7 of rows g and g+8, and k16
+// step s of the chunk pairs its words 2s, 2s+1 with the activation columns
+// 32*(s/2) + 8c + 4*(s%2) + 0..3 (a permutation of the chunk's 64 columns,
+// applied to both operands, so the dot products are unchanged).
+__host__ __device__ __forceinline__ int bf16_bcol(int step, int c)
+{
+    const int s = step & 3;
+    return 64 * (step >> 2) + 32 * (s >> 1) + 8 * c + 4 * (s & 1);
+}
+
+constexpr int BF_DEPTH = 4;            // 64-column chunks in flight per warp
+
+// acc += rows (ra: band rows 0..7, rb: 8..15) x activations over `nch`
+// 64-column chunks starting at column 64*chunk0 (B fragments of the
+// permuted order, k16 steps from 4*chunk0).
+template <int NCH>
+__device__ __forceinline__ void bf16_rows(const __nv_bfloat16 *ra, const __nv_bfloat16 *rb, int chunk0,
+                                          const uint2 *bfrag, int blanes, int lane, float acc[4])
+{
+    static_assert(NCH % BF_DEPTH == 0, "chunks per unit");
+    const int c = lane & 3;
+    uint4 buf[BF_DEPTH][4];
+    auto load = [&](uint4 *dst, int j) {
+        const int col = 64 * (chunk0 + j) + 8 * c;
+        dst[0] = ldg_stream(ra + col);
+        dst[1] = ldg_stream(ra + col + 32);
+        dst[2] = ldg_stream(rb + col);
+        dst[3] = ldg_stream(rb + col + 32);
+    };
+#pragma unroll
+    for (int d = 0; d < BF_DEPTH; ++d)
+        load(buf[d], d);
+#pragma unroll 1
+    for (int j0 = 0; j0 < NCH; j0 += BF_DEPTH) {
+#pragma unroll
+        for (int d = 0; d < BF_DEPTH; ++d) {
+            const int j = j0 + d;
+            const uint32_t wa[8] = {buf[d][0].x, buf[d][0].y, buf[d][0].z, buf[d][0].w,
+                                    buf[d][1].x, buf[d][1].y, buf[d][1].z, buf[d][1].w};
+            const uint32_t wb[8] = {buf[d][2].x, buf[d][2].y, buf[d][2].z, buf[d][2].w,
+                                    buf[d][3].x, buf[d][3].y, buf[d][3].z, buf[d][3].w};
+            if (j + BF_DEPTH < NCH)
+                load(buf[d], j + BF_DEPTH);
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const int step = 4 * (chunk0 + j) + s;
+                const uint2 b = (lane < blanes) ? bfrag[step * blanes + lane] : make_uint2(0u, 0u);
+                mma_bf16_16816(acc, wa[2 * s], wb[2 * s], wa[2 * s + 1], wb[2 * s + 1], b.x, b.y);
+            }
+        }
+    }
+}
+
 // Two consecutive super-chunks of one band (one stage) times the B fragments
 // from k16 step `step0`; blanes = 4T lanes carry tokens.
 __device__ __forceinline__ void mma_stage(const uint8_t *stage, const uint2 *bfrag, int blanes, int step0,
@@ -177,6 +258,12 @@ __device__ __forceinline__ void mma_stage(const uint8_t *stage, const uint2 *bfr
     }
 }
 
+// BF16 gate/up: partial accumulators of warps 1..3 of each group, double
+// buffered by unit parity (placed in the otherwise unused stage ring).
+struct BfRed {
+    float4 p[NG][2][GW - 1][32];
+};
+
 struct Unit {
     bool down;   // down unit (else gate/up)
     int slot;
@@ -185,8 +272,10 @@ struct Unit {
 
 }  // namespace
 
+template <bool BW>
 __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
 {
+    static_assert(sizeof(BfRed) <= sizeof(FSmem::ring), "K-split partials fit the ring");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     FSmem &sm = *reinterpret_cast<FSmem *>(smem_raw);
 
@@ -230,6 +319,17 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
                                                   : a.r_w2 + (size_t)sm.slot_expert[slot] * W2_BYTES;
         return base + (size_t)band * W2_BAND_BYTES;
     };
+    // BF16 banks: W13 [2I][H] and W2 [H][I] row-major per expert
+    auto bf_w13 = [&](int slot) -> const __nv_bfloat16 * {
+        const uint8_t *base = (slot < a.n_shared) ? a.s_w13 + (size_t)slot * W13_BYTES_BF
+                                                  : a.r_w13 + (size_t)sm.slot_expert[slot] * W13_BYTES_BF;
+        return reinterpret_cast<const __nv_bfloat16 *>(base);
+    };
+    auto bf_w2 = [&](int slot) -> const __nv_bfloat16 * {
+        const uint8_t *base = (slot < a.n_shared) ? a.s_w2 + (size_t)slot * W2_BYTES_BF
+                                                  : a.r_w2 + (size_t)sm.slot_expert[slot] * W2_BYTES_BF;
+        return reinterpret_cast<const __nv_bfloat16 *>(base);
+    };
     // one stage = two super-chunks (2304 bytes) of this warp's band: part p
     auto issue_stage = [&](int ring_slot, const Unit &u, int p) {
         if (lane != 0)
@@ -245,7 +345,7 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
     // shared expert's 16 gate/up units (ids 0..15) go to group 0 of CTAs 0..15
     const int n_groups = NG * (int)gridDim.x;
     const int gid = grp * (int)gridDim.x + (int)blockIdx.x;
-    const bool static_shared = (a.n_shared > 0) && gid < GU_UNITS;
+    const bool static_shared = !BW && (a.n_shared > 0) && gid < GU_UNITS;
     if (static_shared) {
         const Unit u0{false, 0, 4 * gid + wq};
         for (int p = 0; p < RING; ++p)
@@ -312,6 +412,15 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
         named_barrier_sync(5, 256);
         if (warp == 8 && lane == 0)
             red_release_add(&ctrl[2], 1u);   // publishes this CTA's logits
+    } else if (warp < 8 && BW) {
+        // BF16 weights: the activations enter the tensor cores as bf16, in
+        // the permuted column order of bf16_rows
+        const uint32_t *xw = reinterpret_cast<const uint32_t *>(xs);
+        for (int idx = threadIdx.x; idx < (H / 16) * blanes; idx += 256) {
+            const int step = idx / blanes, l = idx % blanes, n = l >> 2, c = l & 3;
+            const int w0 = (n * H + bf16_bcol(step, c)) / 2;
+            sm.xfrag[idx] = make_uint2(xw[w0], xw[w0 + 1]);
+        }
     } else if (warp < 8) {
         if (warp < T) {
             const uint4 *row = reinterpret_cast<const uint4 *>(xsh + (size_t)warp * H);
@@ -428,12 +537,13 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
     }
 
     // ---- phase 4: the units ----
-    const int gu_total = n_slots * GU_UNITS;                        // unit ids [0, gu_total): gate/up
+    constexpr int GUU = BW ? GU_UNITS_BF : GU_UNITS;
+    const int gu_total = n_slots * GUU;                             // unit ids [0, gu_total): gate/up
     const int end_id = gu_total + n_slots * DN_UNITS;               // then down units
     auto unit_id = [&](int k) { return gid + k * n_groups; };
     auto decode = [&](int id) -> Unit {
         if (id < gu_total)
-            return Unit{false, id / GU_UNITS, 4 * (id % GU_UNITS) + wq};
+            return BW ? Unit{false, id / GUU, id % GUU} : Unit{false, id / GUU, 4 * (id % GUU) + wq};
         const int d = id - gu_total;
         return Unit{true, d / DN_UNITS, 4 * (d % DN_UNITS) + wq};
     };
@@ -446,7 +556,7 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
 #pragma unroll
         for (int t = 0; t < MAXT; ++t)
             if (t < T)
-                sm.hshift[grp][b][t] = act_shift(__uint_as_float(__ldcg(&hmax[slot * MAXT + t])));
+                sm.hshift[grp][b][t] = BW ? 0 : act_shift(__uint_as_float(__ldcg(&hmax[slot * MAXT + t])));
         fence_proxy_async_global();   // h was published to the generic proxy by releases
         uint64_t *bar = &sm.hbar[grp][b];
         mbar_arrive_expect_tx(bar, (uint32_t)(T * I * 2));
@@ -474,7 +584,8 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             }
         }
     };
-    issue_ahead(RING);
+    if (!BW)
+        issue_ahead(RING);
 
     // ---- leader: h of the group's down units, issued as their slots complete ----
     int h_next = 0;                  // next down unit whose h is not yet requested
@@ -585,9 +696,15 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
                 src0[j] = src1[j] = 0u;
                 if (e < nent) {
                     const int step = e / blanes, l = e % blanes, g = l >> 2, c = l & 3;
-                    const int w0 = (g * HROW) / 4 + 8 * step + c;
-                    src0[j] = hw[w0];
-                    src1[j] = hw[w0 + 4];
+                    if (BW) {
+                        const int w0 = (g * HROW) / 4 + bf16_bcol(step, c) / 2;
+                        src0[j] = hw[w0];
+                        src1[j] = hw[w0 + 1];
+                    } else {
+                        const int w0 = (g * HROW) / 4 + 8 * step + c;
+                        src0[j] = hw[w0];
+                        src1[j] = hw[w0 + 4];
+                    }
                 }
             }
             named_barrier_sync(1 + grp, GW * 32);
@@ -596,8 +713,12 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             for (int j = 0; j < 8; ++j) {
                 const int e = (wq * 32 + lane) + j * (GW * 32);
                 if (e < nent) {
-                    const float p = pow2i(sm.hshift[grp][b][(e % blanes) >> 2]);
-                    hf[e] = make_uint2(bf16x2_to_f16x2_scaled(src0[j], p), bf16x2_to_f16x2_scaled(src1[j], p));
+                    if (BW) {
+                        hf[e] = make_uint2(src0[j], src1[j]);
+                    } else {
+                        const float p = pow2i(sm.hshift[grp][b][(e % blanes) >> 2]);
+                        hf[e] = make_uint2(bf16x2_to_f16x2_scaled(src0[j], p), bf16x2_to_f16x2_scaled(src1[j], p));
+                    }
                 }
             }
             named_barrier_sync(1 + grp, GW * 32);
@@ -605,20 +726,57 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
         }
 
         acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-        const int np = nparts(u);
-        for (int p = 0; p < np; ++p) {
-            const int rs = ccount % RING;
-            mbar_wait_bounded(&sm.full[warp][rs], (ccount / RING) & 1, flag);
-            mma_stage(sm.ring[warp][rs], bfrag, blanes, 16 * p, lane, acc);
-            __syncwarp();
-            ++ccount;
-            issue_ahead(ccount + RING);
+        if (BW) {
+            const int g = lane >> 2;
+            if (!u.down) {
+                // rows: gate 8*band + g, up I + 8*band + g; K quarter wq
+                const __nv_bfloat16 *w = bf_w13(u.slot);
+                bf16_rows<H / 64 / GW>(w + (size_t)(8 * u.band + g) * H, w + (size_t)(I + 8 * u.band + g) * H,
+                                       (H / 64 / GW) * wq, bfrag, blanes, lane, acc);
+            } else {
+                const __nv_bfloat16 *w = bf_w2(u.slot);
+                bf16_rows<I / 64>(w + (size_t)(16 * u.band + g) * I, w + (size_t)(16 * u.band + g + 8) * I,
+                                  0, bfrag, blanes, lane, acc);
+            }
+        } else {
+            const int np = nparts(u);
+            for (int p = 0; p < np; ++p) {
+                const int rs = ccount % RING;
+                mbar_wait_bounded(&sm.full[warp][rs], (ccount / RING) & 1, flag);
+                mma_stage(sm.ring[warp][rs], bfrag, blanes, 16 * p, lane, acc);
+                __syncwarp();
+                ++ccount;
+                issue_ahead(ccount + RING);
+            }
         }
 
         post_signals();    // the previous unit's stores have landed by now
 
         const int g = lane >> 2, c = lane & 3;
-        if (!u.down) {
+        if (!u.down && BW) {
+            // the four K quarters of the band, added in warp order by warp 0
+            BfRed &red = *reinterpret_cast<BfRed *>(&sm.ring[0][0][0]);
+            if (wq > 0)
+                red.p[grp][k & 1][wq - 1][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            named_barrier_sync(1 + grp, GW * 32);
+            if (wq == 0) {
+#pragma unroll
+                for (int q = 0; q < GW - 1; ++q) {
+                    const float4 v = red.p[grp][k & 1][q][lane];
+                    acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
+                }
+#pragma unroll
+                for (int tt = 0; tt < 2; ++tt) {
+                    const int t = 2 * c + tt;
+                    if (t < T) {
+                        const float gv = acc[tt], uv = acc[2 + tt];
+                        hglob[((size_t)u.slot * MAXT + t) * I + u.band * 8 + g] =
+                            __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
+                    }
+                }
+                pend_slot = u.slot;
+            }
+        } else if (!u.down) {
             // SiLU*up for h rows 8 * band + g; running max of |h|
             const float ts = (u.slot < a.n_shared) ? __ldg(a.s_ts13 + u.slot)
                                                    : __ldg(a.r_ts13 + sm.slot_expert[u.slot]);
@@ -649,8 +807,9 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             pend_slot = u.slot;
         } else {
             // down: one band per warp, x routing weight x tensor scale x 2^-shift
-            const float ts = (u.slot < a.n_shared) ? __ldg(a.s_ts2 + u.slot)
-                                                   : __ldg(a.r_ts2 + sm.slot_expert[u.slot]);
+            const float ts = BW ? 1.0f
+                                : (u.slot < a.n_shared) ? __ldg(a.s_ts2 + u.slot)
+                                                        : __ldg(a.r_ts2 + sm.slot_expert[u.slot]);
             float *P = partials + ((size_t)u.slot * H + 16 * u.band) * MAXT;
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt) {
@@ -697,8 +856,11 @@ cudaError_t launch_layer(const LayerArgs &a, int grid, cudaStream_t stream, bool
     if (e != cudaSuccess)
         return e;
     if (dev >= 0 && dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(moe_layer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(moe_layer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)sizeof(FSmem));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(moe_layer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)sizeof(FSmem));
         if (e != cudaSuccess)
             return e;
         configured[dev] = 1;
@@ -713,7 +875,8 @@ cudaError_t launch_layer(const LayerArgs &a, int grid, cudaStream_t stream, bool
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, moe_layer_kernel, a);
+    return a.bf16w ? cudaLaunchKernelEx(&cfg, moe_layer_kernel<true>, a)
+                   : cudaLaunchKernelEx(&cfg, moe_layer_kernel<false>, a);
 }
 
 }  // namespace moe

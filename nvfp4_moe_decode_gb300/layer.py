@@ -11,7 +11,7 @@ from typing import Optional
 
 import torch
 
-from . import (HIDDEN, INTER, MOE_PACK_GATE_UP, MOE_PACK_PLAIN, MOE_W_NVFP4, make_bank,
+from . import (HIDDEN, INTER, MOE_PACK_GATE_UP, MOE_PACK_PLAIN, MOE_W_BF16, MOE_W_NVFP4, make_bank,
                moe_layer_forward, moe_pack_nvfp4, moe_packed_bytes, moe_workspace_bytes,
                moe_workspace_init)
 
@@ -50,6 +50,37 @@ class PackedLayer:
 
     def bytes_resident(self) -> int:
         return self.w13.numel() + self.w2.numel() + self.router_w.numel() * 2
+
+    def forward(self, x: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor, stream=None):
+        moe_layer_forward(x, self.router_w, self.routed, self.shared, out, x.shape[0], workspace, stream)
+
+
+class Bf16Layer:
+    """BF16 weights of one MoE layer (the W16A16 variant): the banks point at the
+    row-major bf16 tensors themselves (W13 [E+S, 2I, H], W2 [E+S, H, I]); no
+    packing."""
+
+    def __init__(self, router_w: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor, n_routed: int,
+                 n_shared: int):
+        H, I = HIDDEN, INTER
+        n = n_routed + n_shared
+        assert w13.dtype == torch.bfloat16 and tuple(w13.shape) == (n, 2 * I, H)
+        assert w2.dtype == torch.bfloat16 and tuple(w2.shape) == (n, H, I)
+        self.router_w = router_w.contiguous()
+        self.w13 = w13.contiguous()
+        self.w2 = w2.contiguous()
+        self.n_routed, self.n_shared = n_routed, n_shared
+        self.routed = make_bank(MOE_W_BF16, n_routed, self.w13, self.w2)
+        self.shared = None
+        if n_shared:
+            self.shared = make_bank(MOE_W_BF16, 1, self.w13[n_routed], self.w2[n_routed])
+
+    @classmethod
+    def from_inputs(cls, li) -> "Bf16Layer":
+        return cls(li.router_w, li.w13, li.w2, li.n_routed, li.n_shared)
+
+    def bytes_resident(self) -> int:
+        return (self.w13.numel() + self.w2.numel() + self.router_w.numel()) * 2
 
     def forward(self, x: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor, stream=None):
         moe_layer_forward(x, self.router_w, self.routed, self.shared, out, x.shape[0], workspace, stream)

@@ -87,6 +87,12 @@ def test_host_argument_errors_enqueue_nothing(moe_lib):
     assert fwd(dummy, dummy, B(bad_w), None, dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_UNSUPPORTED
     assert fwd(dummy, dummy, B(null_w), None, dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_INVALID_ARG
     assert fwd(dummy, dummy, None, None, dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_INVALID_ARG
+    # one weight type per layer: a BF16 routed bank with an NVFP4 shared expert
+    bf = m.moe_expert_bank(m.MOE_W_BF16, 256, dummy, dummy, None, None)
+    sh4 = m.moe_expert_bank(m.MOE_W_NVFP4, 1, dummy, dummy, dummy, dummy)
+    assert fwd(dummy, dummy, B(bf), B(sh4), dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_UNSUPPORTED
+    bf_null = m.moe_expert_bank(m.MOE_W_BF16, 256, dummy, None, None, None)
+    assert fwd(dummy, dummy, B(bf_null), None, dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_INVALID_ARG
     assert lib.moe_workspace_init(None, ws, None) == m.MOE_ERR_INVALID_ARG
     assert lib.moe_workspace_init(dummy, 8, None) == m.MOE_ERR_WORKSPACE
     assert lib.moe_read_device_flag(None, None, None) == m.MOE_ERR_INVALID_ARG
