@@ -8,7 +8,11 @@ steps over L distinct resident layers (the selected-expert bytes of one
 rotation are far larger than the 126 MB L2): step k runs layer k mod L.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--tokens T] [--layers L]
+                    [--tokens T] [--layers L] [--wtype nvfp4|bf16] [--stack NL]
+
+--stack NL measures a pre-norm decoder stack of NL resident layers instead
+(x <- x + MoE_l(RMSNorm(x)), one moe_stack_forward per step; the stack is far
+larger than L2, so it runs cold without rotation).
 
 Prints one JSON line (rank 0).  value = algorithmic bytes of all steps / time
 (GB/s); the bytes of a step are the router weights + the selected and shared
@@ -227,6 +231,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=8)
     ap.add_argument("--layers", type=int, default=16)
     ap.add_argument("--wtype", choices=["nvfp4", "bf16"], default="nvfp4")
+    ap.add_argument("--stack", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -281,6 +286,8 @@ def main():
     from nvfp4_moe_decode_gb300.layer import Bf16Layer, PackedLayer, new_workspace
 
     m.load()
+    if args.stack:
+        return run_stack(args, world, rank, local)
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
@@ -406,6 +413,130 @@ def main():
         line["cpu_baseline"] = {"value": b / s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                                 "sample": f"{n} layer forwards (T={T}) of the fp64 C oracle over "
                                           f"{len(hl)} of the rotated layers, {s:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def run_stack(args, world: int, rank: int, local: int):
+    """A pre-norm stack of args.stack layers (seeds 0..NL-1), T tokens."""
+    import torch
+
+    import nvfp4_moe_decode_gb300 as m
+    from nvfp4_moe_decode_gb300 import synth
+    from nvfp4_moe_decode_gb300.layer import Bf16Layer, PackedLayer, Stack, new_stack_workspace, new_workspace
+
+    T, NL, WT = args.tokens, args.stack, args.wtype
+    WTI = 0 if WT == "nvfp4" else 1
+    eps = 1e-6
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    layers = []
+    with torch.cuda.stream(stream):
+        for s in range(NL):
+            li = synth.make_layer(s, T, wtype=WTI, device=dev)
+            layers.append(PackedLayer.from_inputs(li, stream) if WTI == 0 else Bf16Layer.from_inputs(li))
+            del li
+    stream.synchronize()
+    x0 = synth.make_x(0, T, device=dev)
+    # distinct experts per layer: the stack layer by layer, routing each
+    # layer's own normalised input (outside the timed region)
+    nd = []
+    wsl = new_workspace(T, dev, stream)
+    with torch.cuda.stream(stream):
+        resid, delta = x0.clone(), None
+        idx = torch.empty(T, 6, dtype=torch.int32, device=dev)
+        w = torch.empty(T, 6, dtype=torch.float32, device=dev)
+        for lay in layers:
+            out = torch.empty(T, 2048, dtype=torch.bfloat16, device=dev)
+            v, xn = torch.empty_like(out), torch.empty_like(out)
+            m.moe_layer_forward_prenorm(resid, delta, v, xn, eps, lay.router_w, lay.routed, lay.shared, out, T,
+                                        wsl, stream)
+            m.moe_route(xn, lay.router_w, T, idx, w, None, wsl, stream)
+            stream.synchronize()
+            nd.append(len(set(idx.cpu().reshape(-1).tolist())))
+            resid, delta = v, out
+    st = Stack(layers, eps)
+    ws = new_stack_workspace(T, dev, stream)
+    x = x0.clone()
+    # per layer: the layer's weights + x and out, plus the residual stream
+    # (delta read, residual written); the final add reads two and writes one
+    step_bytes = sum(layer_bytes(T, n, 1, WT) + 2 * T * 2048 * 2 for n in nd) + 3 * T * 2048 * 2
+
+    def step():
+        x.copy_(x0)
+        st.forward(x, ws, stream)
+
+    K, W = args.steps, args.warmup
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            step()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.2)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    clk = clocks.stop()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms_max = reduce_max(e0.elapsed_time(e1), world)
+    value = reduce_sum(float(step_bytes * K), world) / (ms_max * 1e-3) / 1e9
+    us_stack = 1e3 * ms_max / K
+    flag = m.moe_read_device_flag(ws, stream)
+
+    xh = x0.cpu().pin_memory()
+    oh = torch.empty(T, 2048, dtype=torch.bfloat16).pin_memory()
+    ne = max(3, min(args.e2e_steps, K))
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(ne):
+            x.copy_(xh, non_blocking=True)
+            st.forward(x, ws, stream)
+            oh.copy_(x, non_blocking=True)
+            stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_v = reduce_sum(float(step_bytes * ne), world) / reduce_max(e2e_s, world) / 1e9
+
+    peak, peak_src = peaks()
+    workload = (f"{NL}-layer pre-norm stack of {WT.upper()} MoE layers, T={T} tokens (H=2048, 256 routed experts "
+                f"I=512, sigmoid top-6, 1 shared expert), synthetic seeded weights")
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": f"{WT} weights x bf16 activations, f32 accumulate", "data": "synthetic",
+        "config": {"workload": workload, "weights": WT, "tokens": T, "layers": NL, "hidden": 2048,
+                   "experts": 256, "top_k": 6, "inter": 512,
+                   "l2": "cold: the stack's selected weights far exceed L2",
+                   "us_per_stack": us_stack, "us_per_layer": us_stack / NL,
+                   "tokens_per_s": T / (us_stack * 1e-6), "distinct_experts_per_layer": nd,
+                   "algorithmic_bytes_per_step": step_bytes, "hbm_frac": value / world / peak,
+                   "resident_weight_bytes": sum(l.bytes_resident() for l in layers), "device_flag": flag},
+        "roofline": {"bound": "hbm", "achieved": step_bytes / (us_stack * 1e-6) / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": step_bytes / (us_stack * 1e-6) / 1e9 / peak, "traffic": None,
+                     "peak_source": peak_src,
+                     "kernel": "moe_layer_kernel x NL (pre-norm residual fused) + residual_add_kernel"},
+        "e2e": {"value": e2e_v, "unit": "GB/s", "steps": ne, "h2d_bytes_per_step": T * 2048 * 2,
+                "d2h_bytes_per_step": T * 2048 * 2},
+        "gpu_launches": K * (NL + 1),
+        "clocks": clk,
+    }
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

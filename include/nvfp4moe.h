@@ -237,6 +237,63 @@ moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expe
                              size_t workspace_bytes, moe_stream_t stream);
 
 /* ----------------------------------------------------------------------- */
+/* Decoder stacks.  [FLINT, "A 40B MoE that activates 2.5B parameters": a  */
+/* 47-layer pre-norm decoder.]  The pages give only "pre-norm"; this       */
+/* library reads a layer of the stack as x <- x + MoE(RMSNorm(x)) with a   */
+/* unit-weight RMSNorm, the residual stream kept in bf16.                   */
+/* ----------------------------------------------------------------------- */
+
+/* The weights of one layer of a stack (host struct; device pointers).  A
+ * shared bank with n_experts == 0 means no shared expert. */
+typedef struct {
+    const void *router_w;          /* device bf16 [E][H] */
+    moe_expert_bank routed;
+    moe_expert_bank shared;
+} moe_layer_weights;
+
+/*
+ * One pre-norm layer: v = bf16(resid + delta) (v = resid when delta is
+ * NULL), xn = bf16(v / sqrt(mean_k(v_k^2) + eps)) per token (fp32 sum of
+ * squares in a fixed order, IEEE sqrt and divide), out = MoE(xn) exactly as
+ * moe_layer_forward computes it from xn.  The add and the norm run inside
+ * the layer kernel (every CTA forms xn from resid and delta in shared
+ * memory); no extra launch.
+ *  resid, delta: device bf16 [T][H] (delta may be NULL).
+ *  resid_out:    device bf16 [T][H] receiving v, or NULL.
+ *  xn_out:       device bf16 [T][H] receiving xn, or NULL.
+ *  eps:          0 <= eps < 1.
+ *  The other arguments are those of moe_layer_forward.
+ *  out must not overlap resid, delta, resid_out or xn_out; resid_out and
+ *  xn_out must not overlap any other buffer (MOE_ERR_INVALID_ARG).
+ */
+moe_status moe_layer_forward_prenorm(const void *resid, const void *delta, void *resid_out, void *xn_out,
+                                     float eps, const void *router_w, const moe_expert_bank *routed,
+                                     const moe_expert_bank *shared, void *out, int T, void *workspace,
+                                     size_t workspace_bytes, moe_stream_t stream);
+
+/* Workspace bytes of moe_stack_forward with T tokens (0 if unsupported):
+ * a layer workspace plus four bf16 [T][H] buffers. */
+size_t moe_stack_workspace_bytes(int T);
+
+/*
+ * x <- layer_{n-1}(... layer_0(x)) with layer_l(x) = x + MoE_l(RMSNorm(x)),
+ * each layer as moe_layer_forward_prenorm; n_layers + 1 launches chained by
+ * programmatic dependent launch (each layer kernel also adds the previous
+ * layer's output to the residual stream; a last small kernel adds the final
+ * layer's output into x).
+ *  x:         device bf16 [T][H], input x_0, overwritten by x_n.
+ *  layers:    host array [n_layers] (n_layers >= 1); every layer is checked
+ *             before anything is launched.
+ *  workspace: device, >= moe_stack_workspace_bytes(T), initialised with
+ *             moe_workspace_init (its first moe_workspace_bytes(T) bytes are
+ *             the layers' shared workspace; the device flag lives there).
+ * Errors: as moe_layer_forward_prenorm, for the first failing layer; nothing
+ * is enqueued on a host-side error.
+ */
+moe_status moe_stack_forward(void *x, const moe_layer_weights *layers, int n_layers, int T, float eps,
+                             void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* ----------------------------------------------------------------------- */
 /* The layer without a caller-provided workspace.  The pages describe no   */
 /* such entry point; it exists for callers that cannot allocate.           */
 /* ----------------------------------------------------------------------- */

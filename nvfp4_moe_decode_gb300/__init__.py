@@ -45,6 +45,7 @@ EXPORTS = (
     "moe_abi_version", "moe_status_string", "moe_packed_bytes", "moe_pack_nvfp4",
     "moe_unpack_nvfp4", "moe_dequant_nvfp4", "moe_workspace_bytes", "moe_workspace_init",
     "moe_read_device_flag", "moe_route", "moe_layer_forward", "moe_layer_forward_static",
+    "moe_layer_forward_prenorm", "moe_stack_workspace_bytes", "moe_stack_forward",
 )
 
 MOE_STATIC_SCRATCH_BYTES = 3_625_984
@@ -65,6 +66,14 @@ class moe_expert_bank(ctypes.Structure):
         ("w2", ctypes.c_void_p),
         ("tscale13", ctypes.c_void_p),
         ("tscale2", ctypes.c_void_p),
+    ]
+
+
+class moe_layer_weights(ctypes.Structure):
+    _fields_ = [
+        ("router_w", ctypes.c_void_p),
+        ("routed", moe_expert_bank),
+        ("shared", moe_expert_bank),
     ]
 
 
@@ -98,6 +107,14 @@ def _declare(lib):
     lib.moe_layer_forward.restype = i32
     lib.moe_layer_forward_static.argtypes = [vp, vp, bank_p, bank_p, vp, i32, vp]
     lib.moe_layer_forward_static.restype = i32
+    lib.moe_layer_forward_prenorm.argtypes = [vp, vp, vp, vp, ctypes.c_float, vp, bank_p, bank_p, vp, i32, vp,
+                                              sz, vp]
+    lib.moe_layer_forward_prenorm.restype = i32
+    lib.moe_stack_workspace_bytes.argtypes = [i32]
+    lib.moe_stack_workspace_bytes.restype = sz
+    lib.moe_stack_forward.argtypes = [vp, ctypes.POINTER(moe_layer_weights), i32, i32, ctypes.c_float, vp, sz,
+                                      vp]
+    lib.moe_stack_forward.restype = i32
     return lib
 
 
@@ -219,3 +236,38 @@ def moe_layer_forward_static(x, router_w, routed: moe_expert_bank, shared: Optio
                                       ctypes.byref(shared) if shared is not None else None, _ptr(out),
                                       int(T), _stream(stream))
     _check("moe_layer_forward_static", st)
+
+
+def moe_layer_forward_prenorm(resid, delta, resid_out, xn_out, eps: float, router_w, routed: moe_expert_bank,
+                              shared: Optional[moe_expert_bank], out, T: int, workspace, stream=None):
+    lib = load()
+    st = lib.moe_layer_forward_prenorm(_ptr(resid), _ptr(delta), _ptr(resid_out), _ptr(xn_out), float(eps),
+                                       _ptr(router_w), ctypes.byref(routed),
+                                       ctypes.byref(shared) if shared is not None else None, _ptr(out), int(T),
+                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream))
+    _check("moe_layer_forward_prenorm", st)
+
+
+def moe_stack_workspace_bytes(T: int) -> int:
+    return load().moe_stack_workspace_bytes(int(T))
+
+
+def layer_weights_array(layers) -> "ctypes.Array":
+    """A host moe_layer_weights[n] for objects with router_w, routed, shared."""
+    arr = (moe_layer_weights * len(layers))()
+    for i, l in enumerate(layers):
+        arr[i].router_w = _ptr(l.router_w)
+        arr[i].routed = l.routed
+        if l.shared is not None:
+            arr[i].shared = l.shared
+        else:
+            arr[i].shared = moe_expert_bank(int(l.routed.wtype), 0, None, None, None, None)
+    return arr
+
+
+def moe_stack_forward(x, layers_arr, n_layers: int, T: int, eps: float, workspace, stream=None):
+    lib = load()
+    st = lib.moe_stack_forward(_ptr(x), layers_arr, int(n_layers), int(T), float(eps), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("moe_stack_forward", st)

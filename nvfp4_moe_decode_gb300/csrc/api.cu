@@ -182,30 +182,28 @@ moe_status moe_route(const void *x, const void *router_w, int T, int n_experts, 
     return cuda_status(launch_router(a, (cudaStream_t)stream, true));
 }
 
-moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expert_bank *routed,
-                             const moe_expert_bank *shared, void *out, int T, void *workspace,
-                             size_t workspace_bytes, moe_stream_t stream)
+// Host checks of one layer's weights (nothing is launched).
+static moe_status check_layer_weights(const void *router_w, const moe_expert_bank *routed,
+                                      const moe_expert_bank *shared)
 {
-    moe_status s = check_route_args(x, router_w, T, workspace, workspace_bytes);
-    if (s != MOE_OK)
-        return s;
-    if (!out || !aligned16(out) || out == x)
+    if (!router_w || !aligned16(router_w))
         return MOE_ERR_INVALID_ARG;
+    moe_status s;
     if ((s = check_bank(routed, E, false)) != MOE_OK)
         return s;
     if ((s = check_bank(shared, 1, true)) != MOE_OK)
         return s;
-    const int n_shared = (shared && shared->n_experts > 0) ? 1 : 0;
-    if (n_shared && shared->wtype != routed->wtype)
+    if (shared && shared->n_experts > 0 && shared->wtype != routed->wtype)
         return MOE_ERR_UNSUPPORTED;   // one weight type per layer
-    const int nsm = sm_count();
-    if (nsm <= 0)
-        return MOE_ERR_CUDA;
-    cudaStream_t st = (cudaStream_t)stream;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    return MOE_OK;
+}
 
-    LayerArgs la{};
-    la.x = static_cast<const __nv_bfloat16 *>(x);
+// Fill the layer kernel's arguments (weights, workspace, output); the
+// caller sets the input fields.
+static void fill_layer_args(LayerArgs &la, const void *router_w, const moe_expert_bank *routed,
+                            const moe_expert_bank *shared, void *out, int T, void *workspace)
+{
+    const int n_shared = (shared && shared->n_experts > 0) ? 1 : 0;
     la.wr = static_cast<const __nv_bfloat16 *>(router_w);
     la.T = T;
     la.r_w13 = static_cast<const uint8_t *>(routed->w13);
@@ -220,10 +218,144 @@ moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expe
     }
     la.n_shared = n_shared;
     la.bf16w = routed->wtype == MOE_W_BF16 ? 1 : 0;
-    la.ws = ws;
+    la.ws = static_cast<uint8_t *>(workspace);
     la.out = static_cast<__nv_bfloat16 *>(out);
+}
+
+static cudaError_t launch_layer_on_all_sms(const LayerArgs &la, cudaStream_t st)
+{
+    const int nsm = sm_count();
+    if (nsm <= 0)
+        return cudaErrorNoDevice;
     // one CTA per SM; at least 128 for the router phase
-    return cuda_status(launch_layer(la, nsm >= 128 ? nsm : 128, st, true));
+    return launch_layer(la, nsm >= 128 ? nsm : 128, st, true);
+}
+
+moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expert_bank *routed,
+                             const moe_expert_bank *shared, void *out, int T, void *workspace,
+                             size_t workspace_bytes, moe_stream_t stream)
+{
+    moe_status s = check_route_args(x, router_w, T, workspace, workspace_bytes);
+    if (s != MOE_OK)
+        return s;
+    if (!out || !aligned16(out) || out == x)
+        return MOE_ERR_INVALID_ARG;
+    if ((s = check_layer_weights(router_w, routed, shared)) != MOE_OK)
+        return s;
+    const int nsm = sm_count();
+    if (nsm <= 0)
+        return MOE_ERR_CUDA;
+    LayerArgs la{};
+    fill_layer_args(la, router_w, routed, shared, out, T, workspace);
+    la.x = static_cast<const __nv_bfloat16 *>(x);
+    return cuda_status(launch_layer_on_all_sms(la, (cudaStream_t)stream));
+}
+
+static bool disjoint(const void *a, const void *b, size_t n)
+{
+    const uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
+    return pa + n <= pb || pb + n <= pa;
+}
+
+moe_status moe_layer_forward_prenorm(const void *resid, const void *delta, void *resid_out, void *xn_out,
+                                     float eps, const void *router_w, const moe_expert_bank *routed,
+                                     const moe_expert_bank *shared, void *out, int T, void *workspace,
+                                     size_t workspace_bytes, moe_stream_t stream)
+{
+    moe_status s = check_route_args(resid, router_w, T, workspace, workspace_bytes);
+    if (s != MOE_OK)
+        return s;
+    const size_t nb = (size_t)T * H * 2;
+    if (!out || !aligned16(out) || !disjoint(out, resid, nb))
+        return MOE_ERR_INVALID_ARG;
+    if (delta && (!aligned16(delta) || !disjoint(out, delta, nb)))
+        return MOE_ERR_INVALID_ARG;
+    for (const void *p : {resid_out, xn_out}) {
+        if (!p)
+            continue;
+        if (!aligned16(p) || !disjoint(p, out, nb) || !disjoint(p, resid, nb) ||
+            (delta && !disjoint(p, delta, nb)))
+            return MOE_ERR_INVALID_ARG;
+    }
+    if (resid_out && xn_out && !disjoint(resid_out, xn_out, nb))
+        return MOE_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || !(eps < 1.0f))
+        return MOE_ERR_INVALID_ARG;
+    if ((s = check_layer_weights(router_w, routed, shared)) != MOE_OK)
+        return s;
+    if (sm_count() <= 0)
+        return MOE_ERR_CUDA;
+    LayerArgs la{};
+    fill_layer_args(la, router_w, routed, shared, out, T, workspace);
+    la.x = static_cast<const __nv_bfloat16 *>(resid);
+    la.prenorm = 1;
+    la.delta = static_cast<const __nv_bfloat16 *>(delta);
+    la.resid_out = static_cast<__nv_bfloat16 *>(resid_out);
+    la.xn_out = static_cast<__nv_bfloat16 *>(xn_out);
+    la.eps = eps;
+    return cuda_status(launch_layer_on_all_sms(la, (cudaStream_t)stream));
+}
+
+// Stack workspace: the layer workspace, then the residual ping-pong buffers
+// R0, R1 and the layer-output buffers D0, D1 (bf16 [T][H] each).
+static size_t stack_buf_bytes(int T) { return align256((size_t)T * H * 2); }
+
+size_t moe_stack_workspace_bytes(int T)
+{
+    if (T < 1 || T > MAXT)
+        return 0;
+    return ws_layout().total + 4 * stack_buf_bytes(T);
+}
+
+moe_status moe_stack_forward(void *x, const moe_layer_weights *layers, int n_layers, int T, float eps,
+                             void *workspace, size_t workspace_bytes, moe_stream_t stream)
+{
+    if (!x || !aligned16(x) || !layers || n_layers < 1 || !workspace || !aligned16(workspace))
+        return MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > MAXT)
+        return MOE_ERR_UNSUPPORTED;
+    if (workspace_bytes < moe_stack_workspace_bytes(T))
+        return MOE_ERR_WORKSPACE;
+    if (!(eps >= 0.0f) || !(eps < 1.0f))
+        return MOE_ERR_INVALID_ARG;
+    moe_status s;
+    for (int l = 0; l < n_layers; ++l)
+        if ((s = check_layer_weights(layers[l].router_w, &layers[l].routed, &layers[l].shared)) != MOE_OK)
+            return s;
+    if (sm_count() <= 0)
+        return MOE_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t *base = static_cast<uint8_t *>(workspace) + ws_layout().total;
+    __nv_bfloat16 *R[2], *D[2];
+    for (int i = 0; i < 2; ++i) {
+        R[i] = reinterpret_cast<__nv_bfloat16 *>(base + (size_t)i * stack_buf_bytes(T));
+        D[i] = reinterpret_cast<__nv_bfloat16 *>(base + (size_t)(2 + i) * stack_buf_bytes(T));
+    }
+    __nv_bfloat16 *x0 = static_cast<__nv_bfloat16 *>(x);
+    // layer l reads the residual x_l and the previous output D[(l-1)&1]
+    // (none for l = 0), writes x_l's successor's residual part R[l&1] and
+    // its own output D[l&1]
+    for (int l = 0; l < n_layers; ++l) {
+        LayerArgs la{};
+        const moe_layer_weights &w = layers[l];
+        const moe_expert_bank *sh = w.shared.n_experts > 0 ? &w.shared : nullptr;
+        fill_layer_args(la, w.router_w, &w.routed, sh, D[l & 1], T, workspace);
+        la.prenorm = 1;
+        la.eps = eps;
+        if (l == 0) {
+            la.x = x0;
+        } else {
+            la.x = (l == 1) ? x0 : R[(l - 1) & 1];
+            la.delta = D[(l - 1) & 1];
+            la.resid_out = R[l & 1];
+        }
+        cudaError_t e = launch_layer_on_all_sms(la, st);
+        if (e != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+    // x_L = x_{L-1} + D[(L-1)&1]
+    const __nv_bfloat16 *last = (n_layers == 1) ? x0 : R[(n_layers - 1) & 1];
+    return cuda_status(launch_residual_add(last, D[(n_layers - 1) & 1], x0, T * H, st, true));
 }
 
 }  // extern "C"

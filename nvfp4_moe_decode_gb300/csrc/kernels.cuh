@@ -27,6 +27,15 @@ struct LayerArgs {
     const float *s_ts13, *s_ts2;   // NVFP4 only
     int n_shared;
     int bf16w;                     // 1: both banks hold bf16 weights
+    // pre-norm mode (a layer of a decoder stack): the input is
+    // RMSNorm(bf16(x + delta)); x is the residual stream, delta (may be null)
+    // the previous layer's output; resid_out / xn_out (may be null) receive
+    // bf16(x + delta) and the normalised input
+    int prenorm;
+    const __nv_bfloat16 *delta;
+    __nv_bfloat16 *resid_out;
+    __nv_bfloat16 *xn_out;
+    float eps;
     uint8_t *ws;
     __nv_bfloat16 *out;            // [T][H]
 };
@@ -59,5 +68,7 @@ cudaError_t launch_layer(const LayerArgs &a, int grid, cudaStream_t stream, bool
 cudaError_t launch_pack(const PackArgs &a, cudaStream_t s);
 cudaError_t launch_unpack(const UnpackArgs &a, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs &a, cudaStream_t s);
+cudaError_t launch_residual_add(const __nv_bfloat16 *a, const __nv_bfloat16 *b, __nv_bfloat16 *out, int n,
+                                cudaStream_t stream, bool pdl);
 
 }  // namespace moe

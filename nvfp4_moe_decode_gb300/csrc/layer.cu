@@ -84,6 +84,7 @@ struct FSmem {
     int32_t slot_expert[MAX_SLOTS];
     float wts[MAX_SLOTS][MAXT];
     int xshift[MAXT];
+    float sumsq[FW];                   // pre-norm: per-warp partial sums of squares
     int hshift[NG][2][MAXT];           // power-of-two exponents of the h in hbuf[grp][b]
 };
 
@@ -276,6 +277,7 @@ template <bool BW>
 __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
 {
     static_assert(sizeof(BfRed) <= sizeof(FSmem::ring), "K-split partials fit the ring");
+    static_assert(sizeof(FSmem::hbuf) >= (size_t)2 * MAXT * H * 2, "x and delta fit the h buffers");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     FSmem &sm = *reinterpret_cast<FSmem *>(smem_raw);
 
@@ -366,11 +368,83 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
 
     // ---- phase 2: x -> shared memory; router logits | activation fragments ----
     uint8_t *xs = &sm.hbuf[0][0][0];   // T x 4 KB, free until the unit loop
+    uint8_t *ds = xs + MAXT * H * 2;   // pre-norm: the previous layer's output, T x 4 KB
+    const bool has_delta = a.prenorm && a.delta != nullptr;
     if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(&sm.xbar, (uint32_t)(T * H * 2));
+        mbar_arrive_expect_tx(&sm.xbar, (uint32_t)(T * H * 2) * (has_delta ? 2u : 1u));
         bulk_g2s(xs, a.x, (uint32_t)(T * H * 2), &sm.xbar);
+        if (has_delta)
+            bulk_g2s(ds, a.delta, (uint32_t)(T * H * 2), &sm.xbar);
     }
     mbar_wait_bounded(&sm.xbar, 0, flag);
+    if (a.prenorm) {
+        // Pre-norm residual stream of a decoder stack: v = bf16(x + delta)
+        // (the residual after the previous layer), and the layer's input is
+        // xn = bf16(v / sqrt(mean(v^2) + eps)) with unit weight.  Two warps
+        // per token; each lane sums its 32 squares in order, then the warp
+        // butterfly, then the two halves (fixed order).
+        uint4 *xv = reinterpret_cast<uint4 *>(xs);
+        const uint4 *dv = reinterpret_cast<const uint4 *>(ds);
+        const int t = warp >> 1, half = warp & 1;
+        uint4 vv[4];
+        float ss = 0.f;
+        if (t < T) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int idx = t * (H / 8) + half * (H / 16) + 32 * i + lane;
+                uint4 r = xv[idx];
+                if (has_delta) {
+                    const uint4 d = dv[idx];
+                    uint32_t *rw = &r.x;
+                    const uint32_t *dw = &d.x;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const __nv_bfloat16 lo = __float2bfloat16_rn(bf16_bits_to_float(rw[q] & 0xFFFFu) + bf16_bits_to_float(dw[q] & 0xFFFFu));
+                        const __nv_bfloat16 hi = __float2bfloat16_rn(bf16_bits_to_float(rw[q] >> 16) + bf16_bits_to_float(dw[q] >> 16));
+                        rw[q] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+                    }
+                }
+                vv[i] = r;
+                const uint32_t *rw = &r.x;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float lo = bf16_bits_to_float(rw[q] & 0xFFFFu), hi = bf16_bits_to_float(rw[q] >> 16);
+                    ss = fmaf(lo, lo, ss);
+                    ss = fmaf(hi, hi, ss);
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+        if (lane == 0)
+            sm.sumsq[warp] = ss;
+        __syncthreads();
+        if (t < T) {
+            const float ms = (sm.sumsq[2 * t] + sm.sumsq[2 * t + 1]) * (1.0f / H);
+            const float rinv = 1.0f / sqrtf(ms + a.eps);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int idx = t * (H / 8) + half * (H / 16) + 32 * i + lane;
+                uint4 n = vv[i];
+                uint32_t *nw = &n.x;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const __nv_bfloat16 lo = __float2bfloat16_rn(bf16_bits_to_float(nw[q] & 0xFFFFu) * rinv);
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(bf16_bits_to_float(nw[q] >> 16) * rinv);
+                    nw[q] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+                }
+                xv[idx] = n;
+                if (blockIdx.x == 0) {
+                    if (a.resid_out)
+                        reinterpret_cast<uint4 *>(a.resid_out)[idx] = vv[i];
+                    if (a.xn_out)
+                        reinterpret_cast<uint4 *>(a.xn_out)[idx] = n;
+                }
+            }
+        }
+        __syncthreads();
+    }
     const __nv_bfloat16 *xsh = reinterpret_cast<const __nv_bfloat16 *>(xs);
 
     if (router_warp) {

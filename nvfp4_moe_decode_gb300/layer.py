@@ -11,9 +11,9 @@ from typing import Optional
 
 import torch
 
-from . import (HIDDEN, INTER, MOE_PACK_GATE_UP, MOE_PACK_PLAIN, MOE_W_BF16, MOE_W_NVFP4, make_bank,
-               moe_layer_forward, moe_pack_nvfp4, moe_packed_bytes, moe_workspace_bytes,
-               moe_workspace_init)
+from . import (HIDDEN, INTER, MOE_PACK_GATE_UP, MOE_PACK_PLAIN, MOE_W_BF16, MOE_W_NVFP4, layer_weights_array,
+               make_bank, moe_layer_forward, moe_pack_nvfp4, moe_packed_bytes, moe_stack_forward,
+               moe_stack_workspace_bytes, moe_workspace_bytes, moe_workspace_init)
 
 
 class PackedLayer:
@@ -88,6 +88,29 @@ class Bf16Layer:
 
 def new_workspace(T: int, device="cuda", stream=None) -> torch.Tensor:
     nbytes = moe_workspace_bytes(T)
+    if nbytes == 0:
+        raise ValueError(f"unsupported token count {T}")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    moe_workspace_init(ws, stream)
+    return ws
+
+
+class Stack:
+    """A pre-norm decoder stack of MoE layers (PackedLayer or Bf16Layer
+    objects): x <- x + MoE_l(RMSNorm(x)) for each layer, one
+    moe_stack_forward call."""
+
+    def __init__(self, layers, eps: float = 1e-6):
+        self.layers = list(layers)
+        self.eps = float(eps)
+        self.arr = layer_weights_array(self.layers)
+
+    def forward(self, x: torch.Tensor, workspace: torch.Tensor, stream=None):
+        moe_stack_forward(x, self.arr, len(self.layers), x.shape[0], self.eps, workspace, stream)
+
+
+def new_stack_workspace(T: int, device="cuda", stream=None) -> torch.Tensor:
+    nbytes = moe_stack_workspace_bytes(T)
     if nbytes == 0:
         raise ValueError(f"unsupported token count {T}")
     ws = torch.empty(nbytes, dtype=torch.uint8, device=device)

@@ -68,6 +68,10 @@ def _declare(lib):
         [vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp, vp]
         + [c_int, c_int, vp, vp, c_float, vp, vp, c_float, vp, vp, vp, vp])
     lib.oracle_moe_forward.restype = c_int
+    lib.oracle_round_bf16.argtypes = [c_double]
+    lib.oracle_round_bf16.restype = ctypes.c_uint16
+    lib.oracle_prenorm.argtypes = [vp, vp, c_int, c_int, c_double, vp, vp]
+    lib.oracle_prenorm.restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = c_int
     lib.oracle_set_num_threads.argtypes = [c_int]
@@ -223,6 +227,26 @@ def moe_forward(x: np.ndarray, wr: np.ndarray, experts: Sequence[Optional[Expert
     if rc != 0:
         raise ValueError(f"oracle_moe_forward failed ({rc})")
     return out, idx, w, logits
+
+
+def round_bf16(v: float, lib=None) -> int:
+    """Nearest bf16 (ties to even) of an fp64 value, as 16-bit pattern."""
+    return int((lib or load()).oracle_round_bf16(float(v)))
+
+
+def prenorm(x: np.ndarray, delta: Optional[np.ndarray], eps: float, lib=None):
+    """Pre-norm residual step: (v, xn) bf16 bit patterns [T, H] with
+    v = bf16(x + delta) and xn = bf16(v / sqrt(mean(v^2) + eps))."""
+    x = _u16(x)
+    T, H = x.shape
+    d = None
+    if delta is not None:
+        d = _u16(delta)
+        assert d.shape == x.shape
+    v = np.empty((T, H), dtype=np.uint16)
+    xn = np.empty((T, H), dtype=np.uint16)
+    (lib or load()).oracle_prenorm(_ptr(x), None if d is None else _ptr(d), T, H, float(eps), _ptr(v), _ptr(xn))
+    return v, xn
 
 
 def num_threads(lib=None) -> int:

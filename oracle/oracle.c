@@ -397,6 +397,75 @@ done:
     return rc;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Decoder stack: the pre-norm residual step.  [FLINT, "A 40B MoE ...": a    */
+/* 47-layer pre-norm decoder.]  Reading (the pages say only "pre-norm"):     */
+/* layer l maps the bf16 residual stream x to x + MoE(RMSNorm(x)), RMSNorm   */
+/* with unit weight: v / sqrt(mean(v^2) + eps); the normalised activations  */
+/* and the residual stream are bf16 tensors (the activations are BF16).     */
+/* ------------------------------------------------------------------------ */
+
+/* Nearest bf16 to v (ties to even), as bf16 bits.  bf16 keeps 8 significand
+ * bits: with v = m * 2^e, 0.5 <= |m| < 1, the representable neighbours are
+ * multiples of 2^(e-8) (2^-133 below the normal range, exponent e < -125).
+ * Values past the largest bf16 round to infinity; NaN stays NaN. */
+uint16_t oracle_round_bf16(double v)
+{
+    if (v != v)
+        return 0x7FC0;
+    if (v == 0.0)
+        return signbit(v) ? 0x8000 : 0x0000;
+    int e;
+    frexp(v, &e);
+    if (e < -125)
+        e = -125;
+    double q = ldexp(v, 8 - e);          /* |q| < 256, exact */
+#if ORACLE_MUTANT == 14 /* planted: truncation instead of round-to-nearest-even */
+    double r = trunc(q);
+#else
+    double r = nearbyint(q);             /* default rounding mode: nearest, ties to even */
+#endif
+    double rv = ldexp(r, e - 8);
+    float f = (float)rv;                 /* exact: rv has <= 9 significant bits */
+    if (fabs(rv) >= 0x1p128)
+        f = (float)(rv > 0 ? INFINITY : -INFINITY);
+    uint32_t bits;
+    memcpy(&bits, &f, 4);
+    return (uint16_t)(bits >> 16);
+}
+
+/* One pre-norm step for T tokens of H values: v = bf16(x + delta) (delta may
+ * be NULL: v = x), xn = bf16(v / sqrt(mean_k v_k^2 + eps)), both as bf16
+ * bits; the sum, mean, root and quotient in fp64. */
+void oracle_prenorm(const uint16_t *x, const uint16_t *delta, int T, int H, double eps,
+                    uint16_t *v_out, uint16_t *xn_out)
+{
+    double *v = (double *)malloc(sizeof(double) * (size_t)(H > 0 ? H : 1));
+    for (int t = 0; t < T; t++) {
+        double ss = 0.0;
+        for (int k = 0; k < H; k++) {
+            size_t i = (size_t)t * H + k;
+            double s = oracle_bf16_value(x[i]) + (delta ? oracle_bf16_value(delta[i]) : 0.0);
+            v_out[i] = oracle_round_bf16(s);
+            v[k] = oracle_bf16_value(v_out[i]);
+            ss += v[k] * v[k];
+        }
+#if ORACLE_MUTANT == 12 /* planted: sum of squares instead of their mean */
+        double ms = ss;
+#else
+        double ms = ss / H;
+#endif
+#if ORACLE_MUTANT == 13 /* planted: eps added after the root */
+        double scale = 1.0 / (sqrt(ms) + eps);
+#else
+        double scale = 1.0 / sqrt(ms + eps);
+#endif
+        for (int k = 0; k < H; k++)
+            xn_out[(size_t)t * H + k] = oracle_round_bf16(v[k] * scale);
+    }
+    free(v);
+}
+
 /* Threads an OpenMP region in this library uses (1 without OpenMP). */
 int oracle_num_threads(void)
 {

@@ -333,6 +333,89 @@ def pin_expert_permutation_invariance(lib):
     assert np.array_equal(perm.numpy()[idx2], idx)
 
 
+# ---------------------------------------------------------------------------
+# the pre-norm step of a decoder stack and bf16 rounding
+# ---------------------------------------------------------------------------
+
+def _torch_bf16_bits(v32: np.ndarray) -> np.ndarray:
+    """float32 values -> bf16 bit patterns by torch's float32 -> bfloat16 cast
+    (one round-to-nearest-even)."""
+    t = torch.from_numpy(np.ascontiguousarray(v32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _near_bf16_tie(v: float) -> bool:
+    """True when v lies within 2^-20 of a quantum of the midpoint between two
+    bf16 neighbours (where a float32 intermediate could round twice)."""
+    if v == 0.0 or not math.isfinite(v):
+        return False
+    m, e = math.frexp(abs(v))
+    q = m * 256.0
+    return abs((q - math.floor(q)) - 0.5) < 2.0 ** -20
+
+
+def pin_round_bf16_known_answers(lib):
+    rb = lambda v: oracle.round_bf16(v, lib=lib)  # noqa: E731
+    # exact ties go to the even neighbour
+    assert rb(1.0 + 2.0 ** -8) == 0x3F80
+    assert rb(1.0 + 3 * 2.0 ** -8) == 0x3F82
+    assert rb(-(1.0 + 2.0 ** -8)) == 0xBF80
+    # just above a tie (below float32 resolution) rounds up: no double rounding
+    assert rb(1.0 + 2.0 ** -8 + 2.0 ** -40) == 0x3F81
+    assert rb(-(1.0 + 2.0 ** -8 + 2.0 ** -40)) == 0xBF81
+    # the largest finite bf16, overflow, zero signs, subnormals
+    assert rb(3.3895313892515355e38) == 0x7F7F
+    assert rb(3.5e38) == 0x7F80 and rb(-3.5e38) == 0xFF80
+    assert rb(0.0) == 0x0000 and rb(-0.0) == 0x8000
+    assert rb(2.0 ** -130) == 0x0008 and rb(2.0 ** -133) == 0x0001
+    # random float32 values: the same single rounding as torch's cast
+    rng = np.random.default_rng(5)
+    vals = (rng.standard_normal(4000) * np.exp2(rng.integers(-60, 60, 4000))).astype(np.float32)
+    want = _torch_bf16_bits(vals)
+    got = np.array([rb(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, want)
+
+
+def pin_prenorm_constant_vector(lib):
+    """A constant token c: RMSNorm gives c / sqrt(c^2 + eps) in every entry."""
+    H, eps = 256, 1e-3
+    for c in (0.0625, -3.0, 0.75, 40.0):
+        bits = int(_torch_bf16_bits(np.array([c], dtype=np.float32))[0])
+        x = np.full((1, H), bits, dtype=np.uint16)
+        v, xn = oracle.prenorm(x, None, eps, lib=lib)
+        assert np.all(v == bits)
+        val = c / math.sqrt(c * c + eps)
+        assert not _near_bf16_tie(val)
+        want = int(_torch_bf16_bits(np.array([val], dtype=np.float32))[0])
+        assert np.all(xn == want), (c, hex(int(xn[0, 0])), hex(want))
+
+
+def pin_prenorm_matches_torch(lib):
+    """Random tokens: v against torch's bf16 add, xn against
+    torch.nn.functional.rms_norm in float64, rounded once to bf16."""
+    T, H, eps = 3, 512, 1e-6
+    g = torch.Generator().manual_seed(11)
+    x = (torch.randn(T, H, generator=g) * 2.0).to(torch.bfloat16)
+    d = (torch.randn(T, H, generator=g) * 0.5).to(torch.bfloat16)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    db = d.view(torch.int16).numpy().view(np.uint16)
+    v, xn = oracle.prenorm(xb, db, eps, lib=lib)
+    v_t = (x.float() + d.float()).to(torch.bfloat16)
+    assert np.array_equal(v, v_t.view(torch.int16).numpy().view(np.uint16))
+    ref = torch.nn.functional.rms_norm(v_t.double(), (H,), eps=eps).numpy()
+    got = np_bf16(xn)
+    flat_ref = ref.reshape(-1)
+    ok = np.array([not _near_bf16_tie(float(r)) for r in flat_ref])
+    want = _torch_bf16_bits(flat_ref.astype(np.float32))
+    assert np.array_equal(xn.reshape(-1)[ok], want[ok])
+    ulp = np.exp2(np.floor(np.log2(np.abs(ref))) - 7)
+    assert np.all(np.abs(got - ref) <= 0.5 * ulp * (1 + 1e-9))
+    # delta = None is the same as a zero delta
+    v0, xn0 = oracle.prenorm(xb, None, eps, lib=lib)
+    vz, xnz = oracle.prenorm(xb, np.zeros_like(xb), eps, lib=lib)
+    assert np.array_equal(v0, vz) and np.array_equal(xn0, xnz) and np.array_equal(v0, xb)
+
+
 ALL_PINS = [
     pin_e2m1_known_values,
     pin_e4m3_matches_torch,
@@ -350,4 +433,7 @@ ALL_PINS = [
     pin_routed_off_leaves_shared,
     pin_combine_linear_in_down_scale,
     pin_expert_permutation_invariance,
+    pin_round_bf16_known_answers,
+    pin_prenorm_constant_vector,
+    pin_prenorm_matches_torch,
 ]

@@ -3,7 +3,9 @@
 oracle.c carries ORACLE_MUTANT blocks, each a plausible slip: a mis-decoded
 e2m1 subnormal, an off-by-one e4m3 bias, swapped nibbles, a wrong scale
 block, a reversed tie rule, no renormalisation, gate/up swapped, SiLU lost,
-the shared expert dropped, and the router or down matrix read transposed.
+the shared expert dropped, the router or down matrix read transposed, and in
+the pre-norm step of a stack a sum instead of a mean, eps outside the root
+and truncation instead of rounding to bf16.
 Each variant is compiled here; at least one pin must fail on it.
 """
 import os
@@ -13,7 +15,7 @@ import pytest
 import oracle
 from tests import pins
 
-MUTANTS = list(range(1, 12))
+MUTANTS = list(range(1, 15))
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
