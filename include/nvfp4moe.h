@@ -87,6 +87,7 @@ enum {
 #define MOE_EXPERTS 256
 #define MOE_TOPK 6
 #define MOE_MAX_DECODE_T 8
+#define MOE_MAX_TOKENS 65536   /* largest T of moe_route / moe_layer_forward */
 
 /*
  * A bank of experts with identical shapes, stored back to back.
@@ -158,9 +159,12 @@ moe_status moe_dequant_nvfp4(const void *packed, int N, int K, int kind, float t
 /* Workspace.                                                              */
 /* ----------------------------------------------------------------------- */
 
-/* Workspace bytes for moe_route / moe_layer_forward with T tokens (0 if T
- * is unsupported).  The workspace holds routing results, the SiLU*up
- * activations, combine partials, arrival counters and the device flag. */
+/* Workspace bytes for moe_route / moe_layer_forward with T tokens (0 unless
+ * 1 <= T <= MOE_MAX_TOKENS).  The workspace holds routing results, the
+ * SiLU*up activations, combine partials, arrival counters and the device
+ * flag; above MOE_MAX_DECODE_T tokens also the grouped path's expert lists,
+ * the tokens' rows sorted by expert and the per-(token, choice) down outputs
+ * (about 72 KB per token). */
 size_t moe_workspace_bytes(int T);
 
 /* Zero a workspace (enqueued memset).  Required once before the first use of
@@ -185,11 +189,13 @@ moe_status moe_read_device_flag(void *workspace, moe_stream_t stream, uint32_t *
  *  idx:      device int32 [T][top_k] (selection order: best first).
  *  w:        device float [T][top_k], renormalised to sum to 1 per token.
  *  logits:   device float [T][E] fp32 logits, or NULL.
- * Logits are fp32 sums of exact bf16*bf16 products (fixed summation tree of
- * depth <= 24); the selection is taken on them, a tie going to the lower
- * index.  A non-finite logit sets MOE_FLAG_NONFINITE_LOGIT.
+ * T <= MOE_MAX_DECODE_T: logits are fp32 sums of exact bf16*bf16 products
+ * (fixed summation tree of depth <= 24).  Larger T: a tcgen05 GEMM computes
+ * them (bf16 operands, fp32 accumulation in tensor memory, 128 MMAs of
+ * K = 16 in sequence).  The selection is taken on the fp32 logits, a tie
+ * going to the lower index.  A non-finite logit sets MOE_FLAG_NONFINITE_LOGIT.
  * Errors: MOE_ERR_UNSUPPORTED unless H, E, top_k match this build and
- * 1 <= T <= MOE_MAX_DECODE_T; MOE_ERR_WORKSPACE if workspace_bytes is below
+ * 1 <= T <= MOE_MAX_TOKENS; MOE_ERR_WORKSPACE if workspace_bytes is below
  * moe_workspace_bytes(T).
  */
 moe_status moe_route(const void *x, const void *router_w, int T, int n_experts, int top_k,
@@ -204,8 +210,19 @@ moe_status moe_route(const void *x, const void *router_w, int T, int n_experts, 
 /* ----------------------------------------------------------------------- */
 
 /*
- * out = MoE(x) for 1 <= T <= MOE_MAX_DECODE_T tokens (see the top of this
- * header).  One persistent kernel (one CTA per SM, launched with
+ * out = MoE(x) for 1 <= T <= MOE_MAX_TOKENS tokens (see the top of this
+ * header).
+ * Above MOE_MAX_DECODE_T tokens the grouped path runs instead [FLINT,
+ * "From 1,096 kernels to 346": the same packed layout serves the grouped
+ * GEMMs of large batches]: a router GEMM, top-k, per-expert token lists in
+ * token order, then tcgen05 tensor-core GEMMs per expert (weights dequantised
+ * to f16 in shared memory; each token row of x and of h scaled by a power of
+ * two into f16, exactly for every element within 2^24 of the row's largest),
+ * h rounded to bf16 as in the decode path, and a combine that adds the six
+ * weighted expert outputs in choice order and the shared expert's (fp32,
+ * rounded once to bf16; deterministic).  With BF16 weights the grouped GEMMs
+ * use the bf16 values directly.
+ * Up to MOE_MAX_DECODE_T tokens: one persistent kernel (one CTA per SM, launched with
  * programmatic dependent launch so that its weight prefetch overlaps the
  * preceding kernel) runs the router GEMV and the top-k of every token, builds
  * the union of the selected experts with per-token weights, streams each

@@ -12,6 +12,12 @@ constexpr int ABI_VERSION = 1;
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+bool disjoint(const void *a, const void *b, size_t n)
+{
+    const uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
+    return pa + n <= pb || pb + n <= pa;
+}
+
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 int sm_count()
@@ -121,9 +127,12 @@ moe_status moe_dequant_nvfp4(const void *packed, int N, int K, int kind, float t
 
 size_t moe_workspace_bytes(int T)
 {
-    if (T < 1 || T > MAXT)
+    if (T < 1 || T > MAX_TOKENS)
         return 0;
-    return ws_layout().total;
+    if (T <= MAXT)
+        return ws_layout().total;
+    const size_t g = gws_layout(T).total;
+    return g > ws_layout().total ? g : ws_layout().total;
 }
 
 moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, moe_stream_t stream)
@@ -159,9 +168,9 @@ static moe_status check_route_args(const void *x, const void *router_w, int T, v
         return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(router_w) || !aligned16(workspace))
         return MOE_ERR_INVALID_ARG;
-    if (T < 1 || T > MAXT)
+    if (T < 1 || T > MAX_TOKENS)
         return MOE_ERR_UNSUPPORTED;
-    if (workspace_bytes < ws_layout().total)
+    if (workspace_bytes < moe_workspace_bytes(T))
         return MOE_ERR_WORKSPACE;
     return MOE_OK;
 }
@@ -177,6 +186,29 @@ moe_status moe_route(const void *x, const void *router_w, int T, int n_experts, 
         return MOE_ERR_UNSUPPORTED;
     if (!idx || !w)
         return MOE_ERR_INVALID_ARG;
+    if (T > MAXT) {
+        // router GEMM on the tensor cores, top-k per token, then the results
+        // copied out of the workspace
+        const int nsm = sm_count();
+        if (nsm <= 0)
+            return MOE_ERR_CUDA;
+        cudaStream_t st = (cudaStream_t)stream;
+        GroupedArgs ga{};
+        ga.x = static_cast<const __nv_bfloat16 *>(x);
+        ga.wr = static_cast<const __nv_bfloat16 *>(router_w);
+        ga.T = T;
+        ga.ws = static_cast<uint8_t *>(workspace);
+        cudaError_t e = launch_grouped_route(ga, nsm, st);
+        const GWsLayout L = gws_layout(T);
+        const uint8_t *ws = static_cast<const uint8_t *>(workspace);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(idx, ws + L.idx, (size_t)T * TOPK * 4, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(w, ws + L.w, (size_t)T * TOPK * 4, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess && logits)
+            e = cudaMemcpyAsync(logits, ws + L.logits, (size_t)T * E * 4, cudaMemcpyDeviceToDevice, st);
+        return cuda_status(e);
+    }
     RouterArgs a{static_cast<const __nv_bfloat16 *>(x), static_cast<const __nv_bfloat16 *>(router_w),
                  T, 0, static_cast<uint8_t *>(workspace), idx, w, logits};
     return cuda_status(launch_router(a, (cudaStream_t)stream, true));
@@ -245,16 +277,34 @@ moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expe
     const int nsm = sm_count();
     if (nsm <= 0)
         return MOE_ERR_CUDA;
+    if (T > MAXT) {
+        if (!disjoint(out, x, (size_t)T * H * 2))
+            return MOE_ERR_INVALID_ARG;
+        const bool has_shared = shared && shared->n_experts > 0;
+        GroupedArgs ga{};
+        ga.x = static_cast<const __nv_bfloat16 *>(x);
+        ga.wr = static_cast<const __nv_bfloat16 *>(router_w);
+        ga.T = T;
+        ga.bf16w = routed->wtype == MOE_W_BF16 ? 1 : 0;
+        ga.n_shared = has_shared ? 1 : 0;
+        ga.r_w13 = static_cast<const uint8_t *>(routed->w13);
+        ga.r_w2 = static_cast<const uint8_t *>(routed->w2);
+        ga.r_ts13 = routed->tscale13;
+        ga.r_ts2 = routed->tscale2;
+        if (has_shared) {
+            ga.s_w13 = static_cast<const uint8_t *>(shared->w13);
+            ga.s_w2 = static_cast<const uint8_t *>(shared->w2);
+            ga.s_ts13 = shared->tscale13;
+            ga.s_ts2 = shared->tscale2;
+        }
+        ga.ws = static_cast<uint8_t *>(workspace);
+        ga.out = static_cast<__nv_bfloat16 *>(out);
+        return cuda_status(launch_grouped_layer(ga, nsm, (cudaStream_t)stream));
+    }
     LayerArgs la{};
     fill_layer_args(la, router_w, routed, shared, out, T, workspace);
     la.x = static_cast<const __nv_bfloat16 *>(x);
     return cuda_status(launch_layer_on_all_sms(la, (cudaStream_t)stream));
-}
-
-static bool disjoint(const void *a, const void *b, size_t n)
-{
-    const uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
-    return pa + n <= pb || pb + n <= pa;
 }
 
 moe_status moe_layer_forward_prenorm(const void *resid, const void *delta, void *resid_out, void *xn_out,
@@ -265,6 +315,8 @@ moe_status moe_layer_forward_prenorm(const void *resid, const void *delta, void 
     moe_status s = check_route_args(resid, router_w, T, workspace, workspace_bytes);
     if (s != MOE_OK)
         return s;
+    if (T > MAXT)
+        return MOE_ERR_UNSUPPORTED;
     const size_t nb = (size_t)T * H * 2;
     if (!out || !aligned16(out) || !disjoint(out, resid, nb))
         return MOE_ERR_INVALID_ARG;

@@ -1,0 +1,1057 @@
+// grouped.cu -- the MoE layer for many tokens (T > MOE_MAX_DECODE_T): the
+// tokens are grouped by expert and every contraction runs on the tcgen05
+// tensor cores.
+//
+// Flint page ("vLLM adds day-0 support for Recursive's Flint"), section
+// "From 1,096 kernels to 346": the same packed NVFP4 layout serves the
+// small-batch GEMVs and the grouped GEMMs of large batches (the largest
+// prefill gain); the weights are dequantised for the tensor cores and the
+// activations stay 16-bit.
+//
+// Kernel chain (programmatic dependent launch between them):
+//  1. router GEMM   logits[T][E] = x Wr^T (bf16 operands, fp32 accumulator);
+//  2. top-k         one warp per token on the fp32 logits (the decode path's
+//                   selection routine), per-CTA counts per expert, and (NVFP4
+//                   weights) the token in f16 times a power of two, x16;
+//  3. lists         a scan of the counts and a scatter: per expert, the
+//                   (token, choice) pairs v = 6 t + i that selected it, in
+//                   increasing v, and each listed token's row copied to
+//                   xs[list row] (the GEMM operand, x16 or x), so that every
+//                   GEMM reads consecutive rows;
+//  4. gate/up GEMM  for every routed expert its listed tokens, and for the
+//                   shared expert all tokens: SiLU(g) * u -> h (bf16);
+//  5. h rescale     (NVFP4 weights) every h row in place to f16 times a
+//                   power of two;
+//  6. down GEMM     routed experts: y * routing weight -> ybuf[token][choice];
+//  7. shared down   the shared expert's down projection, and the combine
+//                   out = sum over choices of ybuf (in choice order) + y_shared,
+//                   rounded once to bf16 (deterministic: no atomics).
+// Without a shared expert step 7 is a plain combine kernel.
+//
+// NVFP4 operands enter the tensor cores as f16, like the decode path: a
+// weight is e2m1 x e4m3, exact in f16 (at most 6 significant bits, magnitude
+// in [2^-10, 2688]); a token row of x (or of h) is multiplied by the power of
+// two that puts its largest magnitude in [2^14, 2^15), exact for every
+// element within 2^24 of the largest, and the epilogue multiplies by the
+// inverse power and the tensor scale.  BF16 weights use bf16 operands as they
+// are.
+//
+// GEMM kernel (steps 1, 4, 6, 7): persistent, one CTA per SM, 512 threads.
+// A tile is (group, chunk of <= 256 tokens, 128-row M tile) with
+// D[128 weight rows][N tokens] = A[128][K] . B[N][K]^T, N = the chunk's
+// tokens rounded up to 16; tiles are dealt round-robin.  Roles:
+//   warps 0-7   A producers, one 16-row band each: raw NVFP4 super-chunks
+//               (codes of two 64-column chunks and their scales) arrive by
+//               bulk copy three super-chunks ahead and are dequantised into
+//               the 128B-swizzled K-major A stage (bf16 rows are copied there
+//               with cp.async instead);
+//   warp 8      B producer: the tile's token rows, consecutive rows of xs,
+//               x16, h or x, by 16-row TMA tiles;
+//   warp 10     TMEM allocation and the MMA issue (one thread, 4 MMAs of
+//               K = 16 per 64-column chunk, commits to the stages' empty
+//               barriers, and to the accumulator's full barrier per tile);
+//   warps 12-15 epilogue: tcgen05.ld of the accumulator (two 256-column
+//               buffers, so a tile's epilogue overlaps the next tile's MMAs).
+// Every wait is bounded: a wait that runs out sets MOE_FLAG_WAIT_TIMEOUT
+// and makes the CTA skip the rest of its work.
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+#include "tc.cuh"
+#include "topk.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int G_ASTAGES = 3;                           // A (weight) stages
+constexpr int G_BSTAGES = 4;                           // B (token) stages
+constexpr int G_A_BYTES = 128 * TC_ROW_BYTES;          // 16 KB: 128 rows x 64 16-bit values
+constexpr int G_B_BYTES = G_NMAX * TC_ROW_BYTES;       // 32 KB: 256 rows x 64 16-bit values
+constexpr int G_AWARPS = 8;                            // A producers: one 16-row band each
+constexpr int G_BWARP = 8;                             // B producer
+constexpr int G_MMA_WARP = 10;
+constexpr int G_EPI_WARP0 = 12;                        // epilogue warps 12..15 (TMEM lane quarters 0..3)
+constexpr int G_RAW_SLOTS = 4;                         // raw super-chunks per A warp
+constexpr int G_LAG = 2;                               // cp.async chunks in flight before signalling
+constexpr int G_THREADS = 512;
+constexpr int G_MAX_GROUPS = E + 1;
+constexpr int G_TMEM_COLS = 512;
+constexpr uint32_t G_SPIN = 1u << 16;                  // suspended polls before a wait gives up
+constexpr uint32_t G_SUSPEND_NS = 20000;               // suspend-time hint of one poll
+
+struct GSmem {
+    uint8_t a[G_ASTAGES][G_A_BYTES];                   // 1024-byte aligned tiles
+    uint8_t b[G_BSTAGES][G_B_BYTES];
+    uint8_t raw[G_AWARPS][G_RAW_SLOTS][SC_BYTES];      // raw NVFP4 super-chunks per A warp
+    uint64_t full_raw[G_AWARPS][G_RAW_SLOTS];
+    uint64_t full_a[G_ASTAGES], empty_a[G_ASTAGES], full_b[G_BSTAGES], empty_b[G_BSTAGES];
+    uint64_t d_full[2], d_empty[2];
+    uint32_t tmem;
+    int abort;
+    int n_groups;
+    int gn[G_MAX_GROUPS];                              // tokens of group g
+    int goff[G_MAX_GROUPS];                            // first list row of group g
+    int gtile[G_MAX_GROUPS + 1];                       // first tile of group g
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return smem_addr(p); }
+
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes (or the hint expires) instead of taking issue slots from the
+// producer warps on the same scheduler.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "r"(G_SUSPEND_NS) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase; false once the CTA has given up.
+__device__ __forceinline__ bool gwait(uint64_t *bar, uint32_t parity, GSmem &sm, uint32_t *flag)
+{
+    for (uint32_t it = 0; it < G_SPIN; ++it) {
+        if (mbar_try_wait_suspend(bar, parity))
+            return true;
+        if (*(volatile int *)&sm.abort)
+            return false;
+    }
+    atomicOr(flag, FLAG_TIMEOUT);
+    *(volatile int *)&sm.abort = 1;
+    return false;
+}
+
+// gwait by lane 0, result shared with the warp.
+__device__ __forceinline__ bool gwait_warp(uint64_t *bar, uint32_t parity, GSmem &sm, uint32_t *flag, int lane)
+{
+    bool ok = true;
+    if (lane == 0)
+        ok = gwait(bar, parity, sm, flag);
+    return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t a)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+
+// TMA: one box (64 columns x the map's box rows, 128-byte swizzled rows) at (col, row).
+__device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap *map, int col, int row, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(dst), "l"(map), "r"(col), "r"(row), "r"(smem_addr(bar)) : "memory");
+}
+
+// Four e2m1 code pairs (one 32-bit word, byte r = codes of two columns, low
+// nibble first) as f16x2 registers.
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t &h0, uint32_t &h1, uint32_t &h2, uint32_t &h3)
+{
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3) : "r"(w));
+}
+
+// Two e4m3 scale bytes (low byte first) as one f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two)
+{
+    uint32_t h2;
+    asm("{\n\t.reg .b16 b;\n\tcvt.u16.u32 b, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, b;\n\t}" : "=r"(h2) : "r"(two));
+    return h2;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ float pow2f(int k) { return __int_as_float((127 + k) << 23); }
+
+// Power of two that puts max|row| in [2^14, 2^15) (0 for an all-zero row).
+__device__ __forceinline__ int row_shift(float maxabs)
+{
+    const int sh = ACT_EXP - exponent_of(maxabs);
+    return sh < -100 ? -100 : (sh > 100 ? 100 : sh);
+}
+
+struct Tile {
+    int g, n0, nvalid, npad, mt;
+};
+
+__device__ __forceinline__ Tile decode_tile(const GSmem &sm, const GArgs &a, int id)
+{
+    int lo = 0, hi = sm.n_groups - 1;   // last group whose first tile <= id
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sm.gtile[mid] <= id)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    Tile t;
+    t.g = lo;
+    const int local = id - sm.gtile[lo];
+    const int j = local / a.mtiles, mt = local % a.mtiles;
+    t.mt = mt;
+    t.n0 = j * a.nmax;
+    t.nvalid = min(a.nmax, sm.gn[lo] - t.n0);
+    t.npad = (t.nvalid + 15) & ~15;
+    return t;
+}
+
+// The routed expert of group g, or -1 for the shared expert / the router.
+__device__ __forceinline__ int group_expert(const GArgs &a, int g)
+{
+    if (a.mode == GM_ROUTER || a.mode == GM_SHARED_DOWN)
+        return -1;
+    return g < E ? g : -1;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(G_THREADS, 1)
+    moe_grouped_gemm_kernel(const __grid_constant__ GArgs a, const __grid_constant__ CUtensorMap map_routed64,
+                            const __grid_constant__ CUtensorMap map_routed16,
+                            const __grid_constant__ CUtensorMap map_shared64,
+                            const __grid_constant__ CUtensorMap map_shared16)
+{
+    extern __shared__ uint8_t g_smem_raw[];
+    GSmem &sm = *reinterpret_cast<GSmem *>((uint8_t *)(((uintptr_t)g_smem_raw + 1023) & ~(uintptr_t)1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    griddep_wait();       // lists, x16, h and ybuf come from the preceding kernels
+    griddep_launch();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < G_ASTAGES; ++s) {
+            mbar_init(&sm.full_a[s], G_AWARPS);
+            mbar_init(&sm.empty_a[s], 1);
+        }
+        for (int s = 0; s < G_BSTAGES; ++s) {
+            mbar_init(&sm.full_b[s], 1);
+            mbar_init(&sm.empty_b[s], 1);
+        }
+        for (int w = 0; w < G_AWARPS; ++w)
+            for (int s = 0; s < G_RAW_SLOTS; ++s)
+                mbar_init(&sm.full_raw[w][s], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.d_full[i], 1);
+            mbar_init(&sm.d_empty[i], 4);
+        }
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    // group table: tokens, first list row and first tile of every group
+    if (warp == 0) {
+        int ng;
+        if (a.mode == GM_GATE_UP)
+            ng = E + (a.n_shared ? 1 : 0);
+        else if (a.mode == GM_DOWN)
+            ng = E;
+        else
+            ng = 1;
+        int run = 0;
+        for (int base = 0; base < ng; base += 32) {
+            const int g = base + lane;
+            int n = 0, off = 0;
+            if (g < ng) {
+                if ((a.mode == GM_GATE_UP || a.mode == GM_DOWN) && g < E) {
+                    n = a.counts[g];
+                    off = a.offsets[g];
+                } else {
+                    n = a.T;
+                }
+                sm.gn[g] = n;
+                sm.goff[g] = off;
+            }
+            int tiles = (g < ng) ? ((n + a.nmax - 1) / a.nmax) * a.mtiles : 0;
+            int incl = tiles;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o)
+                    incl += v;
+            }
+            if (g < ng)
+                sm.gtile[g] = run + incl - tiles;
+            run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) {
+            sm.gtile[ng] = run;
+            sm.n_groups = ng;
+        }
+    }
+    if (warp == G_MMA_WARP)
+        tc_alloc(&sm.tmem, G_TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const int total_tiles = sm.gtile[sm.n_groups];
+    const int nch = a.K / TC_KCHUNK;
+    const int my_tiles = (int)blockIdx.x < total_tiles ? (total_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int stream_len = my_tiles * nch;          // chunks this CTA streams
+    auto tile_id = [&](int ti) { return (int)blockIdx.x + ti * (int)gridDim.x; };
+    uint32_t *flag = a.flag;
+
+    // A-operand base of group g (bytes): packed NVFP4 or bf16 rows of one matrix
+    auto a_base = [&](int g) -> const uint8_t * {
+        if (a.mode == GM_ROUTER)
+            return reinterpret_cast<const uint8_t *>(a.wr);
+        const int e = group_expert(a, g);
+        return e >= 0 ? a.ra + (size_t)e * a.a_stride : a.sa;
+    };
+    auto a_tscale = [&](int g) -> float {
+        if (a.a_bf16 || a.mode == GM_ROUTER)
+            return 1.0f;
+        const int e = group_expert(a, g);
+        return e >= 0 ? __ldg(a.rts + e) : __ldg(a.sts);
+    };
+
+    if (warp < G_AWARPS) {
+        // ------------------------------------------------------------ A producers
+        if (!a.a_bf16) {
+            // warp w dequantises band 8 mt + w (16 rows) of every chunk to f16;
+            // its raw super-chunks (1152 bytes: codes of 2 chunks + scales) come
+            // by bulk copy G_RAW_SLOTS - 1 super-chunks ahead
+            const int g4 = lane >> 2, c4 = lane & 3;
+            const size_t band_bytes_k = (size_t)9 * a.K;
+            const int nsc = stream_len >> 1;               // super-chunks of this CTA's stream
+            auto fetch_sc = [&](int sci) {
+                if (lane == 0 && sci < nsc) {
+                    const Tile t = decode_tile(sm, a, tile_id((2 * sci) / nch));
+                    const int q = ((2 * sci) % nch) >> 1;
+                    const uint8_t *src = a_base(t.g) + (size_t)(8 * t.mt + warp) * band_bytes_k + (size_t)q * SC_BYTES;
+                    uint64_t *bar = &sm.full_raw[warp][sci % G_RAW_SLOTS];
+                    mbar_arrive_expect_tx(bar, SC_BYTES);
+                    bulk_g2s(sm.raw[warp][sci % G_RAW_SLOTS], src, SC_BYTES, bar);
+                }
+            };
+            for (int p = 0; p < G_RAW_SLOTS - 1; ++p)
+                fetch_sc(p);
+            // lane (g, c) writes 4 bytes at row 16 w + g + 8 (r & 1), 16-byte
+            // chunk (2 st + (r >> 1)) ^ g, byte 4 c, for word st and byte r
+            const uint32_t row0 = (uint32_t)((16 * warp + g4) * TC_ROW_BYTES) + 4u * c4;
+            for (int kk = 0; kk < stream_len; ++kk) {
+                const int sci = kk >> 1, ch = kk % nch;
+                if ((kk & 1) == 0) {
+                    fetch_sc(sci + G_RAW_SLOTS - 1);       // into the slot of super-chunk sci - 1
+                    if (!gwait_warp(&sm.full_raw[warp][sci % G_RAW_SLOTS], (sci / G_RAW_SLOTS) & 1, sm, flag, lane))
+                        break;
+                }
+                const int s = kk % G_ASTAGES;
+                if (kk >= G_ASTAGES && !gwait_warp(&sm.empty_a[s], ((kk / G_ASTAGES) - 1) & 1, sm, flag, lane))
+                    break;
+                const uint32_t raw = smem_u32(sm.raw[warp][sci % G_RAW_SLOTS]);
+                const uint4 cw = lds128(raw + (ch & 1) * 512 + 16 * lane);
+                const uint2 sw = lds64(raw + 1024 + 16 * g4 + 8 * (ch & 1));
+                const uint32_t abase = smem_u32(sm.a[s]) + row0;
+                const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                for (int st = 0; st < 4; ++st) {
+                    // scale bytes 2 st (row g) and 2 st + 1 (row g + 8)
+                    const uint32_t sc = e4m3x2_to_f16x2(((st < 2 ? sw.x : sw.y) >> (16 * (st & 1))) & 0xFFFFu);
+                    const uint32_t s_lo = __byte_perm(sc, 0, 0x1010), s_hi = __byte_perm(sc, 0, 0x3232);
+                    uint32_t h[4];
+                    e2m1x8_to_f16(words[st], h[0], h[1], h[2], h[3]);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const uint32_t v = hmul2_u32(h[r], (r & 1) ? s_hi : s_lo);
+                        const uint32_t off = (uint32_t)(8 * (r & 1) * TC_ROW_BYTES) +
+                                             (uint32_t)(((2 * st + (r >> 1)) ^ g4) << 4);
+                        st_shared32(abase + off, v);
+                    }
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sm.full_a[s]);
+            }
+        } else {
+            // bf16 rows: warp w copies rows 16 w .. 16 w + 15 (16 x 8 chunks of 16 bytes)
+            const int c8 = lane & 7;
+            int kk = 0;
+            for (; kk < stream_len; ++kk) {
+                const int s = kk % G_ASTAGES;
+                if (kk >= G_ASTAGES && !gwait_warp(&sm.empty_a[s], ((kk / G_ASTAGES) - 1) & 1, sm, flag, lane))
+                    break;
+                const Tile t = decode_tile(sm, a, tile_id(kk / nch));
+                const int ch = kk % nch;
+                const __nv_bfloat16 *base = reinterpret_cast<const __nv_bfloat16 *>(a_base(t.g));
+                const uint32_t abase = smem_u32(sm.a[s]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int R = 16 * warp + (lane >> 3) + 4 * i;
+                    int row;
+                    if (a.mode == GM_GATE_UP) {
+                        const int ii = R & 15, b = 8 * t.mt + (R >> 4);
+                        row = ii < 8 ? 8 * b + ii : I + 8 * b + (ii - 8);
+                    } else {
+                        row = 128 * t.mt + R;
+                    }
+                    cp_async16(abase + sw128_offset(R, c8), base + (size_t)row * a.K + ch * TC_KCHUNK + 8 * c8, 16u);
+                }
+                cp_async_commit();
+                if (kk >= G_LAG) {
+                    cp_async_wait<G_LAG>();
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&sm.full_a[(kk - G_LAG) % G_ASTAGES]);
+                }
+            }
+            cp_async_wait<0>();
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0)
+                for (int k2 = max(0, kk - G_LAG); k2 < kk; ++k2)
+                    mbar_arrive(&sm.full_a[k2 % G_ASTAGES]);
+        }
+    } else if (warp == G_BWARP) {
+        // ------------------------------------------------------------ B producer
+        // routed groups read their list rows (xs, or h in list order), the
+        // shared group / the router its token rows; columns beyond the tile's
+        // tokens are loaded too (other rows, or zeros past the end) and are
+        // never stored
+        int cur_tile = -1, npad = 0, row0 = 0;
+        bool routed = false;
+        for (int kk = 0; kk < stream_len; ++kk) {
+            const int ti = kk / nch, ch = kk % nch;
+            if (ti != cur_tile) {
+                cur_tile = ti;
+                const Tile t = decode_tile(sm, a, tile_id(ti));
+                npad = t.npad;
+                routed = group_expert(a, t.g) >= 0;
+                row0 = (routed ? sm.goff[t.g] : 0) + t.n0;
+            }
+            const int s = kk % G_BSTAGES;
+            if (kk >= G_BSTAGES && !gwait_warp(&sm.empty_b[s], ((kk / G_BSTAGES) - 1) & 1, sm, flag, lane))
+                break;
+            if (lane == 0)
+                mbar_arrive_expect_tx(&sm.full_b[s], (uint32_t)(npad * TC_ROW_BYTES));
+            __syncwarp();
+            // 64-row boxes, then 16-row boxes for the rest (at most 3 + 3 copies)
+            const int n64 = npad >> 6, n16 = (npad & 63) >> 4;
+            if (lane < n64 + n16) {
+                const int r = lane < n64 ? 64 * lane : 64 * n64 + 16 * (lane - n64);
+                const CUtensorMap *map = lane < n64 ? (routed ? &map_routed64 : &map_shared64)
+                                                    : (routed ? &map_routed16 : &map_shared16);
+                tma_box(smem_u32(sm.b[s]) + (uint32_t)(r * TC_ROW_BYTES), map, ch * TC_KCHUNK, row0 + r, &sm.full_b[s]);
+            }
+        }
+    } else if (warp == G_MMA_WARP) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint32_t tbase = sm.tmem;
+            int kk = 0;
+            bool ok = true;
+            for (int ti = 0; ti < my_tiles && ok; ++ti) {
+                const Tile t = decode_tile(sm, a, tile_id(ti));
+                const uint32_t idesc = a.f16 ? idesc_f16_m128(t.npad) : idesc_bf16_m128(t.npad);
+                const int ab = ti & 1;
+                ok = gwait(&sm.d_empty[ab], ((ti >> 1) & 1) ^ 1, sm, flag);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const uint32_t d = tbase + (uint32_t)(ab * 256);
+                for (int ch = 0; ch < nch; ++ch, ++kk) {
+                    const int sa_ = kk % G_ASTAGES, sb_ = kk % G_BSTAGES;
+                    if (!gwait(&sm.full_a[sa_], (kk / G_ASTAGES) & 1, sm, flag) ||
+                        !gwait(&sm.full_b[sb_], (kk / G_BSTAGES) & 1, sm, flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t aa = smem_u32(sm.a[sa_]), bb = smem_u32(sm.b[sb_]);
+#pragma unroll
+                    for (int k16 = 0; k16 < 4; ++k16)
+                        tc_mma(d, sw128_desc(aa + 32 * k16), sw128_desc(bb + 32 * k16), idesc,
+                               (ch > 0 || k16 > 0) ? 1u : 0u);
+                    tc_commit(&sm.empty_a[sa_]);
+                    tc_commit(&sm.empty_b[sb_]);
+                }
+                if (ok)
+                    tc_commit(&sm.d_full[ab]);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= G_EPI_WARP0) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int R = 32 * q + lane;                   // tile row = TMEM lane
+        const uint32_t tbase = sm.tmem + ((uint32_t)(32 * q) << 16);
+        for (int ti = 0; ti < my_tiles; ++ti) {
+            const Tile t = decode_tile(sm, a, tile_id(ti));
+            const int ab = ti & 1;
+            if (!gwait_warp(&sm.d_full[ab], (ti >> 1) & 1, sm, flag, lane))
+                break;
+            tc_fence_after();
+            const float ts = a_tscale(t.g);
+            const int e = group_expert(a, t.g);
+            for (int c0 = 0; c0 < t.npad; c0 += 32) {
+                float v[32];
+                tc_ld32(tbase + (uint32_t)(ab * 256 + c0), v);
+                // per-column factors, loaded by lane j for column c0 + j
+                const int colj = c0 + lane;
+                const bool okj = colj < t.nvalid;
+                if (a.mode == GM_GATE_UP) {
+                    // rows 16 bb + i: i < 8 gate, i >= 8 up of feature 8 (8 mt + bb) + (i & 7);
+                    // column pair (2 m, 2 m + 1): gate lanes finish column 2 m, up lanes 2 m + 1
+                    float fj = ts;
+                    if (okj && a.xshift) {
+                        const int tok = (e >= 0) ? __ldg(a.list + sm.goff[t.g] + t.n0 + colj) / TOPK : t.n0 + colj;
+                        fj = ts * pow2f(-__ldg(a.xshift + tok));
+                    }
+                    const int bb = R >> 4, ii = R & 15;
+                    const bool up = ii >= 8;
+                    const int f = 8 * (8 * t.mt + bb) + (ii & 7);
+                    __nv_bfloat16 *hrow = (e >= 0) ? a.h_routed + (size_t)(sm.goff[t.g] + t.n0) * I
+                                                   : a.h_shared + (size_t)t.n0 * I;
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+                        const float send = up ? v[2 * m] : v[2 * m + 1];
+                        const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+                        const int col = c0 + 2 * m + (up ? 1 : 0);
+                        const float fc = __shfl_sync(0xFFFFFFFFu, fj, 2 * m + (up ? 1 : 0));
+                        const float gv = (up ? recv : v[2 * m]) * fc;
+                        const float uv = (up ? v[2 * m + 1] : recv) * fc;
+                        if (col < t.nvalid)
+                            hrow[(size_t)col * I + f] = __float2bfloat16_rn(gv / (1.0f + __expf(-gv)) * uv);
+                    }
+                } else if (a.mode == GM_DOWN) {
+                    const int f = 128 * t.mt + R;
+                    int v6j = 0;
+                    float fj = 0.0f;
+                    if (okj) {
+                        const int row = sm.goff[t.g] + t.n0 + colj;
+                        v6j = __ldg(a.list + row);
+                        fj = __ldg(a.topk_w + v6j) * ts;
+                        if (a.hshift_r)
+                            fj *= pow2f(-__ldg(a.hshift_r + row));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int v6 = __shfl_sync(0xFFFFFFFFu, v6j, j);
+                        const float fc = __shfl_sync(0xFFFFFFFFu, fj, j);
+                        if (c0 + j < t.nvalid)
+                            a.ybuf[(size_t)v6 * H + f] = v[j] * fc;
+                    }
+                } else if (a.mode == GM_SHARED_DOWN) {
+                    const int f = 128 * t.mt + R;
+                    float fj = ts;
+                    if (okj && a.hshift_s)
+                        fj = ts * pow2f(-__ldg(a.hshift_s + t.n0 + colj));
+#pragma unroll
+                    for (int j0 = 0; j0 < 32; j0 += 8) {
+                        float y[8][TOPK];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int col = c0 + j0 + j;
+                            const float *yb = a.ybuf + (size_t)(t.n0 + col) * TOPK * H + f;
+#pragma unroll
+                            for (int i = 0; i < TOPK; ++i)
+                                y[j][i] = (col < t.nvalid) ? __ldcs(yb + (size_t)i * H) : 0.0f;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int col = c0 + j0 + j;
+                            const float fc = __shfl_sync(0xFFFFFFFFu, fj, j0 + j);
+                            if (col < t.nvalid) {
+                                float acc = 0.0f;
+#pragma unroll
+                                for (int i = 0; i < TOPK; ++i)
+                                    acc += y[j][i];
+                                acc += v[j0 + j] * fc;
+                                a.out[(size_t)(t.n0 + col) * H + f] = __float2bfloat16_rn(acc);
+                            }
+                        }
+                    }
+                } else {
+                    const int ee = 128 * t.mt + R;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = c0 + j;
+                        if (col < t.nvalid)
+                            a.logits[(size_t)(t.n0 + col) * E + ee] = v[j];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.d_empty[ab]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == G_MMA_WARP) {
+        tc_fence_after();
+        tc_dealloc(sm.tmem, G_TMEM_COLS);
+    }
+}
+
+// One warp per token: top-k of the fp32 logits, renormalised weights; CTA
+// c (G_TOK_PER_CTA tokens) counts its selections per expert into hist[c][E];
+// with x16 given, the token row is also written as f16 times 2^xshift[t].
+__global__ void __launch_bounds__(1024) moe_grouped_topk_kernel(const float *logits, int T, int32_t *idx, float *w,
+                                                             int32_t *hist, const __nv_bfloat16 *x, __half *x16,
+                                                             int32_t *xshift, uint32_t *flag)
+{
+    griddep_wait();
+    griddep_launch();
+    __shared__ int h[E];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < E; i += blockDim.x)
+        h[i] = 0;
+    __syncthreads();
+    for (int k = 0; k < G_TOK_PER_CTA / 32; ++k) {
+        const int t = blockIdx.x * G_TOK_PER_CTA + k * 32 + warp;
+        if (t >= T)
+            break;
+        int ex;
+        float wt;
+        bool bad;
+        warp_route_token(logits + (size_t)t * E, lane, ex, wt, bad);
+        if (bad && lane == 0)
+            atomicOr(flag, FLAG_NONFINITE);
+        if (lane < TOPK) {
+            idx[(size_t)t * TOPK + lane] = ex;
+            w[(size_t)t * TOPK + lane] = wt;
+            if (ex >= 0 && ex < E)
+                atomicAdd(&h[ex], 1);
+        }
+        if (x16) {
+            const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+            uint4 v[H / 256];
+            float m = 0.0f;
+#pragma unroll
+            for (int i = 0; i < H / 256; ++i) {
+                v[i] = __ldg(row + lane + 32 * i);
+                const uint32_t q4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_float(q4[j] & 0xFFFFu)), fabsf(bf16_bits_to_float(q4[j] >> 16))));
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1)
+                m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            const int sh = row_shift(m);
+            const float p = pow2f(sh);
+            uint4 *dst = reinterpret_cast<uint4 *>(x16 + (size_t)t * H);
+#pragma unroll
+            for (int i = 0; i < H / 256; ++i) {
+                const uint32_t q4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                uint32_t o4[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    o4[j] = bf16x2_to_f16x2_scaled(q4[j], p);
+                dst[lane + 32 * i] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            }
+            if (lane == 0)
+                xshift[t] = sh;
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < E; i += blockDim.x)
+        hist[(size_t)blockIdx.x * E + i] = h[i];
+}
+
+// Expert lists, step 1 of 2 (one CTA of E threads): thread e turns the
+// per-CTA counts hist[c][e] into the first list row of (c, e),
+// base[c][e] = offsets[e] + sum over c' < c of hist[c'][e], where offsets
+// is the exclusive prefix of the expert totals (counts).
+__global__ void __launch_bounds__(E) moe_grouped_scan_kernel(const int32_t *hist, int nc, int32_t *base,
+                                                           int32_t *counts, int32_t *offsets)
+{
+    griddep_wait();
+    griddep_launch();
+    const int e = threadIdx.x;
+    int run = 0;
+    for (int c0 = 0; c0 < nc; c0 += 16) {
+        int hv[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            hv[j] = (c0 + j < nc) ? hist[(size_t)(c0 + j) * E + e] : 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (c0 + j < nc)
+                base[(size_t)(c0 + j) * E + e] = run;
+            run += hv[j];
+        }
+    }
+    // exclusive prefix over experts (E = 256 totals, one warp-scan per 32)
+    const int lane = e & 31, warp = e >> 5;
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    __shared__ int wtot[E / 32];
+    if (lane == 31)
+        wtot[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w2 = 0; w2 < warp; ++w2)
+        before += wtot[w2];
+    const int off = before + incl - run;
+    counts[e] = run;
+    offsets[e] = off;
+    if (e == E - 1)
+        offsets[E] = off + run;
+    for (int c = 0; c < nc; ++c)
+        base[(size_t)c * E + e] += off;
+}
+
+// Expert lists, step 2 of 2: CTA c writes the pairs v = 6 t + i of its
+// tokens to list[base[c][e] + rank], rank = earlier pairs of the CTA that
+// chose the same expert, so every expert's rows are in increasing v; then
+// copies token t's row of src (H 16-bit values) to xs[that list row].
+__global__ void __launch_bounds__(G_TOK_PER_CTA * TOPK) moe_grouped_scatter_kernel(const int32_t *idx, int T,
+                                                                                 const int32_t *base, int32_t *list,
+                                                                                 const uint16_t *src, uint16_t *xs,
+                                                                                 uint32_t *flag)
+{
+    griddep_wait();
+    griddep_launch();
+    __shared__ int ex[G_TOK_PER_CTA * TOPK];
+    __shared__ int pos[G_TOK_PER_CTA * TOPK];
+    const int n = min(G_TOK_PER_CTA, T - (int)blockIdx.x * G_TOK_PER_CTA) * TOPK;
+    const int v0 = blockIdx.x * G_TOK_PER_CTA * TOPK;
+    const int k = threadIdx.x;
+    const int e = (k < n) ? __ldg(idx + v0 + k) : -1;
+    ex[k] = e;
+    __syncthreads();
+    int p = -1;
+    if (k < n) {
+        if (e < 0 || e >= E) {
+            atomicOr(flag, FLAG_BAD_INDEX);
+        } else {
+            int rank = 0;
+            for (int j = 0; j < k; ++j)
+                rank += (ex[j] == e);
+            p = __ldg(base + (size_t)blockIdx.x * E + e) + rank;
+            list[p] = v0 + k;
+        }
+    }
+    pos[k] = p;
+    __syncthreads();
+    // one warp per listed row: H values = 256 x 16 bytes
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int j = warp; j < n; j += blockDim.x >> 5) {
+        const int pj = pos[j];
+        if (pj < 0)
+            continue;
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(src + (size_t)((v0 + j) / TOPK) * H);
+        uint4 *d4 = reinterpret_cast<uint4 *>(xs + (size_t)pj * H);
+#pragma unroll
+        for (int i = 0; i < H / 256; ++i)
+            d4[lane + 32 * i] = __ldg(s4 + lane + 32 * i);
+    }
+}
+
+// h rows (bf16) rescaled in place to f16 times 2^shift[row] (one warp per
+// row of I = 512 values).
+__global__ void __launch_bounds__(256) moe_grouped_hscale_kernel(uint16_t *h, int rows, int32_t *shift)
+{
+    griddep_wait();
+    griddep_launch();
+    const int lane = threadIdx.x & 31;
+    for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < rows; r += gridDim.x * 8) {
+        uint4 *row = reinterpret_cast<uint4 *>(h + (size_t)r * I);
+        uint4 v[I / 256];
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < I / 256; ++i) {
+            v[i] = row[lane + 32 * i];
+            const uint32_t q4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_float(q4[j] & 0xFFFFu)), fabsf(bf16_bits_to_float(q4[j] >> 16))));
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        const int sh = row_shift(m);
+        const float p = pow2f(sh);
+#pragma unroll
+        for (int i = 0; i < I / 256; ++i) {
+            const uint32_t q4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            uint32_t o4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                o4[j] = bf16x2_to_f16x2_scaled(q4[j], p);
+            row[lane + 32 * i] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        }
+        if (lane == 0)
+            shift[r] = sh;
+    }
+}
+
+// out[t] = sum over choices of ybuf[t][i] (choice order), without a shared expert.
+__global__ void __launch_bounds__(256) moe_grouped_combine_kernel(const float *ybuf, int T, __nv_bfloat16 *out)
+{
+    griddep_wait();
+    griddep_launch();
+    const size_t n = (size_t)T * H;
+    for (size_t o = (size_t)blockIdx.x * blockDim.x + threadIdx.x; o < n; o += (size_t)gridDim.x * blockDim.x) {
+        const size_t t = o / H, f = o % H;
+        float acc = 0.0f;
+#pragma unroll
+        for (int i = 0; i < TOPK; ++i)
+            acc += __ldcg(ybuf + (t * TOPK + i) * H + f);
+        out[o] = __float2bfloat16_rn(acc);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+GWsLayout gws_layout(int T)
+{
+    const size_t nc = (size_t)(T + G_TOK_PER_CTA - 1) / G_TOK_PER_CTA;
+    GWsLayout L;
+    size_t o = 0;
+    L.ctrl = o;      o = align256(o + 64 * 4);
+    L.logits = o;    o = align256(o + (size_t)T * E * 4);
+    L.idx = o;       o = align256(o + (size_t)T * TOPK * 4);
+    L.w = o;         o = align256(o + (size_t)T * TOPK * 4);
+    L.counts = o;    o = align256(o + (size_t)E * 4);
+    L.offsets = o;   o = align256(o + (size_t)(E + 1) * 4);
+    L.list = o;      o = align256(o + (size_t)T * TOPK * 4);
+    L.hist = o;      o = align256(o + nc * E * 4);
+    L.base = o;      o = align256(o + nc * E * 4);
+    L.x16 = o;       o = align256(o + (size_t)T * H * 2);
+    L.xs = o;        o = align256(o + (size_t)T * TOPK * H * 2);
+    L.xshift = o;    o = align256(o + (size_t)T * 4);
+    L.hshift = o;    o = align256(o + (size_t)T * (TOPK + 1) * 4);
+    L.h_routed = o;  o = o + (size_t)T * TOPK * I * 2;          // h_shared follows directly
+    L.h_shared = o;  o = align256(o + (size_t)T * I * 2);
+    L.ybuf = o;      o = align256(o + (size_t)T * TOPK * H * 4);
+    L.total = o;
+    return L;
+}
+
+static cudaError_t launch_ex(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void **args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+size_t grouped_smem_bytes() { return sizeof(GSmem) + 1024; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// A 2D map over rows x cols 16-bit values (row pitch cols * 2 bytes), box
+// 64 columns x box_rows rows, 128-byte swizzle.
+static bool make_map(CUtensorMap *m, const void *base, int cols, size_t rows, int box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)TC_KCHUNK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One grouped GEMM launch; B rows come from `routed` (list rows of the
+// routed groups) and `shared` (token rows of the shared group / router), both
+// `cols` 16-bit values wide.
+static cudaError_t launch_gemm(const GArgs &ga, const void *routed, size_t routed_rows, const void *shared,
+                               size_t shared_rows, int cols, int nsm, cudaStream_t st)
+{
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        e = cudaFuncSetAttribute(moe_grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)grouped_smem_bytes());
+        if (e != cudaSuccess)
+            return e;
+        configured[dev] = 1;
+    }
+    alignas(64) CUtensorMap mr64, mr16, ms64, ms16;
+    const void *r = routed ? routed : shared, *s = shared ? shared : routed;
+    const size_t rr = routed ? routed_rows : shared_rows, sr = shared ? shared_rows : routed_rows;
+    if (!make_map(&mr64, r, cols, rr, 64) || !make_map(&mr16, r, cols, rr, 16) || !make_map(&ms64, s, cols, sr, 64) ||
+        !make_map(&ms16, s, cols, sr, 16))
+        return cudaErrorInvalidValue;
+    GArgs copy = ga;
+    void *args[] = {&copy, &mr64, &mr16, &ms64, &ms16};
+    return launch_ex((const void *)moe_grouped_gemm_kernel, dim3(nsm), dim3(G_THREADS), grouped_smem_bytes(), st, args);
+}
+
+cudaError_t launch_grouped_route(const GroupedArgs &a, int nsm, cudaStream_t st)
+{
+    const GWsLayout L = gws_layout(a.T);
+    uint8_t *ws = a.ws;
+    GArgs g{};
+    g.mode = GM_ROUTER;
+    g.T = a.T;
+    g.nmax = 128;
+    g.a_bf16 = 1;
+    g.f16 = 0;
+    g.K = H;
+    g.mtiles = E / 128;
+    g.wr = a.wr;
+    g.flag = reinterpret_cast<uint32_t *>(ws + L.ctrl);
+    g.logits = reinterpret_cast<float *>(ws + L.logits);
+    cudaError_t e = launch_gemm(g, nullptr, 0, a.x, (size_t)a.T, H, nsm, st);
+    if (e != cudaSuccess)
+        return e;
+    float *logits = g.logits;
+    int T = a.T;
+    int32_t *idx = reinterpret_cast<int32_t *>(ws + L.idx);
+    float *w = reinterpret_cast<float *>(ws + L.w);
+    int32_t *hist = reinterpret_cast<int32_t *>(ws + L.hist);
+    const __nv_bfloat16 *x = a.x;
+    __half *x16 = a.convert_x ? reinterpret_cast<__half *>(ws + L.x16) : nullptr;
+    int32_t *xshift = reinterpret_cast<int32_t *>(ws + L.xshift);
+    uint32_t *flag = g.flag;
+    void *targs[] = {&logits, &T, &idx, &w, &hist, &x, &x16, &xshift, &flag};
+    return launch_ex((const void *)moe_grouped_topk_kernel, dim3((a.T + G_TOK_PER_CTA - 1) / G_TOK_PER_CTA), dim3(1024),
+                     0, st, targs);
+}
+
+cudaError_t launch_grouped_layer(const GroupedArgs &a0, int nsm, cudaStream_t st)
+{
+    GroupedArgs a = a0;
+    a.convert_x = a.bf16w ? 0 : 1;
+    cudaError_t e = launch_grouped_route(a, nsm, st);
+    if (e != cudaSuccess)
+        return e;
+    const GWsLayout L = gws_layout(a.T);
+    uint8_t *ws = a.ws;
+    uint32_t *flag = reinterpret_cast<uint32_t *>(ws + L.ctrl);
+    int32_t *idx = reinterpret_cast<int32_t *>(ws + L.idx);
+    int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
+    int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    int32_t *list = reinterpret_cast<int32_t *>(ws + L.list);
+    int32_t *hist = reinterpret_cast<int32_t *>(ws + L.hist);
+    int32_t *base = reinterpret_cast<int32_t *>(ws + L.base);
+    int T = a.T;
+    int nc = (a.T + G_TOK_PER_CTA - 1) / G_TOK_PER_CTA;
+    {
+        void *sargs[] = {&hist, &nc, &base, &counts, &offsets};
+        e = launch_ex((const void *)moe_grouped_scan_kernel, dim3(1), dim3(E), 0, st, sargs);
+        if (e != cudaSuccess)
+            return e;
+        const uint16_t *src = reinterpret_cast<const uint16_t *>(a.bf16w ? (const void *)a.x : (const void *)(ws + L.x16));
+        uint16_t *xs = reinterpret_cast<uint16_t *>(ws + L.xs);
+        void *cargs[] = {&idx, &T, &base, &list, &src, &xs, &flag};
+        e = launch_ex((const void *)moe_grouped_scatter_kernel, dim3(nc), dim3(G_TOK_PER_CTA * TOPK), 0, st, cargs);
+        if (e != cudaSuccess)
+            return e;
+    }
+    const bool f16 = !a.bf16w;
+    GArgs g{};
+    g.T = a.T;
+    g.nmax = G_NMAX;
+    g.a_bf16 = a.bf16w;
+    g.f16 = f16 ? 1 : 0;
+    g.n_shared = a.n_shared;
+    g.flag = flag;
+    g.counts = counts;
+    g.offsets = offsets;
+    g.list = list;
+    g.topk_w = reinterpret_cast<const float *>(ws + L.w);
+    g.h_routed = reinterpret_cast<__nv_bfloat16 *>(ws + L.h_routed);
+    g.h_shared = reinterpret_cast<__nv_bfloat16 *>(ws + L.h_shared);
+    g.ybuf = reinterpret_cast<float *>(ws + L.ybuf);
+    g.out = a.out;
+    int32_t *hshift = reinterpret_cast<int32_t *>(ws + L.hshift);
+    if (f16) {
+        g.xshift = reinterpret_cast<const int32_t *>(ws + L.xshift);
+        g.hshift_r = hshift;
+        g.hshift_s = hshift + (size_t)T * TOPK;
+    }
+    const void *xb = f16 ? (const void *)(ws + L.x16) : (const void *)a.x;
+    const size_t nrows = (size_t)T * TOPK;
+    // gate/up: routed experts (listed tokens) and the shared expert (all tokens)
+    g.mode = GM_GATE_UP;
+    g.K = H;
+    g.mtiles = 2 * I / 128;
+    g.ra = a.r_w13;
+    g.sa = a.s_w13;
+    g.rts = a.r_ts13;
+    g.sts = a.s_ts13;
+    g.a_stride = a.bf16w ? W13_BYTES_BF : W13_BYTES;
+    if ((e = launch_gemm(g, ws + L.xs, nrows, xb, (size_t)T, H, nsm, st)) != cudaSuccess)
+        return e;
+    if (f16) {
+        // h_routed and h_shared are consecutive: one pass over all rows
+        uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h_routed);
+        int rows = T * TOPK + (a.n_shared ? T : 0);
+        void *hargs[] = {&h, &rows, &hshift};
+        if ((e = launch_ex((const void *)moe_grouped_hscale_kernel, dim3(nsm * 8), dim3(256), 0, st, hargs)) !=
+            cudaSuccess)
+            return e;
+    }
+    // down: routed experts -> weighted rows of ybuf
+    g.mode = GM_DOWN;
+    g.K = I;
+    g.mtiles = H / 128;
+    g.ra = a.r_w2;
+    g.sa = a.s_w2;
+    g.rts = a.r_ts2;
+    g.sts = a.s_ts2;
+    g.a_stride = a.bf16w ? W2_BYTES_BF : W2_BYTES;
+    if ((e = launch_gemm(g, ws + L.h_routed, nrows, nullptr, 0, I, nsm, st)) != cudaSuccess)
+        return e;
+    if (a.n_shared) {
+        g.mode = GM_SHARED_DOWN;
+        return launch_gemm(g, nullptr, 0, ws + L.h_shared, (size_t)T, I, nsm, st);
+    }
+    const float *yb = g.ybuf;
+    __nv_bfloat16 *out = a.out;
+    void *cargs[] = {&yb, &T, &out};
+    return launch_ex((const void *)moe_grouped_combine_kernel, dim3(nsm * 4), dim3(256), 0, st, cargs);
+}
+
+}  // namespace moe

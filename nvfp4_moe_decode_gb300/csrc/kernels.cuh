@@ -61,6 +61,80 @@ struct DequantArgs {
     float tscale;
 };
 
+// ---------------------------------------------------------------------------
+// Grouped path (T > MAXT): see grouped.cu.
+// ---------------------------------------------------------------------------
+constexpr int G_NMAX = 256;            // tokens per GEMM tile
+constexpr int G_TOK_PER_CTA = 128;     // tokens per CTA of the top-k / list kernels
+constexpr int MAX_TOKENS = MOE_MAX_TOKENS;
+
+enum GMode { GM_ROUTER = 0, GM_GATE_UP = 1, GM_DOWN = 2, GM_SHARED_DOWN = 3 };
+
+// Workspace of the grouped path for T tokens (bytes from the base).
+struct GWsLayout {
+    size_t ctrl;       // u32[64], [0] device flag (same place as the decode layout)
+    size_t logits;     // f32[T][E]
+    size_t idx;        // i32[T][TOPK]
+    size_t w;          // f32[T][TOPK]
+    size_t counts;     // i32[E]
+    size_t offsets;    // i32[E + 1]
+    size_t list;       // i32[T * TOPK]: 6 t + i, grouped by expert, increasing within an expert
+    size_t hist;       // i32[ceil(T / G_TOK_PER_CTA)][E] selections per expert of each top-k CTA
+    size_t base;       // i32[ceil(T / G_TOK_PER_CTA)][E] first list row of each (CTA, expert)
+    size_t x16;        // f16[T][H]: x times 2^xshift[t] (NVFP4 weights)
+    size_t xs;         // [T * TOPK][H]: the GEMM operand row (x16 or x) of each list row
+    size_t xshift;     // i32[T]
+    size_t hshift;     // i32[T * TOPK + T]: power of two of each h row (routed rows, then shared)
+    size_t h_routed;   // [T * TOPK][I]: SiLU*up of list row r (bf16; f16 x 2^hshift after the rescale)
+    size_t h_shared;   // [T][I], directly after h_routed
+    size_t ybuf;       // f32[T * TOPK][H]: weighted down output of (token, choice)
+    size_t total;
+};
+GWsLayout gws_layout(int T);
+
+// Arguments of one grouped GEMM launch.
+struct GArgs {
+    int mode;                       // GMode
+    int T;
+    int nmax;                       // tokens per tile (multiple of 16, <= G_NMAX)
+    int a_bf16;                     // A rows are bf16 (else packed NVFP4, dequantised to f16)
+    int f16;                        // operands are f16 (else bf16)
+    int K;                          // reduction length
+    int mtiles;                     // 128-row M tiles per group
+    int n_shared;
+    const uint8_t *ra, *sa;         // routed bank / shared expert matrix (packed or bf16)
+    const float *rts, *sts;         // tensor scales (NVFP4)
+    size_t a_stride;                // bytes per routed expert matrix
+    const __nv_bfloat16 *wr;        // router weights (router mode)
+    const __nv_bfloat16 *x;         // [T][H]
+    uint32_t *flag;
+    float *logits;
+    const int32_t *counts, *offsets, *list;
+    const float *topk_w;
+    __nv_bfloat16 *h_routed, *h_shared;
+    float *ybuf;
+    __nv_bfloat16 *out;
+    const int32_t *xshift;          // per token (f16 operands), or null
+    const int32_t *hshift_r, *hshift_s; // per routed / shared h row (f16 operands), or null
+};
+
+// Arguments of the grouped layer (host side).
+struct GroupedArgs {
+    const __nv_bfloat16 *x;
+    const __nv_bfloat16 *wr;
+    int T;
+    int bf16w;
+    int n_shared;
+    int convert_x;                  // also write x16 / xshift (set by the launcher)
+    const uint8_t *r_w13, *r_w2, *s_w13, *s_w2;
+    const float *r_ts13, *r_ts2, *s_ts13, *s_ts2;
+    uint8_t *ws;
+    __nv_bfloat16 *out;
+};
+
+cudaError_t launch_grouped_route(const GroupedArgs &a, int nsm, cudaStream_t stream);
+cudaError_t launch_grouped_layer(const GroupedArgs &a, int nsm, cudaStream_t stream);
+
 size_t layer_smem_bytes();
 
 cudaError_t launch_router(const RouterArgs &a, cudaStream_t stream, bool pdl);

@@ -62,9 +62,9 @@ extern "C" moe_status moe_layer_forward_static(const void *x, const void *router
                                                moe_stream_t stream)
 {
     // the scratch covers T <= MOE_MAX_DECODE_T only
-    const size_t need = moe_workspace_bytes(T);
-    if (need == 0)
+    if (T < 1 || T > MOE_MAX_DECODE_T)
         return MOE_ERR_UNSUPPORTED;
+    const size_t need = moe_workspace_bytes(T);
     if (need > STATIC_SCRATCH_BYTES)
         return MOE_ERR_WORKSPACE;
     void *scratch = nullptr;

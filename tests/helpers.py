@@ -74,13 +74,20 @@ def oracle_layer(li: synth.LayerInputs, top_k: int = 6, tokens: Optional[Iterabl
     return out, idx2, w, lg, tokens
 
 
-def logit_bounds(x_bits: np.ndarray, wr_bits: np.ndarray) -> np.ndarray:
+# Above MAX_DECODE_T tokens the logits come from a tcgen05 GEMM: 128 MMAs of
+# K = 16 accumulate in sequence into fp32.  The rounding inside one MMA is not
+# documented; the bound allows 16 further roundings per MMA and takes the
+# unit as 2^-23 (truncation) instead of 2^-24.
+GEMM_DEPTH = 2 * (2048 // 16 + 16)
+
+
+def logit_bounds(x_bits: np.ndarray, wr_bits: np.ndarray, depth: int = ROUTER_DEPTH) -> np.ndarray:
     """Per-logit bound on |fp32 router logit - exact|, plus the oracle's own
-    fp64 summation error: (gamma_24(fp32) + gamma_H(fp64)) * sum_k |x_k w_ek|."""
+    fp64 summation error: (gamma_depth(fp32) + gamma_H(fp64)) * sum_k |x_k w_ek|."""
     ax = np.abs(np_bf16(x_bits))
     aw = np.abs(np_bf16(wr_bits))
     H = ax.shape[1]
-    return (gamma(ROUTER_DEPTH, U32) + gamma(H, U64)) * (ax @ aw.T) + 1e-300
+    return (gamma(depth, U32) + gamma(H, U64)) * (ax @ aw.T) + 1e-300
 
 
 def classify_selection(logits: np.ndarray, bounds: np.ndarray, oracle_idx: np.ndarray,

@@ -52,7 +52,11 @@ def test_workspace_bytes(moe_lib):
     for T in range(1, 9):
         assert m.moe_workspace_bytes(T) > 0
     assert m.moe_workspace_bytes(0) == 0
-    assert m.moe_workspace_bytes(9) == 0
+    # above the decode range the grouped path takes over, up to MAX_TOKENS
+    assert m.moe_workspace_bytes(9) >= m.moe_workspace_bytes(8)
+    assert m.moe_workspace_bytes(8192) > 400_000_000
+    assert m.moe_workspace_bytes(m.MAX_TOKENS) > m.moe_workspace_bytes(8192)
+    assert m.moe_workspace_bytes(m.MAX_TOKENS + 1) == 0
     # the fixed scratch of moe_layer_forward_static covers the largest batch
     assert m.moe_workspace_bytes(m.MAX_DECODE_T) == m.MOE_STATIC_SCRATCH_BYTES
 
@@ -71,7 +75,8 @@ def test_host_argument_errors_enqueue_nothing(moe_lib):
     ws = m.moe_workspace_bytes(1)
     assert lib.moe_route(None, dummy, 1, 256, 6, dummy, dummy, None, dummy, ws, None) == m.MOE_ERR_INVALID_ARG
     assert lib.moe_route(dummy + 2, dummy, 1, 256, 6, dummy, dummy, None, dummy, ws, None) == m.MOE_ERR_INVALID_ARG
-    assert lib.moe_route(dummy, dummy, 9, 256, 6, dummy, dummy, None, dummy, ws, None) == m.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route(dummy, dummy, m.MAX_TOKENS + 1, 256, 6, dummy, dummy, None, dummy, ws, None) == m.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route(dummy, dummy, 8192, 256, 6, dummy, dummy, None, dummy, ws, None) == m.MOE_ERR_WORKSPACE
     assert lib.moe_route(dummy, dummy, 1, 128, 6, dummy, dummy, None, dummy, ws, None) == m.MOE_ERR_UNSUPPORTED
     assert lib.moe_route(dummy, dummy, 1, 256, 6, dummy, dummy, None, dummy, 16, None) == m.MOE_ERR_WORKSPACE
     bank = m.moe_expert_bank(m.MOE_W_NVFP4, 256, dummy, dummy, dummy, dummy)
