@@ -40,11 +40,11 @@
 // A tile is (group, chunk of <= 256 tokens, 128-row M tile) with
 // D[128 weight rows][N tokens] = A[128][K] . B[N][K]^T, N = the chunk's
 // tokens rounded up to 16; tiles are dealt round-robin.  Roles:
-//   warps 0-7   A producers, one 16-row band each: raw NVFP4 super-chunks
-//               (codes of two 64-column chunks and their scales) arrive by
-//               bulk copy three super-chunks ahead and are dequantised into
-//               the 128B-swizzled K-major A stage (bf16 rows are copied there
-//               with cp.async instead);
+//   warps 0-7   A producers, one 16-row band each: every lane loads its raw
+//               NVFP4 bytes (codes and scales) three super-chunks (six
+//               64-column chunks) ahead into registers and dequantises them
+//               into the 128B-swizzled K-major A stage (bf16 rows are copied
+//               there with cp.async instead);
 //   warp 8      B producer: the tile's token rows, consecutive rows of xs,
 //               x16, h or x, by 16-row TMA tiles;
 //   warp 10     TMEM allocation and the MMA issue (one thread, 4 MMAs of
@@ -72,7 +72,6 @@ constexpr int G_AWARPS = 8;                            // A producers: one 16-ro
 constexpr int G_BWARP = 8;                             // B producer
 constexpr int G_MMA_WARP = 10;
 constexpr int G_EPI_WARP0 = 12;                        // epilogue warps 12..15 (TMEM lane quarters 0..3)
-constexpr int G_RAW_SLOTS = 4;                         // raw super-chunks per A warp
 constexpr int G_LAG = 2;                               // cp.async chunks in flight before signalling
 constexpr int G_THREADS = 512;
 constexpr int G_MAX_GROUPS = E + 1;
@@ -83,8 +82,6 @@ constexpr uint32_t G_SUSPEND_NS = 20000;               // suspend-time hint of o
 struct GSmem {
     uint8_t a[G_ASTAGES][G_A_BYTES];                   // 1024-byte aligned tiles
     uint8_t b[G_BSTAGES][G_B_BYTES];
-    uint8_t raw[G_AWARPS][G_RAW_SLOTS][SC_BYTES];      // raw NVFP4 super-chunks per A warp
-    uint64_t full_raw[G_AWARPS][G_RAW_SLOTS];
     uint64_t full_a[G_ASTAGES], empty_a[G_ASTAGES], full_b[G_BSTAGES], empty_b[G_BSTAGES];
     uint64_t d_full[2], d_empty[2];
     uint32_t tmem;
@@ -131,20 +128,6 @@ __device__ __forceinline__ bool gwait_warp(uint64_t *bar, uint32_t parity, GSmem
     if (lane == 0)
         ok = gwait(bar, parity, sm, flag);
     return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t a)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
-}
-
-__device__ __forceinline__ uint2 lds64(uint32_t a)
-{
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-    return v;
 }
 
 // TMA: one box (64 columns x the map's box rows, 128-byte swizzled rows) at (col, row).
@@ -245,9 +228,6 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             mbar_init(&sm.full_b[s], 1);
             mbar_init(&sm.empty_b[s], 1);
         }
-        for (int w = 0; w < G_AWARPS; ++w)
-            for (int s = 0; s < G_RAW_SLOTS; ++s)
-                mbar_init(&sm.full_raw[w][s], 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.d_full[i], 1);
             mbar_init(&sm.d_empty[i], 4);
@@ -325,46 +305,48 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     if (warp < G_AWARPS) {
         // ------------------------------------------------------------ A producers
         if (!a.a_bf16) {
-            // warp w dequantises band 8 mt + w (16 rows) of every chunk to f16;
-            // its raw super-chunks (1152 bytes: codes of 2 chunks + scales) come
-            // by bulk copy G_RAW_SLOTS - 1 super-chunks ahead
+            // warp w dequantises band 8 mt + w (16 rows) of every chunk to f16.
+            // Each lane loads its own raw bytes with ld.global three
+            // super-chunks ahead (a super-chunk = 1152 bytes of the band: the
+            // codes of two 64-column chunks and their scales): 16 code bytes
+            // per chunk and the 16 scale bytes of its row pair.
             const int g4 = lane >> 2, c4 = lane & 3;
             const size_t band_bytes_k = (size_t)9 * a.K;
+            const int nsc_tile = nch >> 1;                 // super-chunks per tile
             const int nsc = stream_len >> 1;               // super-chunks of this CTA's stream
-            auto fetch_sc = [&](int sci) {
-                if (lane == 0 && sci < nsc) {
-                    const Tile t = decode_tile(sm, a, tile_id((2 * sci) / nch));
-                    const int q = ((2 * sci) % nch) >> 1;
-                    const uint8_t *src = a_base(t.g) + (size_t)(8 * t.mt + warp) * band_bytes_k + (size_t)q * SC_BYTES;
-                    uint64_t *bar = &sm.full_raw[warp][sci % G_RAW_SLOTS];
-                    mbar_arrive_expect_tx(bar, SC_BYTES);
-                    bulk_g2s(sm.raw[warp][sci % G_RAW_SLOTS], src, SC_BYTES, bar);
+            int pf_ti = -1;
+            const uint8_t *pf_band = nullptr;
+            auto sc_ptr = [&](int sci) -> const uint8_t * {   // called with increasing sci
+                const int ti = sci / nsc_tile;
+                if (ti != pf_ti) {
+                    pf_ti = ti;
+                    const Tile t = decode_tile(sm, a, tile_id(ti));
+                    pf_band = a_base(t.g) + (size_t)(8 * t.mt + warp) * band_bytes_k;
+                }
+                return pf_band + (size_t)(sci % nsc_tile) * SC_BYTES;
+            };
+            uint4 rc0[3], rc1[3], rs[3];
+            auto load = [&](int j, int sci) {
+                if (sci < nsc) {
+                    const uint8_t *p = sc_ptr(sci);
+                    rc0[j] = ldg_nc_v4(p + 16 * lane);
+                    rc1[j] = ldg_nc_v4(p + 512 + 16 * lane);
+                    rs[j] = ldg_nc_v4(p + 1024 + 16 * g4);
                 }
             };
-            for (int p = 0; p < G_RAW_SLOTS - 1; ++p)
-                fetch_sc(p);
             // lane (g, c) writes 4 bytes at row 16 w + g + 8 (r & 1), 16-byte
             // chunk (2 st + (r >> 1)) ^ g, byte 4 c, for word st and byte r
             const uint32_t row0 = (uint32_t)((16 * warp + g4) * TC_ROW_BYTES) + 4u * c4;
-            for (int kk = 0; kk < stream_len; ++kk) {
-                const int sci = kk >> 1, ch = kk % nch;
-                if ((kk & 1) == 0) {
-                    fetch_sc(sci + G_RAW_SLOTS - 1);       // into the slot of super-chunk sci - 1
-                    if (!gwait_warp(&sm.full_raw[warp][sci % G_RAW_SLOTS], (sci / G_RAW_SLOTS) & 1, sm, flag, lane))
-                        break;
-                }
+            auto process = [&](int kk, const uint4 &cw, uint32_t s01, uint32_t s23) -> bool {
                 const int s = kk % G_ASTAGES;
                 if (kk >= G_ASTAGES && !gwait_warp(&sm.empty_a[s], ((kk / G_ASTAGES) - 1) & 1, sm, flag, lane))
-                    break;
-                const uint32_t raw = smem_u32(sm.raw[warp][sci % G_RAW_SLOTS]);
-                const uint4 cw = lds128(raw + (ch & 1) * 512 + 16 * lane);
-                const uint2 sw = lds64(raw + 1024 + 16 * g4 + 8 * (ch & 1));
+                    return false;
                 const uint32_t abase = smem_u32(sm.a[s]) + row0;
                 const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
                 for (int st = 0; st < 4; ++st) {
                     // scale bytes 2 st (row g) and 2 st + 1 (row g + 8)
-                    const uint32_t sc = e4m3x2_to_f16x2(((st < 2 ? sw.x : sw.y) >> (16 * (st & 1))) & 0xFFFFu);
+                    const uint32_t sc = e4m3x2_to_f16x2(((st < 2 ? s01 : s23) >> (16 * (st & 1))) & 0xFFFFu);
                     const uint32_t s_lo = __byte_perm(sc, 0, 0x1010), s_hi = __byte_perm(sc, 0, 0x3232);
                     uint32_t h[4];
                     e2m1x8_to_f16(words[st], h[0], h[1], h[2], h[3]);
@@ -380,6 +362,22 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&sm.full_a[s]);
+                return true;
+            };
+            load(0, 0);
+            load(1, 1);
+            load(2, 2);
+            bool ok = true;
+            for (int sc0 = 0; sc0 < nsc && ok; sc0 += 3) {
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    const int sci = sc0 + j;
+                    if (sci < nsc && ok) {
+                        const uint4 c0 = rc0[j], c1 = rc1[j], sw = rs[j];
+                        load(j, sci + 3);                  // refill this slot
+                        ok = process(2 * sci, c0, sw.x, sw.y) && process(2 * sci + 1, c1, sw.z, sw.w);
+                    }
+                }
             }
         } else {
             // bf16 rows: warp w copies rows 16 w .. 16 w + 15 (16 x 8 chunks of 16 bytes)
