@@ -23,7 +23,9 @@
 //     grp * #CTA + cta; a group takes ids gid, gid + G, gid + 2G, ...):
 //       gate/up unit, NVFP4 weights (slot, 4 bands): each warp streams one
 //         whole 16-row band of W13 (8 gate + 8 up rows); SiLU*up -> h (bf16)
-//         and a per-(slot, token) running max of |h|;
+//         and a per-(slot, token) running max of |h|; with at most
+//         KSPLIT_MAX_T tokens (few slots) a unit is one band instead, split
+//         in K quarters like the BF16 units below;
 //       gate/up unit, BF16 weights (slot, band): the 4 warps take one K
 //         quarter each of the band; warp 0 adds the four partials in warp
 //         order and applies SiLU*up;
@@ -63,7 +65,9 @@ constexpr int HROW = I * 2 + 16;       // padded bytes of one token's h row in s
 constexpr int HBUF = MAXT * HROW;      // one slot's h, 8.1 KB at T = 8
 constexpr uint32_t SLOT_DONE = W13_BANDS; // gate/up bands that complete a slot
 constexpr int GU_UNITS = W13_BANDS / GW;  // NVFP4: 16 gate/up units of 4 bands per slot
-constexpr int GU_UNITS_BF = W13_BANDS;    // BF16: 64 gate/up units of one band per slot
+constexpr int GU_UNITS_BF = W13_BANDS;    // BF16 (and NVFP4 at T <= KSPLIT_MAX_T): 64 units of one band per slot
+constexpr int KSPLIT_MAX_T = 2;           // NVFP4 gate/up bands split in K quarters up to this many tokens
+constexpr int KSPLIT_RED_OFF = 16384;     // byte offset of the K-split partials in xfrag (free at T <= 2)
 constexpr int DN_UNITS = W2_BANDS / GW;   // 32 down units of 4 bands per slot
 constexpr int GU_PARTS = (H / 128) / 2;   // 8 stages per W13 band
 constexpr int DN_PARTS = (I / 128) / 2;   // 2 stages per W2 band
@@ -76,10 +80,10 @@ struct FSmem {
     uint64_t full[FW][RING];
     uint64_t hbar[NG][2];
     uint64_t xbar;
-    float rpart[8][MAXT];
     int32_t sel[MAXT][TOPK];
     float selw[MAXT][TOPK];
     uint32_t bitmap[E / 32];
+    int bcnt[E / 32];
     int n_slots;
     int32_t slot_expert[MAX_SLOTS];
     float wts[MAX_SLOTS][MAXT];
@@ -277,6 +281,10 @@ template <bool BW>
 __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
 {
     static_assert(sizeof(BfRed) <= sizeof(FSmem::ring), "K-split partials fit the ring");
+    static_assert(sizeof(RouterRed) <= sizeof(FSmem::ring) / 2, "router partials fit the router warps' rings");
+    static_assert(KSPLIT_RED_OFF + sizeof(BfRed) <= sizeof(FSmem::xfrag) &&
+                      (size_t)(H / 16) * 4 * KSPLIT_MAX_T * sizeof(uint2) <= KSPLIT_RED_OFF,
+                  "K-split partials fit beside the fragments of <= KSPLIT_MAX_T tokens");
     static_assert(sizeof(FSmem::hbuf) >= (size_t)2 * MAXT * H * 2, "x and delta fit the h buffers");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     FSmem &sm = *reinterpret_cast<FSmem *>(smem_raw);
@@ -344,15 +352,21 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
 
     // ---- phase 1: work that needs nothing from the preceding kernel ----
     // units are dealt round-robin: group gid takes ids gid, gid + G, ...; the
-    // shared expert's 16 gate/up units (ids 0..15) go to group 0 of CTAs 0..15
+    // shared expert's gate/up units (ids 0..15, or 0..63 with K quarters) go
+    // to group 0 of the first CTAs.  With few tokens (T <= KSPLIT_MAX_T) an
+    // NVFP4 gate/up unit is one band and each warp takes a K quarter (two of
+    // the band's eight stages), so four times as many warps share the bytes.
+    const bool ksplit = !BW && T <= KSPLIT_MAX_T;
+    const int GUU = (BW || ksplit) ? GU_UNITS_BF : GU_UNITS;
+    auto part0 = [&](const Unit &u) { return (ksplit && !u.down) ? 2 * wq : 0; };
+    auto nparts = [&](const Unit &u) { return u.down ? DN_PARTS : (ksplit ? GU_PARTS / GW : GU_PARTS); };
     const int n_groups = NG * (int)gridDim.x;
     const int gid = grp * (int)gridDim.x + (int)blockIdx.x;
-    const bool static_shared = !BW && (a.n_shared > 0) && gid < GU_UNITS;
-    if (static_shared) {
-        const Unit u0{false, 0, 4 * gid + wq};
-        for (int p = 0; p < RING; ++p)
-            issue_stage(p, u0, p);
-    }
+    const bool static_shared = !BW && (a.n_shared > 0) && gid < GUU;
+    const Unit u0 = ksplit ? Unit{false, 0, gid} : Unit{false, 0, 4 * gid + wq};
+    const int n_pre = static_shared ? min(RING, nparts(u0)) : 0;
+    for (int p = 0; p < n_pre; ++p)
+        issue_stage(p, u0, part0(u0) + p);
     const bool router_warp = blockIdx.x < ROUTER_CTAS && warp >= 8;
     const int r_e = blockIdx.x * 2 + ((warp - 8) >> 2);
     const int r_kq = (warp - 8) & 3;
@@ -466,23 +480,13 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
                 }
             }
         }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-#pragma unroll
-            for (int t = 0; t < MAXT; ++t)
-                if (t < T)
-                    acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], off);
-        if (lane == 0) {
-#pragma unroll
-            for (int t = 0; t < MAXT; ++t)
-                if (t < T)
-                    sm.rpart[warp - 8][t] = acc[t];
-        }
-        named_barrier_sync(5, 256);
-        if ((warp == 8 || warp == 12) && lane < T) {
-            const int t = lane, w0 = warp - 8;
-            logits[t * E + r_e] = ((sm.rpart[w0][t] + sm.rpart[w0 + 1][t]) + sm.rpart[w0 + 2][t]) + sm.rpart[w0 + 3][t];
-        }
+        // the router warps' stage rings are idle until the unit loop
+        RouterRed &red = *reinterpret_cast<RouterRed *>(&sm.ring[8][0][0]);
+        float logit;
+        const int rtid = threadIdx.x - 256;
+        if (router_reduce(acc, rtid, T, red, 5, &logit))
+            logits[(rtid % MAXT) * E + blockIdx.x * 2 + rtid / MAXT] = logit;
+        fence_proxy_async();               // the ring is refilled by bulk copies later
         named_barrier_sync(5, 256);
         if (warp == 8 && lane == 0)
             red_release_add(&ctrl[2], 1u);   // publishes this CTA's logits
@@ -524,6 +528,10 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
     }
 
     // ---- phase 3: routing (every CTA, identically) ----
+    for (int i = threadIdx.x; i < MAX_SLOTS * MAXT; i += FT)
+        sm.wts[i / MAXT][i % MAXT] = 0.0f;
+    if (threadIdx.x < E / 32)
+        sm.bitmap[threadIdx.x] = 0u;
     if (threadIdx.x == 0)
         spin_until(&ctrl[2], (uint32_t)ROUTER_CTAS, flag);
     __syncthreads();
@@ -535,6 +543,7 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
         if (lane < TOPK) {
             sm.sel[warp][lane] = ex;
             sm.selw[warp][lane] = wt;
+            atomicOr(&sm.bitmap[ex >> 5], 1u << (ex & 31));
         }
         if (blockIdx.x == 0) {
             if (bad && lane == 0)
@@ -547,27 +556,19 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
     }
     __syncthreads();
     if (warp == 0) {
-        // slot table by one warp: bitmap of the selected experts, ranks, weights
-        if (lane < E / 32)
-            sm.bitmap[lane] = 0u;
-        for (int i = lane; i < MAX_SLOTS * MAXT; i += 32)
-            sm.wts[i / MAXT][i % MAXT] = 0.0f;
-        __syncwarp();
-        for (int i = lane; i < T * TOPK; i += 32) {
-            const int ei = sm.sel[i / TOPK][i % TOPK];
-            atomicOr(&sm.bitmap[ei >> 5], 1u << (ei & 31));
-        }
-        __syncwarp();
+        // slot table by one warp: ranks of the selected experts (bitmap
+        // prefix counts), then the per-token weights
         const uint32_t bits = lane < E / 32 ? sm.bitmap[lane] : 0u;
-        int cnt = __popc(bits), incl = cnt;
+        if (lane < E / 32)
+            sm.bcnt[lane] = __popc(bits);
+        __syncwarp();
+        int base = a.n_shared, total = 0;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-            if (lane >= off)
-                incl += v;
+        for (int w = 0; w < E / 32; ++w) {
+            const int c = sm.bcnt[w];
+            base += (w < lane) ? c : 0;
+            total += c;
         }
-        const int base = a.n_shared + incl - cnt;
-        const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
         {
             uint32_t b = bits;
             int r = 0;
@@ -591,8 +592,9 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             const uint32_t wbits = sm.bitmap[ei >> 5];
             const int before = __popc(wbits & ((1u << (ei & 31)) - 1u));
             int prefix = 0;
-            for (int w = 0; w < (ei >> 5); ++w)
-                prefix += __popc(sm.bitmap[w]);
+#pragma unroll
+            for (int w = 0; w < E / 32; ++w)
+                prefix += (w < (ei >> 5)) ? sm.bcnt[w] : 0;
             sm.wts[a.n_shared + prefix + before][t] = sm.selw[t][i % TOPK];
         }
     }
@@ -611,17 +613,15 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
     }
 
     // ---- phase 4: the units ----
-    constexpr int GUU = BW ? GU_UNITS_BF : GU_UNITS;
     const int gu_total = n_slots * GUU;                             // unit ids [0, gu_total): gate/up
     const int end_id = gu_total + n_slots * DN_UNITS;               // then down units
     auto unit_id = [&](int k) { return gid + k * n_groups; };
     auto decode = [&](int id) -> Unit {
         if (id < gu_total)
-            return BW ? Unit{false, id / GUU, id % GUU} : Unit{false, id / GUU, 4 * (id % GUU) + wq};
+            return (BW || ksplit) ? Unit{false, id / GUU, id % GUU} : Unit{false, id / GUU, 4 * (id % GUU) + wq};
         const int d = id - gu_total;
         return Unit{true, d / DN_UNITS, 4 * (d % DN_UNITS) + wq};
     };
-    auto nparts = [&](const Unit &u) { return u.down ? DN_PARTS : GU_PARTS; };
     // first down unit of this group, and the down-unit index of unit k
     const int k_down0 = gid >= gu_total ? 0 : (gu_total - gid + n_groups - 1) / n_groups;
     // h of down unit dk: the slot's T rows into padded rows of hbuf[grp][dk & 1]
@@ -640,9 +640,12 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
 
     // ---- stage stream of this warp: (unit k, part p) in order, RING in flight ----
     int ik = 0, ip = 0, icount = 0;      // next stage to issue
-    if (static_shared) {
-        ip = RING;                       // parts 0..RING-1 of unit 0 were issued before the wait
-        icount = RING;
+    if (n_pre > 0) {                     // the first n_pre parts of unit 0 were issued before the wait
+        icount = n_pre;
+        if (n_pre == nparts(u0))
+            ik = 1;
+        else
+            ip = n_pre;
     }
     auto issue_ahead = [&](int limit) {
         while (icount < limit) {
@@ -650,7 +653,7 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             if (id >= end_id)
                 break;
             const Unit u = decode(id);
-            issue_stage(icount % RING, u, ip);
+            issue_stage(icount % RING, u, part0(u) + ip);
             ++icount;
             if (++ip == nparts(u)) {
                 ip = 0;
@@ -817,7 +820,7 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             for (int p = 0; p < np; ++p) {
                 const int rs = ccount % RING;
                 mbar_wait_bounded(&sm.full[warp][rs], (ccount / RING) & 1, flag);
-                mma_stage(sm.ring[warp][rs], bfrag, blanes, 16 * p, lane, acc);
+                mma_stage(sm.ring[warp][rs], bfrag, blanes, 16 * (part0(u) + p), lane, acc);
                 __syncwarp();
                 ++ccount;
                 issue_ahead(ccount + RING);
@@ -827,9 +830,12 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
         post_signals();    // the previous unit's stores have landed by now
 
         const int g = lane >> 2, c = lane & 3;
-        if (!u.down && BW) {
+        bool gu_writer = !u.down;
+        if (!u.down && (BW || ksplit)) {
             // the four K quarters of the band, added in warp order by warp 0
-            BfRed &red = *reinterpret_cast<BfRed *>(&sm.ring[0][0][0]);
+            // (BF16: in the unused stage ring; NVFP4: in the unused part of xfrag)
+            BfRed &red = *reinterpret_cast<BfRed *>(BW ? &sm.ring[0][0][0]
+                                                       : reinterpret_cast<uint8_t *>(sm.xfrag) + KSPLIT_RED_OFF);
             if (wq > 0)
                 red.p[grp][k & 1][wq - 1][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
             named_barrier_sync(1 + grp, GW * 32);
@@ -839,18 +845,21 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
                     const float4 v = red.p[grp][k & 1][q][lane];
                     acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
                 }
-#pragma unroll
-                for (int tt = 0; tt < 2; ++tt) {
-                    const int t = 2 * c + tt;
-                    if (t < T) {
-                        const float gv = acc[tt], uv = acc[2 + tt];
-                        hglob[((size_t)u.slot * MAXT + t) * I + u.band * 8 + g] =
-                            __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
-                    }
-                }
-                pend_slot = u.slot;
             }
-        } else if (!u.down) {
+            gu_writer = (wq == 0);
+        }
+        if (gu_writer && BW) {
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt) {
+                const int t = 2 * c + tt;
+                if (t < T) {
+                    const float gv = acc[tt], uv = acc[2 + tt];
+                    hglob[((size_t)u.slot * MAXT + t) * I + u.band * 8 + g] =
+                        __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
+                }
+            }
+            pend_slot = u.slot;
+        } else if (gu_writer) {
             // SiLU*up for h rows 8 * band + g; running max of |h|
             const float ts = (u.slot < a.n_shared) ? __ldg(a.s_ts13 + u.slot)
                                                    : __ldg(a.r_ts13 + sm.slot_expert[u.slot]);
@@ -879,7 +888,7 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
                         atomicMax(&hmax[u.slot * MAXT + 2 * c + tt], __float_as_uint(hm[tt]));
             }
             pend_slot = u.slot;
-        } else {
+        } else if (u.down) {
             // down: one band per warp, x routing weight x tensor scale x 2^-shift
             const float ts = BW ? 1.0f
                                 : (u.slot < a.n_shared) ? __ldg(a.s_ts2 + u.slot)

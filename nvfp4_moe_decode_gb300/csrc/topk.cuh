@@ -37,7 +37,10 @@ __device__ __forceinline__ float key_logit(unsigned long long key)
 
 // Top-k of one token's E = 256 fp32 logits by one warp: returns in lanes
 // 0..TOPK-1 the selected expert (best first) and its renormalised sigmoid
-// weight, and reports whether a logit was not finite.
+// weight, and reports whether a logit was not finite.  Each lane holds 8
+// keys; every round two warp-wide max reductions (redux.sync, on the high
+// then the low 32 bits of the keys) find the best remaining key, which is
+// unique, and its owner drops it.
 __device__ __forceinline__ void warp_route_token(const float *logits_row, int lane, int &ex, float &wt,
                                                  bool &nonfinite)
 {
@@ -51,24 +54,23 @@ __device__ __forceinline__ void warp_route_token(const float *logits_row, int la
         k[m] = rank_key(v, ee);
     }
     nonfinite = __any_sync(0xFFFFFFFFu, bad);
-    // TOPK rounds of a warp-wide argmax (keys are unique: index in the low bits)
     float s = 0.0f, sum = 0.0f;
     ex = 0;
 #pragma unroll 1
     for (int i = 0; i < TOPK; ++i) {
-        unsigned long long best = k[0];
+        unsigned long long mine = k[0];
 #pragma unroll
         for (int m = 1; m < 8; ++m)
-            best = k[m] > best ? k[m] : best;
+            mine = k[m] > mine ? k[m] : mine;
+        const uint32_t hi = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(mine >> 32));
+        const uint32_t lo = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(mine >> 32) == hi ? (uint32_t)mine : 0u);
+        const unsigned long long best = ((unsigned long long)hi << 32) | lo;
+        if (mine == best) {
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-            const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-            best = o > best ? o : best;
+            for (int m = 0; m < 8; ++m)
+                if (k[m] == best)
+                    k[m] = 0ull;
         }
-#pragma unroll
-        for (int m = 0; m < 8; ++m)
-            if (k[m] == best)
-                k[m] = 0ull;
         const float si = 1.0f / (1.0f + expf(-key_logit(best)));
         sum += si;
         if (lane == i) {
@@ -77,6 +79,61 @@ __device__ __forceinline__ void warp_route_token(const float *logits_row, int la
         }
     }
     wt = s / sum;
+}
+
+// Router partial sums of a 256-thread group (2 experts x 4 warps, each lane
+// a sequential chain of 16 exact bf16 x bf16 products per token) reduced to
+// logits through shared memory: 16 threads per (expert, token) add 16
+// partials each as a balanced tree, then one thread adds those 8 as a
+// balanced tree.  Summation depth 15 + 4 + 3 = 22.
+struct RouterRed {
+    float p[2][MAXT][128];
+    float q[2][MAXT][8];
+};
+
+__device__ __forceinline__ float tree16(const float *v)
+{
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        a[i] = v[2 * i] + v[2 * i + 1];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        a[i] = a[2 * i] + a[2 * i + 1];
+    return (a[0] + a[1]) + (a[2] + a[3]);
+}
+
+__device__ __forceinline__ float tree8(const float *v)
+{
+    return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+}
+
+// tid: 0..255 within the group (warp w of the group: expert w / 4, K quarter
+// w % 4).  Afterwards threads tid < 2 * MAXT with t = tid % MAXT < T return
+// true with the logit of (expert e0 + tid / MAXT, token t) in *logit.
+__device__ __forceinline__ bool router_reduce(const float acc[MAXT], int tid, int T, RouterRed &r, int bar_id,
+                                              float *logit)
+{
+    const int e = tid >> 7, i = tid & 127;
+#pragma unroll
+    for (int t = 0; t < MAXT; ++t)
+        if (t < T)
+            r.p[e][t][i] = acc[t];
+    asm volatile("bar.sync %0, 256;" ::"r"(bar_id) : "memory");
+    if (tid < 2 * MAXT * 8) {
+        const int ee = tid / (MAXT * 8), t = (tid / 8) % MAXT, g = tid % 8;
+        if (t < T)
+            r.q[ee][t][g] = tree16(&r.p[ee][t][16 * g]);
+    }
+    asm volatile("bar.sync %0, 256;" ::"r"(bar_id) : "memory");
+    if (tid < 2 * MAXT) {
+        const int ee = tid / MAXT, t = tid % MAXT;
+        if (t < T) {
+            *logit = tree8(r.q[ee][t]);
+            return true;
+        }
+    }
+    return false;
 }
 
 }  // namespace moe
