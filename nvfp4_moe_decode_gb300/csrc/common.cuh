@@ -79,7 +79,6 @@ struct WsLayout {
     size_t ctrl;       // u32[64]: [0] device flag, [1] routing-kernel arrivals,
                        //   [2] layer-kernel router arrivals, [3] unit queue, [4] CTAs done
     size_t slot_cnt;   // u32[MAX_SLOTS] gate/up bands finished per slot
-    size_t hmax;       // u32[MAX_SLOTS][MAXT] running max |h| (float bits) per slot, token
     size_t band_cnt;   // u32[W2_BANDS] down partials arrived per 16-row band
     size_t logits;     // f32[MAXT][E]
     size_t topk_idx;   // i32[MAXT][TOPK]
@@ -105,7 +104,6 @@ __host__ __device__ inline WsLayout ws_layout()
     size_t o = 0;
     L.ctrl = o;      o = align256(o + 64 * 4);
     L.slot_cnt = o;  o = align256(o + MAX_SLOTS * 4);
-    L.hmax = o;      o = align256(o + (size_t)MAX_SLOTS * MAXT * 4);
     L.band_cnt = o;  o = align256(o + W2_BANDS * 4);
     L.logits = o;    o = align256(o + (size_t)MAXT * E * 4);
     L.topk_idx = o;  o = align256(o + (size_t)MAXT * TOPK * 4);

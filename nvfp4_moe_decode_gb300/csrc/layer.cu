@@ -22,16 +22,16 @@
 //  4. units are dealt round-robin to the 4 x #CTA groups (group id
 //     grp * #CTA + cta; a group takes ids gid, gid + G, gid + 2G, ...):
 //       gate/up unit, NVFP4 weights (slot, 4 bands): each warp streams one
-//         whole 16-row band of W13 (8 gate + 8 up rows); SiLU*up -> h (bf16)
-//         and a per-(slot, token) running max of |h|; with at most
-//         KSPLIT_MAX_T tokens (few slots) a unit is one band instead, split
-//         in K quarters like the BF16 units below;
+//         whole 16-row band of W13 (8 gate + 8 up rows); SiLU*up -> h (bf16);
+//         with at most KSPLIT_MAX_T tokens (few slots) a unit is one band
+//         instead, split in K quarters like the BF16 units below;
 //       gate/up unit, BF16 weights (slot, band): the 4 warps take one K
 //         quarter each of the band; warp 0 adds the four partials in warp
 //         order and applies SiLU*up;
 //       down unit (slot, 4 bands): once the slot's 64 gate/up bands are done,
-//         the slot's h arrives by bulk copy and is rescaled in place to f16
-//         fragments; each warp computes one 16-row band of W2 h, times the
+//         the slot's h arrives by bulk copy, each token's row is scaled by the
+//         power of two of its max |h| (found there) into f16 fragments in
+//         place; each warp computes one 16-row band of W2 h, times the
 //         routing weight;
 //     gate/up ids precede down ids and every group walks its ids in
 //     increasing order, so a down unit only waits on gate/up units that other
@@ -293,7 +293,6 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
     uint32_t *ctrl = reinterpret_cast<uint32_t *>(a.ws + L.ctrl);
     uint32_t *flag = ctrl;
     uint32_t *slot_cnt = reinterpret_cast<uint32_t *>(a.ws + L.slot_cnt);
-    uint32_t *hmax = reinterpret_cast<uint32_t *>(a.ws + L.hmax);
     uint32_t *band_cnt = reinterpret_cast<uint32_t *>(a.ws + L.band_cnt);
     float *logits = reinterpret_cast<float *>(a.ws + L.logits);
     __nv_bfloat16 *hglob = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.h);
@@ -627,10 +626,6 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
     // h of down unit dk: the slot's T rows into padded rows of hbuf[grp][dk & 1]
     // (leader lane only; the slot counter has been acquired)
     auto issue_h = [&](int slot, int b) {
-#pragma unroll
-        for (int t = 0; t < MAXT; ++t)
-            if (t < T)
-                sm.hshift[grp][b][t] = BW ? 0 : act_shift(__uint_as_float(__ldcg(&hmax[slot * MAXT + t])));
         fence_proxy_async_global();   // h was published to the generic proxy by releases
         uint64_t *bar = &sm.hbar[grp][b];
         mbar_arrive_expect_tx(bar, (uint32_t)(T * I * 2));
@@ -763,6 +758,29 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
                 probe_for = -1;
             }
             mbar_wait_bounded(&sm.hbar[grp][b], (dk >> 1) & 1, flag);
+            // the power of two of each token's h row (NVFP4): its max |h|,
+            // 16 lanes per token (warp wq: tokens 2 wq, 2 wq + 1)
+            {
+                const int t = 2 * wq + (lane >> 4), i16 = lane & 15;
+                float mx = 0.f;
+                if (!BW && t < T) {
+                    const uint4 *row = reinterpret_cast<const uint4 *>(sm.hbuf[grp][b] + t * HROW) + 4 * i16;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 v = row[j];
+                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[q] << 16)),
+                                                 fabsf(__uint_as_float(w4[q] & 0xFFFF0000u))));
+                    }
+                }
+#pragma unroll
+                for (int off = 8; off >= 1; off >>= 1)
+                    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+                if (i16 == 0 && t < T)
+                    sm.hshift[grp][b][t] = BW ? 0 : act_shift(mx);
+            }
             // rescale h (padded bf16 rows) in place into f16 fragments [step][4T]
             const uint32_t *hw = reinterpret_cast<const uint32_t *>(sm.hbuf[grp][b]);
             const int nent = (I / 16) * blanes;            // <= 1024
@@ -860,32 +878,18 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             }
             pend_slot = u.slot;
         } else if (gu_writer) {
-            // SiLU*up for h rows 8 * band + g; running max of |h|
+            // SiLU*up for h rows 8 * band + g
             const float ts = (u.slot < a.n_shared) ? __ldg(a.s_ts13 + u.slot)
                                                    : __ldg(a.r_ts13 + sm.slot_expert[u.slot]);
-            float hm[2];
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt) {
                 const int t = 2 * c + tt;
-                hm[tt] = 0.f;
                 if (t < T) {
                     const float f = ts * pow2i(-sm.xshift[t]);
                     const float gv = acc[tt] * f, uv = acc[2 + tt] * f;
-                    const __nv_bfloat16 hv = __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
-                    hglob[((size_t)u.slot * MAXT + t) * I + u.band * 8 + g] = hv;
-                    hm[tt] = fabsf(__bfloat162float(hv));
+                    hglob[((size_t)u.slot * MAXT + t) * I + u.band * 8 + g] =
+                        __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
                 }
-            }
-#pragma unroll
-            for (int off = 4; off <= 16; off <<= 1) {
-                hm[0] = fmaxf(hm[0], __shfl_xor_sync(0xFFFFFFFFu, hm[0], off));
-                hm[1] = fmaxf(hm[1], __shfl_xor_sync(0xFFFFFFFFu, hm[1], off));
-            }
-            if (g == 0) {
-#pragma unroll
-                for (int tt = 0; tt < 2; ++tt)
-                    if (2 * c + tt < T)
-                        atomicMax(&hmax[u.slot * MAXT + 2 * c + tt], __float_as_uint(hm[tt]));
             }
             pend_slot = u.slot;
         } else if (u.down) {
@@ -921,8 +925,6 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             ctrl[2] = 0u;
             for (int s = 0; s < MAX_SLOTS; ++s)
                 slot_cnt[s] = 0u;
-            for (int i = 0; i < MAX_SLOTS * MAXT; ++i)
-                hmax[i] = 0u;
             __threadfence();
             ctrl[4] = 0u;
         }
