@@ -66,14 +66,13 @@ constexpr int HBUF = MAXT * HROW;      // one slot's h, 8.1 KB at T = 8
 constexpr uint32_t SLOT_DONE = W13_BANDS; // gate/up bands that complete a slot
 constexpr int GU_UNITS = W13_BANDS / GW;  // NVFP4: 16 gate/up units of 4 bands per slot
 constexpr int GU_UNITS_BF = W13_BANDS;    // BF16 (and NVFP4 at T <= KSPLIT_MAX_T): 64 units of one band per slot
-constexpr int KSPLIT_MAX_T = 2;           // NVFP4 gate/up bands split in K quarters up to this many tokens
-constexpr int KSPLIT_RED_OFF = 16384;     // byte offset of the K-split partials in xfrag (free at T <= 2)
+constexpr int KSPLIT_MAX_T = MAXT;        // NVFP4 gate/up bands split in K quarters up to this many tokens
 constexpr int DN_UNITS = W2_BANDS / GW;   // 32 down units of 4 bands per slot
 constexpr int GU_PARTS = (H / 128) / 2;   // 8 stages per W13 band
 constexpr int DN_PARTS = (I / 128) / 2;   // 2 stages per W2 band
 
 struct FSmem {
-    uint8_t ring[FW][RING][STG];       // BF16 weights: the K-split partials (BfRed) instead
+    uint8_t ring[FW][RING][STG];
     uint2 xfrag[(H / 16) * 32];        // compact: entry (step, l) at step * 4T + l
     uint8_t hbuf[NG][2][HBUF];         // raw h rows, rescaled in place into fragments;
                                        // before the unit loop: x (T x 4 KB)
@@ -90,6 +89,7 @@ struct FSmem {
     int xshift[MAXT];
     float sumsq[FW];                   // pre-norm: per-warp partial sums of squares
     int hshift[NG][2][MAXT];           // power-of-two exponents of the h in hbuf[grp][b]
+    float4 kred[NG][2][GW - 1][32];    // K-split gate/up: partials of warps 1..3, by unit parity
 };
 
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }
@@ -263,12 +263,6 @@ __device__ __forceinline__ void mma_stage(const uint8_t *stage, const uint2 *bfr
     }
 }
 
-// BF16 gate/up: partial accumulators of warps 1..3 of each group, double
-// buffered by unit parity (placed in the otherwise unused stage ring).
-struct BfRed {
-    float4 p[NG][2][GW - 1][32];
-};
-
 struct Unit {
     bool down;   // down unit (else gate/up)
     int slot;
@@ -280,11 +274,7 @@ struct Unit {
 template <bool BW>
 __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
 {
-    static_assert(sizeof(BfRed) <= sizeof(FSmem::ring), "K-split partials fit the ring");
     static_assert(sizeof(RouterRed) <= sizeof(FSmem::ring) / 2, "router partials fit the router warps' rings");
-    static_assert(KSPLIT_RED_OFF + sizeof(BfRed) <= sizeof(FSmem::xfrag) &&
-                      (size_t)(H / 16) * 4 * KSPLIT_MAX_T * sizeof(uint2) <= KSPLIT_RED_OFF,
-                  "K-split partials fit beside the fragments of <= KSPLIT_MAX_T tokens");
     static_assert(sizeof(FSmem::hbuf) >= (size_t)2 * MAXT * H * 2, "x and delta fit the h buffers");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     FSmem &sm = *reinterpret_cast<FSmem *>(smem_raw);
@@ -851,16 +841,13 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
         bool gu_writer = !u.down;
         if (!u.down && (BW || ksplit)) {
             // the four K quarters of the band, added in warp order by warp 0
-            // (BF16: in the unused stage ring; NVFP4: in the unused part of xfrag)
-            BfRed &red = *reinterpret_cast<BfRed *>(BW ? &sm.ring[0][0][0]
-                                                       : reinterpret_cast<uint8_t *>(sm.xfrag) + KSPLIT_RED_OFF);
             if (wq > 0)
-                red.p[grp][k & 1][wq - 1][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                sm.kred[grp][k & 1][wq - 1][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
             named_barrier_sync(1 + grp, GW * 32);
             if (wq == 0) {
 #pragma unroll
                 for (int q = 0; q < GW - 1; ++q) {
-                    const float4 v = red.p[grp][k & 1][q][lane];
+                    const float4 v = sm.kred[grp][k & 1][q][lane];
                     acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
                 }
             }
