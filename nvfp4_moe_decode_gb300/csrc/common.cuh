@@ -60,6 +60,7 @@ constexpr size_t W2_BYTES = W2_BANDS * W2_BAND_BYTES;       // 589824
 constexpr size_t W13_BYTES_BF = (size_t)2 * I * H * 2;     // 4194304: bf16 W13 of one expert
 constexpr size_t W2_BYTES_BF = (size_t)H * I * 2;          // 2097152: bf16 W2 of one expert
 
+constexpr int H_PITCH = I + 8;          // bf16 elements per h row in the workspace (16 B of padding)
 constexpr int SC_BYTES = 1152;            // one 128-column super-chunk of a band
 constexpr int ACT_EXP = 14;               // activations scaled so max|v| is in [2^14, 2^15)
 
@@ -109,7 +110,7 @@ __host__ __device__ inline WsLayout ws_layout()
     L.topk_idx = o;  o = align256(o + (size_t)MAXT * TOPK * 4);
     L.topk_w = o;    o = align256(o + (size_t)MAXT * TOPK * 4);
     L.slots = o;     o = align256(o + sizeof(SlotTable));
-    L.h = o;         o = align256(o + (size_t)MAX_SLOTS * MAXT * I * 2);
+    L.h = o;         o = align256(o + (size_t)MAX_SLOTS * MAXT * H_PITCH * 2);
     L.partials = o;  o = align256(o + (size_t)MAX_SLOTS * H * MAXT * 4);
     L.total = o;
     return L;
@@ -314,6 +315,13 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t v, float pow
     const float hi = __uint_as_float(v & 0xFFFF0000u) * pow2;
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ __nv_bfloat162 u32_as_bf162(uint32_t v)
+{
+    __nv_bfloat162 r;
+    *reinterpret_cast<uint32_t *>(&r) = v;
+    return r;
 }
 
 __device__ __forceinline__ void fence_proxy_async()

@@ -61,7 +61,7 @@ constexpr int GW = 4;                  // warps per group
 constexpr int RING = 3;                // stages per warp
 constexpr int STG = 2 * SC_BYTES;      // 2304 bytes: two super-chunks
 constexpr int ROUTER_CTAS = E / 2;     // 128 CTAs x 2 experts
-constexpr int HROW = I * 2 + 16;       // padded bytes of one token's h row in shared memory
+constexpr int HROW = H_PITCH * 2;      // padded bytes of one token's h row (shared memory and workspace)
 constexpr int HBUF = MAXT * HROW;      // one slot's h, 8.1 KB at T = 8
 constexpr uint32_t SLOT_DONE = W13_BANDS; // gate/up bands that complete a slot
 constexpr int GU_UNITS = W13_BANDS / GW;  // NVFP4: 16 gate/up units of 4 bands per slot
@@ -89,6 +89,7 @@ struct FSmem {
     int xshift[MAXT];
     float sumsq[FW];                   // pre-norm: per-warp partial sums of squares
     int hshift[NG][2][MAXT];           // power-of-two exponents of the h in hbuf[grp][b]
+    float hmx[NG][GW][32];             // per-thread max |h| of the down unit being converted
     float4 kred[NG][2][GW - 1][32];    // K-split gate/up: partials of warps 1..3, by unit parity
 };
 
@@ -613,14 +614,14 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
     };
     // first down unit of this group, and the down-unit index of unit k
     const int k_down0 = gid >= gu_total ? 0 : (gu_total - gid + n_groups - 1) / n_groups;
-    // h of down unit dk: the slot's T rows into padded rows of hbuf[grp][dk & 1]
-    // (leader lane only; the slot counter has been acquired)
+    // h of down unit dk: the slot's T padded rows, one bulk copy into
+    // hbuf[grp][dk & 1] (leader lane only; the slot counter has been acquired)
     auto issue_h = [&](int slot, int b) {
         fence_proxy_async_global();   // h was published to the generic proxy by releases
         uint64_t *bar = &sm.hbar[grp][b];
-        mbar_arrive_expect_tx(bar, (uint32_t)(T * I * 2));
-        for (int t = 0; t < T; ++t)
-            bulk_g2s(sm.hbuf[grp][b] + t * HROW, hglob + ((size_t)slot * MAXT + t) * I, (uint32_t)(I * 2), bar);
+        const uint32_t bytes = (uint32_t)((T - 1) * HROW + I * 2);
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(sm.hbuf[grp][b], hglob + (size_t)slot * MAXT * H_PITCH, bytes, bar);
     };
 
     // ---- stage stream of this warp: (unit k, part p) in order, RING in flight ----
@@ -748,62 +749,59 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
                 probe_for = -1;
             }
             mbar_wait_bounded(&sm.hbar[grp][b], (dk >> 1) & 1, flag);
-            // the power of two of each token's h row (NVFP4): its max |h|,
-            // 16 lanes per token (warp wq: tokens 2 wq, 2 wq + 1)
-            {
-                const int t = 2 * wq + (lane >> 4), i16 = lane & 15;
-                float mx = 0.f;
-                if (!BW && t < T) {
-                    const uint4 *row = reinterpret_cast<const uint4 *>(sm.hbuf[grp][b] + t * HROW) + 4 * i16;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint4 v = row[j];
-                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[q] << 16)),
-                                                 fabsf(__uint_as_float(w4[q] & 0xFFFF0000u))));
-                    }
-                }
-#pragma unroll
-                for (int off = 8; off >= 1; off >>= 1)
-                    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-                if (i16 == 0 && t < T)
-                    sm.hshift[grp][b][t] = BW ? 0 : act_shift(mx);
-            }
-            // rescale h (padded bf16 rows) in place into f16 fragments [step][4T]
+            // rescale h (padded bf16 rows) in place into fragments [step][4T]:
+            // lane l < 4T of warp wq holds steps wq, wq + 4, ... of token
+            // l / 4; NVFP4 scales each token's row by the power of two of its
+            // max |h|, taken over the 16 threads that hold the row.
             const uint32_t *hw = reinterpret_cast<const uint32_t *>(sm.hbuf[grp][b]);
-            const int nent = (I / 16) * blanes;            // <= 1024
-            uint32_t src0[8], src1[8];
+            const bool hl = lane < blanes;
+            const int hg = lane >> 2, hc = lane & 3;
+            constexpr int HJ = (I / 16) / GW;              // steps per warp
+            uint32_t src0[HJ], src1[HJ];
+            __nv_bfloat162 m2 = __floats2bfloat162_rn(0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int e = (wq * 32 + lane) + j * (GW * 32);
+            for (int j = 0; j < HJ; ++j) {
+                const int step = wq + GW * j;
                 src0[j] = src1[j] = 0u;
-                if (e < nent) {
-                    const int step = e / blanes, l = e % blanes, g = l >> 2, c = l & 3;
+                if (hl) {
                     if (BW) {
-                        const int w0 = (g * HROW) / 4 + bf16_bcol(step, c) / 2;
+                        const int w0 = (hg * HROW) / 4 + bf16_bcol(step, hc) / 2;
                         src0[j] = hw[w0];
                         src1[j] = hw[w0 + 1];
                     } else {
-                        const int w0 = (g * HROW) / 4 + 8 * step + c;
+                        const int w0 = (hg * HROW) / 4 + 8 * step + hc;
                         src0[j] = hw[w0];
                         src1[j] = hw[w0 + 4];
                     }
                 }
+                if (!BW) {
+                    m2 = __hmax2(m2, __habs2(u32_as_bf162(src0[j])));
+                    m2 = __hmax2(m2, __habs2(u32_as_bf162(src1[j])));
+                }
             }
+            if (!BW)
+                sm.hmx[grp][wq][lane] = fmaxf(__low2float(m2), __high2float(m2));
             named_barrier_sync(1 + grp, GW * 32);
+            int sh = 0;
+            if (!BW) {
+                float mx = 0.f;
+#pragma unroll
+                for (int w = 0; w < GW; ++w) {
+                    const float4 v = reinterpret_cast<const float4 *>(sm.hmx[grp][w])[hg];
+                    mx = fmaxf(mx, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+                }
+                sh = act_shift(mx);
+            }
+            const float p = pow2i(sh);
+            if (wq == 0 && hc == 0 && hl)
+                sm.hshift[grp][b][hg] = sh;
             uint2 *hf = reinterpret_cast<uint2 *>(sm.hbuf[grp][b]);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int e = (wq * 32 + lane) + j * (GW * 32);
-                if (e < nent) {
-                    if (BW) {
-                        hf[e] = make_uint2(src0[j], src1[j]);
-                    } else {
-                        const float p = pow2i(sm.hshift[grp][b][(e % blanes) >> 2]);
-                        hf[e] = make_uint2(bf16x2_to_f16x2_scaled(src0[j], p), bf16x2_to_f16x2_scaled(src1[j], p));
-                    }
+            for (int j = 0; j < HJ; ++j) {
+                if (hl) {
+                    const int e = (wq + GW * j) * blanes + lane;
+                    hf[e] = BW ? make_uint2(src0[j], src1[j])
+                               : make_uint2(bf16x2_to_f16x2_scaled(src0[j], p), bf16x2_to_f16x2_scaled(src1[j], p));
                 }
             }
             named_barrier_sync(1 + grp, GW * 32);
@@ -859,7 +857,7 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
                 const int t = 2 * c + tt;
                 if (t < T) {
                     const float gv = acc[tt], uv = acc[2 + tt];
-                    hglob[((size_t)u.slot * MAXT + t) * I + u.band * 8 + g] =
+                    hglob[((size_t)u.slot * MAXT + t) * H_PITCH + u.band * 8 + g] =
                         __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
                 }
             }
@@ -874,7 +872,7 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
                 if (t < T) {
                     const float f = ts * pow2i(-sm.xshift[t]);
                     const float gv = acc[tt] * f, uv = acc[2 + tt] * f;
-                    hglob[((size_t)u.slot * MAXT + t) * I + u.band * 8 + g] =
+                    hglob[((size_t)u.slot * MAXT + t) * H_PITCH + u.band * 8 + g] =
                         __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
                 }
             }
