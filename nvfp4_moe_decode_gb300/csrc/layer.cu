@@ -21,13 +21,9 @@
 //     its per-token routing weight;
 //  4. units are dealt round-robin to the 4 x #CTA groups (group id
 //     grp * #CTA + cta; a group takes ids gid, gid + G, gid + 2G, ...):
-//       gate/up unit, NVFP4 weights (slot, 4 bands): each warp streams one
-//         whole 16-row band of W13 (8 gate + 8 up rows); SiLU*up -> h (bf16);
-//         with at most KSPLIT_MAX_T tokens (few slots) a unit is one band
-//         instead, split in K quarters like the BF16 units below;
-//       gate/up unit, BF16 weights (slot, band): the 4 warps take one K
-//         quarter each of the band; warp 0 adds the four partials in warp
-//         order and applies SiLU*up;
+//       gate/up unit (slot, band): the 4 warps take one K quarter each of
+//         a 16-row band of W13 (8 gate + 8 up rows); warp k % 4 adds the
+//         four partials in warp order and applies SiLU*up -> h (bf16);
 //       down unit (slot, 4 bands): once the slot's 64 gate/up bands are done,
 //         the slot's h arrives by bulk copy, each token's row is scaled by the
 //         power of two of its max |h| (found there) into f16 fragments in
@@ -64,9 +60,7 @@ constexpr int ROUTER_CTAS = E / 2;     // 128 CTAs x 2 experts
 constexpr int HROW = H_PITCH * 2;      // padded bytes of one token's h row (shared memory and workspace)
 constexpr int HBUF = MAXT * HROW;      // one slot's h, 8.1 KB at T = 8
 constexpr uint32_t SLOT_DONE = W13_BANDS; // gate/up bands that complete a slot
-constexpr int GU_UNITS = W13_BANDS / GW;  // NVFP4: 16 gate/up units of 4 bands per slot
-constexpr int GU_UNITS_BF = W13_BANDS;    // BF16 (and NVFP4 at T <= KSPLIT_MAX_T): 64 units of one band per slot
-constexpr int KSPLIT_MAX_T = MAXT;        // NVFP4 gate/up bands split in K quarters up to this many tokens
+constexpr int GUU = W13_BANDS;            // 64 gate/up units (one band each) per slot
 constexpr int DN_UNITS = W2_BANDS / GW;   // 32 down units of 4 bands per slot
 constexpr int GU_PARTS = (H / 128) / 2;   // 8 stages per W13 band
 constexpr int DN_PARTS = (I / 128) / 2;   // 2 stages per W2 band
@@ -78,6 +72,8 @@ struct FSmem {
                                        // before the unit loop: x (T x 4 KB)
     uint64_t full[FW][RING];
     uint64_t hbar[NG][2];
+    uint64_t kfull[NG][2];             // K-split gate/up: the three partials of the unit are in kred
+    uint64_t kempty[NG][2];            // K-split gate/up: the unit's writer has read kred
     uint64_t xbar;
     int32_t sel[MAXT][TOPK];
     float selw[MAXT][TOPK];
@@ -302,6 +298,10 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
         if (leader) {
             mbar_init(&sm.hbar[grp][0], 1);
             mbar_init(&sm.hbar[grp][1], 1);
+            for (int q = 0; q < 2; ++q) {
+                mbar_init(&sm.kfull[grp][q], GW - 1);
+                mbar_init(&sm.kempty[grp][q], 1);
+            }
         }
         if (threadIdx.x == 0)
             mbar_init(&sm.xbar, 1);
@@ -331,29 +331,29 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
         return reinterpret_cast<const __nv_bfloat16 *>(base);
     };
     // one stage = two super-chunks (2304 bytes) of this warp's band: part p
+    auto stage_src = [&](const Unit &u, int p) -> const uint8_t * {
+        return (u.down ? w2_src(u.slot, u.band) : w13_src(u.slot, u.band)) + (size_t)(2 * p) * SC_BYTES;
+    };
     auto issue_stage = [&](int ring_slot, const Unit &u, int p) {
         if (lane != 0)
             return;
-        const uint8_t *src = (u.down ? w2_src(u.slot, u.band) : w13_src(u.slot, u.band)) + (size_t)(2 * p) * SC_BYTES;
         uint64_t *bar = &sm.full[warp][ring_slot];
         mbar_arrive_expect_tx(bar, STG);
-        bulk_g2s(sm.ring[warp][ring_slot], src, STG, bar);
+        bulk_g2s(sm.ring[warp][ring_slot], stage_src(u, p), STG, bar);
     };
 
     // ---- phase 1: work that needs nothing from the preceding kernel ----
     // units are dealt round-robin: group gid takes ids gid, gid + G, ...; the
-    // shared expert's gate/up units (ids 0..15, or 0..63 with K quarters) go
-    // to group 0 of the first CTAs.  With few tokens (T <= KSPLIT_MAX_T) an
-    // NVFP4 gate/up unit is one band and each warp takes a K quarter (two of
-    // the band's eight stages), so four times as many warps share the bytes.
-    const bool ksplit = !BW && T <= KSPLIT_MAX_T;
-    const int GUU = (BW || ksplit) ? GU_UNITS_BF : GU_UNITS;
-    auto part0 = [&](const Unit &u) { return (ksplit && !u.down) ? 2 * wq : 0; };
-    auto nparts = [&](const Unit &u) { return u.down ? DN_PARTS : (ksplit ? GU_PARTS / GW : GU_PARTS); };
+    // shared expert's gate/up units (ids 0..63) go to group 0 of the first
+    // CTAs.  A gate/up unit is one band and each warp takes a K quarter (two
+    // of the band's eight stages), so the few slots of a small batch still
+    // spread over every warp.
+    auto part0 = [&](const Unit &u) { return u.down ? 0 : 2 * wq; };
+    auto nparts = [&](const Unit &u) { return u.down ? DN_PARTS : GU_PARTS / GW; };
     const int n_groups = NG * (int)gridDim.x;
     const int gid = grp * (int)gridDim.x + (int)blockIdx.x;
     const bool static_shared = !BW && (a.n_shared > 0) && gid < GUU;
-    const Unit u0 = ksplit ? Unit{false, 0, gid} : Unit{false, 0, 4 * gid + wq};
+    const Unit u0 = Unit{false, 0, gid};
     const int n_pre = static_shared ? min(RING, nparts(u0)) : 0;
     for (int p = 0; p < n_pre; ++p)
         issue_stage(p, u0, part0(u0) + p);
@@ -480,40 +480,49 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
         named_barrier_sync(5, 256);
         if (warp == 8 && lane == 0)
             red_release_add(&ctrl[2], 1u);   // publishes this CTA's logits
-    } else if (warp < 8 && BW) {
-        // BF16 weights: the activations enter the tensor cores as bf16, in
-        // the permuted column order of bf16_rows
-        const uint32_t *xw = reinterpret_cast<const uint32_t *>(xs);
-        for (int idx = threadIdx.x; idx < (H / 16) * blanes; idx += 256) {
-            const int step = idx / blanes, l = idx % blanes, n = l >> 2, c = l & 3;
-            const int w0 = (n * H + bf16_bcol(step, c)) / 2;
-            sm.xfrag[idx] = make_uint2(xw[w0], xw[w0 + 1]);
-        }
     } else if (warp < 8) {
-        if (warp < T) {
-            const uint4 *row = reinterpret_cast<const uint4 *>(xsh + (size_t)warp * H);
-            float m = 0.f;
-#pragma unroll
-            for (int i = 0; i < H / 256; ++i) {
-                const uint4 v = row[lane + 32 * i];
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[q] << 16)), fabsf(__uint_as_float(w4[q] & 0xFFFF0000u))));
-            }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1)
-                m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-            if (lane == 0)
-                sm.xshift[warp] = act_shift(m);
-        }
-        named_barrier_sync(6, 256);
+        // x -> mma fragments [step][4T]: lane l < 4T of warp w holds steps
+        // w, w + 8, ... of token l / 4.  BF16 weights: bf16 in the permuted
+        // column order of bf16_rows.  NVFP4: f16, each token's row scaled by
+        // the power of two of its max |x| (found first, one warp per token).
         const uint32_t *xw = reinterpret_cast<const uint32_t *>(xs);
-        for (int idx = threadIdx.x; idx < (H / 16) * blanes; idx += 256) {
-            const int step = idx / blanes, l = idx % blanes, g = l >> 2, c = l & 3;
-            const float p = pow2i(sm.xshift[g]);
-            const int w0 = (g * H + 16 * step) / 2 + c;
-            sm.xfrag[idx] = make_uint2(bf16x2_to_f16x2_scaled(xw[w0], p), bf16x2_to_f16x2_scaled(xw[w0 + 4], p));
+        const int g = lane >> 2, c = lane & 3;
+        float p = 1.0f;
+        if (!BW) {
+            if (warp < T) {
+                const uint4 *row = reinterpret_cast<const uint4 *>(xsh + (size_t)warp * H);
+                __nv_bfloat162 m2 = __floats2bfloat162_rn(0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < H / 256; ++i) {
+                    const uint4 v = row[lane + 32 * i];
+                    m2 = __hmax2(m2, __habs2(u32_as_bf162(v.x)));
+                    m2 = __hmax2(m2, __habs2(u32_as_bf162(v.y)));
+                    m2 = __hmax2(m2, __habs2(u32_as_bf162(v.z)));
+                    m2 = __hmax2(m2, __habs2(u32_as_bf162(v.w)));
+                }
+                // max |x| >= 0: its fp32 bit pattern orders like an unsigned int
+                const float m = __uint_as_float(
+                    __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fmaxf(__low2float(m2), __high2float(m2)))));
+                if (lane == 0)
+                    sm.xshift[warp] = act_shift(m);
+            }
+            named_barrier_sync(6, 256);
+            if (lane < blanes)
+                p = pow2i(sm.xshift[g]);
+        }
+        if (lane < blanes) {
+#pragma unroll 4
+            for (int step = warp; step < H / 16; step += 8) {
+                uint2 v;
+                if (BW) {
+                    const int w0 = (g * H + bf16_bcol(step, c)) / 2;
+                    v = make_uint2(xw[w0], xw[w0 + 1]);
+                } else {
+                    const int w0 = (g * H + 16 * step) / 2 + c;
+                    v = make_uint2(bf16x2_to_f16x2_scaled(xw[w0], p), bf16x2_to_f16x2_scaled(xw[w0 + 4], p));
+                }
+                sm.xfrag[step * blanes + lane] = v;
+            }
         }
     }
 
@@ -608,9 +617,9 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
     auto unit_id = [&](int k) { return gid + k * n_groups; };
     auto decode = [&](int id) -> Unit {
         if (id < gu_total)
-            return (BW || ksplit) ? Unit{false, id / GUU, id % GUU} : Unit{false, id / GUU, 4 * (id % GUU) + wq};
+            return Unit{false, (int)((unsigned)id / GUU), (int)((unsigned)id % GUU)};
         const int d = id - gu_total;
-        return Unit{true, d / DN_UNITS, 4 * (d % DN_UNITS) + wq};
+        return Unit{true, (int)((unsigned)d / DN_UNITS), 4 * (int)((unsigned)d % DN_UNITS) + wq};
     };
     // first down unit of this group, and the down-unit index of unit k
     const int k_down0 = gid >= gu_total ? 0 : (gu_total - gid + n_groups - 1) / n_groups;
@@ -833,24 +842,44 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             }
         }
 
-        post_signals();    // the previous unit's stores have landed by now
-
         const int g = lane >> 2, c = lane & 3;
         bool gu_writer = !u.down;
-        if (!u.down && (BW || ksplit)) {
-            // the four K quarters of the band, added in warp order by warp 0
-            if (wq > 0)
-                sm.kred[grp][k & 1][wq - 1][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            named_barrier_sync(1 + grp, GW * 32);
-            if (wq == 0) {
+        if (!u.down) {
+            // The four K quarters of the band are added in warp order by the
+            // unit's writer, warp k % 4; the other three hand over their
+            // partials through kred[k & 1] and go on without waiting.  A
+            // partial buffer is refilled only after its previous writer has
+            // read it.  Completion signals are posted after the handover, so
+            // their fence never delays the writer.
+            const int wr = k & (GW - 1), par = k & 1;
+            gu_writer = (wq == wr);
+            if (!gu_writer) {
+                if (k >= 2)
+                    mbar_wait_bounded(&sm.kempty[grp][par], ((k >> 1) - 1) & 1, flag);
+                sm.kred[grp][par][(wq - wr + GW - 1) & (GW - 1)][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sm.kfull[grp][par]);
+            } else {
+                mbar_wait_bounded(&sm.kfull[grp][par], (k >> 1) & 1, flag);
+                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int q = 0; q < GW - 1; ++q) {
-                    const float4 v = sm.kred[grp][k & 1][q][lane];
-                    acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
+                for (int q = 0; q < GW; ++q) {
+                    const float4 v = (q == wr) ? make_float4(acc[0], acc[1], acc[2], acc[3])
+                                               : sm.kred[grp][par][(q - wr + GW - 1) & (GW - 1)][lane];
+                    if (q == 0) {
+                        sum = v;
+                    } else {
+                        sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+                    }
                 }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sm.kempty[grp][par]);
+                acc[0] = sum.x; acc[1] = sum.y; acc[2] = sum.z; acc[3] = sum.w;
             }
-            gu_writer = (wq == 0);
         }
+        post_signals();    // the previous unit's stores have landed by now
         if (gu_writer && BW) {
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt) {
