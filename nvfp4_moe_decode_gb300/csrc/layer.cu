@@ -8,7 +8,8 @@
 // combine fused into the GEMV kernels, programmatic dependent launch so that
 // a kernel loads weights while its predecessor finishes.
 //
-// One CTA per SM, 16 warps in 4 groups of 4.  Phases:
+// One CTA per SM: 16 compute warps in 4 groups of 4, plus a sync warp.
+// Phases:
 //  1. before waiting on the preceding kernel: router CTAs load their slice of
 //     the router weights; group 0 of the first 64 CTAs starts the bulk copies
 //     of one band of the shared expert (it needs no routing);
@@ -31,12 +32,14 @@
 //         routing weight;
 //     gate/up ids precede down ids and every group walks its ids in
 //     increasing order, so a down unit only waits on gate/up units that other
-//     groups reach without waiting themselves.  Completion (a release-add
-//     after a warp barrier) is posted one unit late, when the stores it covers
-//     have landed, by a lane that issues no bulk copies, and always before the
-//     warp waits on anything;
-//  5. the last down partial of each band adds all partials in slot order
-//     (deterministic) and writes out (bf16).
+//     groups reach without waiting themselves.  A compute warp reports a
+//     finished h band or down partial through a shared-memory counter only;
+//     the sync warp turns those into the cross-CTA counts (slot counters,
+//     band counters) behind one gpu-scope fence per pass, because such a
+//     fence costs a warp about a microsecond while the SM streams weights,
+//     and it issues the h copies;
+//  5. the CTA whose count of a band is the last adds all partials of the band
+//     in slot order (deterministic, on the sync warp) and writes out (bf16).
 // NVFP4: every warp streams its units' weights through a private 3-stage ring
 // of shared-memory buffers filled by cp.async.bulk and decodes them in
 // registers.  BF16 (the W16A16 variant of the Flint page, section "From 1,096
@@ -50,8 +53,10 @@ namespace moe {
 
 namespace {
 
-constexpr int FW = 16;                 // warps per CTA
-constexpr int FT = FW * 32;            // threads per CTA
+constexpr int FW = 16;                 // compute warps per CTA
+constexpr int FT = FW * 32;            // compute threads
+constexpr int SYNC_WARP = FW;          // warp 16: cross-CTA signals, h copies, combines
+constexpr int NT = FT + 32;            // threads per CTA
 constexpr int NG = 4;                  // unit groups per CTA
 constexpr int GW = 4;                  // warps per group
 constexpr int RING = 3;                // stages per warp
@@ -87,6 +92,9 @@ struct FSmem {
     int hshift[NG][2][MAXT];           // power-of-two exponents of the h in hbuf[grp][b]
     float hmx[NG][GW][32];             // per-thread max |h| of the down unit being converted
     float4 kred[NG][2][GW - 1][32];    // K-split gate/up: partials of warps 1..3, by unit parity
+    uint32_t gu_done[NG][GW];          // gate/up units whose h warp wq of the group has stored
+    uint32_t dn_done[NG][GW];          // down units whose partial warp wq of the group has stored
+    uint32_t hrel[NG];                 // down units of the group done with their h buffer
 };
 
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }
@@ -111,14 +119,26 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p)
     return v;
 }
 
-__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v)
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acquire.gpu;" ::: "memory"); }
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ void red_relaxed_add(uint32_t *p, uint32_t v)
 {
-    uint32_t old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acquire.gpu;" ::: "memory"); }
+// CTA-scope release store / acquire load (shared-memory progress counters)
+__device__ __forceinline__ void st_release_cta(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.cta.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.cta.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 __device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v)
@@ -184,7 +204,7 @@ __host__ __device__ __forceinline__ int bf16_bcol(int step, int c)
     return 64 * (step >> 2) + 32 * (s >> 1) + 8 * c + 4 * (s & 1);
 }
 
-constexpr int BF_DEPTH = 4;            // 64-column chunks in flight per warp
+constexpr int BF_DEPTH = 2;            // 64-column chunks in flight per warp
 
 // acc += rows (ra: band rows 0..7, rb: 8..15) x activations over `nch`
 // 64-column chunks starting at column 64*chunk0 (B fragments of the
@@ -269,7 +289,7 @@ struct Unit {
 }  // namespace
 
 template <bool BW>
-__global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
+__global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
 {
     static_assert(sizeof(RouterRed) <= sizeof(FSmem::ring) / 2, "router partials fit the router warps' rings");
     static_assert(sizeof(FSmem::hbuf) >= (size_t)2 * MAXT * H * 2, "x and delta fit the h buffers");
@@ -292,7 +312,7 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
     const int T = a.T;
     const int blanes = 4 * T;
 
-    if (lane == 0) {
+    if (lane == 0 && warp < FW) {
         for (int s = 0; s < RING; ++s)
             mbar_init(&sm.full[warp][s], 1);
         if (leader) {
@@ -352,12 +372,12 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
     auto nparts = [&](const Unit &u) { return u.down ? DN_PARTS : GU_PARTS / GW; };
     const int n_groups = NG * (int)gridDim.x;
     const int gid = grp * (int)gridDim.x + (int)blockIdx.x;
-    const bool static_shared = !BW && (a.n_shared > 0) && gid < GUU;
+    const bool static_shared = !BW && warp < FW && (a.n_shared > 0) && gid < GUU;
     const Unit u0 = Unit{false, 0, gid};
     const int n_pre = static_shared ? min(RING, nparts(u0)) : 0;
     for (int p = 0; p < n_pre; ++p)
         issue_stage(p, u0, part0(u0) + p);
-    const bool router_warp = blockIdx.x < ROUTER_CTAS && warp >= 8;
+    const bool router_warp = blockIdx.x < ROUTER_CTAS && warp >= 8 && warp < FW;
     const int r_e = blockIdx.x * 2 + ((warp - 8) >> 2);
     const int r_kq = (warp - 8) & 3;
     uint4 wv[2];
@@ -421,7 +441,7 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1)
             ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-        if (lane == 0)
+        if (lane == 0 && warp < FW)
             sm.sumsq[warp] = ss;
         __syncthreads();
         if (t < T) {
@@ -531,6 +551,13 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
         sm.wts[i / MAXT][i % MAXT] = 0.0f;
     if (threadIdx.x < E / 32)
         sm.bitmap[threadIdx.x] = 0u;
+    if (threadIdx.x < NG * GW) {
+        (&sm.gu_done[0][0])[threadIdx.x] = 0u;
+        (&sm.dn_done[0][0])[threadIdx.x] = 0u;
+    }
+    if (threadIdx.x < NG)
+        sm.hrel[threadIdx.x] = 0u;
+
     if (threadIdx.x == 0)
         spin_until(&ctrl[2], (uint32_t)ROUTER_CTAS, flag);
     __syncthreads();
@@ -597,6 +624,7 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             sm.wts[a.n_shared + prefix + before][t] = sm.selw[t][i % TOPK];
         }
     }
+    fence_proxy_async();   // generic writes to the x / h region precede later bulk copies into it
     __syncthreads();
     const int n_slots = sm.n_slots;
     if (blockIdx.x == 0) {
@@ -614,7 +642,8 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
     // ---- phase 4: the units ----
     const int gu_total = n_slots * GUU;                             // unit ids [0, gu_total): gate/up
     const int end_id = gu_total + n_slots * DN_UNITS;               // then down units
-    auto unit_id = [&](int k) { return gid + k * n_groups; };
+    auto unit_id_of = [&](int group, int k) { return group + k * n_groups; };
+    auto unit_id = [&](int k) { return unit_id_of(gid, k); };
     auto decode = [&](int id) -> Unit {
         if (id < gu_total)
             return Unit{false, (int)((unsigned)id / GUU), (int)((unsigned)id % GUU)};
@@ -623,72 +652,32 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
     };
     // first down unit of this group, and the down-unit index of unit k
     const int k_down0 = gid >= gu_total ? 0 : (gu_total - gid + n_groups - 1) / n_groups;
-    // h of down unit dk: the slot's T padded rows, one bulk copy into
-    // hbuf[grp][dk & 1] (leader lane only; the slot counter has been acquired)
-    auto issue_h = [&](int slot, int b) {
+    // h of down unit dk of group g: the slot's T padded rows, one bulk copy
+    // into hbuf[g][dk & 1] (the slot counter has been acquired)
+    auto issue_h = [&](int g, int slot, int b) {
         fence_proxy_async_global();   // h was published to the generic proxy by releases
-        uint64_t *bar = &sm.hbar[grp][b];
+        uint64_t *bar = &sm.hbar[g][b];
         const uint32_t bytes = (uint32_t)((T - 1) * HROW + I * 2);
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(sm.hbuf[grp][b], hglob + (size_t)slot * MAXT * H_PITCH, bytes, bar);
+        bulk_g2s(sm.hbuf[g][b], hglob + (size_t)slot * MAXT * H_PITCH, bytes, bar);
     };
 
-    // ---- stage stream of this warp: (unit k, part p) in order, RING in flight ----
-    int ik = 0, ip = 0, icount = 0;      // next stage to issue
-    if (n_pre > 0) {                     // the first n_pre parts of unit 0 were issued before the wait
-        icount = n_pre;
-        if (n_pre == nparts(u0))
-            ik = 1;
-        else
-            ip = n_pre;
-    }
-    auto issue_ahead = [&](int limit) {
-        while (icount < limit) {
-            const int id = unit_id(ik);
-            if (id >= end_id)
-                break;
-            const Unit u = decode(id);
-            issue_stage(icount % RING, u, part0(u) + ip);
-            ++icount;
-            if (++ip == nparts(u)) {
-                ip = 0;
-                ++ik;
-            }
-        }
-    };
-    if (!BW)
-        issue_ahead(RING);
-
-    // ---- leader: h of the group's down units, issued as their slots complete ----
-    int h_next = 0;                  // next down unit whose h is not yet requested
-    int h_done = 0;                  // down units whose buffer has been released
-    int probe_for = -1;              // down unit the pending probe is for
-    uint32_t probe_val = 0u;
-    auto try_issue_h = [&]() {
-        if (!lead_thread)
-            return;
-        while (h_next < h_done + 2) {
-            const int id = unit_id(k_down0 + h_next);
-            if (id >= end_id)
-                return;
-            const int slot = decode(id).slot;
-            if (probe_for == h_next && probe_val >= SLOT_DONE) {
-                fence_acquire_gpu();     // pairs with the releases that counted the slot done
-                issue_h(slot, h_next & 1);
-                ++h_next;
-                probe_for = -1;
-                continue;
-            }
-            probe_val = ld_relaxed(&slot_cnt[slot]);   // looked at on the next call
-            probe_for = h_next;
-            return;
-        }
-    };
-
-    // The last down partial of a band adds every slot's partial in slot order.
+    // The warp that computed a band's partial for the last slot adds up the
+    // band once the other n_slots - 1 partials are counted: every slot's
+    // partial in slot order, its own last.
     auto combine_band = [&](int band) {
         const int r = lane >> 1, th = lane & 1;      // row r, tokens 4*th .. 4*th+3
         const float4 *src = reinterpret_cast<const float4 *>(partials + ((size_t)16 * band + r) * MAXT) + th;
+        if (lane == 0) {
+            for (uint32_t it = 0; ld_acquire(&band_cnt[band]) < (uint32_t)(n_slots - 1); ++it) {
+                if (it == SPIN_LIMIT) {
+                    atomicOr(flag, FLAG_TIMEOUT);
+                    break;
+                }
+                __nanosleep(32);
+            }
+        }
+        __syncwarp();
         float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
         constexpr int BATCH = 16;
         for (int s0 = 0; s0 < n_slots; s0 += BATCH) {
@@ -713,221 +702,316 @@ __global__ void __launch_bounds__(FT, 1) moe_layer_kernel(LayerArgs a)
             band_cnt[band] = 0u;
     };
 
-    // Completion signals of the previous unit, posted one unit late by lane 31
-    // (it issues no bulk copies, so the release only waits for stores).
-    int pend_slot = -1;              // gate/up: slot whose band this warp finished
-    int pend_band = -1;              // down: band whose partial this warp wrote
-    auto post_signals = [&]() {
-        if (pend_slot >= 0) {
-            __syncwarp();
-            if (lane == 31)
-                red_release_add(&slot_cnt[pend_slot], 1u);
-            pend_slot = -1;
+    // ---- the sync warp: every cross-CTA step of the unit phase ----
+    // Lane g < NG follows group g.  Each pass it (1) copies h for the
+    // group's next down unit once the slot's 64 gate/up bands are counted
+    // (two h buffers per group, refilled when the group has released one);
+    // (2) counts the bands whose h the group's warps have stored into the
+    // slot counters and their down partials (all but the last slot's) into
+    // the band counters, with one gpu-scope fence ahead of all the counts of
+    // the pass, so that no compute warp ever waits on a fence or an atomic.
+    auto run_sync_warp = [&]() {
+        const int g = lane;
+        const bool gl = lane < NG;
+        const int gid_g = g * (int)gridDim.x + (int)blockIdx.x;
+        int kd0 = 0, ndn = 0;
+        if (gl) {
+            kd0 = gid_g >= gu_total ? 0 : (gu_total - gid_g + n_groups - 1) / n_groups;
+            const int kend = gid_g >= end_id ? 0 : (end_id - gid_g + n_groups - 1) / n_groups;
+            ndn = kend - kd0;
         }
-        if (pend_band >= 0) {
-            __syncwarp();
-            uint32_t prev = 0;
-            if (lane == 31)
-                prev = atom_add_acq_rel(&band_cnt[pend_band], 1u);
-            prev = __shfl_sync(0xFFFFFFFFu, prev, 31);
-            if (prev == (uint32_t)(n_slots - 1))
-                combine_band(pend_band);
-            pend_band = -1;
+        uint32_t gsig[GW], dsig[GW], n_gu[GW];
+#pragma unroll
+        for (int q = 0; q < GW; ++q) {
+            gsig[q] = dsig[q] = 0u;
+            n_gu[q] = kd0 > q ? (uint32_t)((kd0 - q + GW - 1) / GW) : 0u;   // units k = q + 4n < kd0
+        }
+        int h_next = 0, probe_for = -1;
+        uint32_t probe_val = 0u;
+        for (uint32_t it = 0;; ++it) {
+            if (it == 4 * SPIN_LIMIT) {
+                if (lane == 0)
+                    atomicOr(flag, FLAG_TIMEOUT);
+                break;
+            }
+            bool busy = false;
+            // (1) h of the next down unit
+            if (gl && h_next < ndn && h_next < (int)ld_acquire_cta(&sm.hrel[g]) + 2) {
+                const int slot = (unit_id_of(gid_g, kd0 + h_next) - gu_total) / DN_UNITS;
+                if (probe_for == h_next && probe_val >= SLOT_DONE) {
+                    fence_acquire_gpu();     // pairs with the fences ahead of the slot's counts
+                    issue_h(g, slot, h_next & 1);
+                    ++h_next;
+                    probe_for = -1;
+                    busy = true;
+                } else {
+                    probe_val = ld_relaxed(&slot_cnt[slot]);   // looked at on the next pass
+                    probe_for = h_next;
+                }
+            }
+            // (2) counts
+            uint32_t gd[GW], dd[GW];
+            bool fresh = false;
+#pragma unroll
+            for (int q = 0; q < GW; ++q) {
+                gd[q] = gl ? ld_acquire_cta(&sm.gu_done[g][q]) : 0u;
+                dd[q] = gl ? ld_acquire_cta(&sm.dn_done[g][q]) : 0u;
+                fresh |= gd[q] != gsig[q] || dd[q] != dsig[q];
+            }
+            if (__any_sync(0xFFFFFFFFu, fresh)) {
+                busy = true;
+                fence_acq_rel_gpu();   // the stores counted below become visible before their counts
+                if (gl) {
+#pragma unroll
+                    for (int q = 0; q < GW; ++q)
+                        for (; gsig[q] < gd[q]; ++gsig[q])
+                            red_relaxed_add(&slot_cnt[(unsigned)unit_id_of(gid_g, q + GW * (int)gsig[q]) / GUU], 1u);
+#pragma unroll
+                    for (int q = 0; q < GW; ++q)
+                        for (; dsig[q] < dd[q]; ++dsig[q]) {
+                            const int d = unit_id_of(gid_g, kd0 + (int)dsig[q]) - gu_total;
+                            if (d / DN_UNITS < n_slots - 1)   // the last slot's partial is added where it is made
+                                red_relaxed_add(&band_cnt[4 * (d % DN_UNITS) + q], 1u);
+                        }
+                }
+            }
+            bool done = !gl || h_next == ndn;
+#pragma unroll
+            for (int q = 0; q < GW; ++q)
+                done = done && (!gl || (gsig[q] == n_gu[q] && dsig[q] == (uint32_t)ndn));
+            if (__all_sync(0xFFFFFFFFu, done))
+                break;
+            if (!__any_sync(0xFFFFFFFFu, busy))
+                __nanosleep(64);
         }
     };
 
-    int ccount = 0;                  // stages consumed
-    float acc[4];
-    for (int k = 0;; ++k) {
-        const int id = unit_id(k);
-        if (id >= end_id)
-            break;
-        const Unit u = decode(id);
-        try_issue_h();
-
-        const uint2 *bfrag = sm.xfrag;
-        int b = 0;
-        if (u.down) {
-            const int dk = k - k_down0;
-            b = dk & 1;
-            post_signals();    // never wait while holding a completion signal
-            if (lead_thread && h_next == dk) {
-                spin_until(&slot_cnt[u.slot], SLOT_DONE, flag);
-                issue_h(u.slot, b);
-                ++h_next;
-                probe_for = -1;
+    if (warp == SYNC_WARP) {
+        run_sync_warp();
+    } else {
+        // ---- stage stream of this warp: (unit k, part p) in order, RING in flight ----
+        int ik = 0, ip = 0, icount = 0;      // next stage to issue
+        if (n_pre > 0) {                     // the first n_pre parts of unit 0 were issued before the wait
+            icount = n_pre;
+            if (n_pre == nparts(u0))
+                ik = 1;
+            else
+                ip = n_pre;
+        }
+        auto issue_ahead = [&](int limit) {
+            while (icount < limit) {
+                const int id = unit_id(ik);
+                if (id >= end_id)
+                    break;
+                const Unit u = decode(id);
+                issue_stage(icount % RING, u, part0(u) + ip);
+                ++icount;
+                if (++ip == nparts(u)) {
+                    ip = 0;
+                    ++ik;
+                }
             }
-            mbar_wait_bounded(&sm.hbar[grp][b], (dk >> 1) & 1, flag);
-            // rescale h (padded bf16 rows) in place into fragments [step][4T]:
-            // lane l < 4T of warp wq holds steps wq, wq + 4, ... of token
-            // l / 4; NVFP4 scales each token's row by the power of two of its
-            // max |h|, taken over the 16 threads that hold the row.
-            const uint32_t *hw = reinterpret_cast<const uint32_t *>(sm.hbuf[grp][b]);
-            const bool hl = lane < blanes;
-            const int hg = lane >> 2, hc = lane & 3;
-            constexpr int HJ = (I / 16) / GW;              // steps per warp
-            uint32_t src0[HJ], src1[HJ];
-            __nv_bfloat162 m2 = __floats2bfloat162_rn(0.f, 0.f);
+        };
+        if (!BW)
+            issue_ahead(RING);
+
+        int ccount = 0;                  // stages consumed
+        uint32_t n_written = 0;          // gate/up units whose h this warp wrote
+        uint32_t n_partials = 0;         // down units whose partial this warp wrote
+        // stores of the warp, then one lane counts them (CTA scope; the sync
+        // warp makes them visible to the other CTAs)
+        auto publish = [&](uint32_t *ctr, uint32_t v) {
+            __syncwarp();
+            if (lane == 0)
+                st_release_cta(ctr, v);
+        };
+        float acc[4];
+        for (int k = 0;; ++k) {
+            const int id = unit_id(k);
+            if (id >= end_id)
+                break;
+            const Unit u = decode(id);
+
+            const uint2 *bfrag = sm.xfrag;
+            int b = 0;
+            if (u.down) {
+                const int dk = k - k_down0;
+                b = dk & 1;
+                // the sync warp copies h once the slot's gate/up bands are counted
+                mbar_wait_bounded(&sm.hbar[grp][b], (dk >> 1) & 1, flag);
+                // rescale h (padded bf16 rows) in place into fragments [step][4T]:
+                // lane l < 4T of warp wq holds steps wq, wq + 4, ... of token
+                // l / 4; NVFP4 scales each token's row by the power of two of its
+                // max |h|, taken over the 16 threads that hold the row.
+                const uint32_t *hw = reinterpret_cast<const uint32_t *>(sm.hbuf[grp][b]);
+                const bool hl = lane < blanes;
+                const int hg = lane >> 2, hc = lane & 3;
+                constexpr int HJ = (I / 16) / GW;              // steps per warp
+                uint32_t src0[HJ], src1[HJ];
+                __nv_bfloat162 m2 = __floats2bfloat162_rn(0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < HJ; ++j) {
-                const int step = wq + GW * j;
-                src0[j] = src1[j] = 0u;
-                if (hl) {
-                    if (BW) {
-                        const int w0 = (hg * HROW) / 4 + bf16_bcol(step, hc) / 2;
-                        src0[j] = hw[w0];
-                        src1[j] = hw[w0 + 1];
-                    } else {
-                        const int w0 = (hg * HROW) / 4 + 8 * step + hc;
-                        src0[j] = hw[w0];
-                        src1[j] = hw[w0 + 4];
+                for (int j = 0; j < HJ; ++j) {
+                    const int step = wq + GW * j;
+                    src0[j] = src1[j] = 0u;
+                    if (hl) {
+                        if (BW) {
+                            const int w0 = (hg * HROW) / 4 + bf16_bcol(step, hc) / 2;
+                            src0[j] = hw[w0];
+                            src1[j] = hw[w0 + 1];
+                        } else {
+                            const int w0 = (hg * HROW) / 4 + 8 * step + hc;
+                            src0[j] = hw[w0];
+                            src1[j] = hw[w0 + 4];
+                        }
+                    }
+                    if (!BW) {
+                        m2 = __hmax2(m2, __habs2(u32_as_bf162(src0[j])));
+                        m2 = __hmax2(m2, __habs2(u32_as_bf162(src1[j])));
                     }
                 }
+                if (!BW)
+                    sm.hmx[grp][wq][lane] = fmaxf(__low2float(m2), __high2float(m2));
+                named_barrier_sync(1 + grp, GW * 32);
+                int sh = 0;
                 if (!BW) {
-                    m2 = __hmax2(m2, __habs2(u32_as_bf162(src0[j])));
-                    m2 = __hmax2(m2, __habs2(u32_as_bf162(src1[j])));
-                }
-            }
-            if (!BW)
-                sm.hmx[grp][wq][lane] = fmaxf(__low2float(m2), __high2float(m2));
-            named_barrier_sync(1 + grp, GW * 32);
-            int sh = 0;
-            if (!BW) {
-                float mx = 0.f;
+                    float mx = 0.f;
 #pragma unroll
-                for (int w = 0; w < GW; ++w) {
-                    const float4 v = reinterpret_cast<const float4 *>(sm.hmx[grp][w])[hg];
-                    mx = fmaxf(mx, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+                    for (int w = 0; w < GW; ++w) {
+                        const float4 v = reinterpret_cast<const float4 *>(sm.hmx[grp][w])[hg];
+                        mx = fmaxf(mx, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+                    }
+                    sh = act_shift(mx);
                 }
-                sh = act_shift(mx);
-            }
-            const float p = pow2i(sh);
-            if (wq == 0 && hc == 0 && hl)
-                sm.hshift[grp][b][hg] = sh;
-            uint2 *hf = reinterpret_cast<uint2 *>(sm.hbuf[grp][b]);
+                const float p = pow2i(sh);
+                if (wq == 0 && hc == 0 && hl)
+                    sm.hshift[grp][b][hg] = sh;
+                uint2 *hf = reinterpret_cast<uint2 *>(sm.hbuf[grp][b]);
 #pragma unroll
-            for (int j = 0; j < HJ; ++j) {
-                if (hl) {
-                    const int e = (wq + GW * j) * blanes + lane;
-                    hf[e] = BW ? make_uint2(src0[j], src1[j])
-                               : make_uint2(bf16x2_to_f16x2_scaled(src0[j], p), bf16x2_to_f16x2_scaled(src1[j], p));
-                }
-            }
-            named_barrier_sync(1 + grp, GW * 32);
-            bfrag = hf;
-        }
-
-        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-        if (BW) {
-            const int g = lane >> 2;
-            if (!u.down) {
-                // rows: gate 8*band + g, up I + 8*band + g; K quarter wq
-                const __nv_bfloat16 *w = bf_w13(u.slot);
-                bf16_rows<H / 64 / GW>(w + (size_t)(8 * u.band + g) * H, w + (size_t)(I + 8 * u.band + g) * H,
-                                       (H / 64 / GW) * wq, bfrag, blanes, lane, acc);
-            } else {
-                const __nv_bfloat16 *w = bf_w2(u.slot);
-                bf16_rows<I / 64>(w + (size_t)(16 * u.band + g) * I, w + (size_t)(16 * u.band + g + 8) * I,
-                                  0, bfrag, blanes, lane, acc);
-            }
-        } else {
-            const int np = nparts(u);
-            for (int p = 0; p < np; ++p) {
-                const int rs = ccount % RING;
-                mbar_wait_bounded(&sm.full[warp][rs], (ccount / RING) & 1, flag);
-                mma_stage(sm.ring[warp][rs], bfrag, blanes, 16 * (part0(u) + p), lane, acc);
-                __syncwarp();
-                ++ccount;
-                issue_ahead(ccount + RING);
-            }
-        }
-
-        const int g = lane >> 2, c = lane & 3;
-        bool gu_writer = !u.down;
-        if (!u.down) {
-            // The four K quarters of the band are added in warp order by the
-            // unit's writer, warp k % 4; the other three hand over their
-            // partials through kred[k & 1] and go on without waiting.  A
-            // partial buffer is refilled only after its previous writer has
-            // read it.  Completion signals are posted after the handover, so
-            // their fence never delays the writer.
-            const int wr = k & (GW - 1), par = k & 1;
-            gu_writer = (wq == wr);
-            if (!gu_writer) {
-                if (k >= 2)
-                    mbar_wait_bounded(&sm.kempty[grp][par], ((k >> 1) - 1) & 1, flag);
-                sm.kred[grp][par][(wq - wr + GW - 1) & (GW - 1)][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&sm.kfull[grp][par]);
-            } else {
-                mbar_wait_bounded(&sm.kfull[grp][par], (k >> 1) & 1, flag);
-                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int q = 0; q < GW; ++q) {
-                    const float4 v = (q == wr) ? make_float4(acc[0], acc[1], acc[2], acc[3])
-                                               : sm.kred[grp][par][(q - wr + GW - 1) & (GW - 1)][lane];
-                    if (q == 0) {
-                        sum = v;
-                    } else {
-                        sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+                for (int j = 0; j < HJ; ++j) {
+                    if (hl) {
+                        const int e = (wq + GW * j) * blanes + lane;
+                        hf[e] = BW ? make_uint2(src0[j], src1[j])
+                                   : make_uint2(bf16x2_to_f16x2_scaled(src0[j], p), bf16x2_to_f16x2_scaled(src1[j], p));
                     }
                 }
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&sm.kempty[grp][par]);
-                acc[0] = sum.x; acc[1] = sum.y; acc[2] = sum.z; acc[3] = sum.w;
+                named_barrier_sync(1 + grp, GW * 32);
+                bfrag = hf;
             }
-        }
-        post_signals();    // the previous unit's stores have landed by now
-        if (gu_writer && BW) {
-#pragma unroll
-            for (int tt = 0; tt < 2; ++tt) {
-                const int t = 2 * c + tt;
-                if (t < T) {
-                    const float gv = acc[tt], uv = acc[2 + tt];
-                    hglob[((size_t)u.slot * MAXT + t) * H_PITCH + u.band * 8 + g] =
-                        __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
+
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+            if (BW) {
+                const int g = lane >> 2;
+                if (!u.down) {
+                    // rows: gate 8*band + g, up I + 8*band + g; K quarter wq
+                    const __nv_bfloat16 *w = bf_w13(u.slot);
+                    bf16_rows<H / 64 / GW>(w + (size_t)(8 * u.band + g) * H, w + (size_t)(I + 8 * u.band + g) * H,
+                                           (H / 64 / GW) * wq, bfrag, blanes, lane, acc);
+                } else {
+                    const __nv_bfloat16 *w = bf_w2(u.slot);
+                    bf16_rows<I / 64>(w + (size_t)(16 * u.band + g) * I, w + (size_t)(16 * u.band + g + 8) * I,
+                                      0, bfrag, blanes, lane, acc);
+                }
+            } else {
+                const int np = nparts(u);
+                for (int p = 0; p < np; ++p) {
+                    const int rs = ccount % RING;
+                    mbar_wait_bounded(&sm.full[warp][rs], (ccount / RING) & 1, flag);
+                    mma_stage(sm.ring[warp][rs], bfrag, blanes, 16 * (part0(u) + p), lane, acc);
+                    __syncwarp();
+                    ++ccount;
+                    issue_ahead(ccount + RING);
                 }
             }
-            pend_slot = u.slot;
-        } else if (gu_writer) {
-            // SiLU*up for h rows 8 * band + g
-            const float ts = (u.slot < a.n_shared) ? __ldg(a.s_ts13 + u.slot)
-                                                   : __ldg(a.r_ts13 + sm.slot_expert[u.slot]);
+
+            const int g = lane >> 2, c = lane & 3;
+            bool gu_writer = !u.down;
+            if (!u.down) {
+                // The four K quarters of the band are added in warp order by the
+                // unit's writer, warp k % 4; the other three hand over their
+                // partials through kred[k & 1] and go on without waiting.  A
+                // partial buffer is refilled only after its previous writer has
+                // read it.  Completion signals are posted after the handover, so
+                // their fence never delays the writer.
+                const int wr = k & (GW - 1), par = k & 1;
+                gu_writer = (wq == wr);
+                if (!gu_writer) {
+                    if (k >= 2)
+                        mbar_wait_bounded(&sm.kempty[grp][par], ((k >> 1) - 1) & 1, flag);
+                    sm.kred[grp][par][(wq - wr + GW - 1) & (GW - 1)][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&sm.kfull[grp][par]);
+                } else {
+                    mbar_wait_bounded(&sm.kfull[grp][par], (k >> 1) & 1, flag);
+                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int tt = 0; tt < 2; ++tt) {
-                const int t = 2 * c + tt;
-                if (t < T) {
-                    const float f = ts * pow2i(-sm.xshift[t]);
-                    const float gv = acc[tt] * f, uv = acc[2 + tt] * f;
-                    hglob[((size_t)u.slot * MAXT + t) * H_PITCH + u.band * 8 + g] =
-                        __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
+                    for (int q = 0; q < GW; ++q) {
+                        const float4 v = (q == wr) ? make_float4(acc[0], acc[1], acc[2], acc[3])
+                                                   : sm.kred[grp][par][(q - wr + GW - 1) & (GW - 1)][lane];
+                        if (q == 0) {
+                            sum = v;
+                        } else {
+                            sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&sm.kempty[grp][par]);
+                    acc[0] = sum.x; acc[1] = sum.y; acc[2] = sum.z; acc[3] = sum.w;
                 }
             }
-            pend_slot = u.slot;
-        } else if (u.down) {
-            // down: one band per warp, x routing weight x tensor scale x 2^-shift
-            const float ts = BW ? 1.0f
-                                : (u.slot < a.n_shared) ? __ldg(a.s_ts2 + u.slot)
-                                                        : __ldg(a.r_ts2 + sm.slot_expert[u.slot]);
-            float *P = partials + ((size_t)u.slot * H + 16 * u.band) * MAXT;
+            if (gu_writer && BW) {
 #pragma unroll
-            for (int tt = 0; tt < 2; ++tt) {
-                const int t = 2 * c + tt;
-                if (t < T) {
-                    const float f = sm.wts[u.slot][t] * ts * pow2i(-sm.hshift[grp][b][t]);
-                    P[g * MAXT + t] = acc[tt] * f;
-                    P[(g + 8) * MAXT + t] = acc[2 + tt] * f;
+                for (int tt = 0; tt < 2; ++tt) {
+                    const int t = 2 * c + tt;
+                    if (t < T) {
+                        const float gv = acc[tt], uv = acc[2 + tt];
+                        hglob[((size_t)u.slot * MAXT + t) * H_PITCH + u.band * 8 + g] =
+                            __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
+                    }
                 }
+                publish(&sm.gu_done[grp][wq], ++n_written);
+            } else if (gu_writer) {
+                // SiLU*up for h rows 8 * band + g
+                const float ts = (u.slot < a.n_shared) ? __ldg(a.s_ts13 + u.slot)
+                                                       : __ldg(a.r_ts13 + sm.slot_expert[u.slot]);
+#pragma unroll
+                for (int tt = 0; tt < 2; ++tt) {
+                    const int t = 2 * c + tt;
+                    if (t < T) {
+                        const float f = ts * pow2i(-sm.xshift[t]);
+                        const float gv = acc[tt] * f, uv = acc[2 + tt] * f;
+                        hglob[((size_t)u.slot * MAXT + t) * H_PITCH + u.band * 8 + g] =
+                            __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
+                    }
+                }
+                publish(&sm.gu_done[grp][wq], ++n_written);
+            } else if (u.down) {
+                // down: one band per warp, x routing weight x tensor scale x 2^-shift
+                const float ts = BW ? 1.0f
+                                    : (u.slot < a.n_shared) ? __ldg(a.s_ts2 + u.slot)
+                                                            : __ldg(a.r_ts2 + sm.slot_expert[u.slot]);
+                float *P = partials + ((size_t)u.slot * H + 16 * u.band) * MAXT;
+#pragma unroll
+                for (int tt = 0; tt < 2; ++tt) {
+                    const int t = 2 * c + tt;
+                    if (t < T) {
+                        const float f = sm.wts[u.slot][t] * ts * pow2i(-sm.hshift[grp][b][t]);
+                        P[g * MAXT + t] = acc[tt] * f;
+                        P[(g + 8) * MAXT + t] = acc[2 + tt] * f;
+                    }
+                }
+                publish(&sm.dn_done[grp][wq], ++n_partials);
+                if (u.slot == n_slots - 1)
+                    combine_band(u.band);
+                // the group's hbuf[b] is free once all four warps are done with it
+                fence_proxy_async();   // the fragments were written in place; a bulk copy refills the buffer
+                named_barrier_sync(1 + grp, GW * 32);
+                if (lead_thread)
+                    st_release_cta(&sm.hrel[grp], (uint32_t)(k - k_down0 + 1));
             }
-            pend_band = u.band;
-            // the group's hbuf[b] is free once all four warps are done with it
-            named_barrier_sync(1 + grp, GW * 32);
-            ++h_done;
         }
     }
-    post_signals();
 
     // ---- the last CTA to finish re-arms the counters for the next call ----
     __syncthreads();
@@ -966,7 +1050,7 @@ cudaError_t launch_layer(const LayerArgs &a, int grid, cudaStream_t stream, bool
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(FT);
+    cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = sizeof(FSmem);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
