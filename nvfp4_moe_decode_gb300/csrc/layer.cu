@@ -728,6 +728,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         }
         int h_next = 0, probe_for = -1;
         uint32_t probe_val = 0u;
+        bool counted_out = false;        // this CTA reads no slot counter any more
         for (uint32_t it = 0;; ++it) {
             if (it == 4 * SPIN_LIMIT) {
                 if (lane == 0)
@@ -775,7 +776,21 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                         }
                 }
             }
-            bool done = !gl || h_next == ndn;
+            bool slots_done = !gl || h_next == ndn;
+#pragma unroll
+            for (int q = 0; q < GW; ++q)
+                slots_done = slots_done && (!gl || gsig[q] == n_gu[q]);
+            if (!counted_out && __all_sync(0xFFFFFFFFu, slots_done)) {
+                // this CTA neither reads nor adds to a slot counter any more:
+                // count it out (the fence orders those accesses first)
+                __syncwarp();
+                if (lane == 0) {
+                    fence_acq_rel_gpu();
+                    red_relaxed_add(&ctrl[4], 1u);
+                }
+                counted_out = true;
+            }
+            bool done = counted_out && (!gl || h_next == ndn);
 #pragma unroll
             for (int q = 0; q < GW; ++q)
                 done = done && (!gl || (gsig[q] == n_gu[q] && dsig[q] == (uint32_t)ndn));
@@ -1013,19 +1028,23 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         }
     }
 
-    // ---- the last CTA to finish re-arms the counters for the next call ----
+    // ---- CTA 0 re-arms the counters for the next call once every CTA has
+    // stopped reading them (each sync warp counts itself in ctrl[4] after its
+    // last h copy; the band counters are re-armed by the warps that add the
+    // bands up) ----
     __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const uint32_t prev = atomicAdd(&ctrl[4], 1u);
-        if (prev == gridDim.x - 1) {
-            __threadfence();
-            ctrl[2] = 0u;
-            for (int s = 0; s < MAX_SLOTS; ++s)
-                slot_cnt[s] = 0u;
-            __threadfence();
-            ctrl[4] = 0u;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        for (uint32_t it = 0; ld_acquire(&ctrl[4]) < gridDim.x; ++it) {
+            if (it == SPIN_LIMIT) {
+                atomicOr(flag, FLAG_TIMEOUT);
+                return;
+            }
+            __nanosleep(64);
         }
+        ctrl[2] = 0u;
+        for (int s = 0; s < MAX_SLOTS; ++s)
+            slot_cnt[s] = 0u;
+        ctrl[4] = 0u;
     }
 }
 
