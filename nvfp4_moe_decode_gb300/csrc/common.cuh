@@ -78,10 +78,11 @@ constexpr uint32_t SPIN_LIMIT = 1u << 20;
 // ---------------------------------------------------------------------------
 struct WsLayout {
     size_t ctrl;       // u32[64]: [0] device flag, [1] routing-kernel arrivals,
-                       //   [2] layer-kernel router arrivals, [3] unit queue, [4] CTAs done
+                       //   [4] layer-kernel CTAs counted out, [5] layer-kernel launches
     size_t slot_cnt;   // u32[MAX_SLOTS] gate/up bands finished per slot
     size_t band_cnt;   // u32[W2_BANDS] down partials arrived per 16-row band
     size_t logits;     // f32[MAXT][E]
+    size_t tlogits;    // u64[MAXT][E]: layer kernel, (launch tag << 32) | fp32 logit bits
     size_t topk_idx;   // i32[MAXT][TOPK]
     size_t topk_w;     // f32[MAXT][TOPK]
     size_t slots;      // SlotTable
@@ -107,6 +108,7 @@ __host__ __device__ inline WsLayout ws_layout()
     L.slot_cnt = o;  o = align256(o + MAX_SLOTS * 4);
     L.band_cnt = o;  o = align256(o + W2_BANDS * 4);
     L.logits = o;    o = align256(o + (size_t)MAXT * E * 4);
+    L.tlogits = o;   o = align256(o + (size_t)MAXT * E * 8);
     L.topk_idx = o;  o = align256(o + (size_t)MAXT * TOPK * 4);
     L.topk_w = o;    o = align256(o + (size_t)MAXT * TOPK * 4);
     L.slots = o;     o = align256(o + sizeof(SlotTable));

@@ -122,6 +122,19 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p)
 __device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acquire.gpu;" ::: "memory"); }
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// 64-bit relaxed accesses at gpu scope (single-copy atomic)
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void red_relaxed_add(uint32_t *p, uint32_t v)
 {
     asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -140,23 +153,6 @@ __device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t *p)
     return v;
 }
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-
-__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v)
-{
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Bounded spin until *p >= target.  Returns false (and flags) on timeout.
-__device__ __forceinline__ bool spin_until(const uint32_t *p, uint32_t target, uint32_t *flag)
-{
-    for (uint32_t it = 0; it < SPIN_LIMIT; ++it) {
-        if (ld_acquire(p) >= target)
-            return true;
-        __nanosleep(128);
-    }
-    atomicOr(flag, FLAG_TIMEOUT);
-    return false;
-}
 
 __device__ __forceinline__ void ffma2(float &a0, float &a1, float s, float d0, float d1)
 {
@@ -301,7 +297,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
     uint32_t *flag = ctrl;
     uint32_t *slot_cnt = reinterpret_cast<uint32_t *>(a.ws + L.slot_cnt);
     uint32_t *band_cnt = reinterpret_cast<uint32_t *>(a.ws + L.band_cnt);
-    float *logits = reinterpret_cast<float *>(a.ws + L.logits);
+    unsigned long long *tlogits = reinterpret_cast<unsigned long long *>(a.ws + L.tlogits);
     __nv_bfloat16 *hglob = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.h);
     float *partials = reinterpret_cast<float *>(a.ws + L.partials);
 
@@ -389,6 +385,8 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
 
     griddep_wait();      // x is written by the preceding kernel; the counters are re-armed
     griddep_launch();    // the next kernel may start its own phase 1
+    // this launch's tag on the logits (never 0, the value a zeroed workspace holds)
+    const uint32_t ltag = __ldcg(&ctrl[5]) + 1u;
 
     // ---- phase 2: x -> shared memory; router logits | activation fragments ----
     uint8_t *xs = &sm.hbuf[0][0][0];   // T x 4 KB, free until the unit loop
@@ -494,12 +492,13 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         RouterRed &red = *reinterpret_cast<RouterRed *>(&sm.ring[8][0][0]);
         float logit;
         const int rtid = threadIdx.x - 256;
+        // each logit carries the launch tag in the same 64-bit word, so a
+        // reader that sees the tag sees the logit: no fence, no counter
         if (router_reduce(acc, rtid, T, red, 5, &logit))
-            logits[(rtid % MAXT) * E + blockIdx.x * 2 + rtid / MAXT] = logit;
+            st_relaxed_u64(&tlogits[(rtid % MAXT) * E + blockIdx.x * 2 + rtid / MAXT],
+                           ((unsigned long long)ltag << 32) | __float_as_uint(logit));
         fence_proxy_async();               // the ring is refilled by bulk copies later
         named_barrier_sync(5, 256);
-        if (warp == 8 && lane == 0)
-            red_release_add(&ctrl[2], 1u);   // publishes this CTA's logits
     } else if (warp < 8) {
         // x -> mma fragments [step][4T]: lane l < 4T of warp w holds steps
         // w, w + 8, ... of token l / 4.  BF16 weights: bf16 in the permuted
@@ -558,14 +557,33 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
     if (threadIdx.x < NG)
         sm.hrel[threadIdx.x] = 0u;
 
-    if (threadIdx.x == 0)
-        spin_until(&ctrl[2], (uint32_t)ROUTER_CTAS, flag);
     __syncthreads();
     if (warp < T) {
+        // the token's 256 logits, re-read until every one carries this launch's tag
+        const unsigned long long *row = tlogits + warp * E;
+        float v[8];
+        bool have = false;
+        for (uint32_t it = 0;; ++it) {
+            have = true;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const unsigned long long w = ld_relaxed_u64(row + lane + 32 * m);
+                v[m] = __uint_as_float((uint32_t)w);
+                have = have && (uint32_t)(w >> 32) == ltag;
+            }
+            if (__all_sync(0xFFFFFFFFu, have))
+                break;
+            if (it == SPIN_LIMIT) {
+                if (lane == 0)
+                    atomicOr(flag, FLAG_TIMEOUT);
+                break;
+            }
+            __nanosleep(32);
+        }
         int ex;
         float wt;
         bool bad;
-        warp_route_token(logits + warp * E, lane, ex, wt, bad);
+        warp_route_values(v, lane, ex, wt, bad);
         if (lane < TOPK) {
             sm.sel[warp][lane] = ex;
             sm.selw[warp][lane] = wt;
@@ -759,9 +777,18 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                 dd[q] = gl ? ld_acquire_cta(&sm.dn_done[g][q]) : 0u;
                 fresh |= gd[q] != gsig[q] || dd[q] != dsig[q];
             }
+            // new counts to add (the last slot's partials are not counted)
+            bool need = false;
+#pragma unroll
+            for (int q = 0; q < GW; ++q) {
+                need |= gd[q] != gsig[q];
+                if (dd[q] != dsig[q])
+                    need |= (unit_id_of(gid_g, kd0 + (int)dsig[q]) - gu_total) / DN_UNITS < n_slots - 1;
+            }
             if (__any_sync(0xFFFFFFFFu, fresh)) {
                 busy = true;
-                fence_acq_rel_gpu();   // the stores counted below become visible before their counts
+                if (__any_sync(0xFFFFFFFFu, need))
+                    fence_acq_rel_gpu();   // the stores counted below become visible before their counts
                 if (gl) {
 #pragma unroll
                     for (int q = 0; q < GW; ++q)
@@ -943,15 +970,18 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             if (!u.down) {
                 // The four K quarters of the band are added in warp order by the
                 // unit's writer, warp k % 4; the other three hand over their
-                // partials through kred[k & 1] and go on without waiting.  A
-                // partial buffer is refilled only after its previous writer has
-                // read it.  Completion signals are posted after the handover, so
-                // their fence never delays the writer.
+                // partials through kred[k & 1] and go on.  A partial buffer is
+                // refilled only after its previous writer has read it.
                 const int wr = k & (GW - 1), par = k & 1;
                 gu_writer = (wq == wr);
+                // Every warp, the writer too, first waits until unit k - 2's
+                // writer has read kred[par]: then all of unit k - 2's handovers
+                // have landed, so neither barrier can be a phase behind when a
+                // parity wait below looks at it (a parity wait cannot tell phase
+                // j from phase j - 2).
+                if (k >= 2)
+                    mbar_wait_bounded(&sm.kempty[grp][par], ((k >> 1) - 1) & 1, flag);
                 if (!gu_writer) {
-                    if (k >= 2)
-                        mbar_wait_bounded(&sm.kempty[grp][par], ((k >> 1) - 1) & 1, flag);
                     sm.kred[grp][par][(wq - wr + GW - 1) & (GW - 1)][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
                     __syncwarp();
                     if (lane == 0)
@@ -1030,8 +1060,8 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
 
     // ---- CTA 0 re-arms the counters for the next call once every CTA has
     // stopped reading them (each sync warp counts itself in ctrl[4] after its
-    // last h copy; the band counters are re-armed by the warps that add the
-    // bands up) ----
+    // last h copy, long after its logits were read; the band counters are
+    // re-armed by the warps that add the bands up) ----
     __syncthreads();
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         for (uint32_t it = 0; ld_acquire(&ctrl[4]) < gridDim.x; ++it) {
@@ -1041,10 +1071,10 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             }
             __nanosleep(64);
         }
-        ctrl[2] = 0u;
         for (int s = 0; s < MAX_SLOTS; ++s)
             slot_cnt[s] = 0u;
         ctrl[4] = 0u;
+        ctrl[5] = ltag;   // the next launch tags its logits ltag + 1
     }
 }
 

@@ -35,23 +35,20 @@ __device__ __forceinline__ float key_logit(unsigned long long key)
     return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
 }
 
-// Top-k of one token's E = 256 fp32 logits by one warp: returns in lanes
-// 0..TOPK-1 the selected expert (best first) and its renormalised sigmoid
-// weight, and reports whether a logit was not finite.  Each lane holds 8
-// keys; every round two warp-wide max reductions (redux.sync, on the high
-// then the low 32 bits of the keys) find the best remaining key, which is
-// unique, and its owner drops it.
-__device__ __forceinline__ void warp_route_token(const float *logits_row, int lane, int &ex, float &wt,
-                                                 bool &nonfinite)
+// Top-k of one token's E = 256 fp32 logits by one warp: lane l holds the
+// logits of experts l + 32 m (m = 0..7).  Returns in lanes 0..TOPK-1 the
+// selected expert (best first) and its renormalised sigmoid weight, and
+// reports whether a logit was not finite.  Every round two warp-wide max
+// reductions (redux.sync, on the high then the low 32 bits of the keys) find
+// the best remaining key, which is unique, and its owner drops it.
+__device__ __forceinline__ void warp_route_values(const float v[8], int lane, int &ex, float &wt, bool &nonfinite)
 {
     unsigned long long k[8];
     bool bad = false;
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-        const int ee = lane + 32 * m;
-        const float v = __ldcg(logits_row + ee);
-        bad |= !isfinite(v);
-        k[m] = rank_key(v, ee);
+        bad |= !isfinite(v[m]);
+        k[m] = rank_key(v[m], lane + 32 * m);
     }
     nonfinite = __any_sync(0xFFFFFFFFu, bad);
     float s = 0.0f, sum = 0.0f;
@@ -79,6 +76,17 @@ __device__ __forceinline__ void warp_route_token(const float *logits_row, int la
         }
     }
     wt = s / sum;
+}
+
+// The same, reading the token's logits row from global memory (L2).
+__device__ __forceinline__ void warp_route_token(const float *logits_row, int lane, int &ex, float &wt,
+                                                 bool &nonfinite)
+{
+    float v[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+        v[m] = __ldcg(logits_row + lane + 32 * m);
+    warp_route_values(v, lane, ex, wt, nonfinite);
 }
 
 // Router partial sums of a 256-thread group (2 experts x 4 warps, each lane
