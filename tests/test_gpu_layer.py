@@ -135,3 +135,19 @@ def test_layer_tensor_scales(cuda_dev):
     out, flag, _ = _forward(pl, li.x, cuda_dev)
     assert flag == 0
     _check(li.x, li, out)
+
+
+@pytest.mark.parametrize("seed,T", [(2, 8), (3, 5)])
+def test_layer_repeated_calls_are_clean_and_identical(cuda_dev, seed, T):
+    """Many calls, each on a fresh workspace and on one reused workspace: no
+    device flag (no wait ever runs out) and bit-identical outputs.  The K-split
+    hand-over between the four warps of a group once raced when one warp ran
+    two units ahead; these cases exposed it."""
+    li = synth.make_layer(seed, T, device=cuda_dev)
+    pl = PackedLayer.from_inputs(li)
+    ref, flag, ws = _forward(pl, li.x, cuda_dev)
+    assert flag == 0
+    for i in range(16):
+        out, flag, _ = _forward(pl, li.x, cuda_dev, None if i % 2 else ws)
+        assert flag == 0, f"call {i}: device flag {flag}"
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"call {i}"
