@@ -373,15 +373,14 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
     const int n_pre = static_shared ? min(RING, nparts(u0)) : 0;
     for (int p = 0; p < n_pre; ++p)
         issue_stage(p, u0, part0(u0) + p);
-    const bool router_warp = blockIdx.x < ROUTER_CTAS && warp >= 8 && warp < FW;
-    const int r_e = blockIdx.x * 2 + ((warp - 8) >> 2);
-    const int r_kq = (warp - 8) & 3;
-    uint4 wv[2];
-    if (router_warp) {
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-            wv[m] = ldg_nc_v4(a.wr + (size_t)r_e * H + 512 * r_kq + 256 * m + 8 * lane);
-    }
+    // router CTAs: warp w of the 16 takes expert 2 * cta + w / 8, columns
+    // [256 (w % 8), 256 (w % 8) + 256), eight per lane
+    const bool router_warp = blockIdx.x < ROUTER_CTAS && warp < FW;
+    const int r_e = blockIdx.x * 2 + (warp >> 3);
+    const int r_k8 = warp & 7;
+    uint4 wv = make_uint4(0u, 0u, 0u, 0u);
+    if (router_warp)
+        wv = ldg_nc_v4(a.wr + (size_t)r_e * H + 256 * r_k8 + 8 * lane);
 
     griddep_wait();      // x is written by the preceding kernel; the counters are re-armed
     griddep_launch();    // the next kernel may start its own phase 1
@@ -471,35 +470,32 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
 
     if (router_warp) {
         float acc[MAXT];
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
         for (int t = 0; t < MAXT; ++t) {
             acc[t] = 0.0f;
             if (t < T) {
+                const uint4 xv = *reinterpret_cast<const uint4 *>(xsh + (size_t)t * H + 256 * r_k8 + 8 * lane);
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    const uint4 xv = *reinterpret_cast<const uint4 *>(xsh + (size_t)t * H + 512 * r_kq + 256 * m + 8 * lane);
-                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                    const uint32_t ww[4] = {wv[m].x, wv[m].y, wv[m].z, wv[m].w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc[t] = fmaf(bf16_bits_to_float(xw[q] & 0xFFFFu), bf16_bits_to_float(ww[q] & 0xFFFFu), acc[t]);
-                        acc[t] = fmaf(bf16_bits_to_float(xw[q] >> 16), bf16_bits_to_float(ww[q] >> 16), acc[t]);
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    acc[t] = fmaf(bf16_bits_to_float(xw[q] & 0xFFFFu), bf16_bits_to_float(ww[q] & 0xFFFFu), acc[t]);
+                    acc[t] = fmaf(bf16_bits_to_float(xw[q] >> 16), bf16_bits_to_float(ww[q] >> 16), acc[t]);
                 }
             }
         }
-        // the router warps' stage rings are idle until the unit loop
+        // the stage rings of warps 8..15 are idle until the unit loop (the
+        // shared expert's early copies go to warps 0..3)
         RouterRed &red = *reinterpret_cast<RouterRed *>(&sm.ring[8][0][0]);
         float logit;
-        const int rtid = threadIdx.x - 256;
         // each logit carries the launch tag in the same 64-bit word, so a
         // reader that sees the tag sees the logit: no fence, no counter
-        if (router_reduce(acc, rtid, T, red, 5, &logit))
-            st_relaxed_u64(&tlogits[(rtid % MAXT) * E + blockIdx.x * 2 + rtid / MAXT],
+        if (router_reduce(acc, (int)threadIdx.x, T, red, 5, &logit))
+            st_relaxed_u64(&tlogits[(threadIdx.x % MAXT) * E + blockIdx.x * 2 + threadIdx.x / MAXT],
                            ((unsigned long long)ltag << 32) | __float_as_uint(logit));
         fence_proxy_async();               // the ring is refilled by bulk copies later
-        named_barrier_sync(5, 256);
-    } else if (warp < 8) {
+    }
+    if (warp < 8) {
         // x -> mma fragments [step][4T]: lane l < 4T of warp w holds steps
         // w, w + 8, ... of token l / 4.  BF16 weights: bf16 in the permuted
         // column order of bf16_rows.  NVFP4: f16, each token's row scaled by
@@ -631,15 +627,16 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         if (lane == 0)
             sm.n_slots = a.n_shared + total;
         __syncwarp();
-        for (int i = lane; i < T * TOPK; i += 32) {
-            const int t = i / TOPK, ei = sm.sel[t][i % TOPK];
-            const uint32_t wbits = sm.bitmap[ei >> 5];
-            const int before = __popc(wbits & ((1u << (ei & 31)) - 1u));
-            int prefix = 0;
+        // slot of expert e = base of bitmap word e / 32 + the set bits below it
 #pragma unroll
-            for (int w = 0; w < E / 32; ++w)
-                prefix += (w < (ei >> 5)) ? sm.bcnt[w] : 0;
-            sm.wts[a.n_shared + prefix + before][t] = sm.selw[t][i % TOPK];
+        for (int i0 = 0; i0 < MAXT * TOPK; i0 += 32) {
+            const int i = i0 + lane;
+            const bool ok = i < T * TOPK;
+            const int t = i / TOPK, ei = ok ? sm.sel[t][i % TOPK] : 0;
+            const uint32_t wbits = __shfl_sync(0xFFFFFFFFu, bits, ei >> 5);
+            const int b0 = __shfl_sync(0xFFFFFFFFu, base, ei >> 5);
+            if (ok)
+                sm.wts[b0 + __popc(wbits & ((1u << (ei & 31)) - 1u))][t] = sm.selw[t][i % TOPK];
         }
     }
     fence_proxy_async();   // generic writes to the x / h region precede later bulk copies into it

@@ -51,8 +51,7 @@ __device__ __forceinline__ void warp_route_values(const float v[8], int lane, in
         k[m] = rank_key(v[m], lane + 32 * m);
     }
     nonfinite = __any_sync(0xFFFFFFFFu, bad);
-    float s = 0.0f, sum = 0.0f;
-    ex = 0;
+    unsigned long long chosen = 0ull;   // lane i < TOPK: the i-th best key
 #pragma unroll 1
     for (int i = 0; i < TOPK; ++i) {
         unsigned long long mine = k[0];
@@ -68,14 +67,17 @@ __device__ __forceinline__ void warp_route_values(const float v[8], int lane, in
                 if (k[m] == best)
                     k[m] = 0ull;
         }
-        const float si = 1.0f / (1.0f + expf(-key_logit(best)));
-        sum += si;
-        if (lane == i) {
-            s = si;
-            ex = key_expert(best);
-        }
+        if (lane == i)
+            chosen = best;
     }
-    wt = s / sum;
+    // sigmoid of each chosen logit on its own lane, the sum in selection order
+    const float s = 1.0f / (1.0f + expf(-key_logit(chosen)));
+    float sum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < TOPK; ++i)
+        sum += __shfl_sync(0xFFFFFFFFu, s, i);
+    ex = lane < TOPK ? key_expert(chosen) : 0;
+    wt = lane < TOPK ? s / sum : 0.0f;
 }
 
 // The same, reading the token's logits row from global memory (L2).
@@ -89,14 +91,14 @@ __device__ __forceinline__ void warp_route_token(const float *logits_row, int la
     warp_route_values(v, lane, ex, wt, nonfinite);
 }
 
-// Router partial sums of a 256-thread group (2 experts x 4 warps, each lane
-// a sequential chain of 16 exact bf16 x bf16 products per token) reduced to
-// logits through shared memory: 16 threads per (expert, token) add 16
-// partials each as a balanced tree, then one thread adds those 8 as a
-// balanced tree.  Summation depth 15 + 4 + 3 = 22.
+// Router partial sums of the 16 compute warps of a CTA (2 experts x 8 warps,
+// each lane a sequential chain of 8 exact bf16 x bf16 products per token)
+// reduced to logits through shared memory: 16 threads per (expert, token)
+// add 16 partials each as a balanced tree, then one thread adds those 16 as
+// a balanced tree.  Summation depth 7 + 4 + 4 = 15.
 struct RouterRed {
-    float p[2][MAXT][128];
-    float q[2][MAXT][8];
+    float p[2][MAXT][256];
+    float q[2][MAXT][16];
 };
 
 __device__ __forceinline__ float tree16(const float *v)
@@ -111,33 +113,28 @@ __device__ __forceinline__ float tree16(const float *v)
     return (a[0] + a[1]) + (a[2] + a[3]);
 }
 
-__device__ __forceinline__ float tree8(const float *v)
-{
-    return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
-}
-
-// tid: 0..255 within the group (warp w of the group: expert w / 4, K quarter
-// w % 4).  Afterwards threads tid < 2 * MAXT with t = tid % MAXT < T return
-// true with the logit of (expert e0 + tid / MAXT, token t) in *logit.
+// tid: 0..511 (warp w: expert w / 8, column slice w % 8).  Afterwards threads
+// tid < 2 * MAXT with t = tid % MAXT < T return true with the logit of
+// (expert e0 + tid / MAXT, token t) in *logit.
 __device__ __forceinline__ bool router_reduce(const float acc[MAXT], int tid, int T, RouterRed &r, int bar_id,
                                               float *logit)
 {
-    const int e = tid >> 7, i = tid & 127;
+    const int e = tid >> 8, i = tid & 255;
 #pragma unroll
     for (int t = 0; t < MAXT; ++t)
         if (t < T)
             r.p[e][t][i] = acc[t];
-    asm volatile("bar.sync %0, 256;" ::"r"(bar_id) : "memory");
-    if (tid < 2 * MAXT * 8) {
-        const int ee = tid / (MAXT * 8), t = (tid / 8) % MAXT, g = tid % 8;
+    asm volatile("bar.sync %0, 512;" ::"r"(bar_id) : "memory");
+    if (tid < 2 * MAXT * 16) {
+        const int ee = tid / (MAXT * 16), t = (tid / 16) % MAXT, g = tid % 16;
         if (t < T)
             r.q[ee][t][g] = tree16(&r.p[ee][t][16 * g]);
     }
-    asm volatile("bar.sync %0, 256;" ::"r"(bar_id) : "memory");
+    asm volatile("bar.sync %0, 512;" ::"r"(bar_id) : "memory");
     if (tid < 2 * MAXT) {
         const int ee = tid / MAXT, t = tid % MAXT;
         if (t < T) {
-            *logit = tree8(r.q[ee][t]);
+            *logit = tree16(r.q[ee][t]);
             return true;
         }
     }
