@@ -57,8 +57,8 @@ def layer_bytes(T: int, n_distinct: int, n_shared: int = 1, wtype: str = "nvfp4"
 # (profiles/moe_layer_kernel_t8.md).  It holds only for the kernel sources it
 # was measured on; any change to them makes the bench report traffic as null.
 NCU_TRAFFIC = {
-    "sources_sha256": "44257e23b3f41b1d254f00dd7e3e7586efae72e9552a07be416263ba36cf9d89",
-    "per_algorithmic_byte": 165_042_944 / 161_480_704,
+    "sources_sha256": "c75e35caa8a0557e0919dcb1fc0ae2e486bceedab616f465c1546b85d2515afc",
+    "per_algorithmic_byte": 164_956_928 / 161_480_704,
 }
 KERNEL_SOURCES = ("layer.cu", "common.cuh", "kernels.cuh", "topk.cuh")
 
