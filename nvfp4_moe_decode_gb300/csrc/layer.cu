@@ -13,13 +13,15 @@
 //  1. before waiting on the preceding kernel: router CTAs load their slice of
 //     the router weights; group 0 of the first 64 CTAs starts the bulk copies
 //     of one band of the shared expert (it needs no routing);
-//  2. x arrives in shared memory by one bulk copy; CTAs 0..127 (warps 8..15)
-//     compute the fp32 logits of two experts each and publish them with a
-//     release-add; warps 0..7 turn x into f16 mma fragments;
-//  3. every CTA acquires the logits, takes the top-6 of each token (one warp
-//     per token, identical in every CTA) and builds the slot table: the shared
-//     expert, then the distinct selected experts in ascending order, each with
-//     its per-token routing weight;
+//  2. x arrives in shared memory by one bulk copy; in CTAs 0..127 the 16
+//     compute warps compute the fp32 logits of two experts and store each
+//     with the launch's tag in one 64-bit word; warps 0..7 then turn x into
+//     f16 mma fragments;
+//  3. every CTA reads the logits until each carries the launch's tag, takes
+//     the top-6 of each token (one warp per token, identical in every CTA)
+//     and builds the slot table: the shared expert, then the distinct
+//     selected experts in ascending order, each with its per-token routing
+//     weight;
 //  4. units are dealt round-robin to the 4 x #CTA groups (group id
 //     grp * #CTA + cta; a group takes ids gid, gid + G, gid + 2G, ...):
 //       gate/up unit (slot, band): the 4 warps take one K quarter each of
@@ -38,13 +40,14 @@
 //     band counters) behind one gpu-scope fence per pass, because such a
 //     fence costs a warp about a microsecond while the SM streams weights,
 //     and it issues the h copies;
-//  5. the CTA whose count of a band is the last adds all partials of the band
-//     in slot order (deterministic, on the sync warp) and writes out (bf16).
+//  5. the warp that computes a band's partial for the last slot waits until
+//     the other slots' partials of the band are counted, then adds all of
+//     them in slot order (deterministic) and writes out (bf16).
 // NVFP4: every warp streams its units' weights through a private 3-stage ring
 // of shared-memory buffers filled by cp.async.bulk and decodes them in
 // registers.  BF16 (the W16A16 variant of the Flint page, section "From 1,096
 // kernels to 346": BF16 decode): the rows are row-major in HBM, and each warp
-// loads its 16 rows straight into registers, four 64-column chunks ahead.
+// loads its 16 rows straight into registers, two 64-column chunks ahead.
 // Every wait is bounded and reports MOE_FLAG_WAIT_TIMEOUT instead of hanging.
 #include "kernels.cuh"
 #include "topk.cuh"
@@ -55,7 +58,7 @@ namespace {
 
 constexpr int FW = 16;                 // compute warps per CTA
 constexpr int FT = FW * 32;            // compute threads
-constexpr int SYNC_WARP = FW;          // warp 16: cross-CTA signals, h copies, combines
+constexpr int SYNC_WARP = FW;          // warp 16: cross-CTA counts and the h copies
 constexpr int NT = FT + 32;            // threads per CTA
 constexpr int NG = 4;                  // unit groups per CTA
 constexpr int GW = 4;                  // warps per group
@@ -91,7 +94,7 @@ struct FSmem {
     float sumsq[FW];                   // pre-norm: per-warp partial sums of squares
     int hshift[NG][2][MAXT];           // power-of-two exponents of the h in hbuf[grp][b]
     float hmx[NG][GW][32];             // per-thread max |h| of the down unit being converted
-    float4 kred[NG][2][GW - 1][32];    // K-split gate/up: partials of warps 1..3, by unit parity
+    float4 kred[NG][2][GW - 1][32];    // K-split gate/up: the non-writers' partials, by unit parity
     uint32_t gu_done[NG][GW];          // gate/up units whose h warp wq of the group has stored
     uint32_t dn_done[NG][GW];          // down units whose partial warp wq of the group has stored
     uint32_t hrel[NG];                 // down units of the group done with their h buffer
