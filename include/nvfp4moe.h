@@ -168,7 +168,10 @@ moe_status moe_dequant_nvfp4(const void *packed, int N, int K, int kind, float t
 size_t moe_workspace_bytes(int T);
 
 /* Zero a workspace (enqueued memset).  Required once before the first use of
- * a workspace; the kernels leave the counters zeroed after every call. */
+ * a workspace; every call leaves its counters re-armed for the next call (the
+ * layer kernel's launch tag, which starts at zero, advances by one per call).
+ * After a call that reported MOE_FLAG_WAIT_TIMEOUT, zero the workspace again
+ * before its next use. */
 moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
@@ -331,9 +334,8 @@ moe_status moe_stack_forward(void *x, const moe_layer_weights *layers, int n_lay
  *    cudaGetSymbolAddress (that device current) and zeroes the array on
  *    `stream`; make that first call before any stream capture.  Later calls
  *    only launch the layer.
- *  Zero state: the control words of the scratch (arrival counters, running
- *    maxima, device flag) must be zero when a call starts; the setup zeroes
- *    them and every call leaves them zero when it completes.  The device flag
+ *  Zero state: the setup zeroes the scratch; every call leaves its counters
+ *    re-armed for the next call (the launch tag advances by one).  The device flag
  *    of this scratch is not reported; a caller that needs the flags uses
  *    moe_layer_forward with its own workspace.
  *  Concurrency: one scratch per device.  Calls on the same device must not
