@@ -98,6 +98,7 @@ struct FSmem {
     uint32_t gu_done[NG][GW];          // gate/up units whose h warp wq of the group has stored
     uint32_t dn_done[NG][GW];          // down units whose partial warp wq of the group has stored
     uint32_t hrel[NG];                 // down units of the group done with their h buffer
+    uint32_t hclaim[NG];               // down units of the group whose h copy has been issued
 };
 
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }
@@ -553,8 +554,10 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         (&sm.gu_done[0][0])[threadIdx.x] = 0u;
         (&sm.dn_done[0][0])[threadIdx.x] = 0u;
     }
-    if (threadIdx.x < NG)
+    if (threadIdx.x < NG) {
         sm.hrel[threadIdx.x] = 0u;
+        sm.hclaim[threadIdx.x] = 0u;
+    }
 
     __syncthreads();
     if (warp < T) {
@@ -755,11 +758,19 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             }
             bool busy = false;
             // (1) h of the next down unit
+            if (gl && h_next < ndn) {   // copies the group's leader claimed
+                const int claimed = (int)*reinterpret_cast<volatile uint32_t *>(&sm.hclaim[g]);
+                if (claimed > h_next) {
+                    h_next = claimed;
+                    probe_for = -1;
+                }
+            }
             if (gl && h_next < ndn && h_next < (int)ld_acquire_cta(&sm.hrel[g]) + 2) {
                 const int slot = (unit_id_of(gid_g, kd0 + h_next) - gu_total) / DN_UNITS;
                 if (probe_for == h_next && probe_val >= SLOT_DONE) {
                     fence_acquire_gpu();     // pairs with the fences ahead of the slot's counts
-                    issue_h(g, slot, h_next & 1);
+                    if (atomicCAS(&sm.hclaim[g], (uint32_t)h_next, (uint32_t)h_next + 1u) == (uint32_t)h_next)
+                        issue_h(g, slot, h_next & 1);
                     ++h_next;
                     probe_for = -1;
                     busy = true;
@@ -792,13 +803,18 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                 if (gl) {
 #pragma unroll
                     for (int q = 0; q < GW; ++q)
-                        for (; gsig[q] < gd[q]; ++gsig[q])
-                            red_relaxed_add(&slot_cnt[(unsigned)unit_id_of(gid_g, q + GW * (int)gsig[q]) / GUU], 1u);
+                        for (; gsig[q] < gd[q]; ++gsig[q]) {
+                            const int kq = q + GW * (int)gsig[q];
+                            if (kq != kd0 - 1)   // the group's last gate/up band is counted by its writer
+                                red_relaxed_add(&slot_cnt[(unsigned)unit_id_of(gid_g, kq) / GUU], 1u);
+                        }
 #pragma unroll
                     for (int q = 0; q < GW; ++q)
                         for (; dsig[q] < dd[q]; ++dsig[q]) {
                             const int d = unit_id_of(gid_g, kd0 + (int)dsig[q]) - gu_total;
-                            if (d / DN_UNITS < n_slots - 1)   // the last slot's partial is added where it is made
+                            // the last slot's partial is added where it is made; the
+                            // group's last down unit is counted by its own warps
+                            if (d / DN_UNITS < n_slots - 1 && (int)dsig[q] != ndn - 1)
                                 red_relaxed_add(&band_cnt[4 * (d % DN_UNITS) + q], 1u);
                         }
                 }
@@ -867,6 +883,18 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             if (lane == 0)
                 st_release_cta(ctr, v);
         };
+        // The writer of the group's last gate/up unit goes on to a down unit
+        // that waits for h anyway (or to nothing), so it counts its band
+        // itself; the sync warp skips that count.
+        auto count_now_if_last_gu = [&](int k, int slot) {
+            if (k == k_down0 - 1) {
+                __syncwarp();
+                if (lane == 0) {
+                    fence_acq_rel_gpu();
+                    red_relaxed_add(&slot_cnt[slot], 1u);
+                }
+            }
+        };
         float acc[4];
         for (int k = 0;; ++k) {
             const int id = unit_id(k);
@@ -879,7 +907,22 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             if (u.down) {
                 const int dk = k - k_down0;
                 b = dk & 1;
-                // the sync warp copies h once the slot's gate/up bands are counted
+                // The sync warp copies h once the slot's gate/up bands are
+                // counted.  If it has not yet, the leader waits on the slot
+                // counter itself and claims the copy (whoever moves the claim
+                // counter from dk to dk + 1 issues it).
+                if (lead_thread && *reinterpret_cast<volatile uint32_t *>(&sm.hclaim[grp]) <= (uint32_t)dk) {
+                    for (uint32_t it = 0; ld_acquire(&slot_cnt[u.slot]) < SLOT_DONE; ++it) {
+                        if (it == SPIN_LIMIT) {
+                            atomicOr(flag, FLAG_TIMEOUT);
+                            break;
+                        }
+                        __nanosleep(32);
+                    }
+                    __threadfence_block();   // the counter read precedes the claim the sync warp sees
+                    if (atomicCAS(&sm.hclaim[grp], (uint32_t)dk, (uint32_t)dk + 1u) == (uint32_t)dk)
+                        issue_h(grp, u.slot, b);
+                }
                 mbar_wait_bounded(&sm.hbar[grp][b], (dk >> 1) & 1, flag);
                 // rescale h (padded bf16 rows) in place into fragments [step][4T]:
                 // lane l < 4T of warp wq holds steps wq, wq + 4, ... of token
@@ -1015,6 +1058,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                             __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
                     }
                 }
+                count_now_if_last_gu(k, u.slot);
                 publish(&sm.gu_done[grp][wq], ++n_written);
             } else if (gu_writer) {
                 // SiLU*up for h rows 8 * band + g
@@ -1030,6 +1074,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                             __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
                     }
                 }
+                count_now_if_last_gu(k, u.slot);
                 publish(&sm.gu_done[grp][wq], ++n_written);
             } else if (u.down) {
                 // down: one band per warp, x routing weight x tensor scale x 2^-shift
@@ -1044,6 +1089,14 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                         const float f = sm.wts[u.slot][t] * ts * pow2i(-sm.hshift[grp][b][t]);
                         P[g * MAXT + t] = acc[tt] * f;
                         P[(g + 8) * MAXT + t] = acc[2 + tt] * f;
+                    }
+                }
+                if (unit_id(k + 1) >= end_id && u.slot < n_slots - 1) {
+                    // the group's last unit: nothing else to do, so count it here
+                    __syncwarp();
+                    if (lane == 0) {
+                        fence_acq_rel_gpu();
+                        red_relaxed_add(&band_cnt[u.band], 1u);
                     }
                 }
                 publish(&sm.dn_done[grp][wq], ++n_partials);
