@@ -43,8 +43,13 @@
  *    router logit, an expired bounded wait) set bits of a flag word in the
  *    workspace, read back by moe_read_device_flag.  Kernels never trap.
  *  - Apart from the fixed scratch of moe_layer_forward_static, the library
- *    keeps no mutable global state; calls on different streams with
- *    different workspaces may run concurrently.
+ *    keeps no mutable global state, so calls with different workspaces are
+ *    independent.  But the decode layer kernel (1..MOE_MAX_DECODE_T tokens:
+ *    moe_layer_forward, moe_layer_forward_prenorm, moe_stack_forward) needs
+ *    one CTA on every SM at the same time, so two of them must not overlap
+ *    on one GPU, nor run beside other kernels that hold SMs: order them on
+ *    one stream (or with events).  If that ever fails the bounded waits
+ *    expire and set MOE_FLAG_WAIT_TIMEOUT.
  */
 #ifndef NVFP4MOE_H
 #define NVFP4MOE_H
