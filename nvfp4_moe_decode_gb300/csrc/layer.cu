@@ -184,16 +184,8 @@ __device__ __forceinline__ void mma_bf16_16816(float d[4], uint32_t a0, uint32_t
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint4 ldg_stream(const void *p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
-
 // BF16 rows are consumed in a k order chosen so that each lane's A registers
-// come from two coalesced 16-byte loads per row and 64-column chunk: lane
+// come from two 16-byte words per row and 64-column chunk: lane
 // (g, c) loads columns 8c..8c+7 and 32+8c..32+8c+7 of rows g and g+8, and k16
 // step s of the chunk pairs its words 2s, 2s+1 with the activation columns
 // 32*(s/2) + 8c + 4*(s%2) + 0..3 (a permutation of the chunk's 64 columns,
@@ -204,47 +196,39 @@ __host__ __device__ __forceinline__ int bf16_bcol(int step, int c)
     return 64 * (step >> 2) + 32 * (s >> 1) + 8 * c + 4 * (s & 1);
 }
 
-constexpr int BF_DEPTH = 2;            // 64-column chunks in flight per warp
-
-// acc += rows (ra: band rows 0..7, rb: 8..15) x activations over `nch`
-// 64-column chunks starting at column 64*chunk0 (B fragments of the
-// permuted order, k16 steps from 4*chunk0).
-template <int NCH>
-__device__ __forceinline__ void bf16_rows(const __nv_bfloat16 *ra, const __nv_bfloat16 *rb, int chunk0,
-                                          const uint2 *bfrag, int blanes, int lane, float acc[4])
+// One 64-column chunk of a BF16 band in a ring stage (16 rows x 128 bytes,
+// 16-byte unit u of row r at position u ^ 4 (r & 1), so the reads below are
+// free of bank conflicts) times the B fragments of k16 steps step0 ..
+// step0 + 3.  Lane (g, c) takes units c and 4 + c of rows g and g + 8.
+__device__ __forceinline__ void bf16_stage(const uint8_t *stage, const uint2 *bfrag, int blanes, int step0,
+                                           int lane, float acc[4])
 {
-    static_assert(NCH % BF_DEPTH == 0, "chunks per unit");
-    const int c = lane & 3;
-    uint4 buf[BF_DEPTH][4];
-    auto load = [&](uint4 *dst, int j) {
-        const int col = 64 * (chunk0 + j) + 8 * c;
-        dst[0] = ldg_stream(ra + col);
-        dst[1] = ldg_stream(ra + col + 32);
-        dst[2] = ldg_stream(rb + col);
-        dst[3] = ldg_stream(rb + col + 32);
-    };
+    const int g = lane >> 2, c = lane & 3, sw = 4 * (g & 1);
+    const uint8_t *ra = stage + g * 128, *rb = stage + (g + 8) * 128;
+    const uint4 a0 = *reinterpret_cast<const uint4 *>(ra + 16 * (c ^ sw));
+    const uint4 a1 = *reinterpret_cast<const uint4 *>(ra + 16 * ((4 + c) ^ sw));
+    const uint4 b0 = *reinterpret_cast<const uint4 *>(rb + 16 * (c ^ sw));
+    const uint4 b1 = *reinterpret_cast<const uint4 *>(rb + 16 * ((4 + c) ^ sw));
+    const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-    for (int d = 0; d < BF_DEPTH; ++d)
-        load(buf[d], d);
-#pragma unroll 1
-    for (int j0 = 0; j0 < NCH; j0 += BF_DEPTH) {
-#pragma unroll
-        for (int d = 0; d < BF_DEPTH; ++d) {
-            const int j = j0 + d;
-            const uint32_t wa[8] = {buf[d][0].x, buf[d][0].y, buf[d][0].z, buf[d][0].w,
-                                    buf[d][1].x, buf[d][1].y, buf[d][1].z, buf[d][1].w};
-            const uint32_t wb[8] = {buf[d][2].x, buf[d][2].y, buf[d][2].z, buf[d][2].w,
-                                    buf[d][3].x, buf[d][3].y, buf[d][3].z, buf[d][3].w};
-            if (j + BF_DEPTH < NCH)
-                load(buf[d], j + BF_DEPTH);
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const int step = 4 * (chunk0 + j) + s;
-                const uint2 b = (lane < blanes) ? bfrag[step * blanes + lane] : make_uint2(0u, 0u);
-                mma_bf16_16816(acc, wa[2 * s], wb[2 * s], wa[2 * s + 1], wb[2 * s + 1], b.x, b.y);
-            }
-        }
+    for (int s = 0; s < 4; ++s) {
+        const int step = step0 + s;
+        const uint2 b = (lane < blanes) ? bfrag[step * blanes + lane] : make_uint2(0u, 0u);
+        mma_bf16_16816(acc, wa[2 * s], wb[2 * s], wa[2 * s + 1], wb[2 * s + 1], b.x, b.y);
     }
+}
+
+// 16-byte global -> shared copy that skips L1, and an arrival on an mbarrier
+// once all of this thread's earlier copies have landed.
+__device__ __forceinline__ void cp_async_cg16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 // Two consecutive super-chunks of one band (one stage) times the B fragments
@@ -314,7 +298,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
 
     if (lane == 0 && warp < FW) {
         for (int s = 0; s < RING; ++s)
-            mbar_init(&sm.full[warp][s], 1);
+            mbar_init(&sm.full[warp][s], BW ? 32 : 1);   // BF16: one cp.async arrival per lane
         if (leader) {
             mbar_init(&sm.hbar[grp][0], 1);
             mbar_init(&sm.hbar[grp][1], 1);
@@ -355,9 +339,28 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         return (u.down ? w2_src(u.slot, u.band) : w13_src(u.slot, u.band)) + (size_t)(2 * p) * SC_BYTES;
     };
     auto issue_stage = [&](int ring_slot, const Unit &u, int p) {
+        uint64_t *bar = &sm.full[warp][ring_slot];
+        if (BW) {
+            // chunk p (64 columns) of the 16 rows: lane 2r + h copies bytes
+            // [64 h, 64 h + 64) of row r, then arrives when they have landed
+            const int r = lane >> 1, h = lane & 1;
+            const uint8_t *src;
+            if (!u.down) {
+                const int row = r < 8 ? 8 * u.band + r : I + 8 * u.band + (r - 8);
+                src = reinterpret_cast<const uint8_t *>(bf_w13(u.slot)) + ((size_t)row * H + 64 * p) * 2 + 64 * h;
+            } else {
+                src = reinterpret_cast<const uint8_t *>(bf_w2(u.slot)) + ((size_t)(16 * u.band + r) * I + 64 * p) * 2 +
+                      64 * h;
+            }
+            uint8_t *dst = sm.ring[warp][ring_slot] + r * 128;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                cp_async_cg16(dst + 16 * ((4 * h + i) ^ (4 * (r & 1))), src + 16 * i);
+            cp_async_arrive(bar);
+            return;
+        }
         if (lane != 0)
             return;
-        uint64_t *bar = &sm.full[warp][ring_slot];
         mbar_arrive_expect_tx(bar, STG);
         bulk_g2s(sm.ring[warp][ring_slot], stage_src(u, p), STG, bar);
     };
@@ -368,8 +371,12 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
     // CTAs.  A gate/up unit is one band and each warp takes a K quarter (two
     // of the band's eight stages), so the few slots of a small batch still
     // spread over every warp.
-    auto part0 = [&](const Unit &u) { return u.down ? 0 : 2 * wq; };
-    auto nparts = [&](const Unit &u) { return u.down ? DN_PARTS : GU_PARTS / GW; };
+    // stages of a unit per warp: NVFP4 two super-chunks each, BF16 one
+    // 64-column chunk of the 16 rows each
+    auto nparts = [&](const Unit &u) {
+        return BW ? (u.down ? I / 64 : H / 64 / GW) : (u.down ? DN_PARTS : GU_PARTS / GW);
+    };
+    auto part0 = [&](const Unit &u) { return u.down ? 0 : nparts(u) * wq; };
     const int n_groups = NG * (int)gridDim.x;
     const int gid = grp * (int)gridDim.x + (int)blockIdx.x;
     const bool static_shared = !BW && warp < FW && (a.n_shared > 0) && gid < GUU;
@@ -502,7 +509,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
     if (warp < 8) {
         // x -> mma fragments [step][4T]: lane l < 4T of warp w holds steps
         // w, w + 8, ... of token l / 4.  BF16 weights: bf16 in the permuted
-        // column order of bf16_rows.  NVFP4: f16, each token's row scaled by
+        // column order of bf16_bcol.  NVFP4: f16, each token's row scaled by
         // the power of two of its max |x| (found first, one warp per token).
         const uint32_t *xw = reinterpret_cast<const uint32_t *>(xs);
         const int g = lane >> 2, c = lane & 3;
@@ -870,8 +877,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                 }
             }
         };
-        if (!BW)
-            issue_ahead(RING);
+        issue_ahead(RING);
 
         int ccount = 0;                  // stages consumed
         uint32_t n_written = 0;          // gate/up units whose h this warp wrote
@@ -984,24 +990,15 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             }
 
             acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-            if (BW) {
-                const int g = lane >> 2;
-                if (!u.down) {
-                    // rows: gate 8*band + g, up I + 8*band + g; K quarter wq
-                    const __nv_bfloat16 *w = bf_w13(u.slot);
-                    bf16_rows<H / 64 / GW>(w + (size_t)(8 * u.band + g) * H, w + (size_t)(I + 8 * u.band + g) * H,
-                                           (H / 64 / GW) * wq, bfrag, blanes, lane, acc);
-                } else {
-                    const __nv_bfloat16 *w = bf_w2(u.slot);
-                    bf16_rows<I / 64>(w + (size_t)(16 * u.band + g) * I, w + (size_t)(16 * u.band + g + 8) * I,
-                                      0, bfrag, blanes, lane, acc);
-                }
-            } else {
+            {
                 const int np = nparts(u);
                 for (int p = 0; p < np; ++p) {
                     const int rs = ccount % RING;
                     mbar_wait_bounded(&sm.full[warp][rs], (ccount / RING) & 1, flag);
-                    mma_stage(sm.ring[warp][rs], bfrag, blanes, 16 * (part0(u) + p), lane, acc);
+                    if (BW)
+                        bf16_stage(sm.ring[warp][rs], bfrag, blanes, 4 * (part0(u) + p), lane, acc);
+                    else
+                        mma_stage(sm.ring[warp][rs], bfrag, blanes, 16 * (part0(u) + p), lane, acc);
                     __syncwarp();
                     ++ccount;
                     issue_ahead(ccount + RING);
