@@ -20,7 +20,7 @@
  *           code times an e4m3 scale per block of 16 times a per-tensor fp32
  *           scale ("scale_2").
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *  - canonical byte layout: codes [N][K/2], element (n, 2j) in the LOW nibble
  *    of byte (n, j), element (n, 2j+1) in the HIGH nibble; scales [N][K/16],
  *    block b covers k in [16b, 16b+16) along the reduction (input) axis;

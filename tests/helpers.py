@@ -23,7 +23,7 @@ U64 = 2.0 ** -53
 # depth 24 (16 sequential per lane, a 5-level butterfly, 3 quarter adds).
 ROUTER_DEPTH = 24
 
-# Output tolerances of the layer (the benchmark spec):
+# Output tolerances of the layer (the parity target of this project):
 #   NVFP4: max|gpu - ref| <= 1e-2 * max|ref| + 1e-3
 #   BF16 : max|gpu - ref| <= 5e-3 * max|ref| + 1e-3
 TOL_NVFP4 = (1e-2, 1e-3)
