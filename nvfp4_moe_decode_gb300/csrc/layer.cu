@@ -75,7 +75,7 @@ constexpr int DN_PARTS = (I / 128) / 2;   // 2 stages per W2 band
 
 struct FSmem {
     uint8_t ring[FW][RING][STG];
-    uint2 xfrag[(H / 16) * 32];        // compact: entry (step, l) at step * 4T + l
+    uint2 xfrag[(H / 16) * 32];        // entry (step, l) at step * 32 + l; zero for l >= 4T
     uint8_t hbuf[NG][2][HBUF];         // raw h rows, rescaled in place into fragments;
                                        // before the unit loop: x (T x 4 KB)
     uint64_t full[FW][RING];
@@ -200,8 +200,8 @@ __host__ __device__ __forceinline__ int bf16_bcol(int step, int c)
 // 16-byte unit u of row r at position u ^ 4 (r & 1), so the reads below are
 // free of bank conflicts) times the B fragments of k16 steps step0 ..
 // step0 + 3.  Lane (g, c) takes units c and 4 + c of rows g and g + 8.
-__device__ __forceinline__ void bf16_stage(const uint8_t *stage, const uint2 *bfrag, int blanes, int step0,
-                                           int lane, float acc[4])
+__device__ __forceinline__ void bf16_stage(const uint8_t *stage, const uint2 *bfrag, int step0, int lane,
+                                           float acc[4])
 {
     const int g = lane >> 2, c = lane & 3, sw = 4 * (g & 1);
     const uint8_t *ra = stage + g * 128, *rb = stage + (g + 8) * 128;
@@ -214,7 +214,7 @@ __device__ __forceinline__ void bf16_stage(const uint8_t *stage, const uint2 *bf
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
         const int step = step0 + s;
-        const uint2 b = (lane < blanes) ? bfrag[step * blanes + lane] : make_uint2(0u, 0u);
+        const uint2 b = bfrag[step * 32 + lane];
         mma_bf16_16816(acc, wa[2 * s], wb[2 * s], wa[2 * s + 1], wb[2 * s + 1], b.x, b.y);
     }
 }
@@ -232,9 +232,11 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
 }
 
 // Two consecutive super-chunks of one band (one stage) times the B fragments
-// from k16 step `step0`; blanes = 4T lanes carry tokens.
-__device__ __forceinline__ void mma_stage(const uint8_t *stage, const uint2 *bfrag, int blanes, int step0,
-                                          int lane, float acc[4])
+// from k16 step `step0`.  The fragments of a step fill all 32 lanes (lanes
+// 4T.. hold zeros), so every lane loads unconditionally: a predicated load
+// here cost the loop 18% when measured alone.
+__device__ __forceinline__ void mma_stage(const uint8_t *stage, const uint2 *bfrag, int step0, int lane,
+                                          float acc[4])
 {
     const int g = lane >> 2;
 #pragma unroll
@@ -249,7 +251,7 @@ __device__ __forceinline__ void mma_stage(const uint8_t *stage, const uint2 *bfr
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const int step = step0 + q * 8 + half * 4 + s;
-                const uint2 b = (lane < blanes) ? bfrag[step * blanes + lane] : make_uint2(0u, 0u);
+                const uint2 b = bfrag[step * 32 + lane];
                 uint32_t a0, a1, a2, a3;
                 decode4(words[s], a0, a1, a2, a3);
                 float d[4];
@@ -507,10 +509,11 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         fence_proxy_async();               // the ring is refilled by bulk copies later
     }
     if (warp < 8) {
-        // x -> mma fragments [step][4T]: lane l < 4T of warp w holds steps
-        // w, w + 8, ... of token l / 4.  BF16 weights: bf16 in the permuted
-        // column order of bf16_bcol.  NVFP4: f16, each token's row scaled by
-        // the power of two of its max |x| (found first, one warp per token).
+        // x -> mma fragments [step][32] (zeros in lanes 4T..): lane l < 4T of
+        // warp w holds steps w, w + 8, ... of token l / 4.  BF16 weights:
+        // bf16 in the permuted column order of bf16_bcol.  NVFP4: f16, each
+        // token's row scaled by the power of two of its max |x| (found first,
+        // one warp per token).
         const uint32_t *xw = reinterpret_cast<const uint32_t *>(xs);
         const int g = lane >> 2, c = lane & 3;
         float p = 1.0f;
@@ -536,18 +539,20 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             if (lane < blanes)
                 p = pow2i(sm.xshift[g]);
         }
-        if (lane < blanes) {
+        {
 #pragma unroll 4
             for (int step = warp; step < H / 16; step += 8) {
-                uint2 v;
-                if (BW) {
-                    const int w0 = (g * H + bf16_bcol(step, c)) / 2;
-                    v = make_uint2(xw[w0], xw[w0 + 1]);
-                } else {
-                    const int w0 = (g * H + 16 * step) / 2 + c;
-                    v = make_uint2(bf16x2_to_f16x2_scaled(xw[w0], p), bf16x2_to_f16x2_scaled(xw[w0 + 4], p));
+                uint2 v = make_uint2(0u, 0u);   // lanes 4T.. carry no token
+                if (lane < blanes) {
+                    if (BW) {
+                        const int w0 = (g * H + bf16_bcol(step, c)) / 2;
+                        v = make_uint2(xw[w0], xw[w0 + 1]);
+                    } else {
+                        const int w0 = (g * H + 16 * step) / 2 + c;
+                        v = make_uint2(bf16x2_to_f16x2_scaled(xw[w0], p), bf16x2_to_f16x2_scaled(xw[w0 + 4], p));
+                    }
                 }
-                sm.xfrag[step * blanes + lane] = v;
+                sm.xfrag[step * 32 + lane] = v;
             }
         }
     }
@@ -930,10 +935,11 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                         issue_h(grp, u.slot, b);
                 }
                 mbar_wait_bounded(&sm.hbar[grp][b], (dk >> 1) & 1, flag);
-                // rescale h (padded bf16 rows) in place into fragments [step][4T]:
-                // lane l < 4T of warp wq holds steps wq, wq + 4, ... of token
-                // l / 4; NVFP4 scales each token's row by the power of two of its
-                // max |h|, taken over the 16 threads that hold the row.
+                // rescale h (padded bf16 rows) in place into fragments [step][32]
+                // (zeros in lanes 4T..): lane l < 4T of warp wq holds steps wq,
+                // wq + 4, ... of token l / 4; NVFP4 scales each token's row by the
+                // power of two of its max |h|, taken over the 16 threads that
+                // hold the row.
                 const uint32_t *hw = reinterpret_cast<const uint32_t *>(sm.hbuf[grp][b]);
                 const bool hl = lane < blanes;
                 const int hg = lane >> 2, hc = lane & 3;
@@ -979,11 +985,10 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                 uint2 *hf = reinterpret_cast<uint2 *>(sm.hbuf[grp][b]);
 #pragma unroll
                 for (int j = 0; j < HJ; ++j) {
-                    if (hl) {
-                        const int e = (wq + GW * j) * blanes + lane;
-                        hf[e] = BW ? make_uint2(src0[j], src1[j])
-                                   : make_uint2(bf16x2_to_f16x2_scaled(src0[j], p), bf16x2_to_f16x2_scaled(src1[j], p));
-                    }
+                    // all 32 lanes: lanes 4T.. hold zeros (their src words are 0)
+                    const int e = (wq + GW * j) * 32 + lane;
+                    hf[e] = BW ? make_uint2(src0[j], src1[j])
+                               : make_uint2(bf16x2_to_f16x2_scaled(src0[j], p), bf16x2_to_f16x2_scaled(src1[j], p));
                 }
                 named_barrier_sync(1 + grp, GW * 32);
                 bfrag = hf;
@@ -996,9 +1001,9 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                     const int rs = ccount % RING;
                     mbar_wait_bounded(&sm.full[warp][rs], (ccount / RING) & 1, flag);
                     if (BW)
-                        bf16_stage(sm.ring[warp][rs], bfrag, blanes, 4 * (part0(u) + p), lane, acc);
+                        bf16_stage(sm.ring[warp][rs], bfrag, 4 * (part0(u) + p), lane, acc);
                     else
-                        mma_stage(sm.ring[warp][rs], bfrag, blanes, 16 * (part0(u) + p), lane, acc);
+                        mma_stage(sm.ring[warp][rs], bfrag, 16 * (part0(u) + p), lane, acc);
                     __syncwarp();
                     ++ccount;
                     issue_ahead(ccount + RING);
