@@ -57,8 +57,8 @@ def layer_bytes(T: int, n_distinct: int, n_shared: int = 1, wtype: str = "nvfp4"
 # (profiles/moe_layer_kernel_t8.md).  It holds only for the kernel sources it
 # was measured on; any change to them makes the bench report traffic as null.
 NCU_TRAFFIC = {
-    "sources_sha256": "105f3a1cb60ff6f468d16098f46286af8286428db4dcaf84d8ae7ca3c5e19477",
-    "per_algorithmic_byte": 165_286_400 / 161_480_704,
+    "sources_sha256": "38b4277854f22fef870880dd15640c1e681aa30330edc6bee3bf9c3765026fef",
+    "per_algorithmic_byte": 165_001_728 / 161_480_704,
 }
 KERNEL_SOURCES = ("layer.cu", "common.cuh", "kernels.cuh", "topk.cuh")
 
