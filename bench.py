@@ -53,9 +53,10 @@ def layer_bytes(T: int, n_distinct: int, n_shared: int = 1, wtype: str = "nvfp4"
     return ROUTER_BYTES + (n_distinct + n_shared) * EXPERT_BYTES[wtype] + 2 * T * 2048 * 2
 
 
-# DRAM traffic of moe_layer_kernel per algorithmic byte, from an ncu capture
-# (profiles/moe_layer_kernel_t8.md).  It holds only for the kernel sources it
-# was measured on; any change to them makes the bench report traffic as null.
+# DRAM traffic of moe_layer_kernel per algorithmic byte (dram__bytes_read.sum +
+# dram__bytes_write.sum over the algorithmic bytes of two captured launches at
+# T = 8).  It holds only for the kernel sources it was measured on; any change
+# to them makes the bench report traffic as null.
 NCU_TRAFFIC = {
     "sources_sha256": "38b4277854f22fef870880dd15640c1e681aa30330edc6bee3bf9c3765026fef",
     "per_algorithmic_byte": 165_001_728 / 161_480_704,
@@ -244,6 +245,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="time only the selected workload (by default the T=8 NVFP4 line also times "
+                         "NVFP4 T=1, BF16 T=8 and T=1, and the T=8192 grouped layer)")
     args = ap.parse_args()
     assert args.warmup >= 3
 
@@ -291,27 +295,95 @@ def main():
         return
 
     import nvfp4_moe_decode_gb300 as m
-    from nvfp4_moe_decode_gb300 import synth
-    from nvfp4_moe_decode_gb300.layer import Bf16Layer, PackedLayer, new_workspace
 
     m.load()
     if args.stack:
         return run_stack(args, world, rank, local)
-    if T > 8:
-        return run_grouped(args, world, rank, local)
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    stream = torch.cuda.Stream(dev)
+    K, W = args.steps, args.warmup
+    if T > 8:
+        line = measure_grouped(args, T, WT, world, dev, True, K, W)
+    else:
+        line = measure_decode(args, T, WT, L, world, dev, True, K, W)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args, T, WT, L, dev)
+    if not args.no_secondary and T == 8 and WT == "nvfp4":
+        # the other points of the metric, timed the same way in this process
+        sec = []
+        # secondary step counts: at least as many as the main line up to 2,000
+        # decode steps (40 grouped steps of ~1 ms), after at least 3 warm-ups
+        k2, w2 = max(min(K, 2000), 16), max(min(W, 64), 3)
+        for (t2, wt2) in ((1, "nvfp4"), (8, "bf16"), (1, "bf16")):
+            sec.append(secondary_entry(measure_decode(args, t2, wt2, L, world, dev, False, k2, w2)))
+            torch.cuda.empty_cache()
+        sec.append(secondary_entry(measure_grouped(args, 8192, "nvfp4", world, dev, False,
+                                                   max(min(K, 40), 4), max(min(W, 6), 3))))
+        torch.cuda.empty_cache()
+        line["config"]["secondary"] = sec
+        line["gpu_launches"] += sum(e["gpu_launches"] for e in sec)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
 
+        dist.destroy_process_group()
+
+
+def secondary_entry(line) -> dict:
+    """The summary of a measured line kept under config.secondary."""
+    c = line["config"]
+    return {"workload": c["workload"], "tokens": c["tokens"], "weights": c["weights"],
+            "us_per_layer": c["us_per_layer"], "value": line["value"], "unit": line["unit"],
+            "frac": line["roofline"]["frac"], "bound": line["roofline"]["bound"],
+            "peak": line["roofline"]["peak"], "steps": line["steps"],
+            "device_flag": c["device_flag"], "clocks": line["clocks"], "gpu_launches": line["gpu_launches"]}
+
+
+def timed_replays(stream, graphs, local: int):
+    """Replay ``graphs`` (a list of (graph, times)) between two CUDA events on
+    ``stream``, after a barrier and a device synchronize.  A ~1 ms GPU sleep
+    is enqueued ahead of the start event so that the host's launch latency
+    of the first graph falls outside the timed span.  Returns (ms, clocks)."""
+    import torch
+
+    clocks = ClockSampler(local)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(2_000_000)
+        e0.record(stream)
+        for g, n in graphs:
+            for _ in range(n):
+                g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    clk = clocks.stop()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1), clk
+
+
+def measure_decode(args, T: int, WT: str, L: int, world: int, dev, with_e2e: bool, K: int, W: int) -> dict:
+    """One decode-path layer (T <= 8) per step, rotating over L resident layers."""
+    import torch
+
+    import nvfp4_moe_decode_gb300 as m
+    from nvfp4_moe_decode_gb300 import synth
+    from nvfp4_moe_decode_gb300.layer import Bf16Layer, PackedLayer, new_workspace
+
+    WTI = 0 if WT == "nvfp4" else 1
+    stream = torch.cuda.Stream(dev)
     # ---- resident layers (seeds 0..L-1), x fixed (seed 0) ----
-    lis, packed = [], []
+    packed = []
     x = synth.make_x(0, T, device=dev)
     with torch.cuda.stream(stream):
         for s in range(L):
             li = synth.make_layer(s, T, wtype=WTI, device=dev)
-            pl = PackedLayer.from_inputs(li, stream) if WTI == 0 else Bf16Layer.from_inputs(li)
-            lis.append(li)
-            packed.append(pl)
+            packed.append(PackedLayer.from_inputs(li, stream) if WTI == 0 else Bf16Layer.from_inputs(li))
+            del li
     stream.synchronize()
     # distinct routed experts per layer (from our router, outside the timed region)
     ws = new_workspace(T, dev, stream)
@@ -340,124 +412,128 @@ def main():
     run_steps(0, L)   # eager warm-up before capture
     stream.synchronize()
     g_full = capture(L)
-    K, W = args.steps, args.warmup
-
     with torch.cuda.stream(stream):
-        for _ in range(W // L):
+        for _ in range(max(1, W // L)):
             g_full.replay()
         run_steps(0, W % L)
     stream.synchronize()
     rem_graph = capture(K % L) if K % L else None
     steps_bytes = sum(layer_bytes(T, nd[k % L], 1, WT) for k in range(K))
 
-    clocks = ClockSampler(local)
     barrier(world)
-    torch.cuda.synchronize(dev)
-    clocks.start()
-    time.sleep(0.2)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(K // L):
-            g_full.replay()
-        if rem_graph is not None:
-            rem_graph.replay()
-        e1.record(stream)
-    e1.synchronize()
-    clk = clocks.stop()
-    torch.cuda.synchronize(dev)
+    graphs = [(g_full, K // L)] + ([(rem_graph, 1)] if rem_graph is not None else [])
+    ms, clk = timed_replays(stream, graphs, dev.index)
     barrier(world)
-    ms = e0.elapsed_time(e1)
     ms_max = reduce_max(ms, world)
     total_bytes = reduce_sum(float(steps_bytes), world)
     value = total_bytes / (ms_max * 1e-3) / 1e9
     us_per_layer = 1e3 * ms_max / K
-
     flag = m.moe_read_device_flag(ws, stream)
-
-    # ---- e2e: host x in, host out back, through the public C-ABI ----
-    xh = x.cpu().pin_memory()
-    oh = torch.empty(T, 2048, dtype=torch.bfloat16).pin_memory()
-    ne = args.e2e_steps
-    xd = torch.empty_like(x)
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for k in range(ne):
-            xd.copy_(xh, non_blocking=True)
-            packed[k % L].forward(xd, out, ws, stream)
-            oh.copy_(out, non_blocking=True)
-            stream.synchronize()
-    e2e_s = time.perf_counter() - t0
-    e2e_bytes = sum(layer_bytes(T, nd[k % L], 1, WT) for k in range(ne))
-    e2e_v = reduce_sum(e2e_bytes, world) / reduce_max(e2e_s, world) / 1e9
 
     peak, peak_src = peaks()
     layer_alg = steps_bytes / K
     traffic = None
     if WT == "nvfp4" and kernel_sources_sha256() == NCU_TRAFFIC["sources_sha256"]:
         traffic = layer_alg * NCU_TRAFFIC["per_algorithmic_byte"]
+    workload = (f"one {WT.upper()} MoE layer, T={T} tokens (H=2048, 256 routed experts I=512, sigmoid top-6, "
+                f"1 shared expert), synthetic seeded weights")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"{WT} weights x bf16 activations, f32 accumulate", "data": "synthetic",
-        "config": {**config, "us_per_layer": us_per_layer, "tokens_per_s": T * K / (ms_max * 1e-3),
+        "config": {"workload": workload, "weights": WT, "tokens": T, "hidden": 2048, "experts": 256, "top_k": 6,
+                   "inter": 512, "layers_rotated": L,
+                   "l2": f"cold: steps rotate over {L} distinct resident layers (selected bytes per rotation >> L2)",
+                   "timing": "CUDA events on the launching stream around K graph-replayed steps; a 1 ms GPU sleep "
+                             "ahead of the start event keeps host launch latency out of the span",
+                   "us_per_layer": us_per_layer, "tokens_per_s": T * K / (ms_max * 1e-3),
                    "distinct_experts_per_layer": nd, "algorithmic_bytes_per_layer": layer_alg,
                    "hbm_frac": value / world / peak, "device_flag": flag},
         "roofline": {"bound": "hbm", "achieved": layer_alg / (us_per_layer * 1e-6) / 1e9, "peak": peak,
                      "unit": "GB/s", "frac": layer_alg / (us_per_layer * 1e-6) / 1e9 / peak,
                      "traffic": traffic, "peak_source": peak_src,
                      "kernel": "moe_layer_kernel (router, top-6, gate/up, down, combine fused; one launch per layer)"},
-        "e2e": {"value": e2e_v, "unit": "GB/s", "steps": ne, "h2d_bytes_per_step": T * 2048 * 2,
-                "d2h_bytes_per_step": T * 2048 * 2},
         "gpu_launches": K,
         "clocks": clk,
     }
+    if with_e2e:
+        # ---- e2e: host x in, host out back, through the public C-ABI ----
+        xh = x.cpu().pin_memory()
+        oh = torch.empty(T, 2048, dtype=torch.bfloat16).pin_memory()
+        ne = args.e2e_steps
+        xd = torch.empty_like(x)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for k in range(ne):
+                xd.copy_(xh, non_blocking=True)
+                packed[k % L].forward(xd, out, ws, stream)
+                oh.copy_(out, non_blocking=True)
+                stream.synchronize()
+        e2e_s = time.perf_counter() - t0
+        e2e_bytes = sum(layer_bytes(T, nd[k % L], 1, WT) for k in range(ne))
+        e2e_v = reduce_sum(e2e_bytes, world) / reduce_max(e2e_s, world) / 1e9
+        line["e2e"] = {"value": e2e_v, "unit": "GB/s", "steps": ne, "h2d_bytes_per_step": T * 2048 * 2,
+                       "d2h_bytes_per_step": T * 2048 * 2}
+    del packed, ws
+    return line
 
-    if rank == 0 and not args.no_cpu_baseline:
-        import oracle
 
-        oracle.build()
-        xb, hl = host_layers_for_oracle(lis, x, min(L, 4))
-        s, b, n, threads = oracle_sample(hl, xb, T, args.cpu_budget, WT)
-        line["cpu_baseline"] = {"value": b / s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                                "sample": f"{n} layer forwards (T={T}) of the fp64 C oracle over "
-                                          f"{len(hl)} of the rotated layers, {s:.1f} s"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
+def cpu_baseline(args, T: int, WT: str, L: int, dev) -> dict:
+    """The fp64 oracle on the host cores over a bounded sample of the workload."""
+    from nvfp4_moe_decode_gb300 import synth
 
-        dist.destroy_process_group()
+    import oracle
+
+    oracle.build()
+    WTI = 0 if WT == "nvfp4" else 1
+    if T > 8:
+        n_tok = 4
+        li = synth.make_layer(0, T, wtype=WTI, device=dev)
+        xs = li.x[:n_tok].contiguous()
+        xb, hl = host_layers_for_oracle([synth.LayerInputs(**{**li.__dict__, "x": xs})], xs, 1)
+        del li
+        t0 = time.perf_counter()
+        done = 0
+        while time.perf_counter() - t0 < args.cpu_budget:
+            oracle.moe_forward(xb, hl[0][0], hl[0][1], 6, 512, hl[0][2])
+            done += 1
+        sec = time.perf_counter() - t0
+        return {"value": layer_flops(n_tok) * done / sec / 1e12, "unit": "TFLOP/s",
+                "cores": oracle.num_threads(), "kind": "oracle",
+                "sample": f"{done} oracle layer forwards of {n_tok} of the {T} tokens, {sec:.1f} s"}
+    x = synth.make_x(0, T, device=dev)
+    lis = [synth.make_layer(s, T, wtype=WTI, device=dev) for s in range(min(L, 4))]
+    xb, hl = host_layers_for_oracle(lis, x, len(lis))
+    del lis
+    s, b, n, threads = oracle_sample(hl, xb, T, args.cpu_budget, WT)
+    return {"value": b / s / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} layer forwards (T={T}) of the fp64 C oracle over {len(hl)} of the rotated layers, "
+                      f"{s:.1f} s"}
 
 
-def run_grouped(args, world: int, rank: int, local: int):
-    """One layer at T > 8 tokens (the grouped tensor-core path), two resident
-    layers alternated."""
-    import numpy as np
+def measure_grouped(args, T: int, WT: str, world: int, dev, with_e2e: bool, K: int, W: int) -> dict:
+    """One layer at T > 8 tokens (the grouped tensor-core path) per step, two
+    resident layers alternated."""
     import torch
 
     import nvfp4_moe_decode_gb300 as m
     from nvfp4_moe_decode_gb300 import synth
     from nvfp4_moe_decode_gb300.layer import Bf16Layer, PackedLayer, new_workspace
 
-    T, WT = args.tokens, args.wtype
     WTI = 0 if WT == "nvfp4" else 1
-    dev = torch.device(f"cuda:{local}")
-    torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
     L = 2
-    lis, layers = [], []
+    layers = []
     with torch.cuda.stream(stream):
         for s_ in range(L):
             li = synth.make_layer(s_, T, wtype=WTI, device=dev)
             layers.append(PackedLayer.from_inputs(li, stream) if WTI == 0 else Bf16Layer.from_inputs(li))
-            lis.append(li)
-    x = lis[0].x
+            if s_ == 0:
+                x = li.x
+            del li
     ws = new_workspace(T, dev, stream)
     out = torch.empty(T, 2048, dtype=torch.bfloat16, device=dev)
-    K, W = args.steps, args.warmup
     with torch.cuda.stream(stream):
         for k in range(W):
             layers[k % L].forward(x, out, ws, stream)
@@ -466,25 +542,12 @@ def run_grouped(args, world: int, rank: int, local: int):
     with torch.cuda.graph(g, stream=stream):
         for k in range(L):
             layers[k].forward(x, out, ws, stream)
-    clocks = ClockSampler(local)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    clocks.start()
-    time.sleep(0.2)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     reps = max(1, K // L)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        e1.record(stream)
-    e1.synchronize()
-    clk = clocks.stop()
-    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms, clk = timed_replays(stream, [(g, reps)], dev.index)
     barrier(world)
     steps = reps * L
-    ms_max = reduce_max(e0.elapsed_time(e1), world)
+    ms_max = reduce_max(ms, world)
     fl = layer_flops(T)
     value = reduce_sum(float(fl * steps), world) / (ms_max * 1e-3) / 1e12
     us_layer = 1e3 * ms_max / steps
@@ -493,20 +556,6 @@ def run_grouped(args, world: int, rank: int, local: int):
     w = torch.empty(T, 6, dtype=torch.float32, device=dev)
     m.moe_route(x, layers[0].router_w, T, idx, w, None, ws, stream)
     load = torch.bincount(idx.reshape(-1).long(), minlength=256)
-
-    xh = x.cpu().pin_memory()
-    oh = torch.empty(T, 2048, dtype=torch.bfloat16).pin_memory()
-    xd = torch.empty_like(x)
-    ne = max(3, min(args.e2e_steps, 50))
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for k in range(ne):
-            xd.copy_(xh, non_blocking=True)
-            layers[k % L].forward(xd, out, ws, stream)
-            oh.copy_(out, non_blocking=True)
-            stream.synchronize()
-    e2e_v = reduce_sum(float(fl * ne), world) / reduce_max(time.perf_counter() - t0, world) / 1e12
 
     pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else None
@@ -530,33 +579,27 @@ def run_grouped(args, world: int, rank: int, local: int):
                      "peak_source": "measured (sustained)" if pk else "fallback",
                      "kernel": "the grouped chain per layer (router GEMM, top-k, lists, gate/up, h rescale, down, "
                                "shared down + combine)"},
-        "e2e": {"value": e2e_v, "unit": "TFLOP/s", "steps": ne, "h2d_bytes_per_step": T * 2048 * 2,
-                "d2h_bytes_per_step": T * 2048 * 2},
         "gpu_launches": steps * 8,
         "clocks": clk,
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        import oracle
-
-        oracle.build()
-        n_tok = 4
-        xb, hl = host_layers_for_oracle([synth.LayerInputs(**{**lis[0].__dict__, "x": x[:n_tok].contiguous()})],
-                                        x[:n_tok].contiguous(), 1)
+    if with_e2e:
+        xh = x.cpu().pin_memory()
+        oh = torch.empty(T, 2048, dtype=torch.bfloat16).pin_memory()
+        xd = torch.empty_like(x)
+        ne = max(3, min(args.e2e_steps, 50))
+        torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
-        done = 0
-        while time.perf_counter() - t0 < args.cpu_budget:
-            oracle.moe_forward(xb, hl[0][0], hl[0][1], 6, 512, hl[0][2])
-            done += 1
-        sec = time.perf_counter() - t0
-        line["cpu_baseline"] = {"value": layer_flops(n_tok) * done / sec / 1e12, "unit": "TFLOP/s",
-                                "cores": oracle.num_threads(), "kind": "oracle",
-                                "sample": f"{done} oracle layer forwards of {n_tok} of the {T} tokens, {sec:.1f} s"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.destroy_process_group()
+        with torch.cuda.stream(stream):
+            for k in range(ne):
+                xd.copy_(xh, non_blocking=True)
+                layers[k % L].forward(xd, out, ws, stream)
+                oh.copy_(out, non_blocking=True)
+                stream.synchronize()
+        e2e_v = reduce_sum(float(fl * ne), world) / reduce_max(time.perf_counter() - t0, world) / 1e12
+        line["e2e"] = {"value": e2e_v, "unit": "TFLOP/s", "steps": ne, "h2d_bytes_per_step": T * 2048 * 2,
+                       "d2h_bytes_per_step": T * 2048 * 2}
+    del layers, ws
+    return line
 
 
 def run_stack(args, world: int, rank: int, local: int):

@@ -29,7 +29,9 @@
  *
  * Shapes this build supports: H = 2048, I = 512 (W13 is [2I][H], W2 is
  * [H][I]), E = 256 routed experts, top_k = 6, 0 or 1 shared expert, and
- * 1 <= T <= MOE_MAX_DECODE_T tokens per call.
+ * 1 <= T <= MOE_MAX_TOKENS tokens per call (the decode kernel up to
+ * MOE_MAX_DECODE_T tokens, the grouped tensor-core path above; the stack
+ * and pre-norm calls take 1..MOE_MAX_DECODE_T).
  *
  * Conventions for every entry point:
  *  - All data pointers are DEVICE pointers (cudaMalloc / torch memory) on the
@@ -48,8 +50,12 @@
  *    moe_layer_forward, moe_layer_forward_prenorm, moe_stack_forward) needs
  *    one CTA on every SM at the same time, so two of them must not overlap
  *    on one GPU, nor run beside other kernels that hold SMs: order them on
- *    one stream (or with events).  If that ever fails the bounded waits
- *    expire and set MOE_FLAG_WAIT_TIMEOUT.
+ *    one stream (or with events).  Before each launch the library checks
+ *    that one CTA of the kernel fits on an SM (its shared memory and
+ *    registers) and that the device has at least 128 SMs, and returns
+ *    MOE_ERR_UNSUPPORTED otherwise; if SMs are nonetheless held by other
+ *    work (another process, a partitioned device) the bounded waits expire
+ *    and set MOE_FLAG_WAIT_TIMEOUT.
  */
 #ifndef NVFP4MOE_H
 #define NVFP4MOE_H
@@ -176,8 +182,21 @@ size_t moe_workspace_bytes(int T);
  * a workspace; every call leaves its counters re-armed for the next call (the
  * layer kernel's launch tag, which starts at zero, advances by one per call).
  * After a call that reported MOE_FLAG_WAIT_TIMEOUT, zero the workspace again
- * before its next use. */
+ * or call moe_workspace_recover before its next use. */
 moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Re-arm a decode workspace after a wait timeout, without losing its flag
+ * word: one small kernel, enqueued on `stream` (it waits for the preceding
+ * kernel), that does nothing unless the flag word holds
+ * MOE_FLAG_WAIT_TIMEOUT; then it clears the arrival counters a timed-out
+ * call may have left behind and advances the launch tag, so that the next
+ * layer call ignores router logits tagged by the failed one.  The flag bits
+ * stay until moe_read_device_flag reads them.  Allocates nothing.
+ * Errors: MOE_ERR_INVALID_ARG (null or misaligned workspace),
+ * MOE_ERR_WORKSPACE (smaller than moe_workspace_bytes(1)), MOE_ERR_CUDA.
+ */
+moe_status moe_workspace_recover(void *workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
  * Read and clear the device flag word of a workspace.  SYNCHRONISES the
@@ -210,6 +229,27 @@ moe_status moe_route(const void *x, const void *router_w, int T, int n_experts, 
                      int32_t *idx, float *w, float *logits, void *workspace,
                      size_t workspace_bytes, moe_stream_t stream);
 
+/*
+ * Copy out the routing that the last layer call on `workspace` used: the
+ * most recent moe_layer_forward, moe_layer_forward_prenorm or (its last
+ * layer) moe_stack_forward with the same T.  The layer kernels route
+ * internally; this exposes their own selection so that it can be checked
+ * against a reference.  [FLINT, "A 40B MoE ...": sigmoid top-6 routing]
+ *  idx:    device int32 [T][top_k], selection order (best first), or NULL.
+ *  w:      device float [T][top_k], renormalised weights, or NULL.
+ *  logits: device float [T][E] fp32 router logits, or NULL.
+ *  T <= MOE_MAX_DECODE_T: logits are fp32 sums of exact bf16*bf16 products
+ *  along a fixed tree of depth 15.  Larger T: the grouped path's router GEMM
+ *  (see moe_route).
+ * At least one output must be non-NULL.  Enqueued device-to-device copies;
+ * the result is undefined if no layer call with this T preceded it.
+ * Errors: MOE_ERR_INVALID_ARG (null or misaligned workspace, all outputs
+ * NULL), MOE_ERR_UNSUPPORTED (T outside 1..MOE_MAX_TOKENS), MOE_ERR_WORKSPACE
+ * (workspace_bytes below moe_workspace_bytes(T)), MOE_ERR_CUDA.
+ */
+moe_status moe_read_routing(const void *workspace, size_t workspace_bytes, int T, int32_t *idx, float *w,
+                            float *logits, moe_stream_t stream);
+
 /* ----------------------------------------------------------------------- */
 /* The layer.  [FLINT, "From 1,096 kernels to 346": router and expert GEMVs */
 /* that read only the selected experts' weights, routing and the combine   */
@@ -225,7 +265,7 @@ moe_status moe_route(const void *x, const void *router_w, int T, int n_experts, 
  * GEMMs of large batches]: a router GEMM, top-k, per-expert token lists in
  * token order, then tcgen05 tensor-core GEMMs per expert (weights dequantised
  * to f16 in shared memory; each token row of x and of h scaled by a power of
- * two into f16, exactly for every element within 2^24 of the row's largest),
+ * two into f16, exactly for every element within 2^28 of the row's largest),
  * h rounded to bf16 as in the decode path, and a combine that adds the six
  * weighted expert outputs in choice order and the shared expert's (fp32,
  * rounded once to bf16; deterministic).  With BF16 weights the grouped GEMMs
@@ -337,12 +377,14 @@ moe_status moe_stack_forward(void *x, const moe_layer_weights *layers, int n_lay
  *  Allocation: none; no cudaMalloc / cudaFree and no allocating library call.
  *  First call on each device: looks up the array's device address with
  *    cudaGetSymbolAddress (that device current) and zeroes the array on
- *    `stream`; make that first call before any stream capture.  Later calls
- *    only launch the layer.
+ *    `stream`; make that first call before any stream capture.  Every call
+ *    then launches two kernels: the re-arm kernel of moe_workspace_recover
+ *    on the scratch, then the layer.
  *  Zero state: the setup zeroes the scratch; every call leaves its counters
- *    re-armed for the next call (the launch tag advances by one).  The device flag
- *    of this scratch is not reported; a caller that needs the flags uses
- *    moe_layer_forward with its own workspace.
+ *    re-armed for the next call (the launch tag advances by one), and after a
+ *    call that gave up on a bounded wait the next call's re-arm kernel
+ *    restores them.  moe_static_read_device_flag reports the scratch's
+ *    device flag.
  *  Concurrency: one scratch per device.  Calls on the same device must not
  *    overlap (serialise them on one stream or with events); overlapping calls
  *    race on the scratch and give wrong results.
@@ -354,6 +396,18 @@ moe_status moe_layer_forward_static(const void *x, const void *router_w,
                                     const moe_expert_bank *routed,
                                     const moe_expert_bank *shared, void *out, int T,
                                     moe_stream_t stream);
+
+/*
+ * moe_read_device_flag for the fixed scratch of moe_layer_forward_static on
+ * the current device: SYNCHRONISES `stream`, returns the MOE_FLAG_* bits in
+ * *flag_out (host) and clears them.  A MOE_FLAG_WAIT_TIMEOUT means the call
+ * that set it returned invalid output; the following calls are valid again
+ * (their re-arm kernel restored the scratch).  The first use on a device
+ * does the scratch's set-up (see above) and reports 0.
+ * Errors: MOE_ERR_INVALID_ARG (flag_out NULL), MOE_ERR_DEVICE_FLAG (a bit
+ * was set), MOE_ERR_CUDA.
+ */
+moe_status moe_static_read_device_flag(moe_stream_t stream, uint32_t *flag_out);
 
 #ifdef __cplusplus
 }

@@ -45,7 +45,8 @@ MAX_TOKENS = 65536
 EXPORTS = (
     "moe_abi_version", "moe_status_string", "moe_packed_bytes", "moe_pack_nvfp4",
     "moe_unpack_nvfp4", "moe_dequant_nvfp4", "moe_workspace_bytes", "moe_workspace_init",
-    "moe_read_device_flag", "moe_route", "moe_layer_forward", "moe_layer_forward_static",
+    "moe_read_device_flag", "moe_workspace_recover", "moe_route", "moe_read_routing", "moe_layer_forward",
+    "moe_layer_forward_static", "moe_static_read_device_flag",
     "moe_layer_forward_prenorm", "moe_stack_workspace_bytes", "moe_stack_forward",
 )
 
@@ -103,6 +104,12 @@ def _declare(lib):
     lib.moe_read_device_flag.restype = i32
     lib.moe_route.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp]
     lib.moe_route.restype = i32
+    lib.moe_workspace_recover.argtypes = [vp, sz, vp]
+    lib.moe_workspace_recover.restype = i32
+    lib.moe_static_read_device_flag.argtypes = [vp, u32p]
+    lib.moe_static_read_device_flag.restype = i32
+    lib.moe_read_routing.argtypes = [vp, sz, i32, vp, vp, vp, vp]
+    lib.moe_read_routing.restype = i32
     bank_p = ctypes.POINTER(moe_expert_bank)
     lib.moe_layer_forward.argtypes = [vp, vp, bank_p, bank_p, vp, i32, vp, sz, vp]
     lib.moe_layer_forward.restype = i32
@@ -207,12 +214,37 @@ def moe_read_device_flag(workspace, stream=None) -> int:
     return int(v.value)
 
 
+def moe_workspace_recover(workspace, stream=None):
+    """Re-arm a workspace after a wait timeout (keeps its flag bits)."""
+    lib = load()
+    _check("moe_workspace_recover", lib.moe_workspace_recover(_ptr(workspace),
+                                                                workspace.numel() * workspace.element_size(),
+                                                                _stream(stream)))
+
+
+def moe_static_read_device_flag(stream=None) -> int:
+    """Synchronises the stream; returns and clears the flag bits of the fixed scratch."""
+    lib = load()
+    v = ctypes.c_uint32(0)
+    st = lib.moe_static_read_device_flag(_stream(stream), ctypes.byref(v))
+    if st not in (MOE_OK, MOE_ERR_DEVICE_FLAG):
+        raise MoeError("moe_static_read_device_flag", st, lib)
+    return int(v.value)
+
+
 def moe_route(x, router_w, T: int, idx, w, logits=None, workspace=None, stream=None,
               n_experts: int = EXPERTS, top_k: int = TOPK):
     lib = load()
     _check("moe_route", lib.moe_route(_ptr(x), _ptr(router_w), int(T), n_experts, top_k, _ptr(idx),
                                        _ptr(w), _ptr(logits), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_read_routing(workspace, T: int, idx=None, w=None, logits=None, stream=None):
+    """Copy the routing the last layer call on ``workspace`` used (device tensors)."""
+    lib = load()
+    _check("moe_read_routing", lib.moe_read_routing(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                                      int(T), _ptr(idx), _ptr(w), _ptr(logits), _stream(stream)))
 
 
 def make_bank(wtype: int, n_experts: int, w13, w2, tscale13=None, tscale2=None) -> moe_expert_bank:

@@ -20,20 +20,15 @@ bool disjoint(const void *a, const void *b, size_t n)
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+PerDevice g_sm_count;
+
 int sm_count()
 {
-    static int cached[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return 0;
-    if (dev >= 0 && dev < 64 && cached[dev] > 0)
-        return cached[dev];
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return 0;
-    if (dev >= 0 && dev < 64)
-        cached[dev] = n;
-    return n;
+    const int v = per_device(g_sm_count, [](int dev) {
+        int n = 0;
+        return cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess ? n : -1;
+    });
+    return v > 0 ? v : 0;
 }
 
 moe_status check_bank(const moe_expert_bank *b, int expect_n, bool allow_empty)
@@ -144,6 +139,15 @@ moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, moe_strea
     return cuda_status(cudaMemsetAsync(workspace, 0, ws_layout().total, (cudaStream_t)stream));
 }
 
+moe_status moe_workspace_recover(void *workspace, size_t workspace_bytes, moe_stream_t stream)
+{
+    if (!workspace || !aligned16(workspace))
+        return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < ws_layout().total)
+        return MOE_ERR_WORKSPACE;
+    return cuda_status(launch_rearm(static_cast<uint8_t *>(workspace), (cudaStream_t)stream, true));
+}
+
 moe_status moe_read_device_flag(void *workspace, moe_stream_t stream, uint32_t *flag_out)
 {
     if (!workspace || !flag_out)
@@ -159,6 +163,45 @@ moe_status moe_read_device_flag(void *workspace, moe_stream_t stream, uint32_t *
         return MOE_ERR_CUDA;
     *flag_out = v;
     return v ? MOE_ERR_DEVICE_FLAG : MOE_OK;
+}
+
+moe_status moe_read_routing(const void *workspace, size_t workspace_bytes, int T, int32_t *idx, float *w,
+                            float *logits, moe_stream_t stream)
+{
+    if (!workspace || !aligned16(workspace))
+        return MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > MAX_TOKENS)
+        return MOE_ERR_UNSUPPORTED;
+    if (workspace_bytes < moe_workspace_bytes(T))
+        return MOE_ERR_WORKSPACE;
+    if (!idx && !w && !logits)
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    const uint8_t *ws = static_cast<const uint8_t *>(workspace);
+    size_t o_idx, o_w, o_lg, lg_pitch;
+    if (T <= MAXT) {
+        // the decode kernel keeps each logit in the low word of a 64-bit
+        // (launch tag, logit) pair
+        const WsLayout L = ws_layout();
+        o_idx = L.topk_idx;
+        o_w = L.topk_w;
+        o_lg = L.tlogits;
+        lg_pitch = 8;
+    } else {
+        const GWsLayout L = gws_layout(T);
+        o_idx = L.idx;
+        o_w = L.w;
+        o_lg = L.logits;
+        lg_pitch = 4;
+    }
+    cudaError_t e = cudaSuccess;
+    if (idx)
+        e = cudaMemcpyAsync(idx, ws + o_idx, (size_t)T * TOPK * 4, cudaMemcpyDeviceToDevice, st);
+    if (e == cudaSuccess && w)
+        e = cudaMemcpyAsync(w, ws + o_w, (size_t)T * TOPK * 4, cudaMemcpyDeviceToDevice, st);
+    if (e == cudaSuccess && logits)
+        e = cudaMemcpy2DAsync(logits, 4, ws + o_lg, lg_pitch, 4, (size_t)T * E, cudaMemcpyDeviceToDevice, st);
+    return cuda_status(e);
 }
 
 static moe_status check_route_args(const void *x, const void *router_w, int T, void *workspace,
@@ -254,18 +297,33 @@ static void fill_layer_args(LayerArgs &la, const void *router_w, const moe_exper
     la.out = static_cast<__nv_bfloat16 *>(out);
 }
 
-static cudaError_t launch_layer_on_all_sms(const LayerArgs &la, cudaStream_t st)
+// The decode layer kernel's CTAs wait on one another, so its whole grid (one
+// CTA per SM, at least 128 for the router phase) must be resident at once.
+// With rearm set, the workspace's re-arm kernel runs first (after every
+// host-side check has passed).
+static moe_status launch_layer_on_all_sms(const LayerArgs &la, cudaStream_t st, bool rearm = false)
 {
     const int nsm = sm_count();
     if (nsm <= 0)
-        return cudaErrorNoDevice;
-    // one CTA per SM; at least 128 for the router phase
-    return launch_layer(la, nsm >= 128 ? nsm : 128, st, true);
+        return MOE_ERR_CUDA;
+    const int grid = nsm >= 128 ? nsm : 128;
+    const int per_sm = layer_resident_ctas_per_sm();
+    if (per_sm < 0)
+        return MOE_ERR_CUDA;
+    if ((long)per_sm * nsm < grid)
+        return MOE_ERR_UNSUPPORTED;
+    if (rearm && launch_rearm(la.ws, st, true) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return cuda_status(launch_layer(la, grid, st, true));
 }
 
-moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expert_bank *routed,
-                             const moe_expert_bank *shared, void *out, int T, void *workspace,
-                             size_t workspace_bytes, moe_stream_t stream)
+}  // extern "C"
+
+// moe_layer_forward; with rearm (decode path only) the workspace's re-arm
+// kernel runs ahead of the layer kernel.
+moe_status moe::layer_forward(const void *x, const void *router_w, const moe_expert_bank *routed,
+                              const moe_expert_bank *shared, void *out, int T, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream, bool rearm)
 {
     moe_status s = check_route_args(x, router_w, T, workspace, workspace_bytes);
     if (s != MOE_OK)
@@ -304,7 +362,17 @@ moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expe
     LayerArgs la{};
     fill_layer_args(la, router_w, routed, shared, out, T, workspace);
     la.x = static_cast<const __nv_bfloat16 *>(x);
-    return cuda_status(launch_layer_on_all_sms(la, (cudaStream_t)stream));
+    return launch_layer_on_all_sms(la, (cudaStream_t)stream, rearm);
+}
+
+extern "C" {
+
+moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expert_bank *routed,
+                             const moe_expert_bank *shared, void *out, int T, void *workspace,
+                             size_t workspace_bytes, moe_stream_t stream)
+{
+    return layer_forward(x, router_w, routed, shared, out, T, workspace, workspace_bytes, (cudaStream_t)stream,
+                         false);
 }
 
 moe_status moe_layer_forward_prenorm(const void *resid, const void *delta, void *resid_out, void *xn_out,
@@ -345,7 +413,7 @@ moe_status moe_layer_forward_prenorm(const void *resid, const void *delta, void 
     la.resid_out = static_cast<__nv_bfloat16 *>(resid_out);
     la.xn_out = static_cast<__nv_bfloat16 *>(xn_out);
     la.eps = eps;
-    return cuda_status(launch_layer_on_all_sms(la, (cudaStream_t)stream));
+    return launch_layer_on_all_sms(la, (cudaStream_t)stream);
 }
 
 // Stack workspace: the layer workspace, then the residual ping-pong buffers
@@ -401,9 +469,9 @@ moe_status moe_stack_forward(void *x, const moe_layer_weights *layers, int n_lay
             la.delta = D[(l - 1) & 1];
             la.resid_out = R[l & 1];
         }
-        cudaError_t e = launch_layer_on_all_sms(la, st);
-        if (e != cudaSuccess)
-            return MOE_ERR_CUDA;
+        const moe_status e = launch_layer_on_all_sms(la, st);
+        if (e != MOE_OK)
+            return e;
     }
     // x_L = x_{L-1} + D[(L-1)&1]
     const __nv_bfloat16 *last = (n_layers == 1) ? x0 : R[(n_layers - 1) & 1];

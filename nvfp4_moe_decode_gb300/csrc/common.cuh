@@ -26,9 +26,11 @@
 // exact e2m1 values of an A register.  The activations (bf16) enter the
 // tensor cores as fp16 after an exact per-token power-of-two rescale that puts
 // the token's largest magnitude in [2^14, 2^15): bf16's 8-bit significand
-// fits fp16's 11 bits, so every element within 2^31 of the largest is exact
-// and only smaller ones (whose products lie below the fp32 rounding of the
-// sum) are rounded.  Products are exact and accumulate in fp32; the e4m3
+// fits fp16's 11 bits, so every element within 2^28 of the largest (the
+// normal f16 range after the rescale) is exact; smaller ones become f16
+// subnormals, still exact down to 2^-31 of the largest, and only elements
+// below that (whose products lie far below the fp32 rounding of the sum)
+// are rounded.  Products are exact and accumulate in fp32; the e4m3
 // block scale is applied to each k16 step's fp32 partial, the tensor scale
 // and the power of two at the end.
 #pragma once

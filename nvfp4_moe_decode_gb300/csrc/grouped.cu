@@ -32,7 +32,7 @@
 // weight is e2m1 x e4m3, exact in f16 (at most 6 significant bits, magnitude
 // in [2^-10, 2688]); a token row of x (or of h) is multiplied by the power of
 // two that puts its largest magnitude in [2^14, 2^15), exact for every
-// element within 2^24 of the largest, and the epilogue multiplies by the
+// element within 2^28 of the largest, and the epilogue multiplies by the
 // inverse power and the tensor scale.  BF16 weights use bf16 operands as they
 // are.
 //

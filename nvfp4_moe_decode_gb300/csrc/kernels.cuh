@@ -2,9 +2,43 @@
 // kernels behind libnvfp4moe.so (internal; not part of the public C ABI).
 #pragma once
 
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
+
+// ---------------------------------------------------------------------------
+// Host: a value computed once per device, safe to use from several host
+// threads.  make(dev) runs with that device current and returns the value
+// (> 0), or <= 0 on failure (not cached; the next call tries again).
+// ---------------------------------------------------------------------------
+constexpr int MAX_DEVICES = 64;
+
+struct PerDevice {
+    std::atomic<int> v[MAX_DEVICES];   // 0: not computed yet
+    std::mutex mu;
+};
+
+template <class F>
+int per_device(PerDevice &pd, F make)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES)
+        return -1;
+    int v = pd.v[dev].load(std::memory_order_acquire);
+    if (v > 0)
+        return v;
+    std::lock_guard<std::mutex> lock(pd.mu);
+    v = pd.v[dev].load(std::memory_order_relaxed);
+    if (v > 0)
+        return v;
+    v = make(dev);
+    if (v > 0)
+        pd.v[dev].store(v, std::memory_order_release);
+    return v;
+}
 
 struct RouterArgs {
     const __nv_bfloat16 *x;        // [T][H]
@@ -136,6 +170,17 @@ cudaError_t launch_grouped_route(const GroupedArgs &a, int nsm, cudaStream_t str
 cudaError_t launch_grouped_layer(const GroupedArgs &a, int nsm, cudaStream_t stream);
 
 size_t layer_smem_bytes();
+// CTAs of the decode layer kernel that one SM can hold at once (its shared
+// memory and register needs; sets the kernel's shared-memory attribute on
+// first use), or -1 on a CUDA error.
+int layer_resident_ctas_per_sm();
+// Re-arm a decode workspace after a wait timeout (see moe_workspace_recover).
+cudaError_t launch_rearm(uint8_t *ws, cudaStream_t stream, bool pdl);
+// moe_layer_forward; with rearm, a decode call first enqueues launch_rearm
+// on its workspace (after all host-side checks).
+moe_status layer_forward(const void *x, const void *router_w, const moe_expert_bank *routed,
+                         const moe_expert_bank *shared, void *out, int T, void *workspace, size_t workspace_bytes,
+                         cudaStream_t stream, bool rearm);
 
 cudaError_t launch_router(const RouterArgs &a, cudaStream_t stream, bool pdl);
 cudaError_t launch_layer(const LayerArgs &a, int grid, cudaStream_t stream, bool pdl);

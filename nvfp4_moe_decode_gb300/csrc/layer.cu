@@ -1135,23 +1135,32 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
 
 size_t layer_smem_bytes() { return sizeof(FSmem); }
 
+namespace {
+PerDevice g_layer_attr;   // 1 + resident CTAs per SM, once the attributes are set
+}
+
+int layer_resident_ctas_per_sm()
+{
+    const int v = per_device(g_layer_attr, [](int) {
+        const int smem = (int)sizeof(FSmem);
+        if (cudaFuncSetAttribute(moe_layer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(moe_layer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                cudaSuccess)
+            return -1;
+        int n0 = 0, n1 = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n0, moe_layer_kernel<false>, NT, smem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, moe_layer_kernel<true>, NT, smem) != cudaSuccess)
+            return -1;
+        return 1 + (n0 < n1 ? n0 : n1);
+    });
+    return v > 0 ? v - 1 : -1;
+}
+
 cudaError_t launch_layer(const LayerArgs &a, int grid, cudaStream_t stream, bool pdl)
 {
-    static int configured[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(moe_layer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)sizeof(FSmem));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(moe_layer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)sizeof(FSmem));
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = 1;
-    }
+    if (layer_resident_ctas_per_sm() < 0)
+        return cudaErrorUnknown;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(NT);
@@ -1164,6 +1173,48 @@ cudaError_t launch_layer(const LayerArgs &a, int grid, cudaStream_t stream, bool
     cfg.numAttrs = 1;
     return a.bf16w ? cudaLaunchKernelEx(&cfg, moe_layer_kernel<true>, a)
                    : cudaLaunchKernelEx(&cfg, moe_layer_kernel<false>, a);
+}
+
+// After a call that gave up on a bounded wait, the workspace's counters may
+// hold that call's partial counts and its launch tag may not have advanced
+// (CTA 0 returns before re-arming them).  If the flag word shows a timeout,
+// clear the counters and advance the tag, so that the next layer call
+// ignores the stale tagged logits; the flag bits stay for the caller to read.
+// Runs after the preceding kernel has finished (it waits on it first).
+__global__ void __launch_bounds__(128) rearm_kernel(uint8_t *ws)
+{
+    griddep_launch();
+    griddep_wait();
+    const WsLayout L = ws_layout();
+    uint32_t *ctrl = reinterpret_cast<uint32_t *>(ws + L.ctrl);
+    if ((__ldcg(&ctrl[0]) & FLAG_TIMEOUT) == 0u)
+        return;
+    uint32_t *slot_cnt = reinterpret_cast<uint32_t *>(ws + L.slot_cnt);
+    uint32_t *band_cnt = reinterpret_cast<uint32_t *>(ws + L.band_cnt);
+    for (int i = threadIdx.x; i < MAX_SLOTS; i += blockDim.x)
+        slot_cnt[i] = 0u;
+    for (int i = threadIdx.x; i < W2_BANDS; i += blockDim.x)
+        band_cnt[i] = 0u;
+    if (threadIdx.x == 0) {
+        ctrl[1] = 0u;
+        ctrl[4] = 0u;
+        ctrl[5] = ctrl[5] + 1u;
+    }
+}
+
+cudaError_t launch_rearm(uint8_t *ws, cudaStream_t stream, bool pdl)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, rearm_kernel, ws);
 }
 
 }  // namespace moe

@@ -13,6 +13,12 @@
 // not overlap: two calls in flight at once (two streams, two host threads)
 // share the counters and buffers and race.  Serialise them on one stream or
 // with events.
+//
+// The caller cannot zero this scratch, so a call that gave up on a bounded
+// wait must not leave it unusable: every call first enqueues the library's
+// re-arm kernel, which clears the counters and advances the launch tag when
+// the scratch's flag word reports a timeout (and does nothing otherwise).
+// moe_static_read_device_flag reads and clears that flag word.
 #include <mutex>
 
 #include "kernels.cuh"
@@ -56,6 +62,17 @@ moe_status scratch_for_current_device(cudaStream_t stream, void **ptr)
 
 }  // namespace
 
+extern "C" moe_status moe_static_read_device_flag(moe_stream_t stream, uint32_t *flag_out)
+{
+    if (!flag_out)
+        return MOE_ERR_INVALID_ARG;
+    void *scratch = nullptr;
+    const moe_status s = scratch_for_current_device((cudaStream_t)stream, &scratch);
+    if (s != MOE_OK)
+        return s;
+    return moe_read_device_flag(scratch, stream, flag_out);
+}
+
 extern "C" moe_status moe_layer_forward_static(const void *x, const void *router_w,
                                                const moe_expert_bank *routed,
                                                const moe_expert_bank *shared, void *out, int T,
@@ -68,8 +85,10 @@ extern "C" moe_status moe_layer_forward_static(const void *x, const void *router
     if (need > STATIC_SCRATCH_BYTES)
         return MOE_ERR_WORKSPACE;
     void *scratch = nullptr;
-    const moe_status s = scratch_for_current_device((cudaStream_t)stream, &scratch);
+    moe_status s = scratch_for_current_device((cudaStream_t)stream, &scratch);
     if (s != MOE_OK)
         return s;
-    return moe_layer_forward(x, router_w, routed, shared, out, T, scratch, STATIC_SCRATCH_BYTES, stream);
+    // the re-arm kernel first: recovery from an earlier call's wait timeout
+    return layer_forward(x, router_w, routed, shared, out, T, scratch, STATIC_SCRATCH_BYTES, (cudaStream_t)stream,
+                         true);
 }

@@ -23,6 +23,10 @@ U64 = 2.0 ** -53
 # depth 24 (16 sequential per lane, a 5-level butterfly, 3 quarter adds).
 ROUTER_DEPTH = 24
 
+# The decode layer kernel's own router: each lane chains 8 exact products per
+# token (7 roundings after the first), then two balanced 16-way trees (4 + 4).
+LAYER_ROUTER_DEPTH = 15
+
 # Output tolerances of the layer (the parity target of this project):
 #   NVFP4: max|gpu - ref| <= 1e-2 * max|ref| + 1e-3
 #   BF16 : max|gpu - ref| <= 5e-3 * max|ref| + 1e-3
@@ -120,6 +124,78 @@ def classify_selection(logits: np.ndarray, bounds: np.ndarray, oracle_idx: np.nd
             if not ok:
                 invalid.append(t)
     return certain, near, invalid
+
+
+def read_routing(ws: torch.Tensor, T: int):
+    """The routing the last layer call on ``ws`` used (the GPU's own), as
+    numpy (idx int32 [T, 6], w fp64 [T, 6], logits fp64 [T, 256])."""
+    import nvfp4_moe_decode_gb300 as m
+
+    dev = ws.device
+    idx = torch.full((T, 6), -1, dtype=torch.int32, device=dev)
+    w = torch.full((T, 6), float("nan"), dtype=torch.float32, device=dev)
+    lg = torch.full((T, 256), float("nan"), dtype=torch.float32, device=dev)
+    m.moe_read_routing(ws, T, idx, w, lg)
+    torch.cuda.synchronize(dev)
+    return idx.cpu().numpy(), w.cpu().numpy().astype(np.float64), lg.cpu().numpy().astype(np.float64)
+
+
+def check_gpu_routing(x_bits: np.ndarray, wr_bits: np.ndarray, gidx: np.ndarray, gw: np.ndarray,
+                      glg: np.ndarray, depth: int, w_tol: float):
+    """Check a GPU routing (indices, weights, fp32 logits) against the oracle.
+
+    * every GPU logit lies within the certified bound for a summation of the
+      given depth;
+    * on every token whose selection is certain under those bounds, the GPU
+      selected exactly the oracle's experts; where the six selected logits
+      are also ordered beyond the bounds, in the same order;
+    * every near-tie token's GPU selection is one the bounds allow;
+    * weights: renormalised, positive, and within ``w_tol`` of the oracle's
+      (matched by expert) wherever the two sets agree.
+    Returns (certain, near, same): tokens certain, near ties, and tokens whose
+    GPU set equals the oracle's (the ones whose outputs are comparable)."""
+    T = x_bits.shape[0]
+    lg = oracle.router_logits(x_bits, wr_bits)
+    bounds = logit_bounds(x_bits, wr_bits, depth)
+    err = np.abs(glg - lg)
+    assert np.all(err <= bounds), f"logit outside its bound: max ratio {np.max(err / bounds):.3f}"
+    oidx, ow = oracle.select_topk(lg, 6)
+    certain, near, invalid = classify_selection(lg, bounds, oidx, gidx)
+    assert not invalid, f"invalid selections at tokens {invalid[:8]}"
+    same = []
+    for t in range(T):
+        g = gidx[t].tolist()
+        assert len(set(g)) == 6 and min(g) >= 0 and max(g) < 256
+        assert np.all(gw[t] > 0) and abs(gw[t].sum() - 1.0) <= 1e-5
+        if set(g) != set(oidx[t].tolist()):
+            continue
+        same.append(t)
+        o = oidx[t]
+        ordered = all(lg[t, o[i]] - bounds[t, o[i]] > lg[t, o[i + 1]] + bounds[t, o[i + 1]] for i in range(5))
+        if ordered:
+            assert np.array_equal(gidx[t], o), (t, gidx[t], o)
+        for i in range(6):
+            j = int(np.where(o == gidx[t][i])[0][0])
+            assert abs(gw[t][i] - ow[t][j]) <= w_tol, (t, i, gw[t][i], ow[t][j])
+    assert set(certain) <= set(same)
+    return certain, near, same
+
+
+def check_decode_layer(li: synth.LayerInputs, x: torch.Tensor, out: torch.Tensor, ws: torch.Tensor, tol,
+                       depth: int = LAYER_ROUTER_DEPTH, max_near: int = 1):
+    """A decode-path layer call (T <= 8) on ``ws``: its own routing against the
+    oracle's (check_gpu_routing), then its output against the oracle on every
+    token routed like the oracle.  Returns (gpu out, oracle out) in fp64."""
+    T = x.shape[0]
+    gidx, gw, glg = read_routing(ws, T)
+    _, near, same = check_gpu_routing(bits16(x), bits16(li.router_w), gidx, gw, glg, depth, 2e-6)
+    assert len(near) <= max_near, f"{len(near)} near-tie tokens"
+    sub = synth.LayerInputs(**{**li.__dict__, "x": x})
+    ref, _, _, _, _ = oracle_layer(sub)
+    got = to_f64(out)
+    assert len(same) >= T - len(near)
+    assert within_tol(got[same], ref[same], tol), describe_err(got[same], ref[same])
+    return got, ref
 
 
 def max_abs_err(gpu: np.ndarray, ref: np.ndarray) -> float:

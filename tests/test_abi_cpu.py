@@ -101,6 +101,17 @@ def test_host_argument_errors_enqueue_nothing(moe_lib):
     assert lib.moe_workspace_init(None, ws, None) == m.MOE_ERR_INVALID_ARG
     assert lib.moe_workspace_init(dummy, 8, None) == m.MOE_ERR_WORKSPACE
     assert lib.moe_read_device_flag(None, None, None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_recover(None, ws, None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_recover(dummy + 8, ws, None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_recover(dummy, 8, None) == m.MOE_ERR_WORKSPACE
+    assert lib.moe_static_read_device_flag(None, None) == m.MOE_ERR_INVALID_ARG
+    # routing read-back: null workspace, no output, T out of range, small workspace
+    rr = lib.moe_read_routing
+    assert rr(None, ws, 1, dummy, None, None, None) == m.MOE_ERR_INVALID_ARG
+    assert rr(dummy, ws, 1, None, None, None, None) == m.MOE_ERR_INVALID_ARG
+    assert rr(dummy, ws, 0, dummy, None, None, None) == m.MOE_ERR_UNSUPPORTED
+    assert rr(dummy, ws, m.MAX_TOKENS + 1, dummy, None, None, None) == m.MOE_ERR_UNSUPPORTED
+    assert rr(dummy, ws, 8192, dummy, None, None, None) == m.MOE_ERR_WORKSPACE
     # the no-allocation variant rejects T beyond its scratch before any CUDA call
     fs = lib.moe_layer_forward_static
     assert fs(dummy, dummy, B(bank), None, dummy * 2, 9, None) == m.MOE_ERR_UNSUPPORTED

@@ -24,23 +24,22 @@ def _route(li, dev):
     return idx.cpu().numpy(), w.cpu().numpy(), lg.cpu().numpy().astype(np.float64)
 
 
+# Tokens whose routing is a near tie under the tensor-core GEMM's bound
+# (expected: none at these sizes, a handful at most at 8192).
+MAX_NEAR = {9: 0, 512: 1, 8192: 8}
+
+
 @pytest.mark.parametrize("T", [9, 512, 8192])
 def test_grouped_routing(cuda_dev, T):
     li = synth.make_layer(60 + T % 97, T, device=cuda_dev, weights=False)
     idx, w, lg_gpu = _route(li, cuda_dev)
     xb, wb = hp.bits16(li.x), hp.bits16(li.router_w)
+    certain, near, same = hp.check_gpu_routing(xb, wb, idx, w, lg_gpu, hp.GEMM_DEPTH, 1e-5)
     lg = oracle.router_logits(xb, wb)
-    bounds = hp.logit_bounds(xb, wb, hp.GEMM_DEPTH)
-    # every fp32 logit of the tensor-core GEMM lies within the bound
-    assert np.all(np.abs(lg_gpu - lg) <= bounds)
-    oidx, ow = oracle.select_topk(lg, 6)
-    certain, near, invalid = hp.classify_selection(lg, bounds, oidx, idx)
-    assert not invalid
-    assert len(near) <= max(2, T // 20)
-    c = np.array(certain)
-    assert np.array_equal(idx[c], oidx[c])
-    assert np.max(np.abs(w[c] - ow[c])) <= 1e-5
-    assert np.allclose(w.sum(axis=1), 1.0, atol=1e-5)
+    ratio = np.max(np.abs(lg_gpu - lg) / (np.abs(hp.np_bf16(xb)) @ np.abs(hp.np_bf16(wb)).T + 1e-300))
+    print(f"T={T}: near ties {len(near)}, GPU set differs on {T - len(same)} tokens, "
+          f"max |logit err| / sum|x w| = {ratio:.3e} (bound {hp.gamma(hp.GEMM_DEPTH, 2 ** -23):.3e})")
+    assert len(near) <= MAX_NEAR[T]
 
 
 def _forward(lay, x, dev):
@@ -48,52 +47,60 @@ def _forward(lay, x, dev):
     ws = new_workspace(T, dev)
     out = torch.full((T, m.HIDDEN), float("nan"), dtype=torch.bfloat16, device=dev)
     lay.forward(x.contiguous(), out, ws)
-    return out, m.moe_read_device_flag(ws)
+    return out, m.moe_read_device_flag(ws), ws
 
 
-def _check(li, out, tol, tokens=None):
+def _check(li, out, ws, tol, tokens=None):
+    """The layer's own routing (read back from its workspace, every token)
+    against the oracle's, then the outputs of the sampled tokens that the GPU
+    routed like the oracle (all but near ties whose GPU set differs)."""
     T = li.x.shape[0]
     tokens = list(range(T)) if tokens is None else list(tokens)
-    ref, idx, _, lg, _ = hp.oracle_layer(li, tokens=tokens)
-    xb = np.ascontiguousarray(hp.bits16(li.x)[tokens])
-    bounds = hp.logit_bounds(xb, hp.bits16(li.router_w), hp.GEMM_DEPTH)
-    certain, _, _ = hp.classify_selection(lg, bounds, idx, idx)
+    gidx, gw, glg = hp.read_routing(ws, T)
+    xb, wb = hp.bits16(li.x), hp.bits16(li.router_w)
+    _, near, same = hp.check_gpu_routing(xb, wb, gidx, gw, glg, hp.GEMM_DEPTH, 1e-5)
+    assert len(near) <= max(1, T // 1000), f"{len(near)} near-tie tokens"
+    ref, _, _, _, _ = hp.oracle_layer(li, tokens=tokens)
     got = hp.to_f64(out)[tokens]
-    assert len(certain) >= len(tokens) - max(2, len(tokens) // 20)
-    c = np.array(certain)
-    assert hp.within_tol(got[c], ref[c], tol), hp.describe_err(got[c], ref[c])
+    same_set = set(same)
+    keep = [i for i, t in enumerate(tokens) if t in same_set]
+    assert len(keep) >= len(tokens) - len(near)
+    assert hp.within_tol(got[keep], ref[keep], tol), hp.describe_err(got[keep], ref[keep])
 
 
 @pytest.mark.parametrize("T", [9, 64, 300])
 def test_grouped_layer_small(cuda_dev, T):
     li = synth.make_layer(70 + T, T, device=cuda_dev)
     pl = PackedLayer.from_inputs(li)
-    out, flag = _forward(pl, li.x, cuda_dev)
+    out, flag, ws = _forward(pl, li.x, cuda_dev)
     assert flag == 0
-    _check(li, out, hp.TOL_NVFP4)
+    _check(li, out, ws, hp.TOL_NVFP4)
 
 
 def test_grouped_layer_8192_sampled(cuda_dev):
-    """The 8192-token configuration, all tokens finite, 96 sampled against the
-    oracle (first, last, and random ones)."""
+    """The 8192-token configuration: the routing of all 8192 tokens checked,
+    every output finite, and 512 tokens (first, last and random ones)
+    compared with the oracle."""
     T = 8192
     li = synth.make_layer(0, T, device=cuda_dev)
     pl = PackedLayer.from_inputs(li)
-    out, flag = _forward(pl, li.x, cuda_dev)
+    out, flag, ws = _forward(pl, li.x, cuda_dev)
     assert flag == 0
     assert torch.isfinite(out.float()).all()
     rng = np.random.default_rng(8192)
-    toks = sorted(set([0, 1, T - 1] + rng.choice(T, 93, replace=False).tolist()))
-    _check(li, out, hp.TOL_NVFP4, toks)
+    rest = rng.choice(np.arange(2, T - 1), 509, replace=False).tolist()
+    toks = sorted(set([0, 1, T - 1] + rest))
+    assert len(toks) == 512
+    _check(li, out, ws, hp.TOL_NVFP4, toks)
 
 
 def test_grouped_bf16_weights(cuda_dev):
     T = 200
     li = synth.make_layer(80, T, wtype=synth.BF16, device=cuda_dev)
     bl = Bf16Layer.from_inputs(li)
-    out, flag = _forward(bl, li.x, cuda_dev)
+    out, flag, ws = _forward(bl, li.x, cuda_dev)
     assert flag == 0
-    _check(li, out, hp.TOL_BF16)
+    _check(li, out, ws, hp.TOL_BF16)
 
 
 def test_grouped_without_shared_expert_and_determinism(cuda_dev):
@@ -104,11 +111,11 @@ def test_grouped_without_shared_expert_and_determinism(cuda_dev):
                                  "codes2": li.codes2[:256], "scales2": li.scales2[:256],
                                  "tscale13": li.tscale13[:256], "tscale2": li.tscale2[:256]})
     pl = PackedLayer.from_inputs(li_ns)
-    out1, flag = _forward(pl, li.x, cuda_dev)
-    out2, _ = _forward(pl, li.x, cuda_dev)
+    out1, flag, ws = _forward(pl, li.x, cuda_dev)
+    out2, _, _ = _forward(pl, li.x, cuda_dev)
     assert flag == 0
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
-    _check(li_ns, out1, hp.TOL_NVFP4)
+    _check(li_ns, out1, ws, hp.TOL_NVFP4)
 
 
 def test_grouped_expert_with_more_than_256_tokens(cuda_dev):
@@ -118,7 +125,7 @@ def test_grouped_expert_with_more_than_256_tokens(cuda_dev):
     li = synth.make_layer(82, 1, device=cuda_dev)
     li.x = li.x.repeat(T, 1).contiguous()
     pl = PackedLayer.from_inputs(li)
-    out, flag = _forward(pl, li.x, cuda_dev)
+    out, flag, ws = _forward(pl, li.x, cuda_dev)
     assert flag == 0
     assert torch.equal(out.view(torch.int16), out[:1].repeat(T, 1).view(torch.int16))
-    _check(li, out, hp.TOL_NVFP4, tokens=[0, 299, 599])
+    _check(li, out, ws, hp.TOL_NVFP4, tokens=[0, 299, 599])

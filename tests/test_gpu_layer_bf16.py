@@ -25,24 +25,18 @@ def _forward(bl, x, dev, ws=None):
     return out, m.moe_read_device_flag(ws), ws
 
 
-def _check(x, li, out):
-    sub = synth.LayerInputs(**{**li.__dict__, "x": x})
-    ref, idx, _, lg, _ = hp.oracle_layer(sub)
-    bounds = hp.logit_bounds(hp.bits16(x), hp.bits16(li.router_w))
-    certain, _, _ = hp.classify_selection(lg, bounds, idx, idx)
-    got = hp.to_f64(out)
-    keep = [t for t in range(x.shape[0]) if t in certain]
-    assert len(keep) >= x.shape[0] - max(1, x.shape[0] // 100)
-    assert hp.within_tol(got[keep], ref[keep], hp.TOL_BF16), hp.describe_err(got[keep], ref[keep])
+def _check(x, li, out, ws):
+    """The layer's own routing against the oracle's, then the output."""
+    hp.check_decode_layer(li, x, out, ws, hp.TOL_BF16)
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 5, 8])
 def test_bf16_layer_matches_oracle(layer_bf, cuda_dev, T):
     li, bl = layer_bf
     x = li.x[:T].contiguous()
-    out, flag, _ = _forward(bl, x, cuda_dev)
+    out, flag, ws = _forward(bl, x, cuda_dev)
     assert flag == 0
-    _check(x, li, out)
+    _check(x, li, out, ws)
 
 
 def test_bf16_layer_other_seed_and_determinism(cuda_dev):
@@ -52,7 +46,7 @@ def test_bf16_layer_other_seed_and_determinism(cuda_dev):
     out2, _, _ = _forward(bl, li.x, cuda_dev, ws)
     assert flag == 0
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
-    _check(li.x, li, out1)
+    _check(li.x, li, out1, ws)
 
 
 def test_bf16_layer_without_shared_expert(cuda_dev):
@@ -60,9 +54,9 @@ def test_bf16_layer_without_shared_expert(cuda_dev):
     li_ns = synth.LayerInputs(**{**li.__dict__, "n_shared": 0, "w13": li.w13[:256], "w2": li.w2[:256]})
     bl = Bf16Layer.from_inputs(li_ns)
     assert bl.shared is None
-    out, flag, _ = _forward(bl, li.x, cuda_dev)
+    out, flag, ws = _forward(bl, li.x, cuda_dev)
     assert flag == 0
-    _check(li.x, li_ns, out)
+    _check(li.x, li_ns, out, ws)
 
 
 def test_bf16_one_hot_row_probe(cuda_dev):
@@ -75,6 +69,6 @@ def test_bf16_one_hot_row_probe(cuda_dev):
     for r in range(m.HIDDEN):
         li.w2[256, r, (37 * r) % m.INTER] = 1.0
     bl = Bf16Layer.from_inputs(li)
-    out, flag, _ = _forward(bl, li.x, cuda_dev)
+    out, flag, ws = _forward(bl, li.x, cuda_dev)
     assert flag == 0
-    _check(li.x, li, out)
+    _check(li.x, li, out, ws)

@@ -35,10 +35,11 @@ def _prenorm_step(lay, resid, delta, ws, dev):
     return out, v, xn
 
 
-def _check_layer(li, resid, delta, out, v, xn, tol):
+def _check_layer(li, resid, delta, out, v, xn, tol, ws):
     """Residual add bit-exact; xn within one bf16 ulp of the oracle's (the
-    GPU sums the squares in fp32); the MoE output against the oracle run on
-    the GPU's own xn."""
+    GPU sums the squares in fp32); the layer's own routing and its MoE output
+    against the oracle run on the GPU's own xn (``ws`` holds the routing of
+    this layer call)."""
     rb = hp.bits16(resid)
     db = None if delta is None else hp.bits16(delta)
     v_ref, xn_ref = oracle.prenorm(rb, db, EPS)
@@ -47,14 +48,7 @@ def _check_layer(li, resid, delta, out, v, xn, tol):
     ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(want_xn), 1e-30))) - 7)
     assert np.all(np.abs(got_xn - want_xn) <= ulp)
     assert np.mean(hp.bits16(xn) == xn_ref) >= 0.999
-    sub = synth.LayerInputs(**{**li.__dict__, "x": xn.clone()})
-    ref, idx, _, lg, _ = hp.oracle_layer(sub)
-    bounds = hp.logit_bounds(hp.bits16(xn), hp.bits16(li.router_w))
-    certain, _, _ = hp.classify_selection(lg, bounds, idx, idx)
-    keep = [t for t in range(resid.shape[0]) if t in certain]
-    assert len(keep) >= resid.shape[0] - max(1, resid.shape[0] // 100)
-    g = hp.to_f64(out)
-    assert hp.within_tol(g[keep], ref[keep], tol), hp.describe_err(g[keep], ref[keep])
+    hp.check_decode_layer(li, xn.clone(), out, ws, tol)
 
 
 @pytest.mark.parametrize("wtype,T", [(synth.NVFP4, 8), (synth.NVFP4, 1), (synth.BF16, 5)])
@@ -67,15 +61,18 @@ def test_prenorm_layer_matches_oracle(cuda_dev, wtype, T):
     ws = new_workspace(T, cuda_dev)
     tol = hp.TOL_NVFP4 if wtype == synth.NVFP4 else hp.TOL_BF16
     out, v, xn = _prenorm_step(lay, resid, delta, ws, cuda_dev)
-    _check_layer(li, resid, delta, out, v, xn, tol)
+    _check_layer(li, resid, delta, out, v, xn, tol, ws)
     out0, v0, xn0 = _prenorm_step(lay, resid, None, ws, cuda_dev)   # first layer: no delta
     assert torch.equal(v0.view(torch.int16), resid.view(torch.int16))
-    _check_layer(li, resid, None, out0, v0, xn0, tol)
+    _check_layer(li, resid, None, out0, v0, xn0, tol, ws)
 
 
-def _run_stack_and_steps(layers, x0, dev):
+def _run_stack_and_steps(layers, x0, dev, keep=None):
     """moe_stack_forward, and the same stack layer by layer through
-    moe_layer_forward_prenorm; returns (stack result, per-layer inputs)."""
+    moe_layer_forward_prenorm; returns (stack result, the layer-by-layer
+    result, per-layer tensors).  For the layers in ``keep`` (default: all)
+    each entry also holds a copy of the workspace right after that layer's
+    call, which carries the layer's own routing."""
     T = x0.shape[0]
     st = Stack(layers, EPS)
     ws = new_stack_workspace(T, dev)
@@ -84,9 +81,10 @@ def _run_stack_and_steps(layers, x0, dev):
     assert m.moe_read_device_flag(ws) == 0
     wsl = new_workspace(T, dev)
     resid, delta, steps = x0.clone(), None, []
-    for lay in layers:
+    for l, lay in enumerate(layers):
         out, v, xn = _prenorm_step(lay, resid, delta, wsl, dev)
-        steps.append((resid, delta, out, v, xn))
+        snap = wsl.clone() if keep is None or l in keep else None
+        steps.append((resid, delta, out, v, xn, snap))
         resid, delta = v, out
     final = (resid.float() + delta.float()).to(torch.bfloat16)
     return x, final, steps
@@ -100,29 +98,33 @@ def test_stack_equals_layer_by_layer_and_oracle(cuda_dev, wtype, T, n):
     assert torch.equal(x.view(torch.int16), final.view(torch.int16))
     tol = hp.TOL_NVFP4 if wtype == synth.NVFP4 else hp.TOL_BF16
     for l in (0, n - 1):
-        resid, delta, out, v, xn = steps[l]
-        _check_layer(made[l][0], resid, delta, out, v, xn, tol)
+        resid, delta, out, v, xn, snap = steps[l]
+        _check_layer(made[l][0], resid, delta, out, v, xn, tol, snap)
 
 
-def test_stack_47_nvfp4_layers_t1(cuda_dev):
-    """The full 47-layer NVFP4 stack at T = 1 (21.4 GB resident); the oracle
-    checks the first, a middle and the last layer."""
-    n, T = 47, 1
+@pytest.mark.parametrize("wtype,T", [(synth.NVFP4, 1), (synth.NVFP4, 8), (synth.BF16, 8)])
+def test_stack_47_layers(cuda_dev, wtype, T):
+    """The full 47-layer stacks (21.4 GB resident for NVFP4, 76 GB for BF16):
+    the stack call equals the layers called one by one, and the oracle checks
+    the first, a middle and the last layer, routing included."""
+    n = 47
+    checked = (0, 23, 46)
     layers, lis = [], {}
     for l in range(n):
-        li, lay = _make(l, T, synth.NVFP4, cuda_dev)
+        li, lay = _make(l, T, wtype, cuda_dev)
         layers.append(lay)
-        if l in (0, 23, 46):
+        if l in checked:
             lis[l] = li
         else:
             del li
     x0 = synth.make_x(0, T, device=cuda_dev)
-    x, final, steps = _run_stack_and_steps(layers, x0, cuda_dev)
+    x, final, steps = _run_stack_and_steps(layers, x0, cuda_dev, keep=checked)
     assert torch.equal(x.view(torch.int16), final.view(torch.int16))
     assert torch.isfinite(x.float()).all()
+    tol = hp.TOL_NVFP4 if wtype == synth.NVFP4 else hp.TOL_BF16
     for l, li in lis.items():
-        resid, delta, out, v, xn = steps[l]
-        _check_layer(li, resid, delta, out, v, xn, hp.TOL_NVFP4)
+        resid, delta, out, v, xn, snap = steps[l]
+        _check_layer(li, resid, delta, out, v, xn, tol, snap)
 
 
 def test_stack_host_errors(cuda_dev):
