@@ -24,9 +24,13 @@ def _route(li, dev):
     return idx.cpu().numpy(), w.cpu().numpy(), lg.cpu().numpy().astype(np.float64)
 
 
-# Tokens whose routing is a near tie under the tensor-core GEMM's bound
-# (expected: none at these sizes, a handful at most at 8192).
-MAX_NEAR = {9: 0, 512: 1, 8192: 8}
+# The tensor-core GEMM's logit bound (GEMM_DEPTH roundings of 2^-23) is about
+# 70 times the error actually seen (at most 4.9e-7 of sum|x w| over 8192
+# tokens), so 1-3% of random tokens fall inside it as "near ties" (135 of
+# 8192).  Those must still be valid selections, and the GPU must pick the
+# oracle's own set on all but a few (none so far).
+def _max_differ(T: int) -> int:
+    return 0 if T <= 512 else 2
 
 
 @pytest.mark.parametrize("T", [9, 512, 8192])
@@ -39,7 +43,8 @@ def test_grouped_routing(cuda_dev, T):
     ratio = np.max(np.abs(lg_gpu - lg) / (np.abs(hp.np_bf16(xb)) @ np.abs(hp.np_bf16(wb)).T + 1e-300))
     print(f"T={T}: near ties {len(near)}, GPU set differs on {T - len(same)} tokens, "
           f"max |logit err| / sum|x w| = {ratio:.3e} (bound {hp.gamma(hp.GEMM_DEPTH, 2 ** -23):.3e})")
-    assert len(near) <= MAX_NEAR[T]
+    assert len(near) <= max(4, T // 20)
+    assert T - len(same) <= _max_differ(T)
 
 
 def _forward(lay, x, dev):
@@ -59,7 +64,8 @@ def _check(li, out, ws, tol, tokens=None):
     gidx, gw, glg = hp.read_routing(ws, T)
     xb, wb = hp.bits16(li.x), hp.bits16(li.router_w)
     _, near, same = hp.check_gpu_routing(xb, wb, gidx, gw, glg, hp.GEMM_DEPTH, 1e-5)
-    assert len(near) <= max(1, T // 1000), f"{len(near)} near-tie tokens"
+    assert len(near) <= max(4, T // 20), f"{len(near)} near-tie tokens"
+    assert T - len(same) <= _max_differ(T), f"GPU set differs from the oracle's on {T - len(same)} tokens"
     ref, _, _, _, _ = hp.oracle_layer(li, tokens=tokens)
     got = hp.to_f64(out)[tokens]
     same_set = set(same)
