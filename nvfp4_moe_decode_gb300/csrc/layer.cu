@@ -8,46 +8,50 @@
 // combine fused into the GEMV kernels, programmatic dependent launch so that
 // a kernel loads weights while its predecessor finishes.
 //
-// One CTA per SM: 16 compute warps in 4 groups of 4, plus a sync warp.
-// Phases:
+// One CTA per SM: 16 compute warps, a count warp and an h warp.  Phases:
 //  1. before waiting on the preceding kernel: router CTAs load their slice of
-//     the router weights; group 0 of the first 64 CTAs starts the bulk copies
-//     of one band of the shared expert (it needs no routing);
+//     the router weights; in CTAs 0..63 the compute warps of band parity 0
+//     start the bulk copy of their slice of one band of the shared expert
+//     (it needs no routing);
 //  2. x arrives in shared memory by one bulk copy; in CTAs 0..127 the 16
 //     compute warps compute the fp32 logits of two experts and store each
-//     with the launch's tag in one 64-bit word; warps 0..7 then turn x into
-//     f16 mma fragments;
+//     with the launch's tag in one 64-bit word; every compute warp turns its
+//     256-column slice of x into mma fragments held in registers;
 //  3. every CTA reads the logits until each carries the launch's tag, takes
 //     the top-6 of each token (one warp per token, identical in every CTA)
 //     and builds the slot table: the shared expert, then the distinct
 //     selected experts in ascending order, each with its per-token routing
 //     weight;
-//  4. units are dealt round-robin to the 4 x #CTA groups (group id
-//     grp * #CTA + cta; a group takes ids gid, gid + G, gid + 2G, ...):
-//       gate/up unit (slot, band): the 4 warps take one K quarter each of
-//         a 16-row band of W13 (8 gate + 8 up rows); warp k % 4 adds the
-//         four partials in warp order and applies SiLU*up -> h (bf16);
-//       down unit (slot, 4 bands): once the slot's 64 gate/up bands are done,
-//         the slot's h arrives by bulk copy, each token's row is scaled by the
-//         power of two of its max |h| (found there) into f16 fragments in
-//         place; each warp computes one 16-row band of W2 h, times the
-//         routing weight;
-//     gate/up ids precede down ids and every group walks its ids in
-//     increasing order, so a down unit only waits on gate/up units that other
-//     groups reach without waiting themselves.  A compute warp reports a
-//     finished h band or down partial through a shared-memory counter only;
-//     the sync warp turns those into the cross-CTA counts (slot counters,
-//     band counters) behind one gpu-scope fence per pass, because such a
-//     fence costs a warp about a microsecond while the SM streams weights,
-//     and it issues the h copies;
+//  4. the unit phase.  With U slots and G CTAs:
+//       gate/up: the 64 U bands of W13 (16 rows each: 8 gate + 8 up rows),
+//         slot-major, are dealt round-robin, CTA c taking bands c, c + G,
+//         ...; within the CTA, band k goes to the 8 warps of parity k % 2,
+//         warp q of them taking the band's 256-column slice q (the x
+//         fragments of that slice never leave its registers).  The eight K
+//         partials of a band meet in a shared-memory buffer; the warp that
+//         arrives last adds them in slice order and applies SiLU*up -> h;
+//       down: the 128 (U - 1) bands of W2 (16 rows) of the first U - 1 slots
+//         are cut into G contiguous ranges (a range touches at most two
+//         slots), and band b of the last slot goes to CTA b; within the CTA
+//         the bands are dealt to the 16 warps round-robin, one warp per band
+//         (all of its 512 columns).  The h warp waits until a slot's 64
+//         gate/up bands are counted, copies the slot's h and turns it into
+//         f16 fragments once for the whole CTA;
+//     every warp streams its own stages (2304-byte pieces of its bands)
+//     through a private ring of bulk copies, ahead across all of its bands,
+//     gate/up first: slots complete in order on every CTA, so by the time a
+//     warp reaches its down bands their h is normally ready.  Compute warps
+//     report finished h bands and down partials through shared-memory masks
+//     only; the count warp turns those into the cross-CTA counts behind one
+//     gpu-scope fence per pass (such a fence costs a streaming warp about a
+//     microsecond);
 //  5. the warp that computes a band's partial for the last slot waits until
 //     the other slots' partials of the band are counted, then adds all of
 //     them in slot order (deterministic) and writes out (bf16).
-// NVFP4: every warp streams its units' weights through a private 3-stage ring
-// of shared-memory buffers filled by cp.async.bulk and decodes them in
-// registers.  BF16 (the W16A16 variant of the Flint page, section "From 1,096
-// kernels to 346": BF16 decode): the rows are row-major in HBM, and each warp
-// loads its 16 rows straight into registers, two 64-column chunks ahead.
+// NVFP4: the stages are decoded in registers (cvt.rn.f16x2.e2m1x2) straight
+// into mma.sync A fragments.  BF16 (the W16A16 variant of the Flint page,
+// section "From 1,096 kernels to 346": BF16 decode): a stage is 16 rows x 64
+// columns copied by per-lane cp.async into a swizzled ring slot.
 // Every wait is bounded and reports MOE_FLAG_WAIT_TIMEOUT instead of hanging.
 #include "kernels.cuh"
 #include "topk.cuh"
@@ -58,30 +62,36 @@ namespace {
 
 constexpr int FW = 16;                 // compute warps per CTA
 constexpr int FT = FW * 32;            // compute threads
-constexpr int SYNC_WARP = FW;          // warp 16: cross-CTA counts and the h copies
-constexpr int NT = FT + 32;            // threads per CTA
-constexpr int NG = 4;                  // unit groups per CTA
-constexpr int GW = 4;                  // warps per group
-constexpr int RING = 3;                // stages per warp
-constexpr int STG = 2 * SC_BYTES;      // 2304 bytes: two super-chunks
+constexpr int EP_WARP = FW;            // warps 16, 17: gate/up epilogues (band parity 0, 1)
+constexpr int CNT_WARP = FW + 2;       // warp 18: cross-CTA counts
+constexpr int HW_WARP = FW + 3;        // warp 19: h fragments of the CTA's down slots
+constexpr int NT = FT + 128;           // threads per CTA
+constexpr uint32_t OUT_PER_CTA = 2;    // warps of a CTA that count themselves out of the slot counters
+constexpr int RW = 4;                  // ring stages per compute warp
+constexpr int STG = 2 * SC_BYTES;      // 2304 bytes: two NVFP4 super-chunks (a BF16 stage uses 2048)
+constexpr int GQ = 8;                  // 256-column slices of a gate/up band
+constexpr int NB = 8;                  // gate/up reduction buffers (band k uses k % NB)
+constexpr int XPITCH = H * 2 + 16;     // bytes per staged x row: rows 4 banks apart, so the fragment reads do not conflict
+constexpr int NHB = 3;                 // h buffers: the two range slots and the last slot
 constexpr int ROUTER_CTAS = E / 2;     // 128 CTAs x 2 experts
 constexpr int HROW = H_PITCH * 2;      // padded bytes of one token's h row (shared memory and workspace)
-constexpr int HBUF = MAXT * HROW;      // one slot's h, 8.1 KB at T = 8
-constexpr uint32_t SLOT_DONE = W13_BANDS; // gate/up bands that complete a slot
-constexpr int GUU = W13_BANDS;            // 64 gate/up units (one band each) per slot
-constexpr int DN_UNITS = W2_BANDS / GW;   // 32 down units of 4 bands per slot
-constexpr int GU_PARTS = (H / 128) / 2;   // 8 stages per W13 band
-constexpr int DN_PARTS = (I / 128) / 2;   // 2 stages per W2 band
+constexpr int HBUF = MAXT * HROW;      // one slot's h, 8,320 bytes at T = 8
+constexpr uint32_t SLOT_DONE = W13_BANDS;
+// With at least 128 CTAs a CTA has at most ceil(64 * 49 / 128) = 25 gate/up
+// bands (bits of a 32-bit mask) and ceil(128 * 48 / 128) = 48 range down
+// bands (bits of a 64-bit mask), and its down range touches at most two slots.
 
 struct FSmem {
-    uint8_t ring[FW][RING][STG];
-    uint2 xfrag[(H / 16) * 32];        // entry (step, l) at step * 32 + l; zero for l >= 4T
-    uint8_t hbuf[NG][2][HBUF];         // raw h rows, rescaled in place into fragments;
-                                       // before the unit loop: x (T x 4 KB)
-    uint64_t full[FW][RING];
-    uint64_t hbar[NG][2];
-    uint64_t kfull[NG][2];             // K-split gate/up: the three partials of the unit are in kred
-    uint64_t kempty[NG][2];            // K-split gate/up: the unit's writer has read kred
+    uint8_t ring[FW][RW][STG];         // per-warp stage rings; phase 2: warps 8..15's hold x (and delta)
+    union {
+        RouterRed rred;                // phase 2: the router's partial sums
+        struct {
+            float4 red[NB][GQ][32];    // gate/up K partials, [buffer][slice][lane]
+            uint8_t hbuf[NHB][HBUF];   // h rows of a down slot, turned into f16 fragments in place
+        } u;
+    };
+    uint64_t full[FW][RW];
+    uint64_t hbar[NHB];
     uint64_t xbar;
     int32_t sel[MAXT][TOPK];
     float selw[MAXT][TOPK];
@@ -91,14 +101,18 @@ struct FSmem {
     int32_t slot_expert[MAX_SLOTS];
     float wts[MAX_SLOTS][MAXT];
     int xshift[MAXT];
-    float sumsq[FW];                   // pre-norm: per-warp partial sums of squares
-    int hshift[NG][2][MAXT];           // power-of-two exponents of the h in hbuf[grp][b]
-    float hmx[NG][GW][32];             // per-thread max |h| of the down unit being converted
-    float4 kred[NG][2][GW - 1][32];    // K-split gate/up: the non-writers' partials, by unit parity
-    uint32_t gu_done[NG][GW];          // gate/up units whose h warp wq of the group has stored
-    uint32_t dn_done[NG][GW];          // down units whose partial warp wq of the group has stored
-    uint32_t hrel[NG];                 // down units of the group done with their h buffer
-    uint32_t hclaim[NG];               // down units of the group whose h copy has been issued
+    float xinv[MAXT];                  // NVFP4: 2^-xshift[t]
+    float ts13[MAX_SLOTS];             // tensor scales of the slots' W13 and W2 (NVFP4)
+    float ts2[MAX_SLOTS];
+    float all_ts13[E + MAX_SHARED];    // every expert's tensor scales, routed then shared (NVFP4)
+    float all_ts2[E + MAX_SHARED];
+    float sumsq[FW];
+    int hshift[NHB][MAXT];
+    uint64_t pfull[NB];                // a band's eight K partials are in buffer b
+    uint64_t pempty[NB];               // the epilogue warp has read buffer b
+    uint32_t hready[NHB];              // 1 once the h warp has filled the buffer
+    uint32_t gu_mask;                  // CTA gate/up bands whose h is stored (bit k)
+    uint32_t dn_mask[2];               // CTA range down bands whose partial is stored (bit j)
 };
 
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }
@@ -109,22 +123,15 @@ __device__ __forceinline__ int act_shift(float maxabs)
     return sh < -100 ? -100 : (sh > 100 ? 100 : sh);
 }
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
-{
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acquire.gpu;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p)
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p)
 {
     uint32_t v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-
-__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acquire.gpu;" ::: "memory"); }
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // 64-bit relaxed accesses at gpu scope (single-copy atomic)
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v)
@@ -266,19 +273,92 @@ __device__ __forceinline__ void mma_stage(const uint8_t *stage, const uint2 *bfr
     }
 }
 
-struct Unit {
-    bool down;   // down unit (else gate/up)
-    int slot;
-    int band;    // this warp's 16-row band (W13 band for gate/up, W2 band for down)
-};
+// The same with the B fragments of the warp's own 256-column K slice held in
+// registers: xf[s] is k16 step s of the slice (one NVFP4 stage is the whole
+// slice of one band).
+__device__ __forceinline__ void mma_stage_r(const uint8_t *stage, const uint2 (&xf)[16], int lane, float acc[4])
+{
+    const int g = lane >> 2;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const uint8_t *base = stage + q * SC_BYTES;
+        const uint4 sc = *reinterpret_cast<const uint4 *>(base + 1024 + g * 16);
+        const uint32_t sws[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const uint4 cw = *reinterpret_cast<const uint4 *>(base + half * 512 + lane * 16);
+            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint2 b = xf[q * 8 + half * 4 + s];
+                uint32_t a0, a1, a2, a3;
+                decode4(words[s], a0, a1, a2, a3);
+                float d[4];
+                mma_f16_16816(d, a0, a1, a2, a3, b.x, b.y);
+                const int sb = half * 4 + s;
+                const uint32_t sw = sws[sb >> 1];
+                const float2 sf = e4m3x2_to_float2((sb & 1) ? (sw >> 16) : (sw & 0xFFFFu));
+                ffma2(acc[0], acc[1], sf.x, d[0], d[1]);
+                ffma2(acc[2], acc[3], sf.y, d[2], d[3]);
+            }
+        }
+    }
+}
+
+// BF16: sub-stage SUB (64 columns) of the warp's slice, B fragments xf[4 SUB ..].
+template <int SUB>
+__device__ __forceinline__ void bf16_stage_r(const uint8_t *stage, const uint2 (&xf)[16], int lane, float acc[4])
+{
+    const int g = lane >> 2, c = lane & 3, sw = 4 * (g & 1);
+    const uint8_t *ra = stage + g * 128, *rb = stage + (g + 8) * 128;
+    const uint4 a0 = *reinterpret_cast<const uint4 *>(ra + 16 * (c ^ sw));
+    const uint4 a1 = *reinterpret_cast<const uint4 *>(ra + 16 * ((4 + c) ^ sw));
+    const uint4 b0 = *reinterpret_cast<const uint4 *>(rb + 16 * (c ^ sw));
+    const uint4 b1 = *reinterpret_cast<const uint4 *>(rb + 16 * ((4 + c) ^ sw));
+    const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const uint2 b = xf[4 * SUB + s];
+        mma_bf16_16816(acc, wa[2 * s], wb[2 * s], wa[2 * s + 1], wb[2 * s + 1], b.x, b.y);
+    }
+}
+
+// Bounded wait until a shared-memory counter reaches v.
+__device__ __forceinline__ bool smem_wait_geq(const uint32_t *p, uint32_t v, uint32_t *flag)
+{
+    for (uint32_t it = 0; it < SPIN_LIMIT; ++it) {
+        if (ld_acquire_cta(p) >= v)
+            return true;
+        __nanosleep(20);
+    }
+    atomicOr(flag, FLAG_TIMEOUT);
+    return false;
+}
+
+// Bounded wait until a global counter reaches v: relaxed polls (an acquire
+// load costs about as much as a fence while the SM streams), then one
+// acquire fence.
+__device__ __forceinline__ bool gmem_wait_geq(const uint32_t *p, uint32_t v, uint32_t *flag)
+{
+    for (uint32_t it = 0; it < SPIN_LIMIT; ++it) {
+        if (ld_relaxed_gpu(p) >= v) {
+            fence_acquire_gpu();
+            return true;
+        }
+        __nanosleep(32);
+    }
+    atomicOr(flag, FLAG_TIMEOUT);
+    return false;
+}
 
 }  // namespace
 
 template <bool BW>
 __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
 {
-    static_assert(sizeof(RouterRed) <= sizeof(FSmem::ring) / 2, "router partials fit the router warps' rings");
-    static_assert(sizeof(FSmem::hbuf) >= (size_t)2 * MAXT * H * 2, "x and delta fit the h buffers");
+    static_assert(sizeof(RouterRed) <= sizeof(FSmem::u), "router partials fit the unit-phase buffers");
+    static_assert((size_t)2 * MAXT * XPITCH <= sizeof(FSmem::ring) / 2, "x and delta fit the rings of warps 8..15");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     FSmem &sm = *reinterpret_cast<FSmem *>(smem_raw);
 
@@ -292,104 +372,64 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
     float *partials = reinterpret_cast<float *>(a.ws + L.partials);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int grp = warp / GW, wq = warp % GW;
-    const bool leader = (wq == 0);
-    const bool lead_thread = leader && lane == 0;
+    const int q = warp & (GQ - 1), par = warp >> 3;   // compute warps: K slice and band parity
     const int T = a.T;
     const int blanes = 4 * T;
+    const int G = (int)gridDim.x, cta = (int)blockIdx.x;
 
     if (lane == 0 && warp < FW) {
-        for (int s = 0; s < RING; ++s)
+        for (int s = 0; s < RW; ++s)
             mbar_init(&sm.full[warp][s], BW ? 32 : 1);   // BF16: one cp.async arrival per lane
-        if (leader) {
-            mbar_init(&sm.hbar[grp][0], 1);
-            mbar_init(&sm.hbar[grp][1], 1);
-            for (int q = 0; q < 2; ++q) {
-                mbar_init(&sm.kfull[grp][q], GW - 1);
-                mbar_init(&sm.kempty[grp][q], 1);
-            }
-        }
-        if (threadIdx.x == 0)
-            mbar_init(&sm.xbar, 1);
+    }
+    if (threadIdx.x < NB) {
+        mbar_init(&sm.pfull[threadIdx.x], GQ);   // the band's eight K partials are in
+        mbar_init(&sm.pempty[threadIdx.x], 1);   // the epilogue warp has read them
+    }
+    if (threadIdx.x == 0) {
+        for (int r = 0; r < NHB; ++r)
+            mbar_init(&sm.hbar[r], 1);
+        mbar_init(&sm.xbar, 1);
+    }
+    if (lane == 0 && warp <= FW)
         fence_barrier_init();
+    if (threadIdx.x < NHB)
+        sm.hready[threadIdx.x] = 0u;
+    if (threadIdx.x == 0) {
+        sm.gu_mask = 0u;
+        sm.dn_mask[0] = sm.dn_mask[1] = 0u;
     }
     __syncthreads();
 
-    auto w13_src = [&](int slot, int band) -> const uint8_t * {
-        const uint8_t *base = (slot < a.n_shared) ? a.s_w13 + (size_t)slot * W13_BYTES
-                                                  : a.r_w13 + (size_t)sm.slot_expert[slot] * W13_BYTES;
-        return base + (size_t)band * W13_BAND_BYTES;
+    auto bank13 = [&](int slot) -> const uint8_t * {
+        return (slot < a.n_shared) ? a.s_w13 + (size_t)slot * (BW ? W13_BYTES_BF : W13_BYTES)
+                                   : a.r_w13 + (size_t)sm.slot_expert[slot] * (BW ? W13_BYTES_BF : W13_BYTES);
     };
-    auto w2_src = [&](int slot, int band) -> const uint8_t * {
-        const uint8_t *base = (slot < a.n_shared) ? a.s_w2 + (size_t)slot * W2_BYTES
-                                                  : a.r_w2 + (size_t)sm.slot_expert[slot] * W2_BYTES;
-        return base + (size_t)band * W2_BAND_BYTES;
-    };
-    // BF16 banks: W13 [2I][H] and W2 [H][I] row-major per expert
-    auto bf_w13 = [&](int slot) -> const __nv_bfloat16 * {
-        const uint8_t *base = (slot < a.n_shared) ? a.s_w13 + (size_t)slot * W13_BYTES_BF
-                                                  : a.r_w13 + (size_t)sm.slot_expert[slot] * W13_BYTES_BF;
-        return reinterpret_cast<const __nv_bfloat16 *>(base);
-    };
-    auto bf_w2 = [&](int slot) -> const __nv_bfloat16 * {
-        const uint8_t *base = (slot < a.n_shared) ? a.s_w2 + (size_t)slot * W2_BYTES_BF
-                                                  : a.r_w2 + (size_t)sm.slot_expert[slot] * W2_BYTES_BF;
-        return reinterpret_cast<const __nv_bfloat16 *>(base);
-    };
-    // one stage = two super-chunks (2304 bytes) of this warp's band: part p
-    auto stage_src = [&](const Unit &u, int p) -> const uint8_t * {
-        return (u.down ? w2_src(u.slot, u.band) : w13_src(u.slot, u.band)) + (size_t)(2 * p) * SC_BYTES;
-    };
-    auto issue_stage = [&](int ring_slot, const Unit &u, int p) {
-        uint64_t *bar = &sm.full[warp][ring_slot];
-        if (BW) {
-            // chunk p (64 columns) of the 16 rows: lane 2r + h copies bytes
-            // [64 h, 64 h + 64) of row r, then arrives when they have landed
-            const int r = lane >> 1, h = lane & 1;
-            const uint8_t *src;
-            if (!u.down) {
-                const int row = r < 8 ? 8 * u.band + r : I + 8 * u.band + (r - 8);
-                src = reinterpret_cast<const uint8_t *>(bf_w13(u.slot)) + ((size_t)row * H + 64 * p) * 2 + 64 * h;
-            } else {
-                src = reinterpret_cast<const uint8_t *>(bf_w2(u.slot)) + ((size_t)(16 * u.band + r) * I + 64 * p) * 2 +
-                      64 * h;
-            }
-            uint8_t *dst = sm.ring[warp][ring_slot] + r * 128;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                cp_async_cg16(dst + 16 * ((4 * h + i) ^ (4 * (r & 1))), src + 16 * i);
-            cp_async_arrive(bar);
-            return;
-        }
-        if (lane != 0)
-            return;
-        mbar_arrive_expect_tx(bar, STG);
-        bulk_g2s(sm.ring[warp][ring_slot], stage_src(u, p), STG, bar);
+    auto bank2 = [&](int slot) -> const uint8_t * {
+        return (slot < a.n_shared) ? a.s_w2 + (size_t)slot * (BW ? W2_BYTES_BF : W2_BYTES)
+                                   : a.r_w2 + (size_t)sm.slot_expert[slot] * (BW ? W2_BYTES_BF : W2_BYTES);
     };
 
     // ---- phase 1: work that needs nothing from the preceding kernel ----
-    // units are dealt round-robin: group gid takes ids gid, gid + G, ...; the
-    // shared expert's gate/up units (ids 0..63) go to group 0 of the first
-    // CTAs.  A gate/up unit is one band and each warp takes a K quarter (two
-    // of the band's eight stages), so the few slots of a small batch still
-    // spread over every warp.
-    // stages of a unit per warp: NVFP4 two super-chunks each, BF16 one
-    // 64-column chunk of the 16 rows each
-    auto nparts = [&](const Unit &u) {
-        return BW ? (u.down ? I / 64 : H / 64 / GW) : (u.down ? DN_PARTS : GU_PARTS / GW);
-    };
-    auto part0 = [&](const Unit &u) { return u.down ? 0 : nparts(u) * wq; };
-    const int n_groups = NG * (int)gridDim.x;
-    const int gid = grp * (int)gridDim.x + (int)blockIdx.x;
-    const bool static_shared = !BW && warp < FW && (a.n_shared > 0) && gid < GUU;
-    const Unit u0 = Unit{false, 0, gid};
-    const int n_pre = static_shared ? min(RING, nparts(u0)) : 0;
-    for (int p = 0; p < n_pre; ++p)
-        issue_stage(p, u0, part0(u0) + p);
+    // CTA c's first gate/up band is band c of slot 0: the shared expert when
+    // there is one.  Its parity-0 warps take their slices of it now (NVFP4;
+    // the slot table is not built yet, so the address is computed directly).
+    const bool pre_shared = !BW && warp < FW && par == 0 && a.n_shared > 0 && cta < W13_BANDS;
+    if (pre_shared && lane == 0) {
+        uint64_t *bar = &sm.full[warp][0];
+        mbar_arrive_expect_tx(bar, STG);
+        bulk_g2s(sm.ring[warp][0], a.s_w13 + (size_t)cta * W13_BAND_BYTES + (size_t)q * STG, STG, bar);
+    }
+    // every expert's tensor scales (NVFP4), for the slot table built later
+    if (!BW) {
+        for (int i = threadIdx.x; i < E + a.n_shared; i += NT) {
+            sm.all_ts13[i] = i < E ? __ldg(a.r_ts13 + i) : __ldg(a.s_ts13 + (i - E));
+            sm.all_ts2[i] = i < E ? __ldg(a.r_ts2 + i) : __ldg(a.s_ts2 + (i - E));
+        }
+    }
     // router CTAs: warp w of the 16 takes expert 2 * cta + w / 8, columns
     // [256 (w % 8), 256 (w % 8) + 256), eight per lane
-    const bool router_warp = blockIdx.x < ROUTER_CTAS && warp < FW;
-    const int r_e = blockIdx.x * 2 + (warp >> 3);
+    const bool router_warp = cta < ROUTER_CTAS && warp < FW;
+    const int r_e = cta * 2 + (warp >> 3);
     const int r_k8 = warp & 7;
     uint4 wv = make_uint4(0u, 0u, 0u, 0u);
     if (router_warp)
@@ -401,14 +441,21 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
     const uint32_t ltag = __ldcg(&ctrl[5]) + 1u;
 
     // ---- phase 2: x -> shared memory; router logits | activation fragments ----
-    uint8_t *xs = &sm.hbuf[0][0][0];   // T x 4 KB, free until the unit loop
-    uint8_t *ds = xs + MAXT * H * 2;   // pre-norm: the previous layer's output, T x 4 KB
+    // T rows of XPITCH bytes each, free until the unit phase; lane t of warp 0
+    // copies row t (several issuing threads: one thread issues bulk copies
+    // only about every 200 ns)
+    uint8_t *xs = &sm.ring[8][0][0];
+    uint8_t *ds = xs + MAXT * XPITCH;  // pre-norm: the previous layer's output
     const bool has_delta = a.prenorm && a.delta != nullptr;
-    if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(&sm.xbar, (uint32_t)(T * H * 2) * (has_delta ? 2u : 1u));
-        bulk_g2s(xs, a.x, (uint32_t)(T * H * 2), &sm.xbar);
-        if (has_delta)
-            bulk_g2s(ds, a.delta, (uint32_t)(T * H * 2), &sm.xbar);
+    if (warp == 0) {
+        if (lane == 0)
+            mbar_arrive_expect_tx(&sm.xbar, (uint32_t)(T * H * 2) * (has_delta ? 2u : 1u));
+        __syncwarp();
+        if (lane < T)
+            bulk_g2s(xs + lane * XPITCH, a.x + (size_t)lane * H, (uint32_t)(H * 2), &sm.xbar);
+        else if (has_delta && lane >= MAXT && lane < MAXT + T)
+            bulk_g2s(ds + (lane - MAXT) * XPITCH, a.delta + (size_t)(lane - MAXT) * H, (uint32_t)(H * 2),
+                     &sm.xbar);
     }
     mbar_wait_bounded(&sm.xbar, 0, flag);
     if (a.prenorm) {
@@ -425,7 +472,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         if (t < T) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int idx = t * (H / 8) + half * (H / 16) + 32 * i + lane;
+                const int idx = t * (XPITCH / 16) + half * (H / 16) + 32 * i + lane;
                 uint4 r = xv[idx];
                 if (has_delta) {
                     const uint4 d = dv[idx];
@@ -459,7 +506,8 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             const float rinv = 1.0f / sqrtf(ms + a.eps);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int idx = t * (H / 8) + half * (H / 16) + 32 * i + lane;
+                const int idx = t * (XPITCH / 16) + half * (H / 16) + 32 * i + lane;
+                const int gidx = t * (H / 8) + half * (H / 16) + 32 * i + lane;
                 uint4 n = vv[i];
                 uint32_t *nw = &n.x;
 #pragma unroll
@@ -468,18 +516,18 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                     const __nv_bfloat16 hi = __float2bfloat16_rn(bf16_bits_to_float(nw[q] >> 16) * rinv);
                     nw[q] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
                 }
-                xv[idx] = n;
+                xv[idx] = n;   // (followed by fence_proxy_async below: the rings are refilled by bulk copies)
                 if (blockIdx.x == 0) {
                     if (a.resid_out)
-                        reinterpret_cast<uint4 *>(a.resid_out)[idx] = vv[i];
+                        reinterpret_cast<uint4 *>(a.resid_out)[gidx] = vv[i];
                     if (a.xn_out)
-                        reinterpret_cast<uint4 *>(a.xn_out)[idx] = n;
+                        reinterpret_cast<uint4 *>(a.xn_out)[gidx] = n;
                 }
             }
         }
+        fence_proxy_async();
         __syncthreads();
     }
-    const __nv_bfloat16 *xsh = reinterpret_cast<const __nv_bfloat16 *>(xs);
 
     if (router_warp) {
         float acc[MAXT];
@@ -488,38 +536,36 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         for (int t = 0; t < MAXT; ++t) {
             acc[t] = 0.0f;
             if (t < T) {
-                const uint4 xv = *reinterpret_cast<const uint4 *>(xsh + (size_t)t * H + 256 * r_k8 + 8 * lane);
+                const uint4 xv = *reinterpret_cast<const uint4 *>(xs + (size_t)t * XPITCH + 2 * (256 * r_k8 + 8 * lane));
                 const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    acc[t] = fmaf(bf16_bits_to_float(xw[q] & 0xFFFFu), bf16_bits_to_float(ww[q] & 0xFFFFu), acc[t]);
-                    acc[t] = fmaf(bf16_bits_to_float(xw[q] >> 16), bf16_bits_to_float(ww[q] >> 16), acc[t]);
+                for (int qq = 0; qq < 4; ++qq) {
+                    acc[t] = fmaf(bf16_bits_to_float(xw[qq] & 0xFFFFu), bf16_bits_to_float(ww[qq] & 0xFFFFu), acc[t]);
+                    acc[t] = fmaf(bf16_bits_to_float(xw[qq] >> 16), bf16_bits_to_float(ww[qq] >> 16), acc[t]);
                 }
             }
         }
-        // the stage rings of warps 8..15 are idle until the unit loop (the
-        // shared expert's early copies go to warps 0..3)
-        RouterRed &red = *reinterpret_cast<RouterRed *>(&sm.ring[8][0][0]);
         float logit;
         // each logit carries the launch tag in the same 64-bit word, so a
         // reader that sees the tag sees the logit: no fence, no counter
-        if (router_reduce(acc, (int)threadIdx.x, T, red, 5, &logit))
-            st_relaxed_u64(&tlogits[(threadIdx.x % MAXT) * E + blockIdx.x * 2 + threadIdx.x / MAXT],
+        if (router_reduce(acc, (int)threadIdx.x, T, sm.rred, 5, &logit))
+            st_relaxed_u64(&tlogits[(threadIdx.x % MAXT) * E + cta * 2 + threadIdx.x / MAXT],
                            ((unsigned long long)ltag << 32) | __float_as_uint(logit));
-        fence_proxy_async();               // the ring is refilled by bulk copies later
+        fence_proxy_async();   // these generic writes precede the bulk copies of h into the same buffer
     }
-    if (warp < 8) {
-        // x -> mma fragments [step][32] (zeros in lanes 4T..): lane l < 4T of
-        // warp w holds steps w, w + 8, ... of token l / 4.  BF16 weights:
-        // bf16 in the permuted column order of bf16_bcol.  NVFP4: f16, each
-        // token's row scaled by the power of two of its max |x| (found first,
-        // one warp per token).
+    // x -> the B fragments of this warp's 256-column slice q, in registers:
+    // entry s is k16 step 16 q + s; lane l < 4T holds token l / 4 (zeros
+    // above).  NVFP4: f16, each token's row scaled by the power of two of its
+    // max |x| (found first, one warp per token).  BF16: bf16 in the permuted
+    // column order of bf16_bcol.
+    uint2 xf[16];
+    if (warp < FW) {
         const uint32_t *xw = reinterpret_cast<const uint32_t *>(xs);
         const int g = lane >> 2, c = lane & 3;
         float p = 1.0f;
         if (!BW) {
             if (warp < T) {
-                const uint4 *row = reinterpret_cast<const uint4 *>(xsh + (size_t)warp * H);
+                const uint4 *row = reinterpret_cast<const uint4 *>(xs + (size_t)warp * XPITCH);
                 __nv_bfloat162 m2 = __floats2bfloat162_rn(0.f, 0.f);
 #pragma unroll
                 for (int i = 0; i < H / 256; ++i) {
@@ -532,28 +578,29 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                 // max |x| >= 0: its fp32 bit pattern orders like an unsigned int
                 const float m = __uint_as_float(
                     __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fmaxf(__low2float(m2), __high2float(m2)))));
-                if (lane == 0)
+                if (lane == 0) {
                     sm.xshift[warp] = act_shift(m);
+                    sm.xinv[warp] = pow2i(-act_shift(m));
+                }
             }
-            named_barrier_sync(6, 256);
+            named_barrier_sync(6, FT);
             if (lane < blanes)
                 p = pow2i(sm.xshift[g]);
         }
-        {
-#pragma unroll 4
-            for (int step = warp; step < H / 16; step += 8) {
-                uint2 v = make_uint2(0u, 0u);   // lanes 4T.. carry no token
-                if (lane < blanes) {
-                    if (BW) {
-                        const int w0 = (g * H + bf16_bcol(step, c)) / 2;
-                        v = make_uint2(xw[w0], xw[w0 + 1]);
-                    } else {
-                        const int w0 = (g * H + 16 * step) / 2 + c;
-                        v = make_uint2(bf16x2_to_f16x2_scaled(xw[w0], p), bf16x2_to_f16x2_scaled(xw[w0 + 4], p));
-                    }
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+            const int step = 16 * q + s;
+            uint2 v = make_uint2(0u, 0u);   // lanes 4T.. carry no token
+            if (lane < blanes) {
+                if (BW) {
+                    const int w0 = g * (XPITCH / 4) + bf16_bcol(step, c) / 2;
+                    v = make_uint2(xw[w0], xw[w0 + 1]);
+                } else {
+                    const int w0 = g * (XPITCH / 4) + 8 * step + c;
+                    v = make_uint2(bf16x2_to_f16x2_scaled(xw[w0], p), bf16x2_to_f16x2_scaled(xw[w0 + 4], p));
                 }
-                sm.xfrag[step * 32 + lane] = v;
             }
+            xf[s] = v;
         }
     }
 
@@ -562,14 +609,6 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         sm.wts[i / MAXT][i % MAXT] = 0.0f;
     if (threadIdx.x < E / 32)
         sm.bitmap[threadIdx.x] = 0u;
-    if (threadIdx.x < NG * GW) {
-        (&sm.gu_done[0][0])[threadIdx.x] = 0u;
-        (&sm.dn_done[0][0])[threadIdx.x] = 0u;
-    }
-    if (threadIdx.x < NG) {
-        sm.hrel[threadIdx.x] = 0u;
-        sm.hclaim[threadIdx.x] = 0u;
-    }
 
     __syncthreads();
     if (warp < T) {
@@ -657,7 +696,13 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                 sm.wts[b0 + __popc(wbits & ((1u << (ei & 31)) - 1u))][t] = sm.selw[t][i % TOPK];
         }
     }
-    fence_proxy_async();   // generic writes to the x / h region precede later bulk copies into it
+    __syncthreads();
+    if (!BW && threadIdx.x < (unsigned)sm.n_slots) {
+        const int sl = threadIdx.x;
+        const int ie = sl < a.n_shared ? E + sl : sm.slot_expert[sl];
+        sm.ts13[sl] = sm.all_ts13[ie];
+        sm.ts2[sl] = sm.all_ts2[ie];
+    }
     __syncthreads();
     const int n_slots = sm.n_slots;
     if (blockIdx.x == 0) {
@@ -672,460 +717,397 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             st->wts[i / MAXT][i % MAXT] = sm.wts[i / MAXT][i % MAXT];
     }
 
+
     // ---- phase 4: the units ----
-    const int gu_total = n_slots * GUU;                             // unit ids [0, gu_total): gate/up
-    const int end_id = gu_total + n_slots * DN_UNITS;               // then down units
-    auto unit_id_of = [&](int group, int k) { return group + k * n_groups; };
-    auto unit_id = [&](int k) { return unit_id_of(gid, k); };
-    auto decode = [&](int id) -> Unit {
-        if (id < gu_total)
-            return Unit{false, (int)((unsigned)id / GUU), (int)((unsigned)id % GUU)};
-        const int d = id - gu_total;
-        return Unit{true, (int)((unsigned)d / DN_UNITS), 4 * (int)((unsigned)d % DN_UNITS) + wq};
-    };
-    // first down unit of this group, and the down-unit index of unit k
-    const int k_down0 = gid >= gu_total ? 0 : (gu_total - gid + n_groups - 1) / n_groups;
-    // h of down unit dk of group g: the slot's T padded rows, one bulk copy
-    // into hbuf[g][dk & 1] (the slot counter has been acquired)
-    auto issue_h = [&](int g, int slot, int b) {
-        fence_proxy_async_global();   // h was published to the generic proxy by releases
-        uint64_t *bar = &sm.hbar[g][b];
-        const uint32_t bytes = (uint32_t)((T - 1) * HROW + I * 2);
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(sm.hbuf[g][b], hglob + (size_t)slot * MAXT * H_PITCH, bytes, bar);
+    const int U = n_slots;
+    // gate/up: CTA band k is global band cta + G k (slot-major: slot gb / 64)
+    const int gu_total = W13_BANDS * U;
+    const int n_gu_cta = cta < gu_total ? (gu_total - cta + G - 1) / G : 0;
+    // down: the first U - 1 slots' bands in G contiguous ranges, and band
+    // cta of the last slot (CTA down band j = n_rng for it)
+    const long rng_total = (long)W2_BANDS * (U - 1);
+    const int d0 = (int)(rng_total * cta / G), d1 = (int)(rng_total * (cta + 1) / G);
+    const int n_rng = d1 - d0;
+    const bool has_last = cta < W2_BANDS;
+    const int n_dn_cta = n_rng + (has_last ? 1 : 0);
+    const int s_first = d0 / W2_BANDS;          // h buffer 0 (and 1 for s_first + 1); buffer 2: the last slot
+    auto dn_band = [&](int j, int &slot, int &band, int &hb) {
+        if (j < n_rng) {
+            const int db = d0 + j;
+            slot = db / W2_BANDS;
+            band = db % W2_BANDS;
+            hb = slot - s_first;
+        } else {
+            slot = U - 1;
+            band = cta;
+            hb = 2;
+        }
     };
 
-    // The warp that computed a band's partial for the last slot adds up the
-    // band once the other n_slots - 1 partials are counted: every slot's
-    // partial in slot order, its own last.
-    auto combine_band = [&](int band) {
-        const int r = lane >> 1, th = lane & 1;      // row r, tokens 4*th .. 4*th+3
-        const float4 *src = reinterpret_cast<const float4 *>(partials + ((size_t)16 * band + r) * MAXT) + th;
-        if (lane == 0) {
-            for (uint32_t it = 0; ld_acquire(&band_cnt[band]) < (uint32_t)(n_slots - 1); ++it) {
-                if (it == SPIN_LIMIT) {
-                    atomicOr(flag, FLAG_TIMEOUT);
-                    break;
+    if (warp == EP_WARP || warp == EP_WARP + 1) {
+        // ---- the epilogue warps: the gate/up bands' h ----
+        // Epilogue warp p takes the CTA's gate/up bands k = p, p + 2, ... in
+        // order: once buffer k % NB holds band k's eight K partials it adds
+        // them in slice order, frees the buffer, applies SiLU*up (NVFP4:
+        // times the tensor scale and the token's inverse power of two),
+        // stores h and sets bit k of gu_mask for the count warp.
+        const int p = warp - EP_WARP;
+        const int g = lane >> 2, c = lane & 3;
+#pragma unroll 1
+        for (int k = p; k < n_gu_cta; k += 2) {
+            const int b = k % NB;
+            if (lane == 0)
+                mbar_wait_bounded(&sm.pfull[b], (uint32_t)(k / NB) & 1u, flag);
+            __syncwarp();   // lane 0 saw the partials complete; the others read after it
+            float4 sum = sm.u.red[b][0][lane];
+#pragma unroll
+            for (int qq = 1; qq < GQ; ++qq) {
+                const float4 v = sm.u.red[b][qq][lane];
+                sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.pempty[b]);
+            const int gb = cta + G * k, slot = gb / W13_BANDS, band = gb % W13_BANDS;
+            const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt) {
+                const int t = 2 * c + tt;
+                if (t < T) {
+                    const float f = BW ? 1.0f : sm.ts13[slot] * sm.xinv[t];
+                    const float gv = sv[tt] * f, uv = sv[2 + tt] * f;
+                    hglob[((size_t)slot * MAXT + t) * H_PITCH + band * 8 + g] =
+                        __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
                 }
-                __nanosleep(32);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                atomicOr(&sm.gu_mask, 1u << k);
+            }
+        }
+    } else if (warp == CNT_WARP) {
+        // ---- the count warp: every cross-CTA count of this CTA's work ----
+        // The epilogue warps set a bit of gu_mask when the h of a CTA gate/up
+        // band is stored, the compute warps one of dn_mask when the partial
+        // of a range down band is; each pass adds the newly set ones to the
+        // slot and band counters behind one gpu-scope fence (a fence costs
+        // the issuing warp about a microsecond while the SM streams, so no
+        // other warp executes one).  Lane 0 does the work.
+        if (lane == 0) {
+            const uint32_t gall = n_gu_cta >= 32 ? 0xFFFFFFFFu : ((1u << n_gu_cta) - 1u);
+            const unsigned long long dall = n_rng >= 64 ? ~0ull : ((1ull << n_rng) - 1ull);
+            uint32_t gdone = 0u;
+            unsigned long long ddone = 0ull;
+            bool out = false;
+            for (uint32_t it = 0; it < 4 * SPIN_LIMIT; ++it) {
+                // plain polls: the gpu-scope fence below orders what they saw
+                const uint32_t gm = *reinterpret_cast<volatile uint32_t *>(&sm.gu_mask) & gall;
+                const unsigned long long dm =
+                    ((unsigned long long)*reinterpret_cast<volatile uint32_t *>(&sm.dn_mask[1]) << 32 |
+                     *reinterpret_cast<volatile uint32_t *>(&sm.dn_mask[0])) & dall;
+                uint32_t ng = gm & ~gdone;
+                unsigned long long nd = dm & ~ddone;
+                if (ng | nd) {
+                    fence_acq_rel_gpu();   // the stores counted below become visible before their counts
+                    while (ng) {
+                        const int k = __ffs(ng) - 1;
+                        red_relaxed_add(&slot_cnt[(cta + G * k) / W13_BANDS], 1u);
+                        ng &= ng - 1;
+                    }
+                    while (nd) {
+                        const int j = __ffsll(nd) - 1;
+                        red_relaxed_add(&band_cnt[(d0 + j) % W2_BANDS], 1u);
+                        nd &= nd - 1;
+                    }
+                    gdone |= gm;
+                    ddone |= dm;
+                }
+                if (!out && gdone == gall) {
+                    // no more slot-counter adds from this warp
+                    fence_acq_rel_gpu();
+                    red_relaxed_add(&ctrl[4], 1u);
+                    out = true;
+                }
+                if (out && ddone == dall)
+                    break;
+                if (it + 1 == 4 * SPIN_LIMIT)
+                    atomicOr(flag, FLAG_TIMEOUT);
+                if (!(ng | nd))
+                    __nanosleep(32);
+            }
+            if (!out) {
+                fence_acq_rel_gpu();
+                red_relaxed_add(&ctrl[4], 1u);
             }
         }
         __syncwarp();
-        float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        constexpr int BATCH = 16;
-        for (int s0 = 0; s0 < n_slots; s0 += BATCH) {
-            float4 v[BATCH];
-#pragma unroll
-            for (int j = 0; j < BATCH; ++j)
-                v[j] = (s0 + j < n_slots) ? __ldcg(src + (size_t)(s0 + j) * H * MAXT / 4)
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < BATCH; ++j) {
-                s4.x += v[j].x; s4.y += v[j].y; s4.z += v[j].z; s4.w += v[j].w;
+    } else if (warp == HW_WARP) {
+        // ---- the h warp: h of the CTA's down slots as f16 fragments ----
+        // For each slot (range slots in order, then the last slot): wait until
+        // its 64 gate/up bands are counted, copy its T padded h rows, scale
+        // each token's row by the power of two of its max |h| (NVFP4) and
+        // rewrite the buffer in place as the B fragments of the down GEMV,
+        // [k16 step][lane] (zeros in lanes 4T..).
+        int hslot[NHB];
+        bool hneed[NHB];
+        hslot[0] = s_first;
+        hneed[0] = n_rng > 0;
+        hslot[1] = s_first + 1;
+        hneed[1] = n_rng > 0 && (d1 - 1) / W2_BANDS == s_first + 1;
+        hslot[2] = U - 1;
+        hneed[2] = has_last;
+        const int hg = lane >> 2, hc = lane & 3;
+        const bool hl = lane < blanes;
+#pragma unroll 1
+        for (int r = 0; r < NHB; ++r) {
+            if (!hneed[r])
+                continue;
+            if (lane == 0) {
+                gmem_wait_geq(&slot_cnt[hslot[r]], SLOT_DONE, flag);
+                fence_proxy_async_global();   // h was published to the generic proxy
+                const uint32_t bytes = (uint32_t)((T - 1) * HROW + I * 2);
+                mbar_arrive_expect_tx(&sm.hbar[r], bytes);
+                bulk_g2s(sm.u.hbuf[r], hglob + (size_t)hslot[r] * MAXT * H_PITCH, bytes, &sm.hbar[r]);
             }
-        }
-        const float vals[4] = {s4.x, s4.y, s4.z, s4.w};
+            __syncwarp();
+            mbar_wait_bounded(&sm.hbar[r], 0, flag);
+            const uint32_t *hw = reinterpret_cast<const uint32_t *>(sm.u.hbuf[r]);
+            constexpr int HS = I / 16;   // 32 k16 steps
+            uint32_t src0[HS], src1[HS];
+            __nv_bfloat162 m2 = __floats2bfloat162_rn(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int t = 4 * th + j;
-            if (t < T)
-                a.out[(size_t)t * H + 16 * band + r] = __float2bfloat16_rn(vals[j]);
-        }
-        if (lane == 0)
-            band_cnt[band] = 0u;
-    };
-
-    // ---- the sync warp: every cross-CTA step of the unit phase ----
-    // Lane g < NG follows group g.  Each pass it (1) copies h for the
-    // group's next down unit once the slot's 64 gate/up bands are counted
-    // (two h buffers per group, refilled when the group has released one);
-    // (2) counts the bands whose h the group's warps have stored into the
-    // slot counters and their down partials (all but the last slot's) into
-    // the band counters, with one gpu-scope fence ahead of all the counts of
-    // the pass, so that no compute warp ever waits on a fence or an atomic.
-    auto run_sync_warp = [&]() {
-        const int g = lane;
-        const bool gl = lane < NG;
-        const int gid_g = g * (int)gridDim.x + (int)blockIdx.x;
-        int kd0 = 0, ndn = 0;
-        if (gl) {
-            kd0 = gid_g >= gu_total ? 0 : (gu_total - gid_g + n_groups - 1) / n_groups;
-            const int kend = gid_g >= end_id ? 0 : (end_id - gid_g + n_groups - 1) / n_groups;
-            ndn = kend - kd0;
-        }
-        uint32_t gsig[GW], dsig[GW], n_gu[GW];
-#pragma unroll
-        for (int q = 0; q < GW; ++q) {
-            gsig[q] = dsig[q] = 0u;
-            n_gu[q] = kd0 > q ? (uint32_t)((kd0 - q + GW - 1) / GW) : 0u;   // units k = q + 4n < kd0
-        }
-        int h_next = 0, probe_for = -1;
-        uint32_t probe_val = 0u;
-        bool counted_out = false;        // this CTA reads no slot counter any more
-        for (uint32_t it = 0;; ++it) {
-            if (it == 4 * SPIN_LIMIT) {
-                if (lane == 0)
-                    atomicOr(flag, FLAG_TIMEOUT);
-                break;
-            }
-            bool busy = false;
-            // (1) h of the next down unit
-            if (gl && h_next < ndn) {   // copies the group's leader claimed
-                const int claimed = (int)*reinterpret_cast<volatile uint32_t *>(&sm.hclaim[g]);
-                if (claimed > h_next) {
-                    h_next = claimed;
-                    probe_for = -1;
+            for (int s = 0; s < HS; ++s) {
+                src0[s] = src1[s] = 0u;
+                if (hl) {
+                    if (BW) {
+                        const int w0 = (hg * HROW) / 4 + bf16_bcol(s, hc) / 2;
+                        src0[s] = hw[w0];
+                        src1[s] = hw[w0 + 1];
+                    } else {
+                        const int w0 = (hg * HROW) / 4 + 8 * s + hc;
+                        src0[s] = hw[w0];
+                        src1[s] = hw[w0 + 4];
+                        m2 = __hmax2(m2, __habs2(u32_as_bf162(src0[s])));
+                        m2 = __hmax2(m2, __habs2(u32_as_bf162(src1[s])));
+                    }
                 }
             }
-            if (gl && h_next < ndn && h_next < (int)ld_acquire_cta(&sm.hrel[g]) + 2) {
-                const int slot = (unit_id_of(gid_g, kd0 + h_next) - gu_total) / DN_UNITS;
-                if (probe_for == h_next && probe_val >= SLOT_DONE) {
-                    fence_acquire_gpu();     // pairs with the fences ahead of the slot's counts
-                    if (atomicCAS(&sm.hclaim[g], (uint32_t)h_next, (uint32_t)h_next + 1u) == (uint32_t)h_next)
-                        issue_h(g, slot, h_next & 1);
-                    ++h_next;
-                    probe_for = -1;
-                    busy = true;
-                } else {
-                    probe_val = ld_relaxed(&slot_cnt[slot]);   // looked at on the next pass
-                    probe_for = h_next;
-                }
+            int sh = 0;
+            if (!BW) {
+                // the token's max over its four lanes (all 512 values)
+                float mx = fmaxf(__low2float(m2), __high2float(m2));
+                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+                sh = act_shift(mx);
             }
-            // (2) counts
-            uint32_t gd[GW], dd[GW];
-            bool fresh = false;
+            const float p = pow2i(sh);
+            if (hc == 0 && hl)
+                sm.hshift[r][hg] = sh;
+            __syncwarp();
+            uint2 *hf = reinterpret_cast<uint2 *>(sm.u.hbuf[r]);
 #pragma unroll
-            for (int q = 0; q < GW; ++q) {
-                gd[q] = gl ? ld_acquire_cta(&sm.gu_done[g][q]) : 0u;
-                dd[q] = gl ? ld_acquire_cta(&sm.dn_done[g][q]) : 0u;
-                fresh |= gd[q] != gsig[q] || dd[q] != dsig[q];
+            for (int s = 0; s < HS; ++s)
+                hf[s * 32 + lane] = BW ? make_uint2(src0[s], src1[s])
+                                       : make_uint2(bf16x2_to_f16x2_scaled(src0[s], p),
+                                                    bf16x2_to_f16x2_scaled(src1[s], p));
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                st_release_cta(&sm.hready[r], 1u);
             }
-            // new counts to add (the last slot's partials are not counted)
-            bool need = false;
-#pragma unroll
-            for (int q = 0; q < GW; ++q) {
-                need |= gd[q] != gsig[q];
-                if (dd[q] != dsig[q])
-                    need |= (unit_id_of(gid_g, kd0 + (int)dsig[q]) - gu_total) / DN_UNITS < n_slots - 1;
-            }
-            if (__any_sync(0xFFFFFFFFu, fresh)) {
-                busy = true;
-                if (__any_sync(0xFFFFFFFFu, need))
-                    fence_acq_rel_gpu();   // the stores counted below become visible before their counts
-                if (gl) {
-#pragma unroll
-                    for (int q = 0; q < GW; ++q)
-                        for (; gsig[q] < gd[q]; ++gsig[q]) {
-                            const int kq = q + GW * (int)gsig[q];
-                            if (kq != kd0 - 1)   // the group's last gate/up band is counted by its writer
-                                red_relaxed_add(&slot_cnt[(unsigned)unit_id_of(gid_g, kq) / GUU], 1u);
-                        }
-#pragma unroll
-                    for (int q = 0; q < GW; ++q)
-                        for (; dsig[q] < dd[q]; ++dsig[q]) {
-                            const int d = unit_id_of(gid_g, kd0 + (int)dsig[q]) - gu_total;
-                            // the last slot's partial is added where it is made; the
-                            // group's last down unit is counted by its own warps
-                            if (d / DN_UNITS < n_slots - 1 && (int)dsig[q] != ndn - 1)
-                                red_relaxed_add(&band_cnt[4 * (d % DN_UNITS) + q], 1u);
-                        }
-                }
-            }
-            bool slots_done = !gl || h_next == ndn;
-#pragma unroll
-            for (int q = 0; q < GW; ++q)
-                slots_done = slots_done && (!gl || gsig[q] == n_gu[q]);
-            if (!counted_out && __all_sync(0xFFFFFFFFu, slots_done)) {
-                // this CTA neither reads nor adds to a slot counter any more:
-                // count it out (the fence orders those accesses first)
-                __syncwarp();
-                if (lane == 0) {
-                    fence_acq_rel_gpu();
-                    red_relaxed_add(&ctrl[4], 1u);
-                }
-                counted_out = true;
-            }
-            bool done = counted_out && (!gl || h_next == ndn);
-#pragma unroll
-            for (int q = 0; q < GW; ++q)
-                done = done && (!gl || (gsig[q] == n_gu[q] && dsig[q] == (uint32_t)ndn));
-            if (__all_sync(0xFFFFFFFFu, done))
-                break;
-            if (!__any_sync(0xFFFFFFFFu, busy))
-                __nanosleep(64);
         }
-    };
-
-    if (warp == SYNC_WARP) {
-        run_sync_warp();
+        // this warp reads no slot counter any more
+        if (lane == 0) {
+            fence_acq_rel_gpu();
+            red_relaxed_add(&ctrl[4], 1u);
+        }
     } else {
-        // ---- stage stream of this warp: (unit k, part p) in order, RING in flight ----
-        int ik = 0, ip = 0, icount = 0;      // next stage to issue
-        if (n_pre > 0) {                     // the first n_pre parts of unit 0 were issued before the wait
-            icount = n_pre;
-            if (n_pre == nparts(u0))
-                ik = 1;
-            else
-                ip = n_pre;
-        }
-        auto issue_ahead = [&](int limit) {
-            while (icount < limit) {
-                const int id = unit_id(ik);
-                if (id >= end_id)
-                    break;
-                const Unit u = decode(id);
-                issue_stage(icount % RING, u, part0(u) + ip);
-                ++icount;
-                if (++ip == nparts(u)) {
-                    ip = 0;
-                    ++ik;
+        // ---- a compute warp ----
+        // its gate/up bands: CTA bands k = par, par + 2, ... (slice q each);
+        // its down bands: CTA down bands j = jw, jw + 16, ... (the parity-1
+        // warps start the dealing when the CTA has an odd number of gate/up
+        // bands, so that they, with one band fewer, take the first ones)
+        const int n_gub = n_gu_cta > par ? (n_gu_cta - par + 1) / 2 : 0;
+        const int jw = (warp - ((n_gu_cta & 1) ? 8 : 0) + 16) & 15;
+        const int n_dnb = n_dn_cta > jw ? (n_dn_cta - jw + 15) / 16 : 0;
+        constexpr int SPG = BW ? 4 : 1;   // stages per gate/up slice
+        constexpr int SPD = BW ? 8 : 2;   // stages per down band
+        const int n_stages = n_gub * SPG + n_dnb * SPD;
+
+        // stage i of this warp into ring slot rs
+        auto issue_stage = [&](int rs, int i) {
+            uint64_t *bar = &sm.full[warp][rs];
+            const uint8_t *src;
+            if (i < n_gub * SPG) {
+                const int k = par + 2 * (i / SPG), sub = i % SPG;
+                const int gb = cta + G * k, slot = gb / W13_BANDS, band = gb % W13_BANDS;
+                if (BW) {
+                    // rows: 8 gate rows 8 band.. and the matching up rows;
+                    // columns 256 q + 64 sub ..; lane 2r + h copies bytes
+                    // [64 h, 64 h + 64) of row r
+                    const int r = lane >> 1, h = lane & 1;
+                    const int row = r < 8 ? 8 * band + r : I + 8 * band + (r - 8);
+                    src = bank13(slot) + ((size_t)row * H + 256 * q + 64 * sub) * 2 + 64 * h;
+                } else {
+                    src = bank13(slot) + (size_t)band * W13_BAND_BYTES + (size_t)q * STG;
                 }
+            } else {
+                const int d = i - n_gub * SPG;
+                const int j = jw + 16 * (d / SPD), sub = d % SPD;
+                int slot, band, hb;
+                dn_band(j, slot, band, hb);
+                if (BW) {
+                    const int r = lane >> 1, h = lane & 1;
+                    src = bank2(slot) + ((size_t)(16 * band + r) * I + 64 * sub) * 2 + 64 * h;
+                } else {
+                    src = bank2(slot) + (size_t)band * W2_BAND_BYTES + (size_t)sub * STG;
+                }
+            }
+            if (BW) {
+                const int r = lane >> 1, h = lane & 1;
+                uint8_t *dst = sm.ring[warp][rs] + r * 128;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    cp_async_cg16(dst + 16 * ((4 * h + u) ^ (4 * (r & 1))), src + 16 * u);
+                cp_async_arrive(bar);
+                return;
+            }
+            if (lane != 0)
+                return;
+            mbar_arrive_expect_tx(bar, STG);
+            bulk_g2s(sm.ring[warp][rs], src, STG, bar);
+        };
+        int ic = 0;                                  // next stage to consume
+        int ii = pre_shared ? 1 : 0;                 // next stage to issue
+        auto issue_ahead = [&]() {
+            while (ii < n_stages && ii < ic + RW) {
+                issue_stage(ii % RW, ii);
+                ++ii;
             }
         };
-        issue_ahead(RING);
+        auto wait_stage = [&]() -> const uint8_t * {
+            const int rs = ic % RW;
+            mbar_wait_bounded(&sm.full[warp][rs], (ic / RW) & 1, flag);
+            return sm.ring[warp][rs];
+        };
+        auto next_stage = [&]() {
+            __syncwarp();
+            ++ic;
+            issue_ahead();
+        };
+        issue_ahead();
+        const int g = lane >> 2, c = lane & 3;
 
-        int ccount = 0;                  // stages consumed
-        uint32_t n_written = 0;          // gate/up units whose h this warp wrote
-        uint32_t n_partials = 0;         // down units whose partial this warp wrote
-        // stores of the warp, then one lane counts them (CTA scope; the sync
-        // warp makes them visible to the other CTAs)
-        auto publish = [&](uint32_t *ctr, uint32_t v) {
+        // ---- gate/up slices ----
+#pragma unroll 1
+        for (int bi = 0; bi < n_gub; ++bi) {
+            const int k = par + 2 * bi;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            if (BW) {
+                bf16_stage_r<0>(wait_stage(), xf, lane, acc);
+                next_stage();
+                bf16_stage_r<1>(wait_stage(), xf, lane, acc);
+                next_stage();
+                bf16_stage_r<2>(wait_stage(), xf, lane, acc);
+                next_stage();
+                bf16_stage_r<3>(wait_stage(), xf, lane, acc);
+                next_stage();
+            } else {
+                mma_stage_r(wait_stage(), xf, lane, acc);
+                next_stage();
+            }
+            // the band's eight K partials meet in buffer k % NB (its previous
+            // use, band k - NB, must have been read by the epilogue warp)
+            const int b = k % NB, u = k / NB;
+            if (u > 0)
+                mbar_wait_bounded(&sm.pempty[b], (uint32_t)(u - 1) & 1u, flag);
+            sm.u.red[b][q][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
             __syncwarp();
             if (lane == 0)
-                st_release_cta(ctr, v);
-        };
-        // The writer of the group's last gate/up unit goes on to a down unit
-        // that waits for h anyway (or to nothing), so it counts its band
-        // itself; the sync warp skips that count.
-        auto count_now_if_last_gu = [&](int k, int slot) {
-            if (k == k_down0 - 1) {
-                __syncwarp();
+                mbar_arrive(&sm.pfull[b]);
+        }
+
+        // ---- down bands ----
+#pragma unroll 1
+        for (int m = 0; m < n_dnb; ++m) {
+            const int j = jw + 16 * m;
+            int slot, band, hb;
+            dn_band(j, slot, band, hb);
+            if (lane == 0)
+                smem_wait_geq(&sm.hready[hb], 1u, flag);
+            __syncwarp();
+            const uint2 *bfrag = reinterpret_cast<const uint2 *>(sm.u.hbuf[hb]);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+            for (int sub = 0; sub < SPD; ++sub) {
+                if (BW)
+                    bf16_stage(wait_stage(), bfrag, 4 * sub, lane, acc);
+                else
+                    mma_stage(wait_stage(), bfrag, 16 * sub, lane, acc);
+                next_stage();
+            }
+            // one band per warp, times the routing weight, the tensor scale and
+            // the token's inverse power of two
+            const float ts = BW ? 1.0f : sm.ts2[slot];
+            float *P = partials + ((size_t)slot * H + 16 * band) * MAXT;
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt) {
+                const int t = 2 * c + tt;
+                if (t < T) {
+                    const float f = sm.wts[slot][t] * ts * pow2i(-sm.hshift[hb][t]);
+                    P[g * MAXT + t] = acc[tt] * f;
+                    P[(g + 8) * MAXT + t] = acc[2 + tt] * f;
+                }
+            }
+            __syncwarp();
+            if (slot < U - 1) {
                 if (lane == 0) {
-                    fence_acq_rel_gpu();
-                    red_relaxed_add(&slot_cnt[slot], 1u);
+                    __threadfence_block();
+                    atomicOr(&sm.dn_mask[j >> 5], 1u << (j & 31));
+                }
+                continue;
+            }
+            // the last slot's partial: add every slot's partial of the band
+            // in slot order once the other U - 1 are counted
+            const int r = lane >> 1, th = lane & 1;      // row r, tokens 4 th .. 4 th + 3
+            const float4 *srcp = reinterpret_cast<const float4 *>(partials + ((size_t)16 * band + r) * MAXT) + th;
+            if (lane == 0)
+                gmem_wait_geq(&band_cnt[band], (uint32_t)(U - 1), flag);
+            __syncwarp();
+            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            constexpr int BATCH = 16;
+            for (int s0 = 0; s0 < U; s0 += BATCH) {
+                float4 v[BATCH];
+#pragma unroll
+                for (int jj = 0; jj < BATCH; ++jj)
+                    v[jj] = (s0 + jj < U) ? __ldcg(srcp + (size_t)(s0 + jj) * H * MAXT / 4)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int jj = 0; jj < BATCH; ++jj) {
+                    s4.x += v[jj].x; s4.y += v[jj].y; s4.z += v[jj].z; s4.w += v[jj].w;
                 }
             }
-        };
-        float acc[4];
-        for (int k = 0;; ++k) {
-            const int id = unit_id(k);
-            if (id >= end_id)
-                break;
-            const Unit u = decode(id);
-
-            const uint2 *bfrag = sm.xfrag;
-            int b = 0;
-            if (u.down) {
-                const int dk = k - k_down0;
-                b = dk & 1;
-                // The sync warp copies h once the slot's gate/up bands are
-                // counted.  If it has not yet, the leader waits on the slot
-                // counter itself and claims the copy (whoever moves the claim
-                // counter from dk to dk + 1 issues it).
-                if (lead_thread && *reinterpret_cast<volatile uint32_t *>(&sm.hclaim[grp]) <= (uint32_t)dk) {
-                    for (uint32_t it = 0; ld_acquire(&slot_cnt[u.slot]) < SLOT_DONE; ++it) {
-                        if (it == SPIN_LIMIT) {
-                            atomicOr(flag, FLAG_TIMEOUT);
-                            break;
-                        }
-                        __nanosleep(32);
-                    }
-                    __threadfence_block();   // the counter read precedes the claim the sync warp sees
-                    if (atomicCAS(&sm.hclaim[grp], (uint32_t)dk, (uint32_t)dk + 1u) == (uint32_t)dk)
-                        issue_h(grp, u.slot, b);
-                }
-                mbar_wait_bounded(&sm.hbar[grp][b], (dk >> 1) & 1, flag);
-                // rescale h (padded bf16 rows) in place into fragments [step][32]
-                // (zeros in lanes 4T..): lane l < 4T of warp wq holds steps wq,
-                // wq + 4, ... of token l / 4; NVFP4 scales each token's row by the
-                // power of two of its max |h|, taken over the 16 threads that
-                // hold the row.
-                const uint32_t *hw = reinterpret_cast<const uint32_t *>(sm.hbuf[grp][b]);
-                const bool hl = lane < blanes;
-                const int hg = lane >> 2, hc = lane & 3;
-                constexpr int HJ = (I / 16) / GW;              // steps per warp
-                uint32_t src0[HJ], src1[HJ];
-                __nv_bfloat162 m2 = __floats2bfloat162_rn(0.f, 0.f);
+            const float vals[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-                for (int j = 0; j < HJ; ++j) {
-                    const int step = wq + GW * j;
-                    src0[j] = src1[j] = 0u;
-                    if (hl) {
-                        if (BW) {
-                            const int w0 = (hg * HROW) / 4 + bf16_bcol(step, hc) / 2;
-                            src0[j] = hw[w0];
-                            src1[j] = hw[w0 + 1];
-                        } else {
-                            const int w0 = (hg * HROW) / 4 + 8 * step + hc;
-                            src0[j] = hw[w0];
-                            src1[j] = hw[w0 + 4];
-                        }
-                    }
-                    if (!BW) {
-                        m2 = __hmax2(m2, __habs2(u32_as_bf162(src0[j])));
-                        m2 = __hmax2(m2, __habs2(u32_as_bf162(src1[j])));
-                    }
-                }
-                if (!BW)
-                    sm.hmx[grp][wq][lane] = fmaxf(__low2float(m2), __high2float(m2));
-                named_barrier_sync(1 + grp, GW * 32);
-                int sh = 0;
-                if (!BW) {
-                    float mx = 0.f;
-#pragma unroll
-                    for (int w = 0; w < GW; ++w) {
-                        const float4 v = reinterpret_cast<const float4 *>(sm.hmx[grp][w])[hg];
-                        mx = fmaxf(mx, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-                    }
-                    sh = act_shift(mx);
-                }
-                const float p = pow2i(sh);
-                if (wq == 0 && hc == 0 && hl)
-                    sm.hshift[grp][b][hg] = sh;
-                uint2 *hf = reinterpret_cast<uint2 *>(sm.hbuf[grp][b]);
-#pragma unroll
-                for (int j = 0; j < HJ; ++j) {
-                    // all 32 lanes: lanes 4T.. hold zeros (their src words are 0)
-                    const int e = (wq + GW * j) * 32 + lane;
-                    hf[e] = BW ? make_uint2(src0[j], src1[j])
-                               : make_uint2(bf16x2_to_f16x2_scaled(src0[j], p), bf16x2_to_f16x2_scaled(src1[j], p));
-                }
-                named_barrier_sync(1 + grp, GW * 32);
-                bfrag = hf;
+            for (int jj = 0; jj < 4; ++jj) {
+                const int t = 4 * th + jj;
+                if (t < T)
+                    a.out[(size_t)t * H + 16 * band + r] = __float2bfloat16_rn(vals[jj]);
             }
-
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-            {
-                const int np = nparts(u);
-                for (int p = 0; p < np; ++p) {
-                    const int rs = ccount % RING;
-                    mbar_wait_bounded(&sm.full[warp][rs], (ccount / RING) & 1, flag);
-                    if (BW)
-                        bf16_stage(sm.ring[warp][rs], bfrag, 4 * (part0(u) + p), lane, acc);
-                    else
-                        mma_stage(sm.ring[warp][rs], bfrag, 16 * (part0(u) + p), lane, acc);
-                    __syncwarp();
-                    ++ccount;
-                    issue_ahead(ccount + RING);
-                }
-            }
-
-            const int g = lane >> 2, c = lane & 3;
-            bool gu_writer = !u.down;
-            if (!u.down) {
-                // The four K quarters of the band are added in warp order by the
-                // unit's writer, warp k % 4; the other three hand over their
-                // partials through kred[k & 1] and go on.  A partial buffer is
-                // refilled only after its previous writer has read it.
-                const int wr = k & (GW - 1), par = k & 1;
-                gu_writer = (wq == wr);
-                // Every warp, the writer too, first waits until unit k - 2's
-                // writer has read kred[par]: then all of unit k - 2's handovers
-                // have landed, so neither barrier can be a phase behind when a
-                // parity wait below looks at it (a parity wait cannot tell phase
-                // j from phase j - 2).
-                if (k >= 2)
-                    mbar_wait_bounded(&sm.kempty[grp][par], ((k >> 1) - 1) & 1, flag);
-                if (!gu_writer) {
-                    sm.kred[grp][par][(wq - wr + GW - 1) & (GW - 1)][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&sm.kfull[grp][par]);
-                } else {
-                    mbar_wait_bounded(&sm.kfull[grp][par], (k >> 1) & 1, flag);
-                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int q = 0; q < GW; ++q) {
-                        const float4 v = (q == wr) ? make_float4(acc[0], acc[1], acc[2], acc[3])
-                                                   : sm.kred[grp][par][(q - wr + GW - 1) & (GW - 1)][lane];
-                        if (q == 0) {
-                            sum = v;
-                        } else {
-                            sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&sm.kempty[grp][par]);
-                    acc[0] = sum.x; acc[1] = sum.y; acc[2] = sum.z; acc[3] = sum.w;
-                }
-            }
-            if (gu_writer && BW) {
-#pragma unroll
-                for (int tt = 0; tt < 2; ++tt) {
-                    const int t = 2 * c + tt;
-                    if (t < T) {
-                        const float gv = acc[tt], uv = acc[2 + tt];
-                        hglob[((size_t)u.slot * MAXT + t) * H_PITCH + u.band * 8 + g] =
-                            __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
-                    }
-                }
-                count_now_if_last_gu(k, u.slot);
-                publish(&sm.gu_done[grp][wq], ++n_written);
-            } else if (gu_writer) {
-                // SiLU*up for h rows 8 * band + g
-                const float ts = (u.slot < a.n_shared) ? __ldg(a.s_ts13 + u.slot)
-                                                       : __ldg(a.r_ts13 + sm.slot_expert[u.slot]);
-#pragma unroll
-                for (int tt = 0; tt < 2; ++tt) {
-                    const int t = 2 * c + tt;
-                    if (t < T) {
-                        const float f = ts * pow2i(-sm.xshift[t]);
-                        const float gv = acc[tt] * f, uv = acc[2 + tt] * f;
-                        hglob[((size_t)u.slot * MAXT + t) * H_PITCH + u.band * 8 + g] =
-                            __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
-                    }
-                }
-                count_now_if_last_gu(k, u.slot);
-                publish(&sm.gu_done[grp][wq], ++n_written);
-            } else if (u.down) {
-                // down: one band per warp, x routing weight x tensor scale x 2^-shift
-                const float ts = BW ? 1.0f
-                                    : (u.slot < a.n_shared) ? __ldg(a.s_ts2 + u.slot)
-                                                            : __ldg(a.r_ts2 + sm.slot_expert[u.slot]);
-                float *P = partials + ((size_t)u.slot * H + 16 * u.band) * MAXT;
-#pragma unroll
-                for (int tt = 0; tt < 2; ++tt) {
-                    const int t = 2 * c + tt;
-                    if (t < T) {
-                        const float f = sm.wts[u.slot][t] * ts * pow2i(-sm.hshift[grp][b][t]);
-                        P[g * MAXT + t] = acc[tt] * f;
-                        P[(g + 8) * MAXT + t] = acc[2 + tt] * f;
-                    }
-                }
-                if (unit_id(k + 1) >= end_id && u.slot < n_slots - 1) {
-                    // the group's last unit: nothing else to do, so count it here
-                    __syncwarp();
-                    if (lane == 0) {
-                        fence_acq_rel_gpu();
-                        red_relaxed_add(&band_cnt[u.band], 1u);
-                    }
-                }
-                publish(&sm.dn_done[grp][wq], ++n_partials);
-                if (u.slot == n_slots - 1)
-                    combine_band(u.band);
-                // the group's hbuf[b] is free once all four warps are done with it
-                fence_proxy_async();   // the fragments were written in place; a bulk copy refills the buffer
-                named_barrier_sync(1 + grp, GW * 32);
-                if (lead_thread)
-                    st_release_cta(&sm.hrel[grp], (uint32_t)(k - k_down0 + 1));
-            }
+            if (lane == 0)
+                band_cnt[band] = 0u;   // every other partial of the band has been counted
         }
     }
 
-    // ---- CTA 0 re-arms the counters for the next call once every CTA has
-    // stopped reading them (each sync warp counts itself in ctrl[4] after its
-    // last h copy, long after its logits were read; the band counters are
+    // ---- CTA 0 re-arms the slot counters for the next call once every CTA
+    // has stopped reading and adding to them (the count warp and the h warp
+    // of each CTA count themselves out in ctrl[4]; the band counters are
     // re-armed by the warps that add the bands up) ----
     __syncthreads();
     if (blockIdx.x == 0 && threadIdx.x == 0) {
-        for (uint32_t it = 0; ld_acquire(&ctrl[4]) < gridDim.x; ++it) {
-            if (it == SPIN_LIMIT) {
-                atomicOr(flag, FLAG_TIMEOUT);
-                return;
-            }
-            __nanosleep(64);
-        }
+        if (!gmem_wait_geq(&ctrl[4], OUT_PER_CTA * gridDim.x, flag))
+            return;
         for (int s = 0; s < MAX_SLOTS; ++s)
             slot_cnt[s] = 0u;
         ctrl[4] = 0u;

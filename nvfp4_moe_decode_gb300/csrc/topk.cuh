@@ -35,12 +35,22 @@ __device__ __forceinline__ float key_logit(unsigned long long key)
     return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
 }
 
+// Descending compare-exchange of two keys.
+__device__ __forceinline__ void cx_desc(unsigned long long &a, unsigned long long &b)
+{
+    const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
+    a = hi;
+    b = lo;
+}
+
 // Top-k of one token's E = 256 fp32 logits by one warp: lane l holds the
 // logits of experts l + 32 m (m = 0..7).  Returns in lanes 0..TOPK-1 the
 // selected expert (best first) and its renormalised sigmoid weight, and
-// reports whether a logit was not finite.  Every round two warp-wide max
-// reductions (redux.sync, on the high then the low 32 bits of the keys) find
-// the best remaining key, which is unique, and its owner drops it.
+// reports whether a logit was not finite.  Each lane first sorts its eight
+// keys (a 19-comparator odd-even merge network); then every round two
+// warp-wide max reductions (redux.sync, on the high then the low 32 bits of
+// the lanes' best remaining keys) find the best remaining key, which is
+// unique, and its owner drops it from the head of its list.
 __device__ __forceinline__ void warp_route_values(const float v[8], int lane, int &ex, float &wt, bool &nonfinite)
 {
     unsigned long long k[8];
@@ -51,21 +61,24 @@ __device__ __forceinline__ void warp_route_values(const float v[8], int lane, in
         k[m] = rank_key(v[m], lane + 32 * m);
     }
     nonfinite = __any_sync(0xFFFFFFFFu, bad);
+    cx_desc(k[0], k[2]); cx_desc(k[1], k[3]); cx_desc(k[4], k[6]); cx_desc(k[5], k[7]);
+    cx_desc(k[0], k[4]); cx_desc(k[1], k[5]); cx_desc(k[2], k[6]); cx_desc(k[3], k[7]);
+    cx_desc(k[0], k[1]); cx_desc(k[2], k[3]); cx_desc(k[4], k[5]); cx_desc(k[6], k[7]);
+    cx_desc(k[2], k[4]); cx_desc(k[3], k[5]);
+    cx_desc(k[1], k[4]); cx_desc(k[3], k[6]);
+    cx_desc(k[1], k[2]); cx_desc(k[3], k[4]); cx_desc(k[5], k[6]);
     unsigned long long chosen = 0ull;   // lane i < TOPK: the i-th best key
-#pragma unroll 1
-    for (int i = 0; i < TOPK; ++i) {
-        unsigned long long mine = k[0];
 #pragma unroll
-        for (int m = 1; m < 8; ++m)
-            mine = k[m] > mine ? k[m] : mine;
+    for (int i = 0; i < TOPK; ++i) {
+        const unsigned long long mine = k[0];
         const uint32_t hi = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(mine >> 32));
         const uint32_t lo = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(mine >> 32) == hi ? (uint32_t)mine : 0u);
         const unsigned long long best = ((unsigned long long)hi << 32) | lo;
         if (mine == best) {
 #pragma unroll
-            for (int m = 0; m < 8; ++m)
-                if (k[m] == best)
-                    k[m] = 0ull;
+            for (int m = 0; m < 7; ++m)
+                k[m] = k[m + 1];
+            k[7] = 0ull;
         }
         if (lane == i)
             chosen = best;
