@@ -365,7 +365,7 @@ moe_status moe_stack_forward(void *x, const moe_layer_weights *layers, int n_lay
 
 /* Bytes of the library's fixed per-device scratch: the workspace of
  * moe_layer_forward at T = MOE_MAX_DECODE_T. */
-#define MOE_STATIC_SCRATCH_BYTES 3646976u
+#define MOE_STATIC_SCRATCH_BYTES 7252480u
 
 /*
  * moe_layer_forward with the workspace replaced by a fixed device array of

@@ -50,7 +50,7 @@ EXPORTS = (
     "moe_layer_forward_prenorm", "moe_stack_workspace_bytes", "moe_stack_forward",
 )
 
-MOE_STATIC_SCRATCH_BYTES = 3_646_976
+MOE_STATIC_SCRATCH_BYTES = 7_252_480
 
 
 class MoeError(RuntimeError):

@@ -62,7 +62,6 @@ constexpr size_t W2_BYTES = W2_BANDS * W2_BAND_BYTES;       // 589824
 constexpr size_t W13_BYTES_BF = (size_t)2 * I * H * 2;     // 4194304: bf16 W13 of one expert
 constexpr size_t W2_BYTES_BF = (size_t)H * I * 2;          // 2097152: bf16 W2 of one expert
 
-constexpr int H_PITCH = I + 8;          // bf16 elements per h row in the workspace (16 B of padding)
 constexpr int SC_BYTES = 1152;            // one 128-column super-chunk of a band
 constexpr int ACT_EXP = 14;               // activations scaled so max|v| is in [2^14, 2^15)
 
@@ -80,16 +79,16 @@ constexpr uint32_t SPIN_LIMIT = 1u << 20;
 // ---------------------------------------------------------------------------
 struct WsLayout {
     size_t ctrl;       // u32[64]: [0] device flag, [1] routing-kernel arrivals,
-                       //   [4] layer-kernel CTAs counted out, [5] layer-kernel launches
-    size_t slot_cnt;   // u32[MAX_SLOTS] gate/up bands finished per slot
-    size_t band_cnt;   // u32[W2_BANDS] down partials arrived per 16-row band
+                       //   [4] layer-kernel CTAs that have read the launch tag, [5] layer-kernel launches
     size_t logits;     // f32[MAXT][E]
     size_t tlogits;    // u64[MAXT][E]: layer kernel, (launch tag << 32) | fp32 logit bits
     size_t topk_idx;   // i32[MAXT][TOPK]
     size_t topk_w;     // f32[MAXT][TOPK]
     size_t slots;      // SlotTable
-    size_t h;          // bf16[MAX_SLOTS][MAXT][I]   SiLU*up activations
-    size_t partials;   // f32[MAX_SLOTS][H][MAXT]    per-slot down outputs (weighted)
+    size_t htag;       // u64[MAX_SLOTS][W13_BANDS][MAXT][4]: (launch tag << 32) | the bf16 SiLU*up
+                       //   values of h rows 8 b + 2 w (low half) and 8 b + 2 w + 1 of token t
+    size_t ptag;       // u64[MAX_SLOTS][W2_BANDS][16][MAXT]: (launch tag << 32) | fp32 weighted
+                       //   down output of row 16 b + r, token t
     size_t total;
 };
 
@@ -107,15 +106,13 @@ __host__ __device__ inline WsLayout ws_layout()
     WsLayout L;
     size_t o = 0;
     L.ctrl = o;      o = align256(o + 64 * 4);
-    L.slot_cnt = o;  o = align256(o + MAX_SLOTS * 4);
-    L.band_cnt = o;  o = align256(o + W2_BANDS * 4);
     L.logits = o;    o = align256(o + (size_t)MAXT * E * 4);
     L.tlogits = o;   o = align256(o + (size_t)MAXT * E * 8);
     L.topk_idx = o;  o = align256(o + (size_t)MAXT * TOPK * 4);
     L.topk_w = o;    o = align256(o + (size_t)MAXT * TOPK * 4);
     L.slots = o;     o = align256(o + sizeof(SlotTable));
-    L.h = o;         o = align256(o + (size_t)MAX_SLOTS * MAXT * H_PITCH * 2);
-    L.partials = o;  o = align256(o + (size_t)MAX_SLOTS * H * MAXT * 4);
+    L.htag = o;      o = align256(o + (size_t)MAX_SLOTS * W13_BANDS * MAXT * 4 * 8);
+    L.ptag = o;      o = align256(o + (size_t)MAX_SLOTS * W2_BANDS * 16 * MAXT * 8);
     L.total = o;
     return L;
 }

@@ -63,10 +63,8 @@ namespace {
 constexpr int FW = 16;                 // compute warps per CTA
 constexpr int FT = FW * 32;            // compute threads
 constexpr int EP_WARP = FW;            // warps 16, 17: gate/up epilogues (band parity 0, 1)
-constexpr int CNT_WARP = FW + 2;       // warp 18: cross-CTA counts
-constexpr int HW_WARP = FW + 3;        // warp 19: h fragments of the CTA's down slots
-constexpr int NT = FT + 128;           // threads per CTA
-constexpr uint32_t OUT_PER_CTA = 2;    // warps of a CTA that count themselves out of the slot counters
+constexpr int HW_WARP = FW + 2;        // warp 18: h fragments of the CTA's down slots
+constexpr int NT = FT + 96;            // threads per CTA
 constexpr int RW = 4;                  // ring stages per compute warp
 constexpr int STG = 2 * SC_BYTES;      // 2304 bytes: two NVFP4 super-chunks (a BF16 stage uses 2048)
 constexpr int GQ = 8;                  // 256-column slices of a gate/up band
@@ -74,9 +72,8 @@ constexpr int NB = 8;                  // gate/up reduction buffers (band k uses
 constexpr int XPITCH = H * 2 + 16;     // bytes per staged x row: rows 4 banks apart, so the fragment reads do not conflict
 constexpr int NHB = 3;                 // h buffers: the two range slots and the last slot
 constexpr int ROUTER_CTAS = E / 2;     // 128 CTAs x 2 experts
-constexpr int HROW = H_PITCH * 2;      // padded bytes of one token's h row (shared memory and workspace)
-constexpr int HBUF = MAXT * HROW;      // one slot's h, 8,320 bytes at T = 8
-constexpr uint32_t SLOT_DONE = W13_BANDS;
+constexpr int HS = I / 16;             // 32 k16 steps of the down GEMV
+constexpr int HBUF = HS * 32 * 8;      // one slot's h as B fragments [step][lane] (uint2), 8 KB
 // With at least 128 CTAs a CTA has at most ceil(64 * 49 / 128) = 25 gate/up
 // bands (bits of a 32-bit mask) and ceil(128 * 48 / 128) = 48 range down
 // bands (bits of a 64-bit mask), and its down range touches at most two slots.
@@ -87,11 +84,10 @@ struct FSmem {
         RouterRed rred;                // phase 2: the router's partial sums
         struct {
             float4 red[NB][GQ][32];    // gate/up K partials, [buffer][slice][lane]
-            uint8_t hbuf[NHB][HBUF];   // h rows of a down slot, turned into f16 fragments in place
+            uint8_t hbuf[NHB][HBUF];   // h of a down slot as B fragments (f16 scaled, or bf16)
         } u;
     };
     uint64_t full[FW][RW];
-    uint64_t hbar[NHB];
     uint64_t xbar;
     int32_t sel[MAXT][TOPK];
     float selw[MAXT][TOPK];
@@ -111,8 +107,7 @@ struct FSmem {
     uint64_t pfull[NB];                // a band's eight K partials are in buffer b
     uint64_t pempty[NB];               // the epilogue warp has read buffer b
     uint32_t hready[NHB];              // 1 once the h warp has filled the buffer
-    uint32_t gu_mask;                  // CTA gate/up bands whose h is stored (bit k)
-    uint32_t dn_mask[2];               // CTA range down bands whose partial is stored (bit j)
+    float4 comb[FW][32];               // the final sum of band cta: per-warp sums of every 16th slot
 };
 
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }
@@ -123,7 +118,6 @@ __device__ __forceinline__ int act_shift(float maxabs)
     return sh < -100 ? -100 : (sh > 100 ? 100 : sh);
 }
 
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acquire.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p)
@@ -139,6 +133,13 @@ __device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned l
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const void *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p)
 {
     unsigned long long v;
@@ -146,10 +147,11 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     return v;
 }
 
-__device__ __forceinline__ void red_relaxed_add(uint32_t *p, uint32_t v)
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v)
 {
-    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+
 
 // CTA-scope release store / acquire load (shared-memory progress counters)
 __device__ __forceinline__ void st_release_cta(uint32_t *p, uint32_t v)
@@ -163,7 +165,6 @@ __device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t *p)
     asm volatile("ld.acquire.cta.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 __device__ __forceinline__ void ffma2(float &a0, float &a1, float s, float d0, float d1)
 {
@@ -365,11 +366,9 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
     const WsLayout L = ws_layout();
     uint32_t *ctrl = reinterpret_cast<uint32_t *>(a.ws + L.ctrl);
     uint32_t *flag = ctrl;
-    uint32_t *slot_cnt = reinterpret_cast<uint32_t *>(a.ws + L.slot_cnt);
-    uint32_t *band_cnt = reinterpret_cast<uint32_t *>(a.ws + L.band_cnt);
     unsigned long long *tlogits = reinterpret_cast<unsigned long long *>(a.ws + L.tlogits);
-    __nv_bfloat16 *hglob = reinterpret_cast<__nv_bfloat16 *>(a.ws + L.h);
-    float *partials = reinterpret_cast<float *>(a.ws + L.partials);
+    unsigned long long *htag = reinterpret_cast<unsigned long long *>(a.ws + L.htag);
+    unsigned long long *ptag = reinterpret_cast<unsigned long long *>(a.ws + L.ptag);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & (GQ - 1), par = warp >> 3;   // compute warps: K slice and band parity
@@ -385,19 +384,12 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         mbar_init(&sm.pfull[threadIdx.x], GQ);   // the band's eight K partials are in
         mbar_init(&sm.pempty[threadIdx.x], 1);   // the epilogue warp has read them
     }
-    if (threadIdx.x == 0) {
-        for (int r = 0; r < NHB; ++r)
-            mbar_init(&sm.hbar[r], 1);
+    if (threadIdx.x == 0)
         mbar_init(&sm.xbar, 1);
-    }
     if (lane == 0 && warp <= FW)
         fence_barrier_init();
     if (threadIdx.x < NHB)
         sm.hready[threadIdx.x] = 0u;
-    if (threadIdx.x == 0) {
-        sm.gu_mask = 0u;
-        sm.dn_mask[0] = sm.dn_mask[1] = 0u;
-    }
     __syncthreads();
 
     auto bank13 = [&](int slot) -> const uint8_t * {
@@ -749,8 +741,10 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         // Epilogue warp p takes the CTA's gate/up bands k = p, p + 2, ... in
         // order: once buffer k % NB holds band k's eight K partials it adds
         // them in slice order, frees the buffer, applies SiLU*up (NVFP4:
-        // times the tensor scale and the token's inverse power of two),
-        // stores h and sets bit k of gu_mask for the count warp.
+        // times the tensor scale and the token's inverse power of two) and
+        // stores h with the launch tag in every 64-bit word (two bf16 values
+        // of one token per word), so a reader that sees the tag sees the
+        // values: no fence, no counter.
         const int p = warp - EP_WARP;
         const int g = lane >> 2, c = lane & 3;
 #pragma unroll 1
@@ -773,82 +767,33 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt) {
                 const int t = 2 * c + tt;
+                // h row 8 band + g of token t (bf16 bits); the lane of row g + 1
+                // hands its value down, and the even rows store the pair
+                uint32_t hb = 0u;
                 if (t < T) {
                     const float f = BW ? 1.0f : sm.ts13[slot] * sm.xinv[t];
                     const float gv = sv[tt] * f, uv = sv[2 + tt] * f;
-                    hglob[((size_t)slot * MAXT + t) * H_PITCH + band * 8 + g] =
-                        __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
+                    hb = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv));
                 }
-            }
-            __syncwarp();
-            if (lane == 0) {
-                __threadfence_block();
-                atomicOr(&sm.gu_mask, 1u << k);
+                const uint32_t ob = __shfl_down_sync(0xFFFFFFFFu, hb, 4);
+                if (t < T && (g & 1) == 0)
+                    st_relaxed_u64(&htag[(((size_t)slot * W13_BANDS + band) * MAXT + t) * 4 + (g >> 1)],
+                                   ((unsigned long long)ltag << 32) | (ob << 16) | hb);
             }
         }
-    } else if (warp == CNT_WARP) {
-        // ---- the count warp: every cross-CTA count of this CTA's work ----
-        // The epilogue warps set a bit of gu_mask when the h of a CTA gate/up
-        // band is stored, the compute warps one of dn_mask when the partial
-        // of a range down band is; each pass adds the newly set ones to the
-        // slot and band counters behind one gpu-scope fence (a fence costs
-        // the issuing warp about a microsecond while the SM streams, so no
-        // other warp executes one).  Lane 0 does the work.
-        if (lane == 0) {
-            const uint32_t gall = n_gu_cta >= 32 ? 0xFFFFFFFFu : ((1u << n_gu_cta) - 1u);
-            const unsigned long long dall = n_rng >= 64 ? ~0ull : ((1ull << n_rng) - 1ull);
-            uint32_t gdone = 0u;
-            unsigned long long ddone = 0ull;
-            bool out = false;
-            for (uint32_t it = 0; it < 4 * SPIN_LIMIT; ++it) {
-                // plain polls: the gpu-scope fence below orders what they saw
-                const uint32_t gm = *reinterpret_cast<volatile uint32_t *>(&sm.gu_mask) & gall;
-                const unsigned long long dm =
-                    ((unsigned long long)*reinterpret_cast<volatile uint32_t *>(&sm.dn_mask[1]) << 32 |
-                     *reinterpret_cast<volatile uint32_t *>(&sm.dn_mask[0])) & dall;
-                uint32_t ng = gm & ~gdone;
-                unsigned long long nd = dm & ~ddone;
-                if (ng | nd) {
-                    fence_acq_rel_gpu();   // the stores counted below become visible before their counts
-                    while (ng) {
-                        const int k = __ffs(ng) - 1;
-                        red_relaxed_add(&slot_cnt[(cta + G * k) / W13_BANDS], 1u);
-                        ng &= ng - 1;
-                    }
-                    while (nd) {
-                        const int j = __ffsll(nd) - 1;
-                        red_relaxed_add(&band_cnt[(d0 + j) % W2_BANDS], 1u);
-                        nd &= nd - 1;
-                    }
-                    gdone |= gm;
-                    ddone |= dm;
-                }
-                if (!out && gdone == gall) {
-                    // no more slot-counter adds from this warp
-                    fence_acq_rel_gpu();
-                    red_relaxed_add(&ctrl[4], 1u);
-                    out = true;
-                }
-                if (out && ddone == dall)
-                    break;
-                if (it + 1 == 4 * SPIN_LIMIT)
-                    atomicOr(flag, FLAG_TIMEOUT);
-                if (!(ng | nd))
-                    __nanosleep(32);
-            }
-            if (!out) {
-                fence_acq_rel_gpu();
-                red_relaxed_add(&ctrl[4], 1u);
-            }
-        }
-        __syncwarp();
     } else if (warp == HW_WARP) {
-        // ---- the h warp: h of the CTA's down slots as f16 fragments ----
-        // For each slot (range slots in order, then the last slot): wait until
-        // its 64 gate/up bands are counted, copy its T padded h rows, scale
-        // each token's row by the power of two of its max |h| (NVFP4) and
-        // rewrite the buffer in place as the B fragments of the down GEMV,
-        // [k16 step][lane] (zeros in lanes 4T..).
+        // ---- the h warp: h of the CTA's down slots as B fragments ----
+        // First it counts this CTA in ctrl[4] (every thread of the CTA has
+        // read the launch tag by now; CTA 0 advances the tag once all CTAs
+        // are counted).  Then for each slot (range slots in order, then the
+        // last slot) lane (g, c) polls the 64 tagged words it needs, k16 step
+        // s taking rows 16 s + 2 c, +1 (band 2 s) and 16 s + 8 + 2 c, +1 (band
+        // 2 s + 1) of token g, until every one carries this launch's tag;
+        // NVFP4 then scales each token by the power of two of its max |h|
+        // (over its four lanes) into f16.  The fragments go to the slot's
+        // buffer, [k16 step][lane], zeros in lanes 4T..
+        if (lane == 0)
+            red_release_add(&ctrl[4], 1u);
         int hslot[NHB];
         bool hneed[NHB];
         hslot[0] = s_first;
@@ -863,64 +808,128 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         for (int r = 0; r < NHB; ++r) {
             if (!hneed[r])
                 continue;
-            if (lane == 0) {
-                gmem_wait_geq(&slot_cnt[hslot[r]], SLOT_DONE, flag);
-                fence_proxy_async_global();   // h was published to the generic proxy
-                const uint32_t bytes = (uint32_t)((T - 1) * HROW + I * 2);
-                mbar_arrive_expect_tx(&sm.hbar[r], bytes);
-                bulk_g2s(sm.u.hbuf[r], hglob + (size_t)hslot[r] * MAXT * H_PITCH, bytes, &sm.hbar[r]);
+            const unsigned long long *src = htag + ((size_t)hslot[r] * W13_BANDS * MAXT + hg) * 4 + hc;
+            // word j of the lane: band j, so k16 step j / 2, src0 (j even) or src1
+            auto word = [&](int j) -> unsigned long long { return ld_relaxed_u64(src + (size_t)j * MAXT * 4); };
+            // (1) wait until every word carries this launch's tag: the tag
+            // halves of all pending words at once (the 64-bit reads below
+            // check every tag again, and start over on a mismatch)
+            unsigned long long pend = hl ? ~0ull : 0ull;
+            uint32_t retries = 0;
+        again:
+            if (++retries > 64u) {   // tags seen but values not: give up (never expected)
+                if (lane == 0)
+                    atomicOr(flag, FLAG_TIMEOUT);
+                pend = 0ull;
             }
-            __syncwarp();
-            mbar_wait_bounded(&sm.hbar[r], 0, flag);
-            const uint32_t *hw = reinterpret_cast<const uint32_t *>(sm.u.hbuf[r]);
-            constexpr int HS = I / 16;   // 32 k16 steps
-            uint32_t src0[HS], src1[HS];
+            for (uint32_t it = 0;; ++it) {
+                uint32_t tg[2 * HS];
+#pragma unroll
+                for (int j = 0; j < 2 * HS; ++j)
+                    tg[j] = (pend >> j) & 1ull ? ld_relaxed_u32(reinterpret_cast<const uint32_t *>(src + (size_t)j * MAXT * 4) + 1)
+                                               : ltag;
+#pragma unroll
+                for (int j = 0; j < 2 * HS; ++j)
+                    if (tg[j] == ltag)
+                        pend &= ~(1ull << j);
+                if (__all_sync(0xFFFFFFFFu, pend == 0ull))
+                    break;
+                if (it == SPIN_LIMIT) {
+                    if (lane == 0)
+                        atomicOr(flag, FLAG_TIMEOUT);
+                    break;
+                }
+                __nanosleep(128);
+            }
+            // (2) the raw words, half of the steps at a time (one round trip
+            // each), tags checked again, into the slot's buffer as raw bf16
+            // pairs [k16 step][lane]; NVFP4 also takes each lane's max |h|
+            uint2 *hf = reinterpret_cast<uint2 *>(sm.u.hbuf[r]);
+            constexpr int HH = HS / 2;
+            bool stale = false;
             __nv_bfloat162 m2 = __floats2bfloat162_rn(0.f, 0.f);
 #pragma unroll
-            for (int s = 0; s < HS; ++s) {
-                src0[s] = src1[s] = 0u;
-                if (hl) {
-                    if (BW) {
-                        const int w0 = (hg * HROW) / 4 + bf16_bcol(s, hc) / 2;
-                        src0[s] = hw[w0];
-                        src1[s] = hw[w0 + 1];
-                    } else {
-                        const int w0 = (hg * HROW) / 4 + 8 * s + hc;
-                        src0[s] = hw[w0];
-                        src1[s] = hw[w0 + 4];
-                        m2 = __hmax2(m2, __habs2(u32_as_bf162(src0[s])));
-                        m2 = __hmax2(m2, __habs2(u32_as_bf162(src1[s])));
+            for (int half = 0; half < 2; ++half) {
+                unsigned long long w0[HH], w1[HH];
+#pragma unroll
+                for (int st = 0; st < HH; ++st) {
+                    w0[st] = hl ? word(2 * (HH * half + st)) : ((unsigned long long)ltag << 32);
+                    w1[st] = hl ? word(2 * (HH * half + st) + 1) : ((unsigned long long)ltag << 32);
+                }
+#pragma unroll
+                for (int st = 0; st < HH; ++st) {
+                    stale = stale || (uint32_t)(w0[st] >> 32) != ltag || (uint32_t)(w1[st] >> 32) != ltag;
+                    const uint32_t v0 = hl ? (uint32_t)w0[st] : 0u, v1 = hl ? (uint32_t)w1[st] : 0u;
+                    if (!BW) {
+                        m2 = __hmax2(m2, __habs2(u32_as_bf162(v0)));
+                        m2 = __hmax2(m2, __habs2(u32_as_bf162(v1)));
                     }
+                    hf[(HH * half + st) * 32 + lane] = make_uint2(v0, v1);
                 }
             }
+            if (__any_sync(0xFFFFFFFFu, stale)) {
+                pend = hl ? ~0ull : 0ull;
+                goto again;
+            }
+            __syncwarp();
+            // (3) in place: NVFP4 scales each token by the power of two of its
+            // max |h| (over its four lanes) into f16; BF16 permutes the pairs
+            // into the column order of bf16_bcol
             int sh = 0;
             if (!BW) {
-                // the token's max over its four lanes (all 512 values)
                 float mx = fmaxf(__low2float(m2), __high2float(m2));
                 mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
                 sh = act_shift(mx);
+                const float pw = pow2i(sh);
+#pragma unroll
+                for (int st = 0; st < HS; ++st) {
+                    const uint2 v = hf[st * 32 + lane];
+                    hf[st * 32 + lane] = make_uint2(bf16x2_to_f16x2_scaled(v.x, pw), bf16x2_to_f16x2_scaled(v.y, pw));
+                }
+            } else {
+                // Lane (g, c) holds columns 16 s + 2 c, +1 (.x of step s) and
+                // 16 s + 8 + 2 c, +1 (.y).  Step st needs the pairs starting at
+                // column bf16_bcol(st, c) and 2 after it: for every c they come
+                // from lanes (g, 2 (st & 1)) and (g, 2 (st & 1) + 1), from .x
+                // (c even) or .y (c odd) of step b16 (c < 2) or b16 + 1 (c >= 2);
+                // a step's pairs stay within its half (b16 + 1 < 16 (half + 1)).
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t src0[HH], src1[HH];
+#pragma unroll
+                    for (int st = 0; st < HH; ++st) {
+                        const uint2 v = hf[(HH * half + st) * 32 + lane];
+                        src0[st] = v.x;
+                        src1[st] = v.y;
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int st = 0; st < HH; ++st) {
+                        const int gst = HH * half + st;
+                        const int b16 = 4 * (gst >> 2) + 2 * ((gst & 3) >> 1) - HH * half;
+                        const int sl = 4 * hg + 2 * (gst & 1);
+                        const uint32_t a00 = __shfl_sync(0xFFFFFFFFu, src0[b16], sl);
+                        const uint32_t a01 = __shfl_sync(0xFFFFFFFFu, src1[b16], sl);
+                        const uint32_t a10 = __shfl_sync(0xFFFFFFFFu, src0[b16 + 1], sl);
+                        const uint32_t a11 = __shfl_sync(0xFFFFFFFFu, src1[b16 + 1], sl);
+                        const uint32_t b00 = __shfl_sync(0xFFFFFFFFu, src0[b16], sl + 1);
+                        const uint32_t b01 = __shfl_sync(0xFFFFFFFFu, src1[b16], sl + 1);
+                        const uint32_t b10 = __shfl_sync(0xFFFFFFFFu, src0[b16 + 1], sl + 1);
+                        const uint32_t b11 = __shfl_sync(0xFFFFFFFFu, src1[b16 + 1], sl + 1);
+                        const uint32_t x0 = hc == 0 ? a00 : hc == 1 ? a01 : hc == 2 ? a10 : a11;
+                        const uint32_t x1 = hc == 0 ? b00 : hc == 1 ? b01 : hc == 2 ? b10 : b11;
+                        hf[gst * 32 + lane] = hl ? make_uint2(x0, x1) : make_uint2(0u, 0u);
+                    }
+                }
             }
-            const float p = pow2i(sh);
             if (hc == 0 && hl)
                 sm.hshift[r][hg] = sh;
-            __syncwarp();
-            uint2 *hf = reinterpret_cast<uint2 *>(sm.u.hbuf[r]);
-#pragma unroll
-            for (int s = 0; s < HS; ++s)
-                hf[s * 32 + lane] = BW ? make_uint2(src0[s], src1[s])
-                                       : make_uint2(bf16x2_to_f16x2_scaled(src0[s], p),
-                                                    bf16x2_to_f16x2_scaled(src1[s], p));
             __syncwarp();
             if (lane == 0) {
                 __threadfence_block();
                 st_release_cta(&sm.hready[r], 1u);
             }
-        }
-        // this warp reads no slot counter any more
-        if (lane == 0) {
-            fence_acq_rel_gpu();
-            red_relaxed_add(&ctrl[4], 1u);
         }
     } else {
         // ---- a compute warp ----
@@ -1050,68 +1059,88 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             // one band per warp, times the routing weight, the tensor scale and
             // the token's inverse power of two
             const float ts = BW ? 1.0f : sm.ts2[slot];
-            float *P = partials + ((size_t)slot * H + 16 * band) * MAXT;
+            // tagged partials: (launch tag, fp32) per row and token
+            unsigned long long *P = ptag + ((size_t)slot * W2_BANDS + band) * 16 * MAXT;
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt) {
                 const int t = 2 * c + tt;
                 if (t < T) {
                     const float f = sm.wts[slot][t] * ts * pow2i(-sm.hshift[hb][t]);
-                    P[g * MAXT + t] = acc[tt] * f;
-                    P[(g + 8) * MAXT + t] = acc[2 + tt] * f;
+                    const unsigned long long tag = (unsigned long long)ltag << 32;
+                    st_relaxed_u64(&P[g * MAXT + t], tag | __float_as_uint(acc[tt] * f));
+                    st_relaxed_u64(&P[(g + 8) * MAXT + t], tag | __float_as_uint(acc[2 + tt] * f));
                 }
             }
-            __syncwarp();
-            if (slot < U - 1) {
-                if (lane == 0) {
-                    __threadfence_block();
-                    atomicOr(&sm.dn_mask[j >> 5], 1u << (j & 31));
+        }
+        // ---- the out rows of band cta (CTA b < 128): every slot's partial
+        // of the band, once each carries this launch's tag.  Warp w adds the
+        // slots w, w + 16, w + 32 in order (one round trip of loads), then
+        // warp 0 adds the 16 warp sums in warp order: a fixed order, so the
+        // result is the same from call to call.  Lane (r, th): row r, tokens
+        // 4 th .. 4 th + 3.
+        if (has_last) {
+            const int band = cta;
+            const int r = lane >> 1, th = lane & 1;
+            const unsigned long long *srcp = ptag + ((size_t)band * 16 + r) * MAXT + 4 * th;
+            float s4[4];
+            for (uint32_t it = 0;; ++it) {
+                bool ok = true;
+                s4[0] = s4[1] = s4[2] = s4[3] = 0.f;
+                constexpr int PER_WARP = (MAX_SLOTS + FW - 1) / FW;
+                unsigned long long v[PER_WARP][4];
+#pragma unroll
+                for (int jj = 0; jj < PER_WARP; ++jj)
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int sl = warp + FW * jj;
+                        v[jj][q4] = (sl < U && 4 * th + q4 < T)
+                                        ? ld_relaxed_u64(srcp + (size_t)sl * W2_BANDS * 16 * MAXT + q4)
+                                        : ((unsigned long long)ltag << 32);
+                    }
+#pragma unroll
+                for (int jj = 0; jj < PER_WARP; ++jj)
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        ok = ok && (uint32_t)(v[jj][q4] >> 32) == ltag;
+                        s4[q4] += __uint_as_float((uint32_t)v[jj][q4]);
+                    }
+                if (__all_sync(0xFFFFFFFFu, ok))
+                    break;
+                if (it == SPIN_LIMIT) {
+                    if (lane == 0)
+                        atomicOr(flag, FLAG_TIMEOUT);
+                    break;
                 }
-                continue;
+                __nanosleep(128);
             }
-            // the last slot's partial: add every slot's partial of the band
-            // in slot order once the other U - 1 are counted
-            const int r = lane >> 1, th = lane & 1;      // row r, tokens 4 th .. 4 th + 3
-            const float4 *srcp = reinterpret_cast<const float4 *>(partials + ((size_t)16 * band + r) * MAXT) + th;
-            if (lane == 0)
-                gmem_wait_geq(&band_cnt[band], (uint32_t)(U - 1), flag);
-            __syncwarp();
-            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            constexpr int BATCH = 16;
-            for (int s0 = 0; s0 < U; s0 += BATCH) {
-                float4 v[BATCH];
+            sm.comb[warp][lane] = make_float4(s4[0], s4[1], s4[2], s4[3]);
+            named_barrier_sync(7, FT);
+            if (warp == 0) {
+                float4 tot = sm.comb[0][lane];
+#pragma unroll 1
+                for (int w = 1; w < FW; ++w) {
+                    const float4 v = sm.comb[w][lane];
+                    tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
+                }
+                const float vals[4] = {tot.x, tot.y, tot.z, tot.w};
 #pragma unroll
-                for (int jj = 0; jj < BATCH; ++jj)
-                    v[jj] = (s0 + jj < U) ? __ldcg(srcp + (size_t)(s0 + jj) * H * MAXT / 4)
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int jj = 0; jj < BATCH; ++jj) {
-                    s4.x += v[jj].x; s4.y += v[jj].y; s4.z += v[jj].z; s4.w += v[jj].w;
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int t = 4 * th + jj;
+                    if (t < T)
+                        a.out[(size_t)t * H + 16 * band + r] = __float2bfloat16_rn(vals[jj]);
                 }
             }
-            const float vals[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int t = 4 * th + jj;
-                if (t < T)
-                    a.out[(size_t)t * H + 16 * band + r] = __float2bfloat16_rn(vals[jj]);
-            }
-            if (lane == 0)
-                band_cnt[band] = 0u;   // every other partial of the band has been counted
         }
     }
 
-    // ---- CTA 0 re-arms the slot counters for the next call once every CTA
-    // has stopped reading and adding to them (the count warp and the h warp
-    // of each CTA count themselves out in ctrl[4]; the band counters are
-    // re-armed by the warps that add the bands up) ----
+    // ---- CTA 0 advances the launch tag once every CTA has read it (the h
+    // warp of each CTA counts its CTA in ctrl[4]) ----
     __syncthreads();
     if (blockIdx.x == 0 && threadIdx.x == 0) {
-        if (!gmem_wait_geq(&ctrl[4], OUT_PER_CTA * gridDim.x, flag))
+        if (!gmem_wait_geq(&ctrl[4], gridDim.x, flag))
             return;
-        for (int s = 0; s < MAX_SLOTS; ++s)
-            slot_cnt[s] = 0u;
         ctrl[4] = 0u;
-        ctrl[5] = ltag;   // the next launch tags its logits ltag + 1
+        ctrl[5] = ltag;   // the next launch tags its words ltag + 1
     }
 }
 
@@ -1157,27 +1186,21 @@ cudaError_t launch_layer(const LayerArgs &a, int grid, cudaStream_t stream, bool
                    : cudaLaunchKernelEx(&cfg, moe_layer_kernel<false>, a);
 }
 
-// After a call that gave up on a bounded wait, the workspace's counters may
-// hold that call's partial counts and its launch tag may not have advanced
-// (CTA 0 returns before re-arming them).  If the flag word shows a timeout,
-// clear the counters and advance the tag, so that the next layer call
-// ignores the stale tagged logits; the flag bits stay for the caller to read.
-// Runs after the preceding kernel has finished (it waits on it first).
-__global__ void __launch_bounds__(128) rearm_kernel(uint8_t *ws)
+// After a call that gave up on a bounded wait, the workspace's count of CTAs
+// may hold that call's partial count and its launch tag may not have advanced
+// (CTA 0 returns before advancing it), so the words that call stored (router
+// logits, h, down partials) may carry the tag the next call would use.  If
+// the flag word shows a timeout, clear the counts and advance the tag, so
+// that the next layer call ignores every stale word; the flag bits stay for
+// the caller to read.  Runs after the preceding kernel has finished (it
+// waits on it first).
+__global__ void __launch_bounds__(32) rearm_kernel(uint8_t *ws)
 {
     griddep_launch();
     griddep_wait();
     const WsLayout L = ws_layout();
     uint32_t *ctrl = reinterpret_cast<uint32_t *>(ws + L.ctrl);
-    if ((__ldcg(&ctrl[0]) & FLAG_TIMEOUT) == 0u)
-        return;
-    uint32_t *slot_cnt = reinterpret_cast<uint32_t *>(ws + L.slot_cnt);
-    uint32_t *band_cnt = reinterpret_cast<uint32_t *>(ws + L.band_cnt);
-    for (int i = threadIdx.x; i < MAX_SLOTS; i += blockDim.x)
-        slot_cnt[i] = 0u;
-    for (int i = threadIdx.x; i < W2_BANDS; i += blockDim.x)
-        band_cnt[i] = 0u;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && (__ldcg(&ctrl[0]) & FLAG_TIMEOUT) != 0u) {
         ctrl[1] = 0u;
         ctrl[4] = 0u;
         ctrl[5] = ctrl[5] + 1u;
@@ -1188,7 +1211,7 @@ cudaError_t launch_rearm(uint8_t *ws, cudaStream_t stream, bool pdl)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
