@@ -63,14 +63,14 @@ namespace {
 constexpr int FW = 16;                 // compute warps per CTA
 constexpr int FT = FW * 32;            // compute threads
 constexpr int EP_WARP = FW;            // warps 16, 17: gate/up epilogues (band parity 0, 1)
-constexpr int HW_WARP = FW + 2;        // warp 18: h fragments of the CTA's down slots
-constexpr int NT = FT + 96;            // threads per CTA
+constexpr int HW_WARP = FW + 2;        // warps 18, 19: h fragments of the CTA's down slots (half of the steps each)
+constexpr int NHB = 3;                 // h buffers: the two range slots and the last slot
+constexpr int NT = FT + 128;           // threads per CTA (20 warps: a multiple of 4 keeps 96 registers a thread)
 constexpr int RW = 4;                  // ring stages per compute warp
 constexpr int STG = 2 * SC_BYTES;      // 2304 bytes: two NVFP4 super-chunks (a BF16 stage uses 2048)
 constexpr int GQ = 8;                  // 256-column slices of a gate/up band
 constexpr int NB = 8;                  // gate/up reduction buffers (band k uses k % NB)
 constexpr int XPITCH = H * 2 + 16;     // bytes per staged x row: rows 4 banks apart, so the fragment reads do not conflict
-constexpr int NHB = 3;                 // h buffers: the two range slots and the last slot
 constexpr int ROUTER_CTAS = E / 2;     // 128 CTAs x 2 experts
 constexpr int HS = I / 16;             // 32 k16 steps of the down GEMV
 constexpr int HBUF = HS * 32 * 8;      // one slot's h as B fragments [step][lane] (uint2), 8 KB
@@ -106,8 +106,9 @@ struct FSmem {
     int hshift[NHB][MAXT];
     uint64_t pfull[NB];                // a band's eight K partials are in buffer b
     uint64_t pempty[NB];               // the epilogue warp has read buffer b
-    uint32_t hready[NHB];              // 1 once the h warp has filled the buffer
+    uint32_t hready[NHB];              // h warps done with the buffer (2 when ready)
     float4 comb[FW][32];               // the final sum of band cta: per-warp sums of every 16th slot
+    float hmax[NHB][2][MAXT];          // per h warp, each token's max |h| over its half of a slot
 };
 
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }
@@ -154,10 +155,6 @@ __device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v)
 
 
 // CTA-scope release store / acquire load (shared-memory progress counters)
-__device__ __forceinline__ void st_release_cta(uint32_t *p, uint32_t v)
-{
-    asm volatile("st.release.cta.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 __device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t *p)
 {
@@ -781,59 +778,65 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                                    ((unsigned long long)ltag << 32) | (ob << 16) | hb);
             }
         }
-    } else if (warp == HW_WARP) {
-        // ---- the h warp: h of the CTA's down slots as B fragments ----
-        // First it counts this CTA in ctrl[4] (every thread of the CTA has
-        // read the launch tag by now; CTA 0 advances the tag once all CTAs
-        // are counted).  Then for each slot (range slots in order, then the
-        // last slot) lane (g, c) polls the 64 tagged words it needs, k16 step
-        // s taking rows 16 s + 2 c, +1 (band 2 s) and 16 s + 8 + 2 c, +1 (band
-        // 2 s + 1) of token g, until every one carries this launch's tag;
+    } else if (warp >= HW_WARP) {
+        // ---- the h warps: h of the CTA's down slots as B fragments ----
+        // Buffers: the first range slot (r = 0), the second (r = 1, when the
+        // range reaches it) and the last slot (r = 2, CTAs below 128), in
+        // that order.  h warp hw takes k16 steps 16 hw .. 16 hw + 15 of each:
+        // lane (g, c) needs, for step s, rows 16 s + 2 c, +1 (band 2 s) and
+        // 16 s + 8 + 2 c, +1 (band 2 s + 1) of token g, 32 tagged words in
+        // all.  It probes the tag of one pending word, then reads all 32
+        // words in one batch, until every one carries this launch's tag.
         // NVFP4 then scales each token by the power of two of its max |h|
-        // (over its four lanes) into f16.  The fragments go to the slot's
-        // buffer, [k16 step][lane], zeros in lanes 4T..
-        if (lane == 0)
+        // (over both halves: the two warps exchange their maxima) into f16;
+        // BF16 permutes the pairs into the column order of bf16_bcol.  The
+        // fragments go to the slot's buffer, [k16 step][lane], zeros in
+        // lanes 4T..; hready[r] counts the two warps done.  h warp 0 first
+        // counts this CTA in ctrl[4] (every thread of the CTA has read the
+        // launch tag by now; CTA 0 advances the tag once all CTAs are
+        // counted).
+        const int hw = warp - HW_WARP;
+        if (hw == 0 && lane == 0)
             red_release_add(&ctrl[4], 1u);
-        int hslot[NHB];
-        bool hneed[NHB];
-        hslot[0] = s_first;
-        hneed[0] = n_rng > 0;
-        hslot[1] = s_first + 1;
-        hneed[1] = n_rng > 0 && (d1 - 1) / W2_BANDS == s_first + 1;
-        hslot[2] = U - 1;
-        hneed[2] = has_last;
         const int hg = lane >> 2, hc = lane & 3;
         const bool hl = lane < blanes;
+        constexpr int HH = HS / 2;
+        uint2 *hfa = nullptr;
 #pragma unroll 1
         for (int r = 0; r < NHB; ++r) {
-            if (!hneed[r])
+            const int hslot = r == 0 ? s_first : r == 1 ? s_first + 1 : U - 1;
+            const bool hneed = r == 0   ? n_rng > 0
+                               : r == 1 ? n_rng > 0 && (d1 - 1) / W2_BANDS == s_first + 1
+                                        : has_last;
+            if (!hneed)
                 continue;
-            const unsigned long long *src = htag + ((size_t)hslot[r] * W13_BANDS * MAXT + hg) * 4 + hc;
-            // word j of the lane: band j, so k16 step j / 2, src0 (j even) or src1
-            auto word = [&](int j) -> unsigned long long { return ld_relaxed_u64(src + (size_t)j * MAXT * 4); };
-            // (1) wait until every word carries this launch's tag: the tag
-            // halves of all pending words at once (the 64-bit reads below
-            // check every tag again, and start over on a mismatch)
-            unsigned long long pend = hl ? ~0ull : 0ull;
-            uint32_t retries = 0;
-        again:
-            if (++retries > 64u) {   // tags seen but values not: give up (never expected)
-                if (lane == 0)
-                    atomicOr(flag, FLAG_TIMEOUT);
-                pend = 0ull;
-            }
+            // word j (0..31): band 32 hw + j, i.e. step 16 hw + j / 2, .x (j even) or .y
+            const unsigned long long *src =
+                htag + (((size_t)hslot * W13_BANDS + 2 * HH * hw) * MAXT + hg) * 4 + hc;
+            uint32_t vx[HH], vy[HH];
             for (uint32_t it = 0;; ++it) {
-                uint32_t tg[2 * HS];
+                bool ok = true;
+                // the probe: this lane's last word (the band written latest in
+                // the CTAs' band order is the likeliest to be missing)
+                if (hl)
+                    ok = ld_relaxed_u32(reinterpret_cast<const uint32_t *>(src + (size_t)(2 * HH - 1) * MAXT * 4) +
+                                        1) == ltag;
+                if (__all_sync(0xFFFFFFFFu, ok)) {
+                    unsigned long long w[2 * HH];
 #pragma unroll
-                for (int j = 0; j < 2 * HS; ++j)
-                    tg[j] = (pend >> j) & 1ull ? ld_relaxed_u32(reinterpret_cast<const uint32_t *>(src + (size_t)j * MAXT * 4) + 1)
-                                               : ltag;
+                    for (int j = 0; j < 2 * HH; ++j)
+                        w[j] = hl ? ld_relaxed_u64(src + (size_t)j * MAXT * 4) : ((unsigned long long)ltag << 32);
 #pragma unroll
-                for (int j = 0; j < 2 * HS; ++j)
-                    if (tg[j] == ltag)
-                        pend &= ~(1ull << j);
-                if (__all_sync(0xFFFFFFFFu, pend == 0ull))
-                    break;
+                    for (int j = 0; j < 2 * HH; ++j) {
+                        ok = ok && (uint32_t)(w[j] >> 32) == ltag;
+                        if (j & 1)
+                            vy[j >> 1] = hl ? (uint32_t)w[j] : 0u;
+                        else
+                            vx[j >> 1] = hl ? (uint32_t)w[j] : 0u;
+                    }
+                    if (__all_sync(0xFFFFFFFFu, ok))
+                        break;
+                }
                 if (it == SPIN_LIMIT) {
                     if (lane == 0)
                         atomicOr(flag, FLAG_TIMEOUT);
@@ -841,94 +844,61 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                 }
                 __nanosleep(128);
             }
-            // (2) the raw words, half of the steps at a time (one round trip
-            // each), tags checked again, into the slot's buffer as raw bf16
-            // pairs [k16 step][lane]; NVFP4 also takes each lane's max |h|
-            uint2 *hf = reinterpret_cast<uint2 *>(sm.u.hbuf[r]);
-            constexpr int HH = HS / 2;
-            bool stale = false;
-            __nv_bfloat162 m2 = __floats2bfloat162_rn(0.f, 0.f);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                unsigned long long w0[HH], w1[HH];
-#pragma unroll
-                for (int st = 0; st < HH; ++st) {
-                    w0[st] = hl ? word(2 * (HH * half + st)) : ((unsigned long long)ltag << 32);
-                    w1[st] = hl ? word(2 * (HH * half + st) + 1) : ((unsigned long long)ltag << 32);
-                }
-#pragma unroll
-                for (int st = 0; st < HH; ++st) {
-                    stale = stale || (uint32_t)(w0[st] >> 32) != ltag || (uint32_t)(w1[st] >> 32) != ltag;
-                    const uint32_t v0 = hl ? (uint32_t)w0[st] : 0u, v1 = hl ? (uint32_t)w1[st] : 0u;
-                    if (!BW) {
-                        m2 = __hmax2(m2, __habs2(u32_as_bf162(v0)));
-                        m2 = __hmax2(m2, __habs2(u32_as_bf162(v1)));
-                    }
-                    hf[(HH * half + st) * 32 + lane] = make_uint2(v0, v1);
-                }
-            }
-            if (__any_sync(0xFFFFFFFFu, stale)) {
-                pend = hl ? ~0ull : 0ull;
-                goto again;
-            }
-            __syncwarp();
-            // (3) in place: NVFP4 scales each token by the power of two of its
-            // max |h| (over its four lanes) into f16; BF16 permutes the pairs
-            // into the column order of bf16_bcol
+            hfa = reinterpret_cast<uint2 *>(sm.u.hbuf[r]);
             int sh = 0;
             if (!BW) {
+                __nv_bfloat162 m2 = __floats2bfloat162_rn(0.f, 0.f);
+#pragma unroll
+                for (int st = 0; st < HH; ++st) {
+                    m2 = __hmax2(m2, __habs2(u32_as_bf162(vx[st])));
+                    m2 = __hmax2(m2, __habs2(u32_as_bf162(vy[st])));
+                }
                 float mx = fmaxf(__low2float(m2), __high2float(m2));
                 mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+                if (hc == 0 && hl)
+                    sm.hmax[r][hw][hg] = mx;
+                named_barrier_sync(8, 64);   // the two h warps
+                if (hl)
+                    mx = fmaxf(sm.hmax[r][0][hg], sm.hmax[r][1][hg]);
                 sh = act_shift(mx);
                 const float pw = pow2i(sh);
 #pragma unroll
-                for (int st = 0; st < HS; ++st) {
-                    const uint2 v = hf[st * 32 + lane];
-                    hf[st * 32 + lane] = make_uint2(bf16x2_to_f16x2_scaled(v.x, pw), bf16x2_to_f16x2_scaled(v.y, pw));
-                }
+                for (int st = 0; st < HH; ++st)
+                    hfa[(HH * hw + st) * 32 + lane] =
+                        make_uint2(bf16x2_to_f16x2_scaled(vx[st], pw), bf16x2_to_f16x2_scaled(vy[st], pw));
             } else {
-                // Lane (g, c) holds columns 16 s + 2 c, +1 (.x of step s) and
-                // 16 s + 8 + 2 c, +1 (.y).  Step st needs the pairs starting at
-                // column bf16_bcol(st, c) and 2 after it: for every c they come
-                // from lanes (g, 2 (st & 1)) and (g, 2 (st & 1) + 1), from .x
-                // (c even) or .y (c odd) of step b16 (c < 2) or b16 + 1 (c >= 2);
-                // a step's pairs stay within its half (b16 + 1 < 16 (half + 1)).
+                // Lane (g, c) holds columns 16 s + 2 c, +1 (vx) and 16 s + 8 +
+                // 2 c, +1 (vy) of the steps s of its half.  Step st needs the
+                // pairs starting at column bf16_bcol(st, c) and 2 after it: for
+                // every c they come from lanes (g, 2 (st & 1)) and
+                // (g, 2 (st & 1) + 1), from vx (c even) or vy (c odd) of step
+                // b16 (c < 2) or b16 + 1 (c >= 2); a step's pairs stay within
+                // its half (b16 + 1 < 16 (hw + 1)).
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t src0[HH], src1[HH];
-#pragma unroll
-                    for (int st = 0; st < HH; ++st) {
-                        const uint2 v = hf[(HH * half + st) * 32 + lane];
-                        src0[st] = v.x;
-                        src1[st] = v.y;
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int st = 0; st < HH; ++st) {
-                        const int gst = HH * half + st;
-                        const int b16 = 4 * (gst >> 2) + 2 * ((gst & 3) >> 1) - HH * half;
-                        const int sl = 4 * hg + 2 * (gst & 1);
-                        const uint32_t a00 = __shfl_sync(0xFFFFFFFFu, src0[b16], sl);
-                        const uint32_t a01 = __shfl_sync(0xFFFFFFFFu, src1[b16], sl);
-                        const uint32_t a10 = __shfl_sync(0xFFFFFFFFu, src0[b16 + 1], sl);
-                        const uint32_t a11 = __shfl_sync(0xFFFFFFFFu, src1[b16 + 1], sl);
-                        const uint32_t b00 = __shfl_sync(0xFFFFFFFFu, src0[b16], sl + 1);
-                        const uint32_t b01 = __shfl_sync(0xFFFFFFFFu, src1[b16], sl + 1);
-                        const uint32_t b10 = __shfl_sync(0xFFFFFFFFu, src0[b16 + 1], sl + 1);
-                        const uint32_t b11 = __shfl_sync(0xFFFFFFFFu, src1[b16 + 1], sl + 1);
-                        const uint32_t x0 = hc == 0 ? a00 : hc == 1 ? a01 : hc == 2 ? a10 : a11;
-                        const uint32_t x1 = hc == 0 ? b00 : hc == 1 ? b01 : hc == 2 ? b10 : b11;
-                        hf[gst * 32 + lane] = hl ? make_uint2(x0, x1) : make_uint2(0u, 0u);
-                    }
+                for (int st = 0; st < HH; ++st) {
+                    const int gst = HH * hw + st;
+                    const int b16 = 4 * (gst >> 2) + 2 * ((gst & 3) >> 1) - HH * hw;
+                    const int sl = 4 * hg + 2 * (gst & 1);
+                    const uint32_t a00 = __shfl_sync(0xFFFFFFFFu, vx[b16], sl);
+                    const uint32_t a01 = __shfl_sync(0xFFFFFFFFu, vy[b16], sl);
+                    const uint32_t a10 = __shfl_sync(0xFFFFFFFFu, vx[b16 + 1], sl);
+                    const uint32_t a11 = __shfl_sync(0xFFFFFFFFu, vy[b16 + 1], sl);
+                    const uint32_t b00 = __shfl_sync(0xFFFFFFFFu, vx[b16], sl + 1);
+                    const uint32_t b01 = __shfl_sync(0xFFFFFFFFu, vy[b16], sl + 1);
+                    const uint32_t b10 = __shfl_sync(0xFFFFFFFFu, vx[b16 + 1], sl + 1);
+                    const uint32_t b11 = __shfl_sync(0xFFFFFFFFu, vy[b16 + 1], sl + 1);
+                    const uint32_t x0 = hc == 0 ? a00 : hc == 1 ? a01 : hc == 2 ? a10 : a11;
+                    const uint32_t x1 = hc == 0 ? b00 : hc == 1 ? b01 : hc == 2 ? b10 : b11;
+                    hfa[gst * 32 + lane] = hl ? make_uint2(x0, x1) : make_uint2(0u, 0u);
                 }
             }
-            if (hc == 0 && hl)
+            if (hw == 0 && hc == 0 && hl)
                 sm.hshift[r][hg] = sh;
             __syncwarp();
             if (lane == 0) {
                 __threadfence_block();
-                st_release_cta(&sm.hready[r], 1u);
+                atomicAdd(&sm.hready[r], 1u);
             }
         }
     } else {
@@ -1044,7 +1014,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             int slot, band, hb;
             dn_band(j, slot, band, hb);
             if (lane == 0)
-                smem_wait_geq(&sm.hready[hb], 1u, flag);
+                smem_wait_geq(&sm.hready[hb], 2u, flag);   // both h warps
             __syncwarp();
             const uint2 *bfrag = reinterpret_cast<const uint2 *>(sm.u.hbuf[hb]);
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
