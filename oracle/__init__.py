@@ -58,6 +58,8 @@ def _declare(lib):
     lib.oracle_dequant_nvfp4.restype = None
     lib.oracle_dequant_bf16.argtypes = [vp, c_int, c_int, vp]
     lib.oracle_dequant_bf16.restype = None
+    lib.oracle_dense_gemv_nvfp4.argtypes = [vp, vp, c_float, c_int, c_int, vp, c_int, vp]
+    lib.oracle_dense_gemv_nvfp4.restype = None
     lib.oracle_router_logits.argtypes = [vp, vp, c_int, c_int, c_int, vp]
     lib.oracle_router_logits.restype = None
     lib.oracle_select_topk.argtypes = [vp, c_int, c_int, c_int, vp, vp]
@@ -68,6 +70,12 @@ def _declare(lib):
         [vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp, vp]
         + [c_int, c_int, vp, vp, c_float, vp, vp, c_float, vp, vp, vp, vp])
     lib.oracle_moe_forward.restype = c_int
+    lib.oracle_select_topk_sink.argtypes = [vp, c_int, c_int, c_int, c_int, vp, vp, vp]
+    lib.oracle_select_topk_sink.restype = c_int
+    lib.oracle_moe_forward_sinks.argtypes = (
+        [vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp, vp]
+        + [c_int, c_int, c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp])
+    lib.oracle_moe_forward_sinks.restype = c_int
     lib.oracle_round_bf16.argtypes = [c_double]
     lib.oracle_round_bf16.restype = ctypes.c_uint16
     lib.oracle_prenorm.argtypes = [vp, vp, c_int, c_int, c_double, vp, vp]
@@ -131,6 +139,21 @@ def dequant_bf16(w: np.ndarray, lib=None) -> np.ndarray:
     W = np.empty((N, K), dtype=np.float64)
     (lib or load()).oracle_dequant_bf16(_ptr(w), N, K, _ptr(W))
     return W
+
+
+def dense_gemv_nvfp4(codes: np.ndarray, scales: np.ndarray, tscale: float, x: np.ndarray,
+                     lib=None) -> np.ndarray:
+    """y [T, N] fp64 = W x for canonical NVFP4 W [N, K] and bf16 bits x [T, K]."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    x = _u16(x)
+    N, K = codes.shape[0], codes.shape[1] * 2
+    T = x.shape[0]
+    assert scales.shape == (N, K // 16) and x.shape == (T, K)
+    y = np.empty((T, N), dtype=np.float64)
+    (lib or load()).oracle_dense_gemv_nvfp4(_ptr(codes), _ptr(scales), float(tscale), N, K, _ptr(x), T,
+                                            _ptr(y))
+    return y
 
 
 def router_logits(x: np.ndarray, wr: np.ndarray, lib=None) -> np.ndarray:
@@ -227,6 +250,71 @@ def moe_forward(x: np.ndarray, wr: np.ndarray, experts: Sequence[Optional[Expert
     if rc != 0:
         raise ValueError(f"oracle_moe_forward failed ({rc})")
     return out, idx, w, logits
+
+
+def select_topk_sink(logits: np.ndarray, n_routed: int, top_k: int, lib=None):
+    """Expert-sink routing: logits [T, E+S] (the last S columns the sinks).
+    Returns (idx [T,k], w [T,k], sw [T,S])."""
+    logits = np.ascontiguousarray(logits, dtype=np.float64)
+    T, R = logits.shape
+    E, S = int(n_routed), R - int(n_routed)
+    idx = np.empty((T, top_k), dtype=np.int32)
+    w = np.empty((T, top_k), dtype=np.float64)
+    sw = np.empty((T, S), dtype=np.float64)
+    rc = (lib or load()).oracle_select_topk_sink(_ptr(logits), T, E, S, int(top_k), _ptr(idx), _ptr(w), _ptr(sw))
+    if rc != 0:
+        raise ValueError(f"oracle_select_topk_sink failed ({rc})")
+    return idx, w, sw
+
+
+def _bank_arrays(experts):
+    n = len(experts)
+
+    def parr(getter):
+        arr = (ctypes.c_void_p * max(n, 1))()
+        for i, ex in enumerate(experts):
+            a = None if ex is None else getter(ex)
+            arr[i] = None if a is None else a.ctypes.data
+        return arr
+
+    ts13 = np.array([1.0 if e is None else e.ts13 for e in experts] or [1.0], dtype=np.float32)
+    ts2 = np.array([1.0 if e is None else e.ts2 for e in experts] or [1.0], dtype=np.float32)
+    return (parr(lambda e: e.w13a), parr(lambda e: e.w13b), ts13, parr(lambda e: e.w2a),
+            parr(lambda e: e.w2b), ts2)
+
+
+def moe_forward_sinks(x: np.ndarray, wr: np.ndarray, experts: Sequence[Optional[ExpertWeights]], top_k: int,
+                      inter: int, shared: Sequence[ExpertWeights], sink: bool, lib=None):
+    """The layer with len(shared) shared experts (their own weight type) and,
+    with ``sink``, expert-sink routing (wr has E + S rows).  Returns (out fp64
+    [T,H], idx [T,k], w [T,k], sw [T,S], logits [T, E (+S)])."""
+    x, wr = _u16(x), _u16(wr)
+    T, H = x.shape
+    E = len(experts)
+    S = len(shared)
+    R = wr.shape[0]
+    assert R == E + (S if sink else 0)
+    wtypes = {e.wtype for e in experts if e is not None}
+    assert len(wtypes) <= 1, "one weight type per routed bank"
+    wtype = wtypes.pop() if wtypes else 0
+    stypes = {e.wtype for e in shared}
+    assert len(stypes) <= 1, "one weight type per shared bank"
+    swtype = stypes.pop() if stypes else 0
+    ra, rb, rts13, r2a, r2b, rts2 = _bank_arrays(experts)
+    sa, sb, sts13, s2a, s2b, sts2 = _bank_arrays(shared)
+    out = np.empty((T, H), dtype=np.float64)
+    idx = np.empty((T, top_k), dtype=np.int32)
+    w = np.empty((T, top_k), dtype=np.float64)
+    sw = np.empty((T, max(S, 1)), dtype=np.float64)
+    logits = np.empty((T, R), dtype=np.float64)
+    c = lambda a: ctypes.cast(a, ctypes.c_void_p)  # noqa: E731
+    rc = (lib or load()).oracle_moe_forward_sinks(
+        _ptr(x), _ptr(wr), T, H, E, int(inter), int(top_k), wtype, c(ra), c(rb), _ptr(rts13), c(r2a), c(r2b),
+        _ptr(rts2), S, 1 if sink else 0, swtype, c(sa), c(sb), _ptr(sts13), c(s2a), c(s2b), _ptr(sts2),
+        _ptr(out), _ptr(idx), _ptr(w), _ptr(sw), _ptr(logits))
+    if rc != 0:
+        raise ValueError(f"oracle_moe_forward_sinks failed ({rc})")
+    return out, idx, w, sw[:, :S], logits
 
 
 def round_bf16(v: float, lib=None) -> int:

@@ -15,6 +15,9 @@
  *           activations.
  *  [FLINT-ZH] the Chinese mirror of the same post, section 模型架构 (model
  *           architecture): 256 experts, sigmoid top-6, plus one shared expert.
+ *  [INKLING] "TML Inkling on vLLM", section "MoE": 256 routed experts
+ *           (top-6) plus 2 shared experts that act as expert sinks; only the
+ *           routed experts are NVFP4, the shared experts BF16.
  *  [MOET]   "Frontier MoE on consumer Blackwell (SM120)", section
  *           "GLM-5.2 (753B) - the headline model": an NVFP4 weight is an e2m1
  *           code times an e4m3 scale per block of 16 times a per-tensor fp32
@@ -148,6 +151,35 @@ void oracle_dequant_bf16(const uint16_t *w, int N, int K, double *W)
 {
     for (size_t i = 0; i < (size_t)N * K; i++)
         W[i] = oracle_bf16_value(w[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dense GEMV.  [FLINT, "From 1,096 kernels to 346": the small-batch dense  */
+/* GEMV on the same packed NVFP4 weights]  Its plain definition:            */
+/*   y[t][n] = sum_k W[n][k] * x[t][k],  W dequantised as above, x bf16.    */
+/* fp64 products (exact) and an fp64 sum in k order; no rounding of y.      */
+/* ------------------------------------------------------------------------ */
+
+void oracle_dense_gemv_nvfp4(const uint8_t *codes, const uint8_t *scales, float tscale, int N, int K,
+                             const uint16_t *x, int T, double *y)
+{
+    double *W = (double *)malloc(sizeof(double) * (size_t)N * K);
+#if ORACLE_MUTANT == 15 /* planted: the tensor scale left out */
+    tscale = 1.0f;
+#endif
+    oracle_dequant_nvfp4(codes, scales, tscale, N, K, W);
+    int kend = K;
+#if ORACLE_MUTANT == 16 /* planted: the last column dropped from the sum */
+    kend = K - 1;
+#endif
+    for (int t = 0; t < T; t++)
+        for (int n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (int k = 0; k < kend; k++)
+                acc += W[(size_t)n * K + k] * oracle_bf16_value(x[(size_t)t * K + k]);
+            y[(size_t)t * N + n] = acc;
+        }
+    free(W);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -389,6 +421,170 @@ done:
     free(logits);
     free(idx);
     free(w);
+    free(xd);
+    free(W13);
+    free(W2);
+    free(toks);
+    free(gw);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Expert sinks.  [INKLING, "MoE": 256 routed experts (top-6) plus 2 shared  */
+/* experts; the shared experts take part in the routing-score computation,   */
+/* absorbing probability mass, but are never candidates for the top-6.]      */
+/* Readings (the page gives no formula):                                     */
+/*  - the router has E + S rows, the last S being the shared experts';      */
+/*  - every row gets the score s = sigmoid(logit), as for the routed ones;  */
+/*  - the top_k are chosen among the E routed experts exactly as in          */
+/*    oracle_select_topk;                                                    */
+/*  - with D = (sum of s over the selected) + (sum of s over the S sinks),   */
+/*    selected expert e gets the weight s_e / D and shared expert j the      */
+/*    weight s_{E+j} / D; nothing else scales them.                          */
+/* ------------------------------------------------------------------------ */
+
+/* logits [T][E+S]; idx, w [T][top_k]; sw [T][S].  Returns 0, or -1 on a NaN
+ * logit. */
+int oracle_select_topk_sink(const double *logits, int T, int E, int S, int top_k, int32_t *idx, double *w,
+                            double *sw)
+{
+    double *row = (double *)malloc(sizeof(double) * (size_t)E);
+    int rc = 0;
+    for (int t = 0; t < T && rc == 0; t++) {
+        const double *lg = logits + (size_t)t * (E + S);
+        for (int e = 0; e < E + S; e++)
+            if (isnan(lg[e]))
+                rc = -1;
+        if (rc != 0)
+            break;
+        int32_t *sel = idx + (size_t)t * top_k;
+        double *wt = w + (size_t)t * top_k;
+#if ORACLE_MUTANT == 18 /* planted: the sinks are candidates of the top-k */
+        {
+            int32_t *tmp = (int32_t *)malloc(sizeof(int32_t) * (size_t)top_k);
+            double *tw = (double *)malloc(sizeof(double) * (size_t)top_k);
+            oracle_select_topk(lg, 1, E + S, top_k, tmp, tw);
+            for (int i = 0; i < top_k; i++)
+                sel[i] = tmp[i] < E ? tmp[i] : 0;
+            free(tmp);
+            free(tw);
+        }
+#else
+        memcpy(row, lg, sizeof(double) * (size_t)E);
+        oracle_select_topk(row, 1, E, top_k, sel, wt);   /* the selection; weights recomputed below */
+#endif
+        double denom = 0.0;
+        for (int i = 0; i < top_k; i++)
+            denom += sigmoid(lg[sel[i]]);
+#if ORACLE_MUTANT != 17 /* planted (17): the sinks left out of the denominator */
+        for (int j = 0; j < S; j++)
+            denom += sigmoid(lg[E + j]);
+#endif
+        for (int i = 0; i < top_k; i++)
+            wt[i] = sigmoid(lg[sel[i]]) / denom;
+        for (int j = 0; j < S; j++)
+            sw[(size_t)t * S + j] = sigmoid(lg[E + j]) / denom;
+    }
+    free(row);
+    return rc;
+}
+
+/*
+ * The layer with S shared experts, which may be stored in another weight
+ * type than the routed bank (TML Inkling's NVFP4 checkpoint keeps only the
+ * routed experts in NVFP4; the shared experts are BF16), optionally as
+ * expert sinks:
+ *   out[t] = sum_i w[t][i] * FFN_{idx[t][i]}(x[t]) + sum_j sw[t][j] * FFN_shared_j(x[t])
+ * with sink = 1: wr has E + S rows and (idx, w, sw) come from
+ * oracle_select_topk_sink; sink = 0: wr has E rows, (idx, w) from
+ * oracle_select_topk and sw = 1.  Shared expert j: s_a13[j], s_b13[j],
+ * s_ts13[j], s_a2[j], s_b2[j], s_ts2[j] (dequant_expert's meaning, type
+ * shared_wtype).  Outputs: out [T][H]; idx, w [T][top_k]; sw [T][S];
+ * logits [T][E + sink * S] (any output but out may be NULL).  Returns as
+ * oracle_moe_forward.
+ */
+int oracle_moe_forward_sinks(const uint16_t *x, const uint16_t *wr, int T, int H, int E, int I, int top_k,
+                             int wtype, const void *const *a13, const void *const *b13, const float *ts13,
+                             const void *const *a2, const void *const *b2, const float *ts2, int S, int sink,
+                             int shared_wtype, const void *const *s_a13, const void *const *s_b13,
+                             const float *s_ts13, const void *const *s_a2, const void *const *s_b2,
+                             const float *s_ts2, double *out, int32_t *idx_out, double *w_out, double *sw_out,
+                             double *logits_out)
+{
+    if (T < 0 || H <= 0 || E <= 0 || I <= 0 || top_k <= 0 || top_k > E || H % 16 || I % 16 || S < 0)
+        return -3;
+    const int R = E + (sink ? S : 0);
+    const size_t T1 = (size_t)(T > 0 ? T : 1);
+    int rc = 0;
+    double *logits = (double *)malloc(sizeof(double) * T1 * R);
+    int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * T1 * top_k);
+    double *w = (double *)malloc(sizeof(double) * T1 * top_k);
+    double *sw = (double *)malloc(sizeof(double) * T1 * (S > 0 ? S : 1));
+    double *xd = (double *)malloc(sizeof(double) * T1 * H);
+    double *W13 = (double *)malloc(sizeof(double) * (size_t)2 * I * H);
+    double *W2 = (double *)malloc(sizeof(double) * (size_t)H * I);
+    int *toks = (int *)malloc(sizeof(int) * T1);
+    double *gw = (double *)malloc(sizeof(double) * T1);
+
+    for (size_t i = 0; i < (size_t)T * H; i++) {
+        xd[i] = oracle_bf16_value(x[i]);
+        out[i] = 0.0;
+    }
+    oracle_router_logits(x, wr, T, H, R, logits);
+    if (sink) {
+        if (oracle_select_topk_sink(logits, T, E, S, top_k, idx, w, sw) != 0) {
+            rc = -1;
+            goto done;
+        }
+    } else {
+        if (oracle_select_topk(logits, T, E, top_k, idx, w) != 0) {
+            rc = -1;
+            goto done;
+        }
+        for (size_t i = 0; i < (size_t)T * S; i++)
+            sw[i] = 1.0;
+    }
+    for (int e = 0; e < E; e++) {
+        int n = 0;
+        for (int t = 0; t < T; t++)
+            for (int i = 0; i < top_k; i++)
+                if (idx[(size_t)t * top_k + i] == e) {
+                    toks[n] = t;
+                    gw[n] = w[(size_t)t * top_k + i];
+                    n++;
+                }
+        if (n == 0)
+            continue;
+        rc = dequant_expert(wtype, a13[e], b13 ? b13[e] : NULL, ts13 ? ts13[e] : 1.0f, a2[e],
+                            b2 ? b2[e] : NULL, ts2 ? ts2[e] : 1.0f, H, I, W13, W2);
+        if (rc != 0)
+            goto done;
+        apply_expert(W13, W2, xd, H, I, toks, gw, n, out);
+    }
+    for (int j = 0; j < S && T > 0; j++) {
+        rc = dequant_expert(shared_wtype, s_a13[j], s_b13 ? s_b13[j] : NULL, s_ts13 ? s_ts13[j] : 1.0f,
+                            s_a2[j], s_b2 ? s_b2[j] : NULL, s_ts2 ? s_ts2[j] : 1.0f, H, I, W13, W2);
+        if (rc != 0)
+            goto done;
+        for (int t = 0; t < T; t++) {
+            toks[t] = t;
+            gw[t] = sw[(size_t)t * S + j];
+        }
+        apply_expert(W13, W2, xd, H, I, toks, gw, T, out);
+    }
+done:
+    if (idx_out)
+        memcpy(idx_out, idx, sizeof(int32_t) * (size_t)T * top_k);
+    if (w_out)
+        memcpy(w_out, w, sizeof(double) * (size_t)T * top_k);
+    if (sw_out)
+        memcpy(sw_out, sw, sizeof(double) * (size_t)T * S);
+    if (logits_out)
+        memcpy(logits_out, logits, sizeof(double) * (size_t)T * R);
+    free(logits);
+    free(idx);
+    free(w);
+    free(sw);
     free(xd);
     free(W13);
     free(W2);

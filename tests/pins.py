@@ -334,6 +334,201 @@ def pin_expert_permutation_invariance(lib):
 
 
 # ---------------------------------------------------------------------------
+# expert sinks (shared experts in the normalisation, not in the top-k)
+# ---------------------------------------------------------------------------
+
+def host_inputs_sinks(li: synth.LayerInputs):
+    """LayerInputs with S shared experts -> bits + routed and shared ExpertWeights lists."""
+    x = li.x.view(torch.int16).numpy().view(np.uint16)
+    wr = li.router_w.view(torch.int16).numpy().view(np.uint16)
+    E, S = li.n_routed, li.n_shared
+
+    def nv(e):
+        return oracle.ExpertWeights(0, li.codes13[e].numpy(), li.scales13[e].numpy(), float(li.tscale13[e]),
+                                    li.codes2[e].numpy(), li.scales2[e].numpy(), float(li.tscale2[e]))
+
+    def bf(w13, w2):
+        return oracle.ExpertWeights(1, w13.view(torch.int16).numpy().view(np.uint16), None, 1.0,
+                                    w2.view(torch.int16).numpy().view(np.uint16), None, 1.0)
+
+    if li.wtype == synth.NVFP4:
+        routed = [nv(e) for e in range(E)]
+        shared = ([bf(li.sw13[j], li.sw2[j]) for j in range(S)] if li.shared_bf16
+                  else [nv(E + j) for j in range(S)])
+    else:
+        routed = [bf(li.w13[e], li.w2[e]) for e in range(E)]
+        shared = [bf(li.w13[E + j], li.w2[E + j]) for j in range(S)]
+    return x, wr, routed, shared
+
+
+def brute_layer_sinks(li: synth.LayerInputs, top_k: int):
+    """Dense masked evaluation with S shared experts (numpy/scipy only)."""
+    x = np_bf16(li.x.view(torch.int16).numpy())
+    wr = np_bf16(li.router_w.view(torch.int16).numpy())
+    E, S, I = li.n_routed, li.n_shared, li.inter
+    logits = x @ wr.T
+    T = x.shape[0]
+    gate = np.zeros((T, E))
+    sw = np.ones((T, S))
+    idx = np.zeros((T, top_k), dtype=np.int32)
+    for t in range(T):
+        sel = brute_topk(logits[t, :E], top_k)
+        idx[t] = sel
+        s_ = scipy.special.expit(logits[t, sel])
+        d = s_.sum()
+        if li.sink:
+            ss = scipy.special.expit(logits[t, E:E + S])
+            d += ss.sum()
+            sw[t] = ss / d
+        gate[t, sel] = s_ / d
+
+    def nv(e):
+        return (np_dequant(li.codes13[e].numpy(), li.scales13[e].numpy(), float(li.tscale13[e])),
+                np_dequant(li.codes2[e].numpy(), li.scales2[e].numpy(), float(li.tscale2[e])))
+
+    def bf(w13, w2):
+        return np_bf16(w13.view(torch.int16).numpy()), np_bf16(w2.view(torch.int16).numpy())
+
+    out = np.zeros_like(x)
+    for e in range(E):
+        W13, W2 = nv(e) if li.wtype == synth.NVFP4 else bf(li.w13[e], li.w2[e])
+        out += gate[:, e:e + 1] * dense_expert_outputs(W13, W2, x, I)
+    for j in range(S):
+        if li.shared_bf16:
+            W13, W2 = bf(li.sw13[j], li.sw2[j])
+        elif li.wtype == synth.NVFP4:
+            W13, W2 = nv(E + j)
+        else:
+            W13, W2 = bf(li.w13[E + j], li.w2[E + j])
+        out += sw[:, j:j + 1] * dense_expert_outputs(W13, W2, x, I)
+    return out, idx, gate, sw
+
+
+def pin_topk_sink_bruteforce(lib):
+    """Top-k over the routed columns only (brute force over k-subsets); the
+    sinks' scores join the denominator.  Half of the rows give the sinks
+    the largest logits, so a sink taken as a candidate would be selected."""
+    rng = np.random.default_rng(13)
+    for E, S, k in [(6, 2, 3), (8, 2, 6), (5, 1, 2), (7, 2, 1)]:
+        lg = rng.normal(size=(20, E + S))
+        lg[::2, E:] += 4.0
+        idx, w, sw = oracle.select_topk_sink(lg, E, k, lib=lib)
+        for t in range(lg.shape[0]):
+            sel = brute_topk(lg[t, :E], k)
+            assert np.array_equal(idx[t], sel), (E, S, k, t)
+            s_ = scipy.special.expit(lg[t, sel])
+            ss = scipy.special.expit(lg[t, E:])
+            d = s_.sum() + ss.sum()
+            assert np.allclose(w[t], s_ / d, rtol=1e-14, atol=0)
+            assert np.allclose(sw[t], ss / d, rtol=1e-14, atol=0)
+            assert abs(w[t].sum() + sw[t].sum() - 1.0) < 1e-14
+
+
+def pin_topk_sink_limits(lib):
+    """Sink logits -inf: the sinks absorb nothing and the routing is the plain
+    sigmoid top-k.  +inf: each sink scores exactly 1."""
+    rng = np.random.default_rng(17)
+    E, S, k = 12, 2, 4
+    lg = rng.normal(size=(16, E + S))
+    lo = lg.copy()
+    lo[:, E:] = -np.inf
+    idx, w, sw = oracle.select_topk_sink(lo, E, k, lib=lib)
+    idx0, w0 = oracle.select_topk(lg[:, :E], k, lib=lib)
+    assert np.array_equal(idx, idx0) and np.all(sw == 0.0)
+    assert np.allclose(w, w0, rtol=1e-15, atol=0)
+    hi = lg.copy()
+    hi[:, E:] = np.inf
+    idx, w, sw = oracle.select_topk_sink(hi, E, k, lib=lib)
+    for t in range(lg.shape[0]):
+        s_ = scipy.special.expit(lg[t, idx[t]])
+        d = s_.sum() + S
+        assert np.allclose(w[t], s_ / d, rtol=1e-14, atol=0)
+        assert np.allclose(sw[t], 1.0 / d, rtol=1e-14, atol=0)
+
+
+def _check_sink_layer(lib, li, top_k):
+    x, wr, routed, shared = host_inputs_sinks(li)
+    out, idx, w, sw, _ = oracle.moe_forward_sinks(x, wr, routed, top_k, li.inter, shared, li.sink, lib=lib)
+    ref, ridx, _, rsw = brute_layer_sinks(li, top_k)
+    assert np.array_equal(idx, ridx)
+    assert np.allclose(sw, rsw, rtol=1e-12, atol=0)
+    assert np.allclose(out, ref, rtol=1e-10, atol=1e-12 * np.abs(ref).max())
+
+
+def pin_layer_sinks_bruteforce(lib):
+    """Two BF16 shared experts as sinks beside NVFP4 routed experts, and the
+    same layer shape without sinks (shared weight 1)."""
+    _check_sink_layer(lib, synth.make_layer(12, 3, hidden=32, n_routed=6, inter=16, n_shared=2, sink=True,
+                                            shared_bf16=True), 2)
+    _check_sink_layer(lib, synth.make_layer(13, 2, hidden=32, n_routed=7, inter=16, n_shared=2, sink=False,
+                                            shared_bf16=True), 3)
+    _check_sink_layer(lib, synth.make_layer(14, 2, hidden=48, n_routed=5, inter=32, n_shared=1, sink=True,
+                                            wtype=synth.BF16), 2)
+
+
+# ---------------------------------------------------------------------------
+# the dense GEMV
+# ---------------------------------------------------------------------------
+
+def _bf16_bits(v: torch.Tensor) -> np.ndarray:
+    return v.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def pin_dense_gemv_one_hot(lib):
+    """One non-zero code (6.0 at row 17, column 45, block scale 2.0) and a
+    tensor scale of 0.5: y[t][17] = 6 * 2 * 0.5 * x[t][45], every other y is 0."""
+    N, K, T = 32, 64, 3
+    codes = np.zeros((N, K // 2), dtype=np.uint8)
+    codes[17, 45 // 2] = 0x7 << 4            # odd column: the high nibble; e2m1 code 7 = 6.0
+    scales = np.full((N, K // 16), 0x38, dtype=np.uint8)   # e4m3 1.0
+    scales[17, 45 // 16] = 0x40                           # e4m3 2.0
+    x = _bf16_bits(torch.randn(T, K, generator=torch.Generator().manual_seed(3)))
+    y = oracle.dense_gemv_nvfp4(codes, scales, 0.5, x, lib=lib)
+    xv = np_bf16(x)
+    want = np.zeros((T, N))
+    want[:, 17] = 6.0 * xv[:, 45]
+    assert np.array_equal(y, want)
+
+
+def pin_dense_gemv_row_sums(lib):
+    """Every code 1.0, every scale 1.0, tensor scale 1: y[t][n] is the sum of
+    token t's activations (math.fsum, correctly rounded)."""
+    N, K, T = 16, 256, 4
+    codes = np.full((N, K // 2), 0x22, dtype=np.uint8)    # both nibbles e2m1 1.0
+    scales = np.full((N, K // 16), 0x38, dtype=np.uint8)
+    x = _bf16_bits(torch.randn(T, K, generator=torch.Generator().manual_seed(4)) * 3)
+    y = oracle.dense_gemv_nvfp4(codes, scales, 1.0, x, lib=lib)
+    xv = np_bf16(x)
+    for t in range(T):
+        s_ = math.fsum(xv[t])
+        bound = 1e-13 * np.abs(xv[t]).sum()
+        assert np.all(np.abs(y[t] - s_) <= bound), (t, y[t, 0], s_)
+
+
+def pin_dense_gemv_bruteforce(lib):
+    """Tiny random matrix: loops over the e2m1 table and torch's e4m3 decode."""
+    N, K, T = 16, 32, 2
+    rng = np.random.default_rng(21)
+    codes = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    scales = (np.abs(rng.standard_normal((N, K // 16))) * 0.3).astype(np.float32)
+    scales = torch.from_numpy(scales).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    x = _bf16_bits(torch.randn(T, K, generator=torch.Generator().manual_seed(5)))
+    ts = 0.75
+    y = oracle.dense_gemv_nvfp4(codes, scales, ts, x, lib=lib)
+    xv = np_bf16(x)
+    sv = np_e4m3(scales)
+    for t in range(T):
+        for n in range(N):
+            terms = []
+            for k in range(K):
+                byte = int(codes[n, k // 2])
+                code = (byte >> 4) if k % 2 else (byte & 0xF)
+                terms.append(E2M1_KNOWN[code] * float(sv[n, k // 16]) * ts * float(xv[t, k]))
+            want = math.fsum(terms)
+            assert abs(y[t, n] - want) <= 1e-13 * sum(abs(v) for v in terms), (t, n)
+
+
+# ---------------------------------------------------------------------------
 # the pre-norm step of a decoder stack and bf16 rounding
 # ---------------------------------------------------------------------------
 
@@ -433,6 +628,12 @@ ALL_PINS = [
     pin_routed_off_leaves_shared,
     pin_combine_linear_in_down_scale,
     pin_expert_permutation_invariance,
+    pin_topk_sink_bruteforce,
+    pin_topk_sink_limits,
+    pin_layer_sinks_bruteforce,
+    pin_dense_gemv_one_hot,
+    pin_dense_gemv_row_sums,
+    pin_dense_gemv_bruteforce,
     pin_round_bf16_known_answers,
     pin_prenorm_constant_vector,
     pin_prenorm_matches_torch,

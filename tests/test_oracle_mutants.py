@@ -5,7 +5,9 @@ e2m1 subnormal, an off-by-one e4m3 bias, swapped nibbles, a wrong scale
 block, a reversed tie rule, no renormalisation, gate/up swapped, SiLU lost,
 the shared expert dropped, the router or down matrix read transposed, and in
 the pre-norm step of a stack a sum instead of a mean, eps outside the root
-and truncation instead of rounding to bf16.
+and truncation instead of rounding to bf16; in the dense GEMV the tensor
+scale left out and the last column dropped; in expert-sink routing the
+sinks left out of the denominator and the sinks taken as top-k candidates.
 Each variant is compiled here; at least one pin must fail on it.
 """
 import os
@@ -15,7 +17,7 @@ import pytest
 import oracle
 from tests import pins
 
-MUTANTS = list(range(1, 15))
+MUTANTS = list(range(1, 19))
 
 
 @pytest.mark.parametrize("mutant", MUTANTS)
