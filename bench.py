@@ -320,6 +320,13 @@ def main():
         sec.append(secondary_entry(measure_grouped(args, 8192, "nvfp4", world, dev, False,
                                                    max(min(K, 40), 4), max(min(W, 6), 3))))
         torch.cuda.empty_cache()
+        # the dense GEMV on the packed layout: the attention projections of a
+        # 2048-wide decoder (qkv 5120 x 2048, o 2048 x 4096), and a large matrix
+        for (t2, shapes, nm, label) in ((8, [(5120, 2048), (2048, 4096)], 32, "attention projections"),
+                                        (1, [(5120, 2048), (2048, 4096)], 32, "attention projections"),
+                                        (8, [(16384, 4096)], 8, "one large matrix")):
+            sec.append(secondary_entry(measure_dense(args, t2, shapes, nm, world, dev, k2, w2, label)))
+            torch.cuda.empty_cache()
         line["config"]["secondary"] = sec
         line["gpu_launches"] += sum(e["gpu_launches"] for e in sec)
     if rank == 0:
@@ -599,6 +606,81 @@ def measure_grouped(args, T: int, WT: str, world: int, dev, with_e2e: bool, K: i
         line["e2e"] = {"value": e2e_v, "unit": "TFLOP/s", "steps": ne, "h2d_bytes_per_step": T * 2048 * 2,
                        "d2h_bytes_per_step": T * 2048 * 2}
     del layers, ws
+    return line
+
+
+def measure_dense(args, T: int, shapes, n_mats: int, world: int, dev, K: int, W: int, label: str) -> dict:
+    """Dense NVFP4 GEMVs (moe_dense_gemv_nvfp4), one per step, over n_mats
+    distinct resident matrices whose (N, K) cycle through ``shapes``; step k
+    runs matrix k mod n_mats (the matrices of one rotation are far larger than
+    L2).  The bytes of a step are the packed matrix + x + y."""
+    import torch
+
+    import nvfp4_moe_decode_gb300 as m
+    from nvfp4_moe_decode_gb300 import synth
+
+    stream = torch.cuda.Stream(dev)
+    mats = []
+    with torch.cuda.stream(stream):
+        for i in range(n_mats):
+            N, Kd = shapes[i % len(shapes)]
+            d = synth.make_dense(1000 + i, T, N, Kd, device=dev)
+            pk = torch.empty(m.moe_packed_bytes(N, Kd), dtype=torch.uint8, device=dev)
+            m.moe_pack_nvfp4(d.codes, d.scales, N, Kd, m.MOE_PACK_PLAIN, 1, pk, stream)
+            mats.append((N, Kd, pk, d.x.clone(), torch.empty(T, N, dtype=torch.bfloat16, device=dev)))
+            del d
+    stream.synchronize()
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+
+    def step_bytes(N, Kd):
+        return m.moe_packed_bytes(N, Kd) + 4 + T * Kd * 2 + T * N * 2
+
+    def run_steps(n: int):
+        for k in range(n):
+            N, Kd, pk, xx, yy = mats[k % n_mats]
+            m.moe_dense_gemv_nvfp4(xx, pk, 1.0, N, Kd, T, yy, ws, stream)
+
+    with torch.cuda.stream(stream):
+        run_steps(n_mats)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run_steps(n_mats)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, W // n_mats)):
+            g.replay()
+    stream.synchronize()
+    reps = max(1, K // n_mats)
+    steps = reps * n_mats
+    barrier(world)
+    ms, clk = timed_replays(stream, [(g, reps)], dev.index)
+    barrier(world)
+    ms_max = reduce_max(ms, world)
+    rot_bytes = sum(step_bytes(N, Kd) for (N, Kd, _, _, _) in mats)
+    alg = rot_bytes / n_mats
+    value = reduce_sum(float(rot_bytes * reps), world) / (ms_max * 1e-3) / 1e9
+    us = 1e3 * ms_max / steps
+    flag = m.moe_read_device_flag(ws, stream)
+    peak, peak_src = peaks()
+    shp = ", ".join(f"{N}x{Kd}" for (N, Kd) in shapes)
+    workload = (f"dense NVFP4 GEMV y = W x, T={T} tokens, W of {shp} ({label}), packed layout, "
+                f"synthetic seeded weights")
+    line = {
+        "metric": "dense NVFP4 GEMV weight-read GB/s (% of HBM peak)", "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": steps, "warmup": W, "ms_per_step": ms_max / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 weights x bf16 activations, f32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": workload, "weights": "nvfp4", "tokens": T, "layers_rotated": n_mats,
+                   "l2": f"cold: steps rotate over {n_mats} distinct resident matrices "
+                         f"({rot_bytes / 1e6:.0f} MB, above L2)",
+                   "us_per_layer": us, "algorithmic_bytes_per_step": alg, "device_flag": flag},
+        "roofline": {"bound": "hbm", "achieved": alg / (us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": alg / (us * 1e-6) / 1e9 / peak, "traffic": None, "peak_source": peak_src,
+                     "kernel": "dense_gemv_kernel"},
+        "gpu_launches": steps,
+        "clocks": clk,
+    }
+    del mats
     return line
 
 

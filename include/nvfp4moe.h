@@ -16,6 +16,8 @@
  *  [MOET]   "Frontier MoE on consumer Blackwell (SM120)", section
  *           "GLM-5.2 (753B) - the headline model": NVFP4 = e2m1 code x e4m3
  *           scale per block of 16 x per-tensor fp32 scale.
+ *  [INKLING] "TML Inkling on vLLM", section "MoE": two shared experts that
+ *           act as expert sinks; only the routed experts are NVFP4.
  *
  * For T tokens x[T][H] (bf16) the layer computes
  *     logit[t][e] = sum_k x[t][k] * router_w[e][k]
@@ -28,7 +30,8 @@
  * BF16), and out rounded once to bf16.
  *
  * Shapes this build supports: H = 2048, I = 512 (W13 is [2I][H], W2 is
- * [H][I]), E = 256 routed experts, top_k = 6, 0 or 1 shared expert, and
+ * [H][I]), E = 256 routed experts, top_k = 6, 0 or 1 shared expert (up to
+ * 2, of either weight type, for 1..MOE_MAX_DECODE_T tokens), and
  * 1 <= T <= MOE_MAX_TOKENS tokens per call (the decode kernel up to
  * MOE_MAX_DECODE_T tokens, the grouped tensor-core path above; the stack
  * and pre-norm calls take 1..MOE_MAX_DECODE_T).
@@ -281,14 +284,22 @@ moe_status moe_read_routing(const void *workspace, size_t workspace_bytes, int T
  *  x:        device bf16 [T][H]; must not alias out.
  *  router_w: device bf16 [E][H].
  *  routed:   host struct describing E = 256 routed experts.
- *  shared:   host struct with n_experts 0 or 1 (NULL = no shared expert).
+ *  shared:   host struct with n_experts 0, 1 or 2 (NULL = no shared expert);
+ *            each shared expert is added with weight 1.
  *  out:      device bf16 [T][H].
  *  workspace: device, >= moe_workspace_bytes(T), initialised once with
  *            moe_workspace_init; one workspace per concurrently running call.
  * Weight types: both banks NVFP4 (W4A16), or both BF16 (the W16A16 variant
  * [FLINT, "From 1,096 kernels to 346": BF16 decode]: same routing, same
- * combine, bf16 weights read row-major); a shared bank of the other type than
- * the routed one gives MOE_ERR_UNSUPPORTED.
+ * combine, bf16 weights read row-major).  Up to MOE_MAX_DECODE_T tokens the
+ * shared bank may also hold 2 experts, or be of the other type than the
+ * routed one (TML Inkling's NVFP4 checkpoint: BF16 shared experts beside
+ * NVFP4 routed ones [INKLING, "MoE"]): those shared experts then run ahead of
+ * the layer kernel as two dense GEMV launches (gate/up with SiLU*up, then
+ * down, see moe_dense_gemv_nvfp4; h rounded to bf16, their fp32 outputs kept
+ * in the workspace), and the layer kernel adds them in its combine, after
+ * the routed experts, before the one rounding to bf16.  Above
+ * MOE_MAX_DECODE_T tokens such a shared bank gives MOE_ERR_UNSUPPORTED.
  * Activations must be finite; with NVFP4 weights also max|x[t]| < 2^114 per
  * token: each token is scaled by a power of two into f16 for the tensor cores
  * (see csrc/common.cuh).  With BF16 weights the activations and h enter the
@@ -300,6 +311,87 @@ moe_status moe_read_routing(const void *workspace, size_t workspace_bytes, int T
 moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expert_bank *routed,
                              const moe_expert_bank *shared, void *out, int T, void *workspace,
                              size_t workspace_bytes, moe_stream_t stream);
+
+/* ----------------------------------------------------------------------- */
+/* Dense small-batch GEMV.  [FLINT, "From 1,096 kernels to 346": the       */
+/* small-batch dense GEMV (dense MLP layers, projections) runs on the same */
+/* packed NVFP4 weights as the large-batch kernel.]                        */
+/* ----------------------------------------------------------------------- */
+
+/*
+ * y[t][n] = bf16( tscale * sum_k W[n][k] x[t][k] ) for 1 <= T <= MOE_MAX_DECODE_T
+ * tokens, W[n][k] = e2m1 * e4m3 (exact) of one packed NVFP4 matrix.
+ *  x:        device bf16 [T][K], row-major; must not overlap y.
+ *  w_packed: device, moe_packed_bytes(N, K) bytes from moe_pack_nvfp4 with
+ *            kind MOE_PACK_PLAIN (row n of y is row n of W).
+ *  tscale:   the matrix's per-tensor fp32 scale (host value).
+ *  y:        device bf16 [T][N], row-major.
+ *  workspace: device, >= 256 bytes, zeroed once (moe_workspace_init on a
+ *            layer workspace, or a plain memset); only its device flag word
+ *            (read by moe_read_device_flag) is used, so a layer workspace
+ *            may be shared with this call when the two do not overlap.
+ * Arithmetic: as the decode layer's gate/up GEMV -- each token scaled by a
+ * power of two into f16 (exact for every element within 2^28 of the
+ * token's largest), e2m1 x f16 products exact in fp32 mma accumulation,
+ * the e4m3 block scale applied to each 16-column partial, the K partials
+ * added in a fixed order (deterministic, bit-identical between calls), the
+ * tensor scale and the power of two applied at the end, one rounding to
+ * bf16.  Activations must be finite with max|x[t]| < 2^114.
+ * One kernel, one CTA per SM (each CTA streams a contiguous range of 16-row
+ * bands), launched with programmatic dependent launch: it starts reading W
+ * while the preceding kernel finishes and waits for it only before reading x.
+ * So W must not be written by a kernel that may still be running when this
+ * call starts (one that signals programmatic completion early); the packing
+ * kernel of moe_pack_nvfp4 never does.
+ * Errors: MOE_ERR_INVALID_ARG (null or misaligned pointer, x and y overlap),
+ * MOE_ERR_UNSUPPORTED (T outside 1..MOE_MAX_DECODE_T, N not a positive
+ * multiple of 16, K not a multiple of 256 in 256..8192), MOE_ERR_WORKSPACE
+ * (workspace_bytes < 256), MOE_ERR_CUDA.
+ */
+moe_status moe_dense_gemv_nvfp4(const void *x, const void *w_packed, float tscale, int N, int K, int T,
+                                void *y, void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * The layer with expert-sink routing [INKLING, "MoE": 256 routed experts
+ * (top-6) plus 2 shared experts that take part in the routing-score
+ * computation, absorbing probability mass, but are never candidates for the
+ * top-6].  This library reads it as: router_w has E + S rows, the last S
+ * being the S shared experts'; every row's score is sigmoid(logit); the
+ * top_k are chosen among the E routed experts as in moe_layer_forward; with
+ * D = (sum of the selected scores) + (sum of the S shared scores), selected
+ * expert e gets the weight s_e / D and shared expert j the weight
+ * s_{E+j} / D:
+ *     out[t] = sum_i w[t][i] FFN_{sel_i}(x[t]) + sum_j sw[t][j] FFN_shared_j(x[t])
+ *  router_w: device bf16 [E + S][H].
+ *  shared:   host struct with n_experts S = 1 or 2, NVFP4 or BF16 (the routed
+ *            bank may be either type): run ahead of the layer kernel as in
+ *            moe_layer_forward.
+ *  The logits (all E + S per token, fp32 as in moe_layer_forward), the
+ *  selection and the denominator are computed in the layer kernel; the
+ *  fp32 denominator adds the selected scores in selection order, then the
+ *  shared ones in order.  moe_read_routing returns the routed part
+ *  (selection, weights, the E routed logits); moe_read_shared_weights the
+ *  shared experts' weights.
+ *  The other arguments are those of moe_layer_forward.
+ * Errors: as moe_layer_forward; MOE_ERR_INVALID_ARG without a shared expert;
+ * MOE_ERR_UNSUPPORTED for T > MOE_MAX_DECODE_T.
+ */
+moe_status moe_layer_forward_sink(const void *x, const void *router_w, const moe_expert_bank *routed,
+                                  const moe_expert_bank *shared, void *out, int T, void *workspace,
+                                  size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Copy out the weights of the shared experts that the last decode-path call
+ * on `workspace` with this T used: sw (device float [T][n_shared]) receives
+ * s_{E+j} / D per token for moe_layer_forward_sink, 1 for shared experts run
+ * ahead by moe_layer_forward.  Undefined unless such a call with S >= n_shared
+ * shared experts run ahead preceded it.  Enqueued device-to-device copy.
+ * Errors: MOE_ERR_INVALID_ARG (null or misaligned workspace, null sw),
+ * MOE_ERR_UNSUPPORTED (T outside 1..MOE_MAX_DECODE_T, n_shared outside 1..2),
+ * MOE_ERR_WORKSPACE (workspace_bytes below moe_workspace_bytes(T)), MOE_ERR_CUDA.
+ */
+moe_status moe_read_shared_weights(const void *workspace, size_t workspace_bytes, int T, int n_shared, float *sw,
+                                   moe_stream_t stream);
 
 /* ----------------------------------------------------------------------- */
 /* Decoder stacks.  [FLINT, "A 40B MoE that activates 2.5B parameters": a  */
@@ -327,7 +419,8 @@ typedef struct {
  *  resid_out:    device bf16 [T][H] receiving v, or NULL.
  *  xn_out:       device bf16 [T][H] receiving xn, or NULL.
  *  eps:          0 <= eps < 1.
- *  The other arguments are those of moe_layer_forward.
+ *  The other arguments are those of moe_layer_forward; the shared bank must
+ *  be one expert of the routed bank's type (MOE_ERR_UNSUPPORTED otherwise).
  *  out must not overlap resid, delta, resid_out or xn_out; resid_out and
  *  xn_out must not overlap any other buffer (MOE_ERR_INVALID_ARG).
  */
@@ -365,7 +458,7 @@ moe_status moe_stack_forward(void *x, const moe_layer_weights *layers, int n_lay
 
 /* Bytes of the library's fixed per-device scratch: the workspace of
  * moe_layer_forward at T = MOE_MAX_DECODE_T. */
-#define MOE_STATIC_SCRATCH_BYTES 7252480u
+#define MOE_STATIC_SCRATCH_BYTES 7400448u
 
 /*
  * moe_layer_forward with the workspace replaced by a fixed device array of

@@ -48,9 +48,10 @@ EXPORTS = (
     "moe_read_device_flag", "moe_workspace_recover", "moe_route", "moe_read_routing", "moe_layer_forward",
     "moe_layer_forward_static", "moe_static_read_device_flag",
     "moe_layer_forward_prenorm", "moe_stack_workspace_bytes", "moe_stack_forward",
+    "moe_dense_gemv_nvfp4", "moe_layer_forward_sink", "moe_read_shared_weights",
 )
 
-MOE_STATIC_SCRATCH_BYTES = 7_252_480
+MOE_STATIC_SCRATCH_BYTES = 7_400_448
 
 
 class MoeError(RuntimeError):
@@ -123,6 +124,12 @@ def _declare(lib):
     lib.moe_stack_forward.argtypes = [vp, ctypes.POINTER(moe_layer_weights), i32, i32, ctypes.c_float, vp, sz,
                                       vp]
     lib.moe_stack_forward.restype = i32
+    lib.moe_dense_gemv_nvfp4.argtypes = [vp, vp, ctypes.c_float, i32, i32, i32, vp, vp, sz, vp]
+    lib.moe_dense_gemv_nvfp4.restype = i32
+    lib.moe_layer_forward_sink.argtypes = [vp, vp, bank_p, bank_p, vp, i32, vp, sz, vp]
+    lib.moe_layer_forward_sink.restype = i32
+    lib.moe_read_shared_weights.argtypes = [vp, sz, i32, i32, vp, vp]
+    lib.moe_read_shared_weights.restype = i32
     return lib
 
 
@@ -304,3 +311,29 @@ def moe_stack_forward(x, layers_arr, n_layers: int, T: int, eps: float, workspac
     st = lib.moe_stack_forward(_ptr(x), layers_arr, int(n_layers), int(T), float(eps), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream))
     _check("moe_stack_forward", st)
+
+
+def moe_dense_gemv_nvfp4(x, w_packed, tscale: float, N: int, K: int, T: int, y, workspace, stream=None):
+    """y[T][N] (bf16) = W x for a packed NVFP4 matrix W [N][K] (MOE_PACK_PLAIN)."""
+    lib = load()
+    st = lib.moe_dense_gemv_nvfp4(_ptr(x), _ptr(w_packed), float(tscale), int(N), int(K), int(T), _ptr(y),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream))
+    _check("moe_dense_gemv_nvfp4", st)
+
+
+def moe_layer_forward_sink(x, router_w, routed: moe_expert_bank, shared: moe_expert_bank, out, T: int, workspace,
+                           stream=None):
+    """The layer with the shared experts as expert sinks (router_w [E + S][H])."""
+    lib = load()
+    st = lib.moe_layer_forward_sink(_ptr(x), _ptr(router_w), ctypes.byref(routed), ctypes.byref(shared), _ptr(out),
+                                    int(T), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream))
+    _check("moe_layer_forward_sink", st)
+
+
+def moe_read_shared_weights(workspace, T: int, n_shared: int, sw, stream=None):
+    lib = load()
+    st = lib.moe_read_shared_weights(_ptr(workspace), workspace.numel() * workspace.element_size(), int(T),
+                                     int(n_shared), _ptr(sw), _stream(stream))
+    _check("moe_read_shared_weights", st)

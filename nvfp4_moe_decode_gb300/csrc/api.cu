@@ -199,8 +199,16 @@ moe_status moe_read_routing(const void *workspace, size_t workspace_bytes, int T
         e = cudaMemcpyAsync(idx, ws + o_idx, (size_t)T * TOPK * 4, cudaMemcpyDeviceToDevice, st);
     if (e == cudaSuccess && w)
         e = cudaMemcpyAsync(w, ws + o_w, (size_t)T * TOPK * 4, cudaMemcpyDeviceToDevice, st);
-    if (e == cudaSuccess && logits)
-        e = cudaMemcpy2DAsync(logits, 4, ws + o_lg, lg_pitch, 4, (size_t)T * E, cudaMemcpyDeviceToDevice, st);
+    if (e == cudaSuccess && logits) {
+        if (T <= MAXT) {
+            // token t's row: E of its LE (launch tag, logit) words
+            for (int t = 0; t < T && e == cudaSuccess; ++t)
+                e = cudaMemcpy2DAsync(logits + (size_t)t * E, 4, ws + o_lg + (size_t)t * LE * 8, lg_pitch, 4, E,
+                                      cudaMemcpyDeviceToDevice, st);
+        } else {
+            e = cudaMemcpyAsync(logits, ws + o_lg, (size_t)T * E * 4, cudaMemcpyDeviceToDevice, st);
+        }
+    }
     return cuda_status(e);
 }
 
@@ -257,7 +265,8 @@ moe_status moe_route(const void *x, const void *router_w, int T, int n_experts, 
     return cuda_status(launch_router(a, (cudaStream_t)stream, true));
 }
 
-// Host checks of one layer's weights (nothing is launched).
+// Host checks of one layer's weights (nothing is launched): E routed
+// experts, and 0..MAX_EXT shared experts of either weight type.
 static moe_status check_layer_weights(const void *router_w, const moe_expert_bank *routed,
                                       const moe_expert_bank *shared)
 {
@@ -266,19 +275,75 @@ static moe_status check_layer_weights(const void *router_w, const moe_expert_ban
     moe_status s;
     if ((s = check_bank(routed, E, false)) != MOE_OK)
         return s;
-    if ((s = check_bank(shared, 1, true)) != MOE_OK)
+    const int ns = shared ? shared->n_experts : 0;
+    if (ns < 0 || ns > MAX_EXT)
+        return MOE_ERR_UNSUPPORTED;
+    if (ns > 0 && (s = check_bank(shared, ns, false)) != MOE_OK)
         return s;
-    if (shared && shared->n_experts > 0 && shared->wtype != routed->wtype)
-        return MOE_ERR_UNSUPPORTED;   // one weight type per layer
     return MOE_OK;
+}
+
+// The shared experts run ahead of the layer kernel on the dense GEMV (two
+// launches) when the kernel cannot take them as its own slot 0: expert
+// sinks, two of them, or another weight type than the routed bank.
+static bool shared_ahead(const moe_expert_bank *routed, const moe_expert_bank *shared, bool sink)
+{
+    const int ns = shared ? shared->n_experts : 0;
+    return ns > 0 && (sink || ns > MAX_SHARED || shared->wtype != routed->wtype);
+}
+
+// Gate/up (SiLU*up into the workspace's ext_h) and down (fp32 into ext_y) of
+// the shared experts for T <= MAXT tokens of x.
+static cudaError_t launch_shared_ahead(const void *x, const moe_expert_bank *shared, int T, uint8_t *ws,
+                                       int nsm, cudaStream_t st)
+{
+    const WsLayout L = ws_layout();
+    const bool bw = shared->wtype == MOE_W_BF16;
+    GemvArgs g{};
+    g.x = static_cast<const __nv_bfloat16 *>(x);
+    g.x_mat_stride = 0;
+    g.w = static_cast<const uint8_t *>(shared->w13);
+    g.w_mat_stride = bw ? W13_BYTES_BF : W13_BYTES;
+    g.ts_dev = bw ? nullptr : shared->tscale13;
+    g.N = 2 * I;
+    g.K = H;
+    g.T = T;
+    g.n_mat = shared->n_experts;
+    g.kind = MOE_PACK_GATE_UP;
+    g.bf16w = bw ? 1 : 0;
+    g.epi = GEMV_SILU_H;
+    g.y = ws + L.ext_h;
+    g.y_mat_stride = (size_t)MAXT * I;
+    g.flag = reinterpret_cast<uint32_t *>(ws + L.ctrl);
+    cudaError_t e = launch_gemv(g, nsm, st);
+    if (e != cudaSuccess)
+        return e;
+    g.x = reinterpret_cast<const __nv_bfloat16 *>(ws + L.ext_h);
+    g.x_mat_stride = (size_t)MAXT * I;
+    g.w = static_cast<const uint8_t *>(shared->w2);
+    g.w_mat_stride = bw ? W2_BYTES_BF : W2_BYTES;
+    g.ts_dev = bw ? nullptr : shared->tscale2;
+    g.N = H;
+    g.K = I;
+    g.kind = MOE_PACK_PLAIN;
+    g.epi = GEMV_OUT_F32;
+    g.y = ws + L.ext_y;
+    g.y_mat_stride = (size_t)MAXT * H;
+    return launch_gemv(g, nsm, st);
 }
 
 // Fill the layer kernel's arguments (weights, workspace, output); the
 // caller sets the input fields.
 static void fill_layer_args(LayerArgs &la, const void *router_w, const moe_expert_bank *routed,
-                            const moe_expert_bank *shared, void *out, int T, void *workspace)
+                            const moe_expert_bank *shared, void *out, int T, void *workspace, bool sink = false)
 {
-    const int n_shared = (shared && shared->n_experts > 0) ? 1 : 0;
+    const bool ahead = shared_ahead(routed, shared, sink);
+    const int n_shared = (!ahead && shared && shared->n_experts > 0) ? 1 : 0;
+    if (ahead) {
+        la.n_ext = shared->n_experts;
+        la.n_sink = sink ? shared->n_experts : 0;
+        la.ext_y = reinterpret_cast<const float *>(static_cast<uint8_t *>(workspace) + ws_layout().ext_y);
+    }
     la.wr = static_cast<const __nv_bfloat16 *>(router_w);
     la.T = T;
     la.r_w13 = static_cast<const uint8_t *>(routed->w13);
@@ -298,20 +363,34 @@ static void fill_layer_args(LayerArgs &la, const void *router_w, const moe_exper
 }
 
 // The decode layer kernel's CTAs wait on one another, so its whole grid (one
-// CTA per SM, at least 128 for the router phase) must be resident at once.
-// With rearm set, the workspace's re-arm kernel runs first (after every
-// host-side check has passed).
-static moe_status launch_layer_on_all_sms(const LayerArgs &la, cudaStream_t st, bool rearm = false)
+// CTA per SM, at least 128 for the router phase) must be resident at once:
+// the grid, or a status when that cannot hold (nothing is launched).
+static moe_status layer_grid(int &grid)
 {
     const int nsm = sm_count();
     if (nsm <= 0)
         return MOE_ERR_CUDA;
-    const int grid = nsm >= 128 ? nsm : 128;
+    grid = nsm >= 128 ? nsm : 128;
     const int per_sm = layer_resident_ctas_per_sm();
     if (per_sm < 0)
         return MOE_ERR_CUDA;
     if ((long)per_sm * nsm < grid)
         return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+// Launch the decode layer kernel on every SM (after layer_grid's checks).
+// With rearm set, the workspace's re-arm kernel runs first; with `shared`
+// (shared experts run ahead), their two dense GEMV launches before that.
+static moe_status launch_layer_on_all_sms(const LayerArgs &la, cudaStream_t st, bool rearm = false,
+                                          const moe_expert_bank *shared = nullptr)
+{
+    int grid = 0;
+    const moe_status s = layer_grid(grid);
+    if (s != MOE_OK)
+        return s;
+    if (shared && launch_shared_ahead(la.x, shared, la.T, la.ws, sm_count(), st) != cudaSuccess)
+        return MOE_ERR_CUDA;
     if (rearm && launch_rearm(la.ws, st, true) != cudaSuccess)
         return MOE_ERR_CUDA;
     return cuda_status(launch_layer(la, grid, st, true));
@@ -323,7 +402,7 @@ static moe_status launch_layer_on_all_sms(const LayerArgs &la, cudaStream_t st, 
 // kernel runs ahead of the layer kernel.
 moe_status moe::layer_forward(const void *x, const void *router_w, const moe_expert_bank *routed,
                               const moe_expert_bank *shared, void *out, int T, void *workspace,
-                              size_t workspace_bytes, cudaStream_t stream, bool rearm)
+                              size_t workspace_bytes, cudaStream_t stream, bool rearm, bool sink)
 {
     moe_status s = check_route_args(x, router_w, T, workspace, workspace_bytes);
     if (s != MOE_OK)
@@ -332,6 +411,13 @@ moe_status moe::layer_forward(const void *x, const void *router_w, const moe_exp
         return MOE_ERR_INVALID_ARG;
     if ((s = check_layer_weights(router_w, routed, shared)) != MOE_OK)
         return s;
+    const bool ahead = shared_ahead(routed, shared, sink);
+    if (sink && !ahead)
+        return MOE_ERR_INVALID_ARG;   // expert sinks need at least one shared expert
+    if (T > MAXT && ahead)
+        return MOE_ERR_UNSUPPORTED;   // the grouped path takes one shared expert of the routed type
+    if (ahead && !disjoint(out, x, (size_t)T * H * 2))
+        return MOE_ERR_INVALID_ARG;
     const int nsm = sm_count();
     if (nsm <= 0)
         return MOE_ERR_CUDA;
@@ -360,9 +446,9 @@ moe_status moe::layer_forward(const void *x, const void *router_w, const moe_exp
         return cuda_status(launch_grouped_layer(ga, nsm, (cudaStream_t)stream));
     }
     LayerArgs la{};
-    fill_layer_args(la, router_w, routed, shared, out, T, workspace);
+    fill_layer_args(la, router_w, routed, shared, out, T, workspace, sink);
     la.x = static_cast<const __nv_bfloat16 *>(x);
-    return launch_layer_on_all_sms(la, (cudaStream_t)stream, rearm);
+    return launch_layer_on_all_sms(la, (cudaStream_t)stream, rearm, ahead ? shared : nullptr);
 }
 
 extern "C" {
@@ -372,7 +458,30 @@ moe_status moe_layer_forward(const void *x, const void *router_w, const moe_expe
                              size_t workspace_bytes, moe_stream_t stream)
 {
     return layer_forward(x, router_w, routed, shared, out, T, workspace, workspace_bytes, (cudaStream_t)stream,
-                         false);
+                         false, false);
+}
+
+moe_status moe_layer_forward_sink(const void *x, const void *router_w, const moe_expert_bank *routed,
+                                  const moe_expert_bank *shared, void *out, int T, void *workspace,
+                                  size_t workspace_bytes, moe_stream_t stream)
+{
+    return layer_forward(x, router_w, routed, shared, out, T, workspace, workspace_bytes, (cudaStream_t)stream,
+                         false, true);
+}
+
+moe_status moe_read_shared_weights(const void *workspace, size_t workspace_bytes, int T, int n_shared, float *sw,
+                                   moe_stream_t stream)
+{
+    if (!workspace || !aligned16(workspace) || !sw)
+        return MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > MAXT || n_shared < 1 || n_shared > MAX_EXT)
+        return MOE_ERR_UNSUPPORTED;
+    if (workspace_bytes < moe_workspace_bytes(T))
+        return MOE_ERR_WORKSPACE;
+    const uint8_t *ws = static_cast<const uint8_t *>(workspace);
+    return cuda_status(cudaMemcpy2DAsync(sw, (size_t)n_shared * 4, ws + ws_layout().sinkw, MAX_EXT * 4,
+                                         (size_t)n_shared * 4, (size_t)T, cudaMemcpyDeviceToDevice,
+                                         (cudaStream_t)stream));
 }
 
 moe_status moe_layer_forward_prenorm(const void *resid, const void *delta, void *resid_out, void *xn_out,
@@ -403,6 +512,8 @@ moe_status moe_layer_forward_prenorm(const void *resid, const void *delta, void 
         return MOE_ERR_INVALID_ARG;
     if ((s = check_layer_weights(router_w, routed, shared)) != MOE_OK)
         return s;
+    if (shared_ahead(routed, shared, false))
+        return MOE_ERR_UNSUPPORTED;   // the pre-norm input exists only inside the layer kernel
     if (sm_count() <= 0)
         return MOE_ERR_CUDA;
     LayerArgs la{};
@@ -439,9 +550,13 @@ moe_status moe_stack_forward(void *x, const moe_layer_weights *layers, int n_lay
     if (!(eps >= 0.0f) || !(eps < 1.0f))
         return MOE_ERR_INVALID_ARG;
     moe_status s;
-    for (int l = 0; l < n_layers; ++l)
-        if ((s = check_layer_weights(layers[l].router_w, &layers[l].routed, &layers[l].shared)) != MOE_OK)
+    for (int l = 0; l < n_layers; ++l) {
+        s = check_layer_weights(layers[l].router_w, &layers[l].routed, &layers[l].shared);
+        if (s == MOE_OK && shared_ahead(&layers[l].routed, &layers[l].shared, false))
+            s = MOE_ERR_UNSUPPORTED;   // a layer's shared expert must fit the layer kernel's slot 0
+        if (s != MOE_OK)
             return s;
+    }
     if (sm_count() <= 0)
         return MOE_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;
@@ -476,6 +591,42 @@ moe_status moe_stack_forward(void *x, const moe_layer_weights *layers, int n_lay
     // x_L = x_{L-1} + D[(L-1)&1]
     const __nv_bfloat16 *last = (n_layers == 1) ? x0 : R[(n_layers - 1) & 1];
     return cuda_status(launch_residual_add(last, D[(n_layers - 1) & 1], x0, T * H, st, true));
+}
+
+}  // extern "C"
+
+extern "C" {
+
+moe_status moe_dense_gemv_nvfp4(const void *x, const void *w_packed, float tscale, int N, int K, int T, void *y,
+                                void *workspace, size_t workspace_bytes, moe_stream_t stream)
+{
+    if (!x || !w_packed || !y || !workspace || !aligned16(x) || !aligned16(w_packed) || !aligned16(y) ||
+        !aligned16(workspace))
+        return MOE_ERR_INVALID_ARG;
+    if (T < 1 || T > MAXT || N < 16 || N % 16 != 0 || K < 256 || K % 256 != 0 || K > GEMV_MAX_K)
+        return MOE_ERR_UNSUPPORTED;
+    if (workspace_bytes < 256)
+        return MOE_ERR_WORKSPACE;
+    const uintptr_t px = (uintptr_t)x, py = (uintptr_t)y;
+    if (px < py + (size_t)T * N * 2 && py < px + (size_t)T * K * 2)
+        return MOE_ERR_INVALID_ARG;
+    const int nsm = sm_count();
+    if (nsm <= 0)
+        return MOE_ERR_CUDA;
+    GemvArgs ga{};
+    ga.x = static_cast<const __nv_bfloat16 *>(x);
+    ga.w = static_cast<const uint8_t *>(w_packed);
+    ga.ts_host = tscale;
+    ga.N = N;
+    ga.K = K;
+    ga.T = T;
+    ga.n_mat = 1;
+    ga.kind = MOE_PACK_PLAIN;
+    ga.bf16w = 0;
+    ga.epi = GEMV_OUT_BF16;
+    ga.y = y;
+    ga.flag = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + ws_layout().ctrl);
+    return cuda_status(launch_gemv(ga, nsm, (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -49,8 +49,13 @@ constexpr int I = MOE_INTER;             // 512
 constexpr int E = MOE_EXPERTS;           // 256
 constexpr int TOPK = MOE_TOPK;           // 6
 constexpr int MAXT = MOE_MAX_DECODE_T;   // 8
-constexpr int MAX_SHARED = 1;
+constexpr int MAX_SHARED = 1;                        // shared experts inside the layer kernel
 constexpr int MAX_SLOTS = MAX_SHARED + MAXT * TOPK;  // 49
+// Shared experts computed ahead of the layer kernel by the dense GEMV (two
+// at most: a pair of expert sinks, or shared experts of another weight type
+// than the routed bank); their router rows follow the routed ones.
+constexpr int MAX_EXT = 2;
+constexpr int LE = E + MAX_EXT;                      // router rows the tagged logits have room for
 
 __host__ __device__ constexpr size_t band_bytes(int K) { return (size_t)9 * K; }
 constexpr int W13_BANDS = 2 * I / 16;                       // 64
@@ -81,7 +86,7 @@ struct WsLayout {
     size_t ctrl;       // u32[64]: [0] device flag, [1] routing-kernel arrivals,
                        //   [4] layer-kernel CTAs that have read the launch tag, [5] layer-kernel launches
     size_t logits;     // f32[MAXT][E]
-    size_t tlogits;    // u64[MAXT][E]: layer kernel, (launch tag << 32) | fp32 logit bits
+    size_t tlogits;    // u64[MAXT][LE]: layer kernel, (launch tag << 32) | fp32 logit bits
     size_t topk_idx;   // i32[MAXT][TOPK]
     size_t topk_w;     // f32[MAXT][TOPK]
     size_t slots;      // SlotTable
@@ -89,6 +94,9 @@ struct WsLayout {
                        //   values of h rows 8 b + 2 w (low half) and 8 b + 2 w + 1 of token t
     size_t ptag;       // u64[MAX_SLOTS][W2_BANDS][16][MAXT]: (launch tag << 32) | fp32 weighted
                        //   down output of row 16 b + r, token t
+    size_t ext_h;      // bf16[MAX_EXT][MAXT][I]: SiLU*up of the shared experts run ahead
+    size_t ext_y;      // f32[MAX_EXT][MAXT][H]: their down outputs (unweighted)
+    size_t sinkw;      // f32[MAXT][MAX_EXT]: the weight of each of them per token
     size_t total;
 };
 
@@ -107,12 +115,15 @@ __host__ __device__ inline WsLayout ws_layout()
     size_t o = 0;
     L.ctrl = o;      o = align256(o + 64 * 4);
     L.logits = o;    o = align256(o + (size_t)MAXT * E * 4);
-    L.tlogits = o;   o = align256(o + (size_t)MAXT * E * 8);
+    L.tlogits = o;   o = align256(o + (size_t)MAXT * LE * 8);
     L.topk_idx = o;  o = align256(o + (size_t)MAXT * TOPK * 4);
     L.topk_w = o;    o = align256(o + (size_t)MAXT * TOPK * 4);
     L.slots = o;     o = align256(o + sizeof(SlotTable));
     L.htag = o;      o = align256(o + (size_t)MAX_SLOTS * W13_BANDS * MAXT * 4 * 8);
     L.ptag = o;      o = align256(o + (size_t)MAX_SLOTS * W2_BANDS * 16 * MAXT * 8);
+    L.ext_h = o;     o = align256(o + (size_t)MAX_EXT * MAXT * I * 2);
+    L.ext_y = o;     o = align256(o + (size_t)MAX_EXT * MAXT * H * 4);
+    L.sinkw = o;     o = align256(o + (size_t)MAXT * MAX_EXT * 4);
     L.total = o;
     return L;
 }

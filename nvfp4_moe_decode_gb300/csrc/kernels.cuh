@@ -60,7 +60,14 @@ struct LayerArgs {
     const uint8_t *s_w13, *s_w2;   // shared expert (same weight type), if n_shared
     const float *s_ts13, *s_ts2;   // NVFP4 only
     int n_shared;
-    int bf16w;                     // 1: both banks hold bf16 weights
+    int bf16w;                     // 1: the routed bank (and an inside shared expert) holds bf16 weights
+    // shared experts run ahead by the dense GEMV: n_ext (0..MAX_EXT) down
+    // outputs in ext_y, added in the combine with weight 1, or, when they are
+    // expert sinks (n_sink = n_ext), their sigmoid score over the
+    // denominator, which their router rows E.. join
+    int n_ext;
+    int n_sink;
+    const float *ext_y;            // f32 [MAX_EXT][MAXT][H]
     // pre-norm mode (a layer of a decoder stack): the input is
     // RMSNorm(bf16(x + delta)); x is the residual stream, delta (may be null)
     // the previous layer's output; resid_out / xn_out (may be null) receive
@@ -94,6 +101,39 @@ struct DequantArgs {
     int N, K, kind;
     float tscale;
 };
+
+// ---------------------------------------------------------------------------
+// Dense small-batch GEMV (T <= MAXT): see gemv.cu.
+// ---------------------------------------------------------------------------
+enum GemvEpi {
+    GEMV_OUT_BF16 = 0,   // y[m][t][n] = bf16(sum)
+    GEMV_OUT_F32 = 1,    // y[m][t][n] = sum (fp32)
+    GEMV_SILU_H = 2,     // GATE_UP bands: y[m][t][i] = bf16(silu(gate_i) * up_i), i < N / 2
+};
+constexpr int GEMV_MAX_K_RW4 = 4096;   // four ring stages per warp up to here
+constexpr int GEMV_MAX_K = 8192;       // two beyond (the B fragments take 16 K bytes of shared memory)
+
+struct GemvArgs {
+    const __nv_bfloat16 *x;        // [n_mat][T][K] (x_mat_stride elements apart; 0: one x for all)
+    size_t x_mat_stride;
+    const uint8_t *w;              // n_mat matrices, w_mat_stride bytes apart: packed NVFP4 or bf16 [N][K]
+    size_t w_mat_stride;
+    const float *ts_dev;           // NVFP4: per-matrix tensor scales on the device, or null (ts_host)
+    float ts_host;
+    int N, K, T, n_mat;
+    int kind;                      // MOE_PACK_PLAIN or MOE_PACK_GATE_UP (band rows)
+    int bf16w;
+    int epi;                       // GemvEpi
+    void *y;                       // output, y_mat_stride elements apart
+    size_t y_mat_stride;
+    uint32_t *flag;                // device flag word
+    int q;                         // set by launch_gemv: warps per band
+    int ctas_per_mat;              // set by launch_gemv
+};
+
+// Warps per band for a CTA holding `bands_per_cta` bands of `stages` stages.
+int gemv_warps_per_band(int bands_per_cta, int stages);
+cudaError_t launch_gemv(GemvArgs a, int sm_count, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Grouped path (T > MAXT): see grouped.cu.
@@ -176,11 +216,12 @@ size_t layer_smem_bytes();
 int layer_resident_ctas_per_sm();
 // Re-arm a decode workspace after a wait timeout (see moe_workspace_recover).
 cudaError_t launch_rearm(uint8_t *ws, cudaStream_t stream, bool pdl);
-// moe_layer_forward; with rearm, a decode call first enqueues launch_rearm
-// on its workspace (after all host-side checks).
+// moe_layer_forward (sink: moe_layer_forward_sink); with rearm, a decode
+// call first enqueues launch_rearm on its workspace (after all host-side
+// checks).
 moe_status layer_forward(const void *x, const void *router_w, const moe_expert_bank *routed,
                          const moe_expert_bank *shared, void *out, int T, void *workspace, size_t workspace_bytes,
-                         cudaStream_t stream, bool rearm);
+                         cudaStream_t stream, bool rearm, bool sink = false);
 
 cudaError_t launch_router(const RouterArgs &a, cudaStream_t stream, bool pdl);
 cudaError_t launch_layer(const LayerArgs &a, int grid, cudaStream_t stream, bool pdl);

@@ -54,6 +54,7 @@
 // columns copied by per-lane cp.async into a swizzled ring slot.
 // Every wait is bounded and reports MOE_FLAG_WAIT_TIMEOUT instead of hanging.
 #include "kernels.cuh"
+#include "stage.cuh"
 #include "topk.cuh"
 
 namespace moe {
@@ -109,15 +110,8 @@ struct FSmem {
     uint32_t hready[NHB];              // h warps done with the buffer (2 when ready)
     float4 comb[FW][32];               // the final sum of band cta: per-warp sums of every 16th slot
     float hmax[NHB][2][MAXT];          // per h warp, each token's max |h| over its half of a slot
+    float extw[MAX_EXT][MAXT];         // weight of each shared expert run ahead, per token
 };
-
-__device__ __forceinline__ float pow2i(int k) { return __int_as_float((127 + k) << 23); }
-
-__device__ __forceinline__ int act_shift(float maxabs)
-{
-    int sh = ACT_EXP - exponent_of(maxabs);
-    return sh < -100 ? -100 : (sh > 100 ? 100 : sh);
-}
 
 __device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acquire.gpu;" ::: "memory"); }
 
@@ -161,114 +155,6 @@ __device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t *p)
     uint32_t v;
     asm volatile("ld.acquire.cta.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
-}
-
-__device__ __forceinline__ void ffma2(float &a0, float &a1, float s, float d0, float d1)
-{
-    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %2};\n\tmov.b64 y, {%3, %4};\n\t"
-        "mov.b64 z, {%0, %1};\n\tfma.rn.f32x2 z, x, y, z;\n\tmov.b64 {%0, %1}, z;\n\t}"
-        : "+f"(a0), "+f"(a1) : "f"(s), "f"(d0), "f"(d1));
-}
-
-__device__ __forceinline__ void decode4(uint32_t w, uint32_t &a0, uint32_t &a1, uint32_t &a2, uint32_t &a3)
-{
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-        : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3) : "r"(w));
-}
-
-// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32.
-__device__ __forceinline__ void mma_bf16_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// BF16 rows are consumed in a k order chosen so that each lane's A registers
-// come from two 16-byte words per row and 64-column chunk: lane
-// (g, c) loads columns 8c..8c+7 and 32+8c..32+8c+7 of rows g and g+8, and k16
-// step s of the chunk pairs its words 2s, 2s+1 with the activation columns
-// 32*(s/2) + 8c + 4*(s%2) + 0..3 (a permutation of the chunk's 64 columns,
-// applied to both operands, so the dot products are unchanged).
-__host__ __device__ __forceinline__ int bf16_bcol(int step, int c)
-{
-    const int s = step & 3;
-    return 64 * (step >> 2) + 32 * (s >> 1) + 8 * c + 4 * (s & 1);
-}
-
-// One 64-column chunk of a BF16 band in a ring stage (16 rows x 128 bytes,
-// 16-byte unit u of row r at position u ^ 4 (r & 1), so the reads below are
-// free of bank conflicts) times the B fragments of k16 steps step0 ..
-// step0 + 3.  Lane (g, c) takes units c and 4 + c of rows g and g + 8.
-__device__ __forceinline__ void bf16_stage(const uint8_t *stage, const uint2 *bfrag, int step0, int lane,
-                                           float acc[4])
-{
-    const int g = lane >> 2, c = lane & 3, sw = 4 * (g & 1);
-    const uint8_t *ra = stage + g * 128, *rb = stage + (g + 8) * 128;
-    const uint4 a0 = *reinterpret_cast<const uint4 *>(ra + 16 * (c ^ sw));
-    const uint4 a1 = *reinterpret_cast<const uint4 *>(ra + 16 * ((4 + c) ^ sw));
-    const uint4 b0 = *reinterpret_cast<const uint4 *>(rb + 16 * (c ^ sw));
-    const uint4 b1 = *reinterpret_cast<const uint4 *>(rb + 16 * ((4 + c) ^ sw));
-    const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-        const int step = step0 + s;
-        const uint2 b = bfrag[step * 32 + lane];
-        mma_bf16_16816(acc, wa[2 * s], wb[2 * s], wa[2 * s + 1], wb[2 * s + 1], b.x, b.y);
-    }
-}
-
-// 16-byte global -> shared copy that skips L1, and an arrival on an mbarrier
-// once all of this thread's earlier copies have landed.
-__device__ __forceinline__ void cp_async_cg16(void *dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// Two consecutive super-chunks of one band (one stage) times the B fragments
-// from k16 step `step0`.  The fragments of a step fill all 32 lanes (lanes
-// 4T.. hold zeros), so every lane loads unconditionally: a predicated load
-// here cost the loop 18% when measured alone.
-__device__ __forceinline__ void mma_stage(const uint8_t *stage, const uint2 *bfrag, int step0, int lane,
-                                          float acc[4])
-{
-    const int g = lane >> 2;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        const uint8_t *base = stage + q * SC_BYTES;
-        const uint4 sc = *reinterpret_cast<const uint4 *>(base + 1024 + g * 16);
-        const uint32_t sws[4] = {sc.x, sc.y, sc.z, sc.w};
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const uint4 cw = *reinterpret_cast<const uint4 *>(base + half * 512 + lane * 16);
-            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const int step = step0 + q * 8 + half * 4 + s;
-                const uint2 b = bfrag[step * 32 + lane];
-                uint32_t a0, a1, a2, a3;
-                decode4(words[s], a0, a1, a2, a3);
-                float d[4];
-                mma_f16_16816(d, a0, a1, a2, a3, b.x, b.y);
-                const int sb = half * 4 + s;
-                const uint32_t sw = sws[sb >> 1];
-                const float2 sf = e4m3x2_to_float2((sb & 1) ? (sw >> 16) : (sw & 0xFFFFu));
-                ffma2(acc[0], acc[1], sf.x, d[0], d[1]);
-                ffma2(acc[2], acc[3], sf.y, d[2], d[3]);
-            }
-        }
-    }
 }
 
 // The same with the B fragments of the warp's own 256-column K slice held in
@@ -416,12 +302,14 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         }
     }
     // router CTAs: warp w of the 16 takes expert 2 * cta + w / 8, columns
-    // [256 (w % 8), 256 (w % 8) + 256), eight per lane
-    const bool router_warp = cta < ROUTER_CTAS && warp < FW;
+    // [256 (w % 8), 256 (w % 8) + 256), eight per lane; CTA 128 takes the
+    // router rows of the expert sinks (experts 256, 257)
+    const int n_rows = E + a.n_sink;
+    const bool router_warp = (cta < ROUTER_CTAS || (cta == ROUTER_CTAS && a.n_sink > 0)) && warp < FW;
     const int r_e = cta * 2 + (warp >> 3);
     const int r_k8 = warp & 7;
     uint4 wv = make_uint4(0u, 0u, 0u, 0u);
-    if (router_warp)
+    if (router_warp && r_e < n_rows)
         wv = ldg_nc_v4(a.wr + (size_t)r_e * H + 256 * r_k8 + 8 * lane);
 
     griddep_wait();      // x is written by the preceding kernel; the counters are re-armed
@@ -537,8 +425,8 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         float logit;
         // each logit carries the launch tag in the same 64-bit word, so a
         // reader that sees the tag sees the logit: no fence, no counter
-        if (router_reduce(acc, (int)threadIdx.x, T, sm.rred, 5, &logit))
-            st_relaxed_u64(&tlogits[(threadIdx.x % MAXT) * E + cta * 2 + threadIdx.x / MAXT],
+        if (router_reduce(acc, (int)threadIdx.x, T, sm.rred, 5, &logit) && cta * 2 + (int)threadIdx.x / MAXT < n_rows)
+            st_relaxed_u64(&tlogits[(threadIdx.x % MAXT) * LE + cta * 2 + threadIdx.x / MAXT],
                            ((unsigned long long)ltag << 32) | __float_as_uint(logit));
         fence_proxy_async();   // these generic writes precede the bulk copies of h into the same buffer
     }
@@ -601,9 +489,10 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
 
     __syncthreads();
     if (warp < T) {
-        // the token's 256 logits, re-read until every one carries this launch's tag
-        const unsigned long long *row = tlogits + warp * E;
-        float v[8];
+        // the token's 256 logits (and its sink logits, lanes < n_sink),
+        // re-read until every one carries this launch's tag
+        const unsigned long long *row = tlogits + warp * LE;
+        float v[8], sv = 0.0f;
         bool have = false;
         for (uint32_t it = 0;; ++it) {
             have = true;
@@ -611,6 +500,11 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             for (int m = 0; m < 8; ++m) {
                 const unsigned long long w = ld_relaxed_u64(row + lane + 32 * m);
                 v[m] = __uint_as_float((uint32_t)w);
+                have = have && (uint32_t)(w >> 32) == ltag;
+            }
+            if (lane < a.n_sink) {
+                const unsigned long long w = ld_relaxed_u64(row + E + lane);
+                sv = __uint_as_float((uint32_t)w);
                 have = have && (uint32_t)(w >> 32) == ltag;
             }
             if (__all_sync(0xFFFFFFFFu, have))
@@ -623,14 +517,17 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             __nanosleep(32);
         }
         int ex;
-        float wt;
+        float wt, swt;
         bool bad;
-        warp_route_values(v, lane, ex, wt, bad);
+        warp_route_values_t<true>(v, lane, ex, wt, bad, sv, a.n_sink, swt);
         if (lane < TOPK) {
             sm.sel[warp][lane] = ex;
             sm.selw[warp][lane] = wt;
             atomicOr(&sm.bitmap[ex >> 5], 1u << (ex & 31));
         }
+        // the shared experts run ahead: a sink's weight, else 1
+        if (lane < a.n_ext)
+            sm.extw[lane][warp] = a.n_sink ? swt : 1.0f;
         if (blockIdx.x == 0) {
             if (bad && lane == 0)
                 atomicOr(flag, FLAG_NONFINITE);
@@ -638,6 +535,8 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                 reinterpret_cast<int32_t *>(a.ws + L.topk_idx)[warp * TOPK + lane] = ex;
                 reinterpret_cast<float *>(a.ws + L.topk_w)[warp * TOPK + lane] = wt;
             }
+            if (lane < a.n_ext)
+                reinterpret_cast<float *>(a.ws + L.sinkw)[warp * MAX_EXT + lane] = a.n_sink ? swt : 1.0f;
         }
     }
     __syncthreads();
@@ -1092,7 +991,16 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                     const float4 v = sm.comb[w][lane];
                     tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
                 }
-                const float vals[4] = {tot.x, tot.y, tot.z, tot.w};
+                float vals[4] = {tot.x, tot.y, tot.z, tot.w};
+                // the shared experts run ahead, in order, after the slots
+                for (int j = 0; j < a.n_ext; ++j)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int t = 4 * th + jj;
+                        if (t < T)
+                            vals[jj] = fmaf(sm.extw[j][t],
+                                            __ldcg(a.ext_y + ((size_t)j * MAXT + t) * H + 16 * band + r), vals[jj]);
+                    }
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     const int t = 4 * th + jj;

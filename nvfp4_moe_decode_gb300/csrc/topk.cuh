@@ -51,7 +51,13 @@ __device__ __forceinline__ void cx_desc(unsigned long long &a, unsigned long lon
 // warp-wide max reductions (redux.sync, on the high then the low 32 bits of
 // the lanes' best remaining keys) find the best remaining key, which is
 // unique, and its owner drops it from the head of its list.
-__device__ __forceinline__ void warp_route_values(const float v[8], int lane, int &ex, float &wt, bool &nonfinite)
+// SINK: lanes j < n_sink also hold the logit of expert sink j (a shared
+// expert that joins the normalisation but is never selected; TML Inkling
+// page, section "MoE"): its sigmoid is added to the denominator after the
+// selected ones (sink order), and swt of lane j receives its weight.
+template <bool SINK>
+__device__ __forceinline__ void warp_route_values_t(const float v[8], int lane, int &ex, float &wt, bool &nonfinite,
+                                                    float sink_v, int n_sink, float &swt)
 {
     unsigned long long k[8];
     bool bad = false;
@@ -60,6 +66,8 @@ __device__ __forceinline__ void warp_route_values(const float v[8], int lane, in
         bad |= !isfinite(v[m]);
         k[m] = rank_key(v[m], lane + 32 * m);
     }
+    if (SINK && lane < n_sink)
+        bad |= !isfinite(sink_v);
     nonfinite = __any_sync(0xFFFFFFFFu, bad);
     cx_desc(k[0], k[2]); cx_desc(k[1], k[3]); cx_desc(k[4], k[6]); cx_desc(k[5], k[7]);
     cx_desc(k[0], k[4]); cx_desc(k[1], k[5]); cx_desc(k[2], k[6]); cx_desc(k[3], k[7]);
@@ -89,8 +97,21 @@ __device__ __forceinline__ void warp_route_values(const float v[8], int lane, in
 #pragma unroll
     for (int i = 0; i < TOPK; ++i)
         sum += __shfl_sync(0xFFFFFFFFu, s, i);
+    float ss = 0.0f;
+    if (SINK) {
+        ss = lane < n_sink ? 1.0f / (1.0f + expf(-sink_v)) : 0.0f;
+        for (int j = 0; j < n_sink; ++j)
+            sum += __shfl_sync(0xFFFFFFFFu, ss, j);
+    }
     ex = lane < TOPK ? key_expert(chosen) : 0;
     wt = lane < TOPK ? s / sum : 0.0f;
+    swt = SINK && lane < n_sink ? ss / sum : 0.0f;
+}
+
+__device__ __forceinline__ void warp_route_values(const float v[8], int lane, int &ex, float &wt, bool &nonfinite)
+{
+    float unused;
+    warp_route_values_t<false>(v, lane, ex, wt, nonfinite, 0.0f, 0, unused);
 }
 
 // The same, reading the token's logits row from global memory (L2).

@@ -92,10 +92,32 @@ def test_host_argument_errors_enqueue_nothing(moe_lib):
     assert fwd(dummy, dummy, B(bad_w), None, dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_UNSUPPORTED
     assert fwd(dummy, dummy, B(null_w), None, dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_INVALID_ARG
     assert fwd(dummy, dummy, None, None, dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_INVALID_ARG
-    # one weight type per layer: a BF16 routed bank with an NVFP4 shared expert
+    # a shared bank of the other weight type runs ahead on the dense GEMV, on
+    # the decode path only
     bf = m.moe_expert_bank(m.MOE_W_BF16, 256, dummy, dummy, None, None)
     sh4 = m.moe_expert_bank(m.MOE_W_NVFP4, 1, dummy, dummy, dummy, dummy)
-    assert fwd(dummy, dummy, B(bf), B(sh4), dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_UNSUPPORTED
+    ws9 = m.moe_workspace_bytes(9)
+    assert fwd(dummy, dummy, B(bf), B(sh4), dummy * 2, 9, dummy, ws9, None) == m.MOE_ERR_UNSUPPORTED
+    # up to two shared experts; expert sinks need one, and the decode path
+    sh2 = m.moe_expert_bank(m.MOE_W_BF16, 2, dummy, dummy, None, None)
+    sh3 = m.moe_expert_bank(m.MOE_W_BF16, 3, dummy, dummy, None, None)
+    assert fwd(dummy, dummy, B(bank), B(sh3), dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_UNSUPPORTED
+    assert fwd(dummy, dummy, B(bank), B(sh2), dummy * 2, 9, dummy, ws9, None) == m.MOE_ERR_UNSUPPORTED
+    snk = lib.moe_layer_forward_sink
+    assert snk(dummy, dummy, B(bank), None, dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_INVALID_ARG
+    assert snk(dummy, dummy, B(bank), B(sh3), dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_UNSUPPORTED
+    assert snk(dummy, dummy, B(bank), B(sh2), dummy * 2, 9, dummy, ws9, None) == m.MOE_ERR_UNSUPPORTED
+    assert snk(dummy, dummy, B(bank), B(sh2), dummy, 1, dummy, ws, None) == m.MOE_ERR_INVALID_ARG  # out aliases x
+    rsw = lib.moe_read_shared_weights
+    assert rsw(None, ws, 1, 2, dummy, None) == m.MOE_ERR_INVALID_ARG
+    assert rsw(dummy, ws, 1, 2, None, None) == m.MOE_ERR_INVALID_ARG
+    assert rsw(dummy, ws9, 9, 2, dummy, None) == m.MOE_ERR_UNSUPPORTED
+    assert rsw(dummy, ws, 1, 3, dummy, None) == m.MOE_ERR_UNSUPPORTED
+    assert rsw(dummy, 64, 1, 2, dummy, None) == m.MOE_ERR_WORKSPACE
+    # the pre-norm layer takes its shared expert inside the layer kernel only
+    pre = lib.moe_layer_forward_prenorm
+    assert pre(dummy, None, None, None, 1e-6, dummy, B(bank), B(sh2), dummy * 2, 1, dummy, ws,
+               None) == m.MOE_ERR_UNSUPPORTED
     bf_null = m.moe_expert_bank(m.MOE_W_BF16, 256, dummy, None, None, None)
     assert fwd(dummy, dummy, B(bf_null), None, dummy * 2, 1, dummy, ws, None) == m.MOE_ERR_INVALID_ARG
     assert lib.moe_workspace_init(None, ws, None) == m.MOE_ERR_INVALID_ARG
@@ -112,6 +134,17 @@ def test_host_argument_errors_enqueue_nothing(moe_lib):
     assert rr(dummy, ws, 0, dummy, None, None, None) == m.MOE_ERR_UNSUPPORTED
     assert rr(dummy, ws, m.MAX_TOKENS + 1, dummy, None, None, None) == m.MOE_ERR_UNSUPPORTED
     assert rr(dummy, ws, 8192, dummy, None, None, None) == m.MOE_ERR_WORKSPACE
+    # dense GEMV: T, N, K outside the supported set, aliasing, small workspace
+    gv = lib.moe_dense_gemv_nvfp4
+    assert gv(dummy, dummy, 1.0, 2048, 2048, 9, dummy * 2, dummy, 256, None) == m.MOE_ERR_UNSUPPORTED
+    assert gv(dummy, dummy, 1.0, 2048, 2048, 0, dummy * 2, dummy, 256, None) == m.MOE_ERR_UNSUPPORTED
+    assert gv(dummy, dummy, 1.0, 24, 2048, 1, dummy * 2, dummy, 256, None) == m.MOE_ERR_UNSUPPORTED
+    assert gv(dummy, dummy, 1.0, 2048, 384, 1, dummy * 2, dummy, 256, None) == m.MOE_ERR_UNSUPPORTED
+    assert gv(dummy, dummy, 1.0, 2048, 8448, 1, dummy * 2, dummy, 256, None) == m.MOE_ERR_UNSUPPORTED
+    assert gv(dummy, dummy, 1.0, 2048, 2048, 1, dummy + 64, dummy, 256, None) == m.MOE_ERR_INVALID_ARG
+    assert gv(dummy, dummy, 1.0, 2048, 2048, 1, dummy * 2, dummy, 255, None) == m.MOE_ERR_WORKSPACE
+    assert gv(None, dummy, 1.0, 2048, 2048, 1, dummy * 2, dummy, 256, None) == m.MOE_ERR_INVALID_ARG
+    assert gv(dummy, dummy + 8, 1.0, 2048, 2048, 1, dummy * 2, dummy, 256, None) == m.MOE_ERR_INVALID_ARG
     # the no-allocation variant rejects T beyond its scratch before any CUDA call
     fs = lib.moe_layer_forward_static
     assert fs(dummy, dummy, B(bank), None, dummy * 2, 9, None) == m.MOE_ERR_UNSUPPORTED
