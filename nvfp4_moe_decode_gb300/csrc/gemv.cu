@@ -20,9 +20,12 @@
 // before the wait on the preceding kernel (the weights do not depend on it).
 // A round's Q partials of a band meet in a shared-memory buffer and the
 // epilogue warp adds them in warp order (deterministic), scales and stores.
-// x enters as mma B fragments in shared memory, built once per CTA: NVFP4,
-// f16 after the exact per-token power-of-two rescale (common.cuh); BF16, bf16
-// in the column order of bf16_bcol.
+// x enters shared memory once per CTA by whole-row bulk copies, rows 16
+// bytes apart so that the fragment loads of the 32 lanes hit 32 banks (a
+// tensor-map box of 32-byte pieces, or 16-byte loads by every thread, took
+// several times longer for the same bytes); NVFP4 converts it in place to
+// f16 after the exact per-token power-of-two rescale (common.cuh), BF16 uses
+// the bf16 words as they are.
 // Every wait is bounded and reports MOE_FLAG_WAIT_TIMEOUT instead of hanging.
 #include "kernels.cuh"
 #include "stage.cuh"
@@ -37,21 +40,27 @@ constexpr int GSTG = 2 * SC_BYTES;      // ring slot: one NVFP4 stage (a BF16 st
 
 template <int RW>
 struct GSmem {
-    uint8_t ring[GW][RW][GSTG];
+    uint8_t ring[RW][GW][GSTG];
     float4 red[2][GW][32];              // a round's partials (round r uses r % 2)
     uint64_t full[GW][RW];
     uint64_t pfull[2];                  // all 16 warps stored their round-r partials
     uint64_t pempty[2];                 // the epilogue warp has read them
+    uint64_t xbar;                      // x has landed
     float xinv[MAXT];                   // NVFP4: 2^-xshift[t]
-    float hmx[MAXT][2];                 // NVFP4: max |x| of each half of a token's row
-    uint2 xfrag[1];                     // [K / 16][32]: B fragments (extends past the struct)
+    uint32_t xmax[MAXT];                // NVFP4: max |x| of each token (fp32 bits)
+    alignas(128) uint32_t xs[1];        // x row-major, 8 rows 2 K + 16 bytes apart (extends past the struct)
 };
 
 template <int RW>
 constexpr size_t gsmem_bytes(int K)
 {
-    return offsetof(GSmem<RW>, xfrag) + (size_t)K * 16;
+    return offsetof(GSmem<RW>, xs) + (size_t)MAXT * (2 * K + 16);
 }
+
+// Ring stages issued before the wait on the preceding kernel (the weights do
+// not depend on it): about what lands during that wait; the rest follow x's
+// copy so that x does not queue behind them.
+constexpr int PRE = 1;
 
 template <bool BW, int RW>
 __global__ void __launch_bounds__(GNT, 1) dense_gemv_kernel(GemvArgs a)
@@ -78,6 +87,10 @@ __global__ void __launch_bounds__(GNT, 1) dense_gemv_kernel(GemvArgs a)
         mbar_init(&sm.pfull[threadIdx.x], GW);
         mbar_init(&sm.pempty[threadIdx.x], 1);
     }
+    if (threadIdx.x == 0)
+        mbar_init(&sm.xbar, 1);
+    if (threadIdx.x < MAXT)
+        sm.xmax[threadIdx.x] = 0u;
     if (lane == 0)
         fence_barrier_init();
     __syncthreads();
@@ -92,6 +105,7 @@ __global__ void __launch_bounds__(GNT, 1) dense_gemv_kernel(GemvArgs a)
         const int r = i / per, s = s0 + i % per;
         const int band = b0 + G * r + g;
         uint64_t *bar = &sm.full[warp][rs];
+        uint8_t *slot = sm.ring[rs][warp];
         if (BW) {
             // rows of the band (GATE_UP: 8 gate rows 8 band.. and the matching
             // up rows), columns 64 s ..; lane 2 rr + h copies bytes [64 h, 64 h
@@ -100,7 +114,7 @@ __global__ void __launch_bounds__(GNT, 1) dense_gemv_kernel(GemvArgs a)
             const int row = a.kind == MOE_PACK_GATE_UP ? (rr < 8 ? 8 * band + rr : N / 2 + 8 * band + (rr - 8))
                                                        : 16 * band + rr;
             const uint8_t *src = w + ((size_t)row * K + 64 * s) * 2 + 64 * h;
-            uint8_t *dst = sm.ring[warp][rs] + rr * 128;
+            uint8_t *dst = slot + rr * 128;
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 cp_async_cg16(dst + 16 * ((4 * h + u) ^ (4 * (rr & 1))), src + 16 * u);
@@ -110,115 +124,90 @@ __global__ void __launch_bounds__(GNT, 1) dense_gemv_kernel(GemvArgs a)
         if (lane != 0)
             return;
         mbar_arrive_expect_tx(bar, GSTG);
-        bulk_g2s(sm.ring[warp][rs], w + (size_t)band * band_bytes(K) + (size_t)s * GSTG, GSTG, bar);
+        bulk_g2s(slot, w + (size_t)band * band_bytes(K) + (size_t)s * GSTG, GSTG, bar);
     };
     int ic = 0, ii = 0;
-    auto issue_ahead = [&]() {
-        while (ii < n_stages && ii < ic + RW) {
+    auto issue_upto = [&](int depth) {
+        while (ii < n_stages && ii < ic + depth) {
             issue_stage(ii % RW, ii);
             ++ii;
         }
     };
+    auto issue_ahead = [&]() { issue_upto(RW); };
     if (warp < GW)
-        issue_ahead();
+        issue_upto(PRE);
 
     griddep_wait();      // x is written by the preceding kernel
     griddep_launch();
 
-    // ---- x -> B fragments [k16 step][lane] in shared memory ----
-    // Two warps per token (warp 2 t + hf takes columns [hf K / 2, (hf + 1)
-    // K / 2)); each lane holds up to XCH 16-byte pieces at once, all loads of
-    // a chunk issued before any is used.  NVFP4: the token's max |x| first
-    // (both halves, exchanged through shared memory), then each piece -- 8
-    // columns = the .x (or .y) words of the 4 lanes (t, c) of one k16 step --
-    // is scaled into f16.  BF16: a piece is the two uint2 fragments of lane
-    // (t, c) for a pair of steps (the column order of bf16_bcol).
-    const __nv_bfloat16 *x = a.x + (size_t)m * a.x_mat_stride;
-    constexpr int XCH = 8;
-    const int nh = K / 16;                    // pieces per half row
-    const int nper = (nh + 31) / 32;          // per lane
-    const int xt = warp >> 1, hf = warp & 1;
-    const bool xwarp = warp < 2 * T;
-    const uint4 *xrow = reinterpret_cast<const uint4 *>(x + (size_t)xt * K) + hf * nh;
-    uint4 xv[XCH];
-    auto load_chunk = [&](int c0) {
+    // ---- x -> shared memory, row-major (rows 16 bytes apart) ----
+    // Lanes t < T of warp 0 each bulk-copy token t's row (rows T.. stay
+    // unwritten: their mma columns are never stored).  NVFP4 then converts
+    // the words in place to f16 after the exact per-token power-of-two
+    // rescale.
+    const int rpw = K / 2 + 4;                 // row pitch in 32-bit words
+    if (warp == 0) {
+        if (lane == 0)
+            mbar_arrive_expect_tx(&sm.xbar, (uint32_t)(T * K * 2));
+        __syncwarp();
+        if (lane < T)
+            bulk_g2s(sm.xs + lane * rpw, a.x + (size_t)m * a.x_mat_stride + (size_t)lane * K, (uint32_t)(K * 2),
+                     &sm.xbar);
+    }
+    if (warp < GW)
+        issue_ahead();
+    mbar_wait_bounded(&sm.xbar, 0, flag);
+    if (!BW) {
+        // warp w < 2 T takes half hf = w % 2 of row t = w / 2: K / 16
+        // pieces, XH at a time per lane (all of them at K <= 4096); the
+        // row's max |x| is one reduction per warp and one shared-memory max
+        // per warp, then the pieces go back converted (re-read above 4096)
+        constexpr int XH = GEMV_MAX_K_RW4 / 16 / 32;   // 8 pieces per lane
+        const int xrow = warp >> 1, xhf = warp & 1;
+        const bool xw = warp < 2 * T;
+        const int nh = K / 16;                        // pieces per half row
+        uint4 *hp = reinterpret_cast<uint4 *>(sm.xs + xrow * rpw) + xhf * nh;
+        uint4 hv[XH];
+        uint32_t mx = 0u;
+        if (xw) {
+            for (int c0 = 0; c0 < nh; c0 += 32 * XH) {
 #pragma unroll
-        for (int i = 0; i < XCH; ++i) {
-            const int j = lane + 32 * (c0 + i);
-            xv[i] = (c0 + i < nper && j < nh) ? __ldg(xrow + j) : make_uint4(0u, 0u, 0u, 0u);
-        }
-    };
-    uint32_t *xf32 = reinterpret_cast<uint32_t *>(sm.xfrag);
-    auto store_chunk = [&](int c0, float p) {
+                for (int i = 0; i < XH; ++i) {
+                    const int j = c0 + 32 * i + lane;
+                    hv[i] = j < nh ? hp[j] : make_uint4(0u, 0u, 0u, 0u);
+                }
 #pragma unroll
-        for (int i = 0; i < XCH; ++i) {
-            const int j = lane + 32 * (c0 + i);
-            if (c0 + i >= nper || j >= nh)
-                continue;
-            const int jj = hf * nh + j;        // piece index in the row: columns 8 jj .. 8 jj + 7
-            const uint32_t w4[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
-            if (BW) {
-                // columns 64 ch + 32 aa + 8 c + 0..7: steps 4 ch + 2 aa (+1), lane 4 t + c
-                const int ch = jj >> 3, aa = (jj >> 2) & 1, c = jj & 3;
-                const int s0 = 4 * ch + 2 * aa;
-                uint2 *f = sm.xfrag;
-                f[s0 * 32 + 4 * xt + c] = make_uint2(w4[0], w4[1]);
-                f[(s0 + 1) * 32 + 4 * xt + c] = make_uint2(w4[2], w4[3]);
-            } else {
-                // columns 16 step + 8 h + 2 c, +1 for c = 0..3: token t's words
-                // of a step lie in 8 banks, so each store takes c in lane
-                // order (8 distinct banks per instruction, not 2)
-                const int step = jj >> 1, h = jj & 1;
+                for (int i = 0; i < XH; ++i) {
+                    const uint32_t w4[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int c = (cc + lane) & 3;
-                    const uint32_t wc = c == 0 ? w4[0] : c == 1 ? w4[1] : c == 2 ? w4[2] : w4[3];
-                    xf32[(step * 32 + 4 * xt + c) * 2 + h] = bf16x2_to_f16x2_scaled(wc, p);
+                    for (int u = 0; u < 4; ++u)   // |bf16| bit patterns order like their values
+                        mx = max(mx, max(w4[u] & 0x7FFFu, (w4[u] >> 16) & 0x7FFFu));
                 }
             }
+            mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+            if (lane == 0)
+                atomicMax(&sm.xmax[xrow], mx);
         }
-    };
-    // fragments of the lanes of absent tokens (4 T ..) are zero
-    for (int i = threadIdx.x; i < (K / 16) * 32; i += GNT)
-        if (((i & 31) >> 2) >= T)
-            sm.xfrag[i] = make_uint2(0u, 0u);
-    if (BW) {
-        if (xwarp)
-            for (int c0 = 0; c0 < nper; c0 += XCH) {
-                load_chunk(c0);
-                store_chunk(c0, 1.0f);
-            }
-    } else {
-        float mx = 0.0f;
-        if (xwarp)
-            for (int c0 = 0; c0 < nper; c0 += XCH) {
-                load_chunk(c0);
-                __nv_bfloat162 m2 = __floats2bfloat162_rn(0.f, 0.f);
-#pragma unroll
-                for (int i = 0; i < XCH; ++i) {
-                    m2 = __hmax2(m2, __habs2(u32_as_bf162(xv[i].x)));
-                    m2 = __hmax2(m2, __habs2(u32_as_bf162(xv[i].y)));
-                    m2 = __hmax2(m2, __habs2(u32_as_bf162(xv[i].z)));
-                    m2 = __hmax2(m2, __habs2(u32_as_bf162(xv[i].w)));
-                }
-                mx = fmaxf(mx, fmaxf(__low2float(m2), __high2float(m2)));
-            }
-        // max |x| >= 0: its fp32 bit pattern orders like an unsigned int
-        mx = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mx)));
-        if (xwarp && lane == 0)
-            sm.hmx[xt][hf] = mx;
         __syncthreads();
-        if (xwarp) {
-            const int sh = act_shift(fmaxf(sm.hmx[xt][0], sm.hmx[xt][1]));
-            if (hf == 0 && lane == 0)
-                sm.xinv[xt] = pow2i(-sh);
-            const float p = pow2i(sh);
-            if (nper <= XCH) {
-                store_chunk(0, p);   // the only chunk is still in registers
-            } else {
-                for (int c0 = 0; c0 < nper; c0 += XCH) {
-                    load_chunk(c0);
-                    store_chunk(c0, p);
+        if (threadIdx.x < MAXT)
+            sm.xinv[threadIdx.x] = pow2i(-act_shift(bf16_bits_to_float(sm.xmax[threadIdx.x])));
+        if (xw) {
+            const float p = pow2i(act_shift(bf16_bits_to_float(sm.xmax[xrow])));
+            for (int c0 = 0; c0 < nh; c0 += 32 * XH) {
+                if (nh > 32 * XH) {   // more than one chunk: the registers hold the last one only
+#pragma unroll
+                    for (int i = 0; i < XH; ++i) {
+                        const int j = c0 + 32 * i + lane;
+                        if (j < nh)
+                            hv[i] = hp[j];
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < XH; ++i) {
+                    const int j = c0 + 32 * i + lane;
+                    if (j < nh)
+                        hp[j] = make_uint4(bf16x2_to_f16x2_scaled(hv[i].x, p), bf16x2_to_f16x2_scaled(hv[i].y, p),
+                                           bf16x2_to_f16x2_scaled(hv[i].z, p), bf16x2_to_f16x2_scaled(hv[i].w, p));
                 }
             }
         }
@@ -240,11 +229,26 @@ __global__ void __launch_bounds__(GNT, 1) dense_gemv_kernel(GemvArgs a)
                 const int band = b0 + G * r + gi;
                 if (band >= b1)
                     break;
-                float4 sum = sm.red[bb][gi * Q][lane];
-#pragma unroll 1
-                for (int qq = 1; qq < Q; ++qq) {
-                    const float4 v = sm.red[bb][gi * Q + qq][lane];
-                    sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+                // the Q partials added in warp order, loaded eight at a time
+                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int h8 = 0; h8 < GW; h8 += 8) {
+                    if (h8 >= Q)
+                        break;
+                    float4 pv[8];
+#pragma unroll
+                    for (int qq = 0; qq < 8; ++qq)
+                        if (h8 + qq < Q)
+                            pv[qq] = sm.red[bb][gi * Q + h8 + qq][lane];
+#pragma unroll
+                    for (int qq = 0; qq < 8; ++qq)
+                        if (h8 + qq < Q) {
+                            if (h8 + qq == 0) {
+                                sum = pv[0];
+                            } else {
+                                sum.x += pv[qq].x; sum.y += pv[qq].y; sum.z += pv[qq].z; sum.w += pv[qq].w;
+                            }
+                        }
                 }
                 const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
@@ -277,7 +281,6 @@ __global__ void __launch_bounds__(GNT, 1) dense_gemv_kernel(GemvArgs a)
     }
 
     // ---- a compute warp ----
-    const uint2 *bfrag = sm.xfrag;
 #pragma unroll 1
     for (int r = 0; r < rounds; ++r) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -287,9 +290,9 @@ __global__ void __launch_bounds__(GNT, 1) dense_gemv_kernel(GemvArgs a)
                 const int rs = ic % RW;
                 mbar_wait_bounded(&sm.full[warp][rs], (ic / RW) & 1, flag);
                 if (BW)
-                    bf16_stage(sm.ring[warp][rs], bfrag, 4 * s, lane, acc);
+                    bf16_stage_xs(sm.ring[rs][warp], sm.xs, rpw, 4 * s, lane, acc);
                 else
-                    mma_stage(sm.ring[warp][rs], bfrag, 16 * s, lane, acc);
+                    mma_stage_xs(sm.ring[rs][warp], sm.xs, rpw, 16 * s, lane, acc);
                 __syncwarp();
                 ++ic;
                 issue_ahead();

@@ -865,18 +865,18 @@ static cudaError_t launch_ex(const void *fn, dim3 grid, dim3 block, size_t smem,
 size_t grouped_smem_bytes() { return sizeof(GSmem) + 1024; }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against the driver library).
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+// against the driver library); looked up once (a thread-safe static).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+    }();
     return fn;
 }
 
@@ -902,18 +902,14 @@ static bool make_map(CUtensorMap *m, const void *base, int cols, size_t rows, in
 static cudaError_t launch_gemm(const GArgs &ga, const void *routed, size_t routed_rows, const void *shared,
                                size_t shared_rows, int cols, int nsm, cudaStream_t st)
 {
-    static int configured[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-        e = cudaFuncSetAttribute(moe_grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)grouped_smem_bytes());
-        if (e != cudaSuccess)
-            return e;
-        configured[dev] = 1;
-    }
+    static PerDevice configured;
+    if (per_device(configured, [](int) {
+            return cudaFuncSetAttribute(moe_grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)grouped_smem_bytes()) == cudaSuccess
+                       ? 1
+                       : -1;
+        }) <= 0)
+        return cudaErrorInvalidValue;
     alignas(64) CUtensorMap mr64, mr16, ms64, ms16;
     const void *r = routed ? routed : shared, *s = shared ? shared : routed;
     const size_t rr = routed ? routed_rows : shared_rows, sr = shared ? shared_rows : routed_rows;

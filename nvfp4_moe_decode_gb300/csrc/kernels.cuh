@@ -2,6 +2,8 @@
 // kernels behind libnvfp4moe.so (internal; not part of the public C ABI).
 #pragma once
 
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <mutex>
 
@@ -111,7 +113,7 @@ enum GemvEpi {
     GEMV_SILU_H = 2,     // GATE_UP bands: y[m][t][i] = bf16(silu(gate_i) * up_i), i < N / 2
 };
 constexpr int GEMV_MAX_K_RW4 = 4096;   // four ring stages per warp up to here
-constexpr int GEMV_MAX_K = 8192;       // two beyond (the B fragments take 16 K bytes of shared memory)
+constexpr int GEMV_MAX_K = 8192;       // two beyond (x takes 16 K bytes of shared memory)
 
 struct GemvArgs {
     const __nv_bfloat16 *x;        // [n_mat][T][K] (x_mat_stride elements apart; 0: one x for all)
@@ -133,6 +135,8 @@ struct GemvArgs {
 
 // Warps per band for a CTA holding `bands_per_cta` bands of `stages` stages.
 int gemv_warps_per_band(int bands_per_cta, int stages);
+// cuTensorMapEncodeTiled (null if the driver does not provide it).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 cudaError_t launch_gemv(GemvArgs a, int sm_count, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------

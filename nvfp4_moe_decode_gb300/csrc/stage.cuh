@@ -129,5 +129,62 @@ __device__ __forceinline__ void mma_stage(const uint8_t *stage, const uint2 *bfr
     }
 }
 
+// The same with the B fragments read from activations staged row-major in
+// shared memory, token t's row at word t * rpw (rpw = K / 2 + 4: rows 16
+// bytes apart, so that the 32 lanes' words fall in 32 different banks):
+// lane (g, c) takes words 8 step + c and 8 step + 4 + c of token g's row
+// (columns 16 step + 2 c, +1 and 16 step + 8 + 2 c, +1).
+__device__ __forceinline__ void mma_stage_xs(const uint8_t *stage, const uint32_t *xs, int rpw, int step0, int lane,
+                                             float acc[4])
+{
+    const int g = lane >> 2, c = lane & 3;
+    const uint32_t *xrow = xs + g * rpw + c;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const uint8_t *base = stage + q * SC_BYTES;
+        const uint4 sc = *reinterpret_cast<const uint4 *>(base + 1024 + g * 16);
+        const uint32_t sws[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const uint4 cw = *reinterpret_cast<const uint4 *>(base + half * 512 + lane * 16);
+            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const int step = step0 + q * 8 + half * 4 + s;
+                uint32_t a0, a1, a2, a3;
+                decode4(words[s], a0, a1, a2, a3);
+                float d[4];
+                mma_f16_16816(d, a0, a1, a2, a3, xrow[8 * step], xrow[8 * step + 4]);
+                const int sb = half * 4 + s;
+                const uint32_t sw = sws[sb >> 1];
+                const float2 sf = e4m3x2_to_float2((sb & 1) ? (sw >> 16) : (sw & 0xFFFFu));
+                ffma2(acc[0], acc[1], sf.x, d[0], d[1]);
+                ffma2(acc[2], acc[3], sf.y, d[2], d[3]);
+            }
+        }
+    }
+}
+
+// BF16: one 64-column ring stage (see bf16_stage) with the B fragments of
+// k16 steps step0 .. step0 + 3 read from the row-major staging (the four
+// columns of lane (g, c) at bf16_bcol(step, c)).
+__device__ __forceinline__ void bf16_stage_xs(const uint8_t *stage, const uint32_t *xs, int rpw, int step0, int lane,
+                                              float acc[4])
+{
+    const int g = lane >> 2, c = lane & 3, sw = 4 * (g & 1);
+    const uint8_t *ra = stage + g * 128, *rb = stage + (g + 8) * 128;
+    const uint4 a0 = *reinterpret_cast<const uint4 *>(ra + 16 * (c ^ sw));
+    const uint4 a1 = *reinterpret_cast<const uint4 *>(ra + 16 * ((4 + c) ^ sw));
+    const uint4 b0 = *reinterpret_cast<const uint4 *>(rb + 16 * (c ^ sw));
+    const uint4 b1 = *reinterpret_cast<const uint4 *>(rb + 16 * ((4 + c) ^ sw));
+    const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const uint2 b = *reinterpret_cast<const uint2 *>(xs + g * rpw + bf16_bcol(step0 + s, c) / 2);
+        mma_bf16_16816(acc, wa[2 * s], wb[2 * s], wa[2 * s + 1], wb[2 * s + 1], b.x, b.y);
+    }
+}
+
 }  // namespace
 }  // namespace moe
