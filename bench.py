@@ -302,7 +302,7 @@ def main():
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     K, W = args.steps, args.warmup
-    if T > 8:
+    if T > 160:
         line = measure_grouped(args, T, WT, world, dev, True, K, W)
     else:
         line = measure_decode(args, T, WT, L, world, dev, True, K, W)
@@ -319,6 +319,10 @@ def main():
             torch.cuda.empty_cache()
         sec.append(secondary_entry(measure_grouped(args, 8192, "nvfp4", world, dev, False,
                                                    max(min(K, 40), 4), max(min(W, 6), 3))))
+        torch.cuda.empty_cache()
+        # a mid-size batch: the decode kernel on chunks of at most 8 tokens
+        sec.append(secondary_entry(measure_decode(args, 64, "nvfp4", L, world, dev, False,
+                                                  max(min(K, 200), 16), w2)))
         torch.cuda.empty_cache()
         # the dense GEMV on the packed layout: the attention projections of a
         # 2048-wide decoder (qkv 5120 x 2048, o 2048 x 4096), and a large matrix
@@ -373,8 +377,17 @@ def timed_replays(stream, graphs, local: int):
     return e0.elapsed_time(e1), clk
 
 
+def chunks_of(T: int):
+    """The library's balanced chunks of at most 8 tokens (T <= 160)."""
+    n = (T + 7) // 8
+    return [(T * c // n, T * (c + 1) // n) for c in range(n)]
+
+
 def measure_decode(args, T: int, WT: str, L: int, world: int, dev, with_e2e: bool, K: int, W: int) -> dict:
-    """One decode-path layer (T <= 8) per step, rotating over L resident layers."""
+    """One decode-path layer (T <= 8, or up to 160 tokens in chunks of at
+    most 8) per step, rotating over L resident layers.  The bytes of a step
+    add up the chunks: each reads the router, its own selected and the
+    shared experts, its x and out."""
     import torch
 
     import nvfp4_moe_decode_gb300 as m
@@ -401,7 +414,8 @@ def measure_decode(args, T: int, WT: str, L: int, world: int, dev, with_e2e: boo
         for pl in packed:
             m.moe_route(x, pl.router_w, T, idx, w, None, ws, stream)
             stream.synchronize()
-            nd.append(len(set(idx.cpu().reshape(-1).tolist())))
+            ih = idx.cpu().numpy()
+            nd.append([len(set(ih[t0:t1].reshape(-1).tolist())) for (t0, t1) in chunks_of(T)])
     m.moe_workspace_init(ws, stream)
     out = torch.empty(T, 2048, dtype=torch.bfloat16, device=dev)
 
@@ -425,7 +439,10 @@ def measure_decode(args, T: int, WT: str, L: int, world: int, dev, with_e2e: boo
         run_steps(0, W % L)
     stream.synchronize()
     rem_graph = capture(K % L) if K % L else None
-    steps_bytes = sum(layer_bytes(T, nd[k % L], 1, WT) for k in range(K))
+    def step_bytes(k):
+        return sum(layer_bytes(t1 - t0, u, 1, WT) for (t0, t1), u in zip(chunks_of(T), nd[k % L]))
+
+    steps_bytes = sum(step_bytes(k) for k in range(K))
 
     barrier(world)
     graphs = [(g_full, K // L)] + ([(rem_graph, 1)] if rem_graph is not None else [])
@@ -443,7 +460,8 @@ def measure_decode(args, T: int, WT: str, L: int, world: int, dev, with_e2e: boo
     if WT == "nvfp4" and kernel_sources_sha256() == NCU_TRAFFIC["sources_sha256"]:
         traffic = layer_alg * NCU_TRAFFIC["per_algorithmic_byte"]
     workload = (f"one {WT.upper()} MoE layer, T={T} tokens (H=2048, 256 routed experts I=512, sigmoid top-6, "
-                f"1 shared expert), synthetic seeded weights")
+                f"1 shared expert), synthetic seeded weights"
+                + (f"; decode kernel on {len(chunks_of(T))} chunks of at most 8 tokens" if T > 8 else ""))
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -454,13 +472,14 @@ def measure_decode(args, T: int, WT: str, L: int, world: int, dev, with_e2e: boo
                    "timing": "CUDA events on the launching stream around K graph-replayed steps; a 1 ms GPU sleep "
                              "ahead of the start event keeps host launch latency out of the span",
                    "us_per_layer": us_per_layer, "tokens_per_s": T * K / (ms_max * 1e-3),
-                   "distinct_experts_per_layer": nd, "algorithmic_bytes_per_layer": layer_alg,
+                   "distinct_experts_per_layer": [v[0] if len(v) == 1 else v for v in nd],
+                   "algorithmic_bytes_per_layer": layer_alg,
                    "hbm_frac": value / world / peak, "device_flag": flag},
         "roofline": {"bound": "hbm", "achieved": layer_alg / (us_per_layer * 1e-6) / 1e9, "peak": peak,
                      "unit": "GB/s", "frac": layer_alg / (us_per_layer * 1e-6) / 1e9 / peak,
                      "traffic": traffic, "peak_source": peak_src,
                      "kernel": "moe_layer_kernel (router, top-6, gate/up, down, combine fused; one launch per layer)"},
-        "gpu_launches": K,
+        "gpu_launches": K * len(chunks_of(T)),
         "clocks": clk,
     }
     if with_e2e:
@@ -478,7 +497,7 @@ def measure_decode(args, T: int, WT: str, L: int, world: int, dev, with_e2e: boo
                 oh.copy_(out, non_blocking=True)
                 stream.synchronize()
         e2e_s = time.perf_counter() - t0
-        e2e_bytes = sum(layer_bytes(T, nd[k % L], 1, WT) for k in range(ne))
+        e2e_bytes = sum(step_bytes(k) for k in range(ne))
         e2e_v = reduce_sum(e2e_bytes, world) / reduce_max(e2e_s, world) / 1e9
         line["e2e"] = {"value": e2e_v, "unit": "GB/s", "steps": ne, "h2d_bytes_per_step": T * 2048 * 2,
                        "d2h_bytes_per_step": T * 2048 * 2}

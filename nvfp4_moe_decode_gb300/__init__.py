@@ -39,6 +39,7 @@ INTER = 512
 EXPERTS = 256
 TOPK = 6
 MAX_DECODE_T = 8
+MAX_CHUNKED_T = 160
 MAX_TOKENS = 65536
 
 # Exported symbols (kept in step with include/nvfp4moe.h; a CPU test checks).

@@ -126,8 +126,9 @@ size_t moe_workspace_bytes(int T)
         return 0;
     if (T <= MAXT)
         return ws_layout().total;
-    const size_t g = gws_layout(T).total;
-    return g > ws_layout().total ? g : ws_layout().total;
+    const size_t g = gws_layout(T).total;   // moe_route above MAXT tokens
+    const size_t d = T <= CHUNK_MAX_T ? chunk_route_layout(T).total : ws_layout().total;
+    return g > d ? g : d;
 }
 
 moe_status moe_workspace_init(void *workspace, size_t workspace_bytes, moe_stream_t stream)
@@ -187,6 +188,13 @@ moe_status moe_read_routing(const void *workspace, size_t workspace_bytes, int T
         o_w = L.topk_w;
         o_lg = L.tlogits;
         lg_pitch = 8;
+    } else if (T <= CHUNK_MAX_T) {
+        // the decode kernel's chunks wrote their routing here
+        const ChunkRouteLayout C = chunk_route_layout(T);
+        o_idx = C.idx;
+        o_w = C.w;
+        o_lg = C.logits;
+        lg_pitch = 4;
     } else {
         const GWsLayout L = gws_layout(T);
         o_idx = L.idx;
@@ -398,6 +406,37 @@ static moe_status launch_layer_on_all_sms(const LayerArgs &la, cudaStream_t st, 
 
 }  // extern "C"
 
+// MAXT < T <= CHUNK_MAX_T: the decode kernel on ceil(T / MAXT) balanced
+// chunks (each token's output depends only on that token), every chunk's
+// routing copied out for moe_read_routing.
+static moe_status layer_forward_chunked(const void *x, const void *router_w, const moe_expert_bank *routed,
+                                        const moe_expert_bank *shared, void *out, int T, void *workspace,
+                                        cudaStream_t st)
+{
+    int grid = 0;
+    const moe_status s = layer_grid(grid);
+    if (s != MOE_OK)
+        return s;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const ChunkRouteLayout C = chunk_route_layout(T);
+    const int n = (T + MAXT - 1) / MAXT;
+    for (int c = 0; c < n; ++c) {
+        const int t0 = (int)((long)T * c / n), t1 = (int)((long)T * (c + 1) / n);
+        LayerArgs la{};
+        fill_layer_args(la, router_w, routed, shared, static_cast<__nv_bfloat16 *>(out) + (size_t)t0 * H,
+                        t1 - t0, workspace);
+        la.x = static_cast<const __nv_bfloat16 *>(x) + (size_t)t0 * H;
+        la.r_idx = reinterpret_cast<int32_t *>(ws + C.idx);
+        la.r_w = reinterpret_cast<float *>(ws + C.w);
+        la.r_logits = reinterpret_cast<float *>(ws + C.logits);
+        la.t0 = t0;
+        const cudaError_t e = launch_layer(la, grid, st, true);
+        if (e != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
 // moe_layer_forward; with rearm (decode path only) the workspace's re-arm
 // kernel runs ahead of the layer kernel.
 moe_status moe::layer_forward(const void *x, const void *router_w, const moe_expert_bank *routed,
@@ -421,6 +460,11 @@ moe_status moe::layer_forward(const void *x, const void *router_w, const moe_exp
     const int nsm = sm_count();
     if (nsm <= 0)
         return MOE_ERR_CUDA;
+    if (T > MAXT && T <= CHUNK_MAX_T) {
+        if (!disjoint(out, x, (size_t)T * H * 2))
+            return MOE_ERR_INVALID_ARG;
+        return layer_forward_chunked(x, router_w, routed, shared, out, T, workspace, (cudaStream_t)stream);
+    }
     if (T > MAXT) {
         if (!disjoint(out, x, (size_t)T * H * 2))
             return MOE_ERR_INVALID_ARG;
@@ -450,6 +494,8 @@ moe_status moe::layer_forward(const void *x, const void *router_w, const moe_exp
     la.x = static_cast<const __nv_bfloat16 *>(x);
     return launch_layer_on_all_sms(la, (cudaStream_t)stream, rearm, ahead ? shared : nullptr);
 }
+
+
 
 extern "C" {
 

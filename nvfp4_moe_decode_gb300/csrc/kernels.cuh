@@ -70,6 +70,12 @@ struct LayerArgs {
     int n_ext;
     int n_sink;
     const float *ext_y;            // f32 [MAX_EXT][MAXT][H]
+    // a chunk of a larger batch: CTA 0 also writes this chunk's selection,
+    // weights and fp32 logits at token offset t0 of these arrays (or null)
+    int32_t *r_idx;                // [..][TOPK]
+    float *r_w;                    // [..][TOPK]
+    float *r_logits;               // [..][E]
+    int t0;
     // pre-norm mode (a layer of a decoder stack): the input is
     // RMSNorm(bf16(x + delta)); x is the residual stream, delta (may be null)
     // the previous layer's output; resid_out / xn_out (may be null) receive
@@ -103,6 +109,33 @@ struct DequantArgs {
     int N, K, kind;
     float tscale;
 };
+
+// ---------------------------------------------------------------------------
+// Mid-size batches: MAXT < T <= CHUNK_MAX_T tokens run the decode kernel on
+// balanced chunks of at most MAXT tokens (the grouped path's fixed cost is
+// far higher there; its time and ceil(T / 8) decode launches cross near 160
+// tokens on GB300).  Each chunk's routing is kept after the decode
+// workspace, for moe_read_routing.
+// ---------------------------------------------------------------------------
+constexpr int CHUNK_MAX_T = MOE_MAX_CHUNKED_T;
+
+struct ChunkRouteLayout {
+    size_t idx;      // i32 [T][TOPK]
+    size_t w;        // f32 [T][TOPK]
+    size_t logits;   // f32 [T][E]
+    size_t total;
+};
+
+__host__ __device__ inline ChunkRouteLayout chunk_route_layout(int T)
+{
+    ChunkRouteLayout c;
+    size_t o = ws_layout().total;
+    c.idx = o;     o = align256(o + (size_t)T * TOPK * 4);
+    c.w = o;       o = align256(o + (size_t)T * TOPK * 4);
+    c.logits = o;  o = align256(o + (size_t)T * E * 4);
+    c.total = o;
+    return c;
+}
 
 // ---------------------------------------------------------------------------
 // Dense small-batch GEMV (T <= MAXT): see gemv.cu.

@@ -537,6 +537,16 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             }
             if (lane < a.n_ext)
                 reinterpret_cast<float *>(a.ws + L.sinkw)[warp * MAX_EXT + lane] = a.n_sink ? swt : 1.0f;
+            if (a.r_idx) {
+                const int tg = a.t0 + warp;
+                if (lane < TOPK) {
+                    a.r_idx[tg * TOPK + lane] = ex;
+                    a.r_w[tg * TOPK + lane] = wt;
+                }
+#pragma unroll
+                for (int mm = 0; mm < 8; ++mm)
+                    a.r_logits[(size_t)tg * E + lane + 32 * mm] = v[mm];
+            }
         }
     }
     __syncthreads();
