@@ -870,7 +870,24 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         int ii = pre_shared ? 1 : 0;                 // next stage to issue
         auto issue_ahead = [&]() {
             while (ii < n_stages && ii < ic + RW) {
-                issue_stage(ii % RW, ii);
+                const int rs = ii % RW;
+                const int d = ii - n_gub * SPG;
+                if (!BW && d >= 0 && (d & 1) == 0 && rs + 1 < RW && ii + 1 < ic + RW) {
+                    // both stages of an NVFP4 down band into adjacent slots by
+                    // one copy; the second slot's barrier completes at once
+                    // (its data is covered by the first slot's)
+                    if (lane == 0) {
+                        int slot, band, hb;
+                        dn_band(jw + 16 * (d >> 1), slot, band, hb);
+                        mbar_arrive_expect_tx(&sm.full[warp][rs], 2 * STG);
+                        bulk_g2s(sm.ring[warp][rs], bank2(slot) + (size_t)band * W2_BAND_BYTES, 2 * STG,
+                                 &sm.full[warp][rs]);
+                        mbar_arrive(&sm.full[warp][rs + 1]);
+                    }
+                    ii += 2;
+                    continue;
+                }
+                issue_stage(rs, ii);
                 ++ii;
             }
         };
