@@ -751,7 +751,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                         atomicOr(flag, FLAG_TIMEOUT);
                     break;
                 }
-                __nanosleep(128);
+                __nanosleep(64);
             }
             hfa = reinterpret_cast<uint2 *>(sm.u.hbuf[r]);
             int sh = 0;
@@ -1007,7 +1007,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                         atomicOr(flag, FLAG_TIMEOUT);
                     break;
                 }
-                __nanosleep(128);
+                __nanosleep(64);
             }
             sm.comb[warp][lane] = make_float4(s4[0], s4[1], s4[2], s4[3]);
             named_barrier_sync(7, FT);

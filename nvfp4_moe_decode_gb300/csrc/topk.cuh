@@ -75,21 +75,37 @@ __device__ __forceinline__ void warp_route_values_t(const float v[8], int lane, 
     cx_desc(k[2], k[4]); cx_desc(k[3], k[5]);
     cx_desc(k[1], k[4]); cx_desc(k[3], k[6]);
     cx_desc(k[1], k[2]); cx_desc(k[3], k[4]); cx_desc(k[5], k[6]);
+    // Round i: the largest high word (the logit) over the lanes' best keys;
+    // when one lane holds it, that lane wins without a second reduction (a
+    // tie on the logit takes the larger low word: the lower expert index).
+    // The winners' keys reach lanes 0..5 after the rounds.
     unsigned long long chosen = 0ull;   // lane i < TOPK: the i-th best key
+    int winner[TOPK];
+    unsigned long long won[TOPK];       // on the winner lane of round i: its key
 #pragma unroll
     for (int i = 0; i < TOPK; ++i) {
         const unsigned long long mine = k[0];
-        const uint32_t hi = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(mine >> 32));
-        const uint32_t lo = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(mine >> 32) == hi ? (uint32_t)mine : 0u);
-        const unsigned long long best = ((unsigned long long)hi << 32) | lo;
-        if (mine == best) {
+        const uint32_t mh = (uint32_t)(mine >> 32);
+        const uint32_t hi = __reduce_max_sync(0xFFFFFFFFu, mh);
+        uint32_t cand = __ballot_sync(0xFFFFFFFFu, mh == hi);
+        if (cand & (cand - 1)) {
+            const uint32_t lo = __reduce_max_sync(0xFFFFFFFFu, mh == hi ? (uint32_t)mine : 0u);
+            cand = __ballot_sync(0xFFFFFFFFu, mh == hi && (uint32_t)mine == lo);
+        }
+        winner[i] = __ffs(cand) - 1;
+        if (lane == winner[i]) {
+            won[i] = mine;
 #pragma unroll
             for (int m = 0; m < 7; ++m)
                 k[m] = k[m + 1];
             k[7] = 0ull;
         }
+    }
+#pragma unroll
+    for (int i = 0; i < TOPK; ++i) {
+        const unsigned long long w = __shfl_sync(0xFFFFFFFFu, won[i], winner[i]);
         if (lane == i)
-            chosen = best;
+            chosen = w;
     }
     // sigmoid of each chosen logit on its own lane, the sum in selection order
     const float s = 1.0f / (1.0f + expf(-key_logit(chosen)));
