@@ -9,14 +9,22 @@ rotation are far larger than the 126 MB L2): step k runs layer k mod L.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--tokens T] [--layers L] [--wtype nvfp4|bf16] [--stack NL]
+                    [--dense proj|large] [--no-secondary] [--no-cpu-baseline]
 
 --stack NL measures a pre-norm decoder stack of NL resident layers instead
 (x <- x + MoE_l(RMSNorm(x)), one moe_stack_forward per step; the stack is far
 larger than L2, so it runs cold without rotation).
 
-T > 8 tokens take the grouped tensor-core path; the line then reports the
-layer's dense-equivalent TFLOP/s (router + 7 expert MLPs per token, padding
-excluded) against the measured bf16 tensor peak.
+9..160 tokens run the decode kernel on chunks of at most 8 tokens (bytes
+summed over the chunks).  Above 160 tokens the grouped tensor-core path runs;
+the line then reports the layer's dense-equivalent TFLOP/s (router + 7 expert
+MLPs per token, padding excluded) against the measured bf16 tensor peak.
+--dense times the dense NVFP4 GEMV (moe_dense_gemv_nvfp4) instead.
+
+By default the T = 8 NVFP4 line also times, in the same process and listed
+under config.secondary: NVFP4 T = 1, BF16 T = 8 and T = 1, the T = 8192
+grouped layer, T = 64 (chunked), and the dense GEMV on the attention
+projections (T = 8 and 1) and on one large matrix.
 
 Prints one JSON line (rank 0).  value = algorithmic bytes of all steps / time
 (GB/s); the bytes of a step are the router weights + the selected and shared
@@ -245,9 +253,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dense", choices=["proj", "large"], default=None,
+                    help="time the dense NVFP4 GEMV instead: the attention projections (qkv 5120 x 2048, "
+                         "o 2048 x 4096, 32 matrices) or one large matrix (16384 x 4096, --dense-mats of them)")
+    ap.add_argument("--dense-mats", type=int, default=8)
     ap.add_argument("--no-secondary", action="store_true",
                     help="time only the selected workload (by default the T=8 NVFP4 line also times "
-                         "NVFP4 T=1, BF16 T=8 and T=1, and the T=8192 grouped layer)")
+                         "NVFP4 T=1, BF16 T=8 and T=1, T=8192, T=64 and the dense GEMV)")
     args = ap.parse_args()
     assert args.warmup >= 3
 
@@ -302,6 +314,14 @@ def main():
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     K, W = args.steps, args.warmup
+    if args.dense:
+        shapes, nm = (([(5120, 2048), (2048, 4096)], 32) if args.dense == "proj"
+                      else ([(16384, 4096)], args.dense_mats))
+        line = measure_dense(args, T, shapes, nm, world, dev, K, W,
+                             "attention projections" if args.dense == "proj" else "one large matrix")
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     if T > 160:
         line = measure_grouped(args, T, WT, world, dev, True, K, W)
     else:
