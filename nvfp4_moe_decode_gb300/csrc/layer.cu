@@ -726,8 +726,11 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             for (uint32_t it = 0;; ++it) {
                 bool ok = true;
                 // the probe: this lane's last word (the band written latest in
-                // the CTAs' band order is the likeliest to be missing)
-                if (hl)
+                // the CTAs' band order is the likeliest to be missing).  The
+                // last slot, whose h gates the end of the launch and which
+                // these warps usually wait for, is read whole on every poll
+                // instead (one L2 round trip fewer once it is complete).
+                if (hl && r != 2)
                     ok = ld_relaxed_u32(reinterpret_cast<const uint32_t *>(src + (size_t)(2 * HH - 1) * MAXT * 4) +
                                         1) == ltag;
                 if (__all_sync(0xFFFFFFFFu, ok)) {
