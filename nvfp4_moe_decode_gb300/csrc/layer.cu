@@ -8,46 +8,51 @@
 // combine fused into the GEMV kernels, programmatic dependent launch so that
 // a kernel loads weights while its predecessor finishes.
 //
-// One CTA per SM: 16 compute warps, a count warp and an h warp.  Phases:
+// One CTA per SM, 20 warps: 16 compute warps (each with a private ring of
+// stage copies), two epilogue warps (they finish gate/up bands) and two h
+// warps (they prepare the down projections' B operands).  Phases:
 //  1. before waiting on the preceding kernel: router CTAs load their slice of
 //     the router weights; in CTAs 0..63 the compute warps of band parity 0
 //     start the bulk copy of their slice of one band of the shared expert
-//     (it needs no routing);
-//  2. x arrives in shared memory by one bulk copy; in CTAs 0..127 the 16
-//     compute warps compute the fp32 logits of two experts and store each
-//     with the launch's tag in one 64-bit word; every compute warp turns its
-//     256-column slice of x into mma fragments held in registers;
-//  3. every CTA reads the logits until each carries the launch's tag, takes
-//     the top-6 of each token (one warp per token, identical in every CTA)
-//     and builds the slot table: the shared expert, then the distinct
-//     selected experts in ascending order, each with its per-token routing
-//     weight;
+//     (it needs no routing); every tensor scale goes to shared memory;
+//  2. x arrives in shared memory by bulk copies (in a stack, also the
+//     previous layer's output: every CTA forms the residual and its RMSNorm);
+//     CTAs 0..127 compute the fp32 logits of two experts each (CTA 128 those
+//     of up to two expert sinks) and store each with the launch's tag in one
+//     64-bit word; every compute warp turns its 256-column slice of x into
+//     mma fragments held in registers;
+//  3. every CTA reads the logits until each carries the launch's tag (a
+//     reader that sees the tag sees the logit: no fence, no counter), takes
+//     the top-6 of each token (one warp per token, identical in every CTA;
+//     sink scores join the denominator) and builds the slot table: the shared
+//     expert, then the distinct selected experts in ascending order, each
+//     with its per-token routing weight;
 //  4. the unit phase.  With U slots and G CTAs:
 //       gate/up: the 64 U bands of W13 (16 rows each: 8 gate + 8 up rows),
 //         slot-major, are dealt round-robin, CTA c taking bands c, c + G,
 //         ...; within the CTA, band k goes to the 8 warps of parity k % 2,
 //         warp q of them taking the band's 256-column slice q (the x
 //         fragments of that slice never leave its registers).  The eight K
-//         partials of a band meet in a shared-memory buffer; the warp that
-//         arrives last adds them in slice order and applies SiLU*up -> h;
+//         partials of a band meet in a shared-memory buffer; an epilogue
+//         warp adds them in slice order, applies SiLU*up and stores h as
+//         tagged 64-bit words (two bf16 values and the launch tag);
 //       down: the 128 (U - 1) bands of W2 (16 rows) of the first U - 1 slots
 //         are cut into G contiguous ranges (a range touches at most two
 //         slots), and band b of the last slot goes to CTA b; within the CTA
 //         the bands are dealt to the 16 warps round-robin, one warp per band
-//         (all of its 512 columns).  The h warp waits until a slot's 64
-//         gate/up bands are counted, copies the slot's h and turns it into
-//         f16 fragments once for the whole CTA;
-//     every warp streams its own stages (2304-byte pieces of its bands)
-//     through a private ring of bulk copies, ahead across all of its bands,
+//         (all of its 512 columns).  The h warps read a slot's tagged h words
+//         until every one carries the tag, scale each token by a power of two
+//         into f16 fragments once for the whole CTA, and count themselves
+//         done; each down partial goes out as tagged fp32 words;
+//     every compute warp streams its own stages (2304-byte pieces of its
+//     bands) through its ring of bulk copies, ahead across all of its bands,
 //     gate/up first: slots complete in order on every CTA, so by the time a
-//     warp reaches its down bands their h is normally ready.  Compute warps
-//     report finished h bands and down partials through shared-memory masks
-//     only; the count warp turns those into the cross-CTA counts behind one
-//     gpu-scope fence per pass (such a fence costs a streaming warp about a
-//     microsecond);
-//  5. the warp that computes a band's partial for the last slot waits until
-//     the other slots' partials of the band are counted, then adds all of
-//     them in slot order (deterministic) and writes out (bf16).
+//     warp reaches its down bands their h is normally ready;
+//  5. CTA b < 128 writes out rows 16 b .. 16 b + 15: its compute warps read
+//     every slot's tagged partials of the band, each warp summing every 16th
+//     slot in order, then warp 0 adds the 16 sums in warp order and the
+//     shared experts run ahead of the kernel (if any), and rounds once to
+//     bf16 (deterministic, bit-identical between calls).
 // NVFP4: the stages are decoded in registers (cvt.rn.f16x2.e2m1x2) straight
 // into mma.sync A fragments.  BF16 (the W16A16 variant of the Flint page,
 // section "From 1,096 kernels to 346": BF16 decode): a stage is 16 rows x 64
@@ -76,8 +81,9 @@ constexpr int ROUTER_CTAS = E / 2;     // 128 CTAs x 2 experts
 constexpr int HS = I / 16;             // 32 k16 steps of the down GEMV
 constexpr int HBUF = HS * 32 * 8;      // one slot's h as B fragments [step][lane] (uint2), 8 KB
 // With at least 128 CTAs a CTA has at most ceil(64 * 49 / 128) = 25 gate/up
-// bands (bits of a 32-bit mask) and ceil(128 * 48 / 128) = 48 range down
-// bands (bits of a 64-bit mask), and its down range touches at most two slots.
+// bands and ceil(128 * 48 / 128) = 48 range down bands, and its down range
+// touches at most two slots (hence three h buffers: two range slots and the
+// last slot).
 
 struct FSmem {
     uint8_t ring[FW][RW][STG];         // per-warp stage rings; phase 2: warps 8..15's hold x (and delta)
