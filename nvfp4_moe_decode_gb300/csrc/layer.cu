@@ -795,9 +795,12 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                 // its half (b16 + 1 < 16 (hw + 1)).
 #pragma unroll
                 for (int st = 0; st < HH; ++st) {
+                    // HH * hw is a multiple of 4, so the register index and the
+                    // source lane depend on st alone: written that way they are
+                    // compile-time constants (vx, vy stay in registers)
                     const int gst = HH * hw + st;
-                    const int b16 = 4 * (gst >> 2) + 2 * ((gst & 3) >> 1) - HH * hw;
-                    const int sl = 4 * hg + 2 * (gst & 1);
+                    const int b16 = 4 * (st >> 2) + 2 * ((st & 3) >> 1);
+                    const int sl = 4 * hg + 2 * (st & 1);
                     const uint32_t a00 = __shfl_sync(0xFFFFFFFFu, vx[b16], sl);
                     const uint32_t a01 = __shfl_sync(0xFFFFFFFFu, vy[b16], sl);
                     const uint32_t a10 = __shfl_sync(0xFFFFFFFFu, vx[b16 + 1], sl);
