@@ -114,6 +114,9 @@ struct FSmem {
     uint64_t pfull[NB];                // a band's eight K partials are in buffer b
     uint64_t pempty[NB];               // the epilogue warp has read buffer b
     uint32_t hready[NHB];              // h warps done with the buffer (2 when ready)
+    float4 dhalf[8][32];               // BF16: the second K half of a down band, per warp pair
+    uint32_t dh_full[8];               // BF16: halves written by the pair's second warp
+    uint32_t dh_empty[8];              // BF16: halves read by the pair's first warp
     float4 comb[FW][32];               // the final sum of band cta: per-warp sums of every 16th slot
     float hmax[NHB][2][MAXT];          // per h warp, each token's max |h| over its half of a slot
     float extw[MAX_EXT][MAXT];         // weight of each shared expert run ahead, per token
@@ -155,6 +158,11 @@ __device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v)
 
 
 // CTA-scope release store / acquire load (shared-memory progress counters)
+
+__device__ __forceinline__ void st_release_cta(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.cta.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 __device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t *p)
 {
@@ -279,6 +287,10 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         fence_barrier_init();
     if (threadIdx.x < NHB)
         sm.hready[threadIdx.x] = 0u;
+    if (threadIdx.x < 8) {
+        sm.dh_full[threadIdx.x] = 0u;
+        sm.dh_empty[threadIdx.x] = 0u;
+    }
     __syncthreads();
 
     auto bank13 = [&](int slot) -> const uint8_t * {
@@ -830,9 +842,13 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         // bands, so that they, with one band fewer, take the first ones)
         const int n_gub = n_gu_cta > par ? (n_gu_cta - par + 1) / 2 : 0;
         const int jw = (warp - ((n_gu_cta & 1) ? 8 : 0) + 16) & 15;
-        const int n_dnb = n_dn_cta > jw ? (n_dn_cta - jw + 15) / 16 : 0;
+        // BF16: a down band (eight 64-column stages) is split between the
+        // warps jw and jw + 8 (four stages each, all of them in the ring at
+        // once), which take the bands jw % 8, jw % 8 + 8, ...
+        const int jp = BW ? (jw & 7) : jw, dh = BW ? (jw >> 3) : 0, jstride = BW ? 8 : 16;
+        const int n_dnb = n_dn_cta > jp ? (n_dn_cta - jp + jstride - 1) / jstride : 0;
         constexpr int SPG = BW ? 4 : 1;   // stages per gate/up slice
-        constexpr int SPD = BW ? 8 : 2;   // stages per down band
+        constexpr int SPD = BW ? 4 : 2;   // stages per down band (BF16: per half band)
         const int n_stages = n_gub * SPG + n_dnb * SPD;
 
         // stage i of this warp into ring slot rs
@@ -854,7 +870,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                 }
             } else {
                 const int d = i - n_gub * SPG;
-                const int j = jw + 16 * (d / SPD), sub = d % SPD;
+                const int j = jp + jstride * (d / SPD), sub = d % SPD + SPD * dh;
                 int slot, band, hb;
                 dn_band(j, slot, band, hb);
                 if (BW) {
@@ -890,7 +906,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                     // (its data is covered by the first slot's)
                     if (lane == 0) {
                         int slot, band, hb;
-                        dn_band(jw + 16 * (d >> 1), slot, band, hb);
+                        dn_band(jp + jstride * (d >> 1), slot, band, hb);
                         mbar_arrive_expect_tx(&sm.full[warp][rs], 2 * STG);
                         bulk_g2s(sm.ring[warp][rs], bank2(slot) + (size_t)band * W2_BAND_BYTES, 2 * STG,
                                  &sm.full[warp][rs]);
@@ -948,7 +964,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         // ---- down bands ----
 #pragma unroll 1
         for (int m = 0; m < n_dnb; ++m) {
-            const int j = jw + 16 * m;
+            const int j = jp + jstride * m;
             int slot, band, hb;
             dn_band(j, slot, band, hb);
             if (lane == 0)
@@ -959,10 +975,33 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
 #pragma unroll 1
             for (int sub = 0; sub < SPD; ++sub) {
                 if (BW)
-                    bf16_stage(wait_stage(), bfrag, 4 * sub, lane, acc);
+                    bf16_stage(wait_stage(), bfrag, 4 * (sub + SPD * dh), lane, acc);
                 else
                     mma_stage(wait_stage(), bfrag, 16 * sub, lane, acc);
                 next_stage();
+            }
+            if (BW) {
+                // the pair's two K halves meet in shared memory: the second
+                // warp hands its half over, the first adds it to its own
+                // (first half + second half, always in that order)
+                if (dh == 1) {
+                    if (lane == 0)
+                        smem_wait_geq(&sm.dh_empty[jp], (uint32_t)m, flag);
+                    __syncwarp();
+                    sm.dhalf[jp][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                    __syncwarp();
+                    if (lane == 0)
+                        st_release_cta(&sm.dh_full[jp], (uint32_t)m + 1u);
+                    continue;
+                }
+                if (lane == 0)
+                    smem_wait_geq(&sm.dh_full[jp], (uint32_t)m + 1u, flag);
+                __syncwarp();
+                const float4 o = sm.dhalf[jp][lane];
+                acc[0] += o.x; acc[1] += o.y; acc[2] += o.z; acc[3] += o.w;
+                __syncwarp();
+                if (lane == 0)
+                    st_release_cta(&sm.dh_empty[jp], (uint32_t)m + 1u);
             }
             // one band per warp, times the routing weight, the tensor scale and
             // the token's inverse power of two
