@@ -68,10 +68,10 @@ def layer_bytes(T: int, n_distinct: int, n_shared: int = 1, wtype: str = "nvfp4"
 NCU_TRAFFIC = {
     # DRAM bytes read + written per algorithmic byte of the decode kernel at
     # T = 8, from one ncu capture of two launches (layers with 46 and 42
-    # distinct experts: 168,192,256 bytes against 161,480,704), valid while
+    # distinct experts: 168,355,328 bytes against 161,480,704), valid while
     # the kernel's sources hash to this value
-    "sources_sha256": "aa426d1886ba3642cb8b5aa0a7677f45df3be637bf4bb417ba1009da642cc811",
-    "per_algorithmic_byte": 168_192_256 / 161_480_704,
+    "sources_sha256": "70e5d90fe03076f7678d28234abb2a378119a4458f0438171b81b51079cf93e6",
+    "per_algorithmic_byte": 168_355_328 / 161_480_704,
 }
 KERNEL_SOURCES = ("layer.cu", "stage.cuh", "common.cuh", "kernels.cuh", "topk.cuh")
 
