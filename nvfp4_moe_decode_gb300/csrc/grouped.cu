@@ -48,8 +48,16 @@
 //   warp 8      B producer: the tile's token rows, consecutive rows of xs,
 //               x16, h or x, by 16-row TMA tiles;
 //   warp 10     TMEM allocation and the MMA issue (one thread, 4 MMAs of
-//               K = 16 per 64-column chunk, commits to the stages' empty
-//               barriers, and to the accumulator's full barrier per tile);
+//               K = 16 per 64-column chunk, one commit to the stage's empty
+//               barrier, and one to the accumulator's full barrier per tile);
+// Synchronisation is per pair of chunks (128 columns of K; every K here is a
+// multiple of 128): the A and B tiles of both chunks share one full/empty
+// barrier pair.  On GB300 an mbarrier wait costs ~200 cycles even when the
+// phase is complete, and the MMA thread's waits and commits sit between its
+// MMAs (measured: four MMAs of N = 192 take 0.22 us, with two waits and two
+// commits 0.55 us), so every role makes one wait and one signal per 128
+// columns: the MMA thread 8 MMAs per wait and commit, the A warps one fence
+// and arrive per super-chunk, the B producer one expect-tx for both chunks.
 //   warps 12-15 epilogue: tcgen05.ld of the accumulator (two 256-column
 //               buffers, so a tile's epilogue overlaps the next tile's MMAs).
 // Every wait is bounded: a wait that runs out sets MOE_FLAG_WAIT_TIMEOUT
@@ -64,15 +72,14 @@ namespace moe {
 
 namespace {
 
-constexpr int G_ASTAGES = 3;                           // A (weight) stages
-constexpr int G_BSTAGES = 4;                           // B (token) stages
+constexpr int G_STAGES = 4;                            // 64-column sub-stages (an A and a B tile each)
+constexpr int G_PAIRS = G_STAGES / 2;                  // barrier slots, one per two sub-stages
 constexpr int G_A_BYTES = 128 * TC_ROW_BYTES;          // 16 KB: 128 rows x 64 16-bit values
 constexpr int G_B_BYTES = G_NMAX * TC_ROW_BYTES;       // 32 KB: 256 rows x 64 16-bit values
 constexpr int G_AWARPS = 8;                            // A producers: one 16-row band each
 constexpr int G_BWARP = 8;                             // B producer
 constexpr int G_MMA_WARP = 10;
 constexpr int G_EPI_WARP0 = 12;                        // epilogue warps 12..15 (TMEM lane quarters 0..3)
-constexpr int G_LAG = 2;                               // cp.async chunks in flight before signalling
 constexpr int G_THREADS = 512;
 constexpr int G_MAX_GROUPS = E + 1;
 constexpr int G_TMEM_COLS = 512;
@@ -80,9 +87,12 @@ constexpr uint32_t G_SPIN = 1u << 16;                  // suspended polls before
 constexpr uint32_t G_SUSPEND_NS = 20000;               // suspend-time hint of one poll
 
 struct GSmem {
-    uint8_t a[G_ASTAGES][G_A_BYTES];                   // 1024-byte aligned tiles
-    uint8_t b[G_BSTAGES][G_B_BYTES];
-    uint64_t full_a[G_ASTAGES], empty_a[G_ASTAGES], full_b[G_BSTAGES], empty_b[G_BSTAGES];
+    uint8_t a[G_STAGES][G_A_BYTES];                    // 1024-byte aligned tiles
+    uint8_t b[G_STAGES][G_B_BYTES];
+    // one barrier pair per two sub-stages (128 columns of K) for both
+    // operands: full completes once the eight A warps have arrived and the B
+    // tiles' bytes have landed, empty once the pair's MMAs have completed
+    uint64_t full[G_PAIRS], empty[G_PAIRS];
     uint64_t d_full[2], d_empty[2];
     uint32_t tmem;
     int abort;
@@ -220,13 +230,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     griddep_launch();
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < G_ASTAGES; ++s) {
-            mbar_init(&sm.full_a[s], G_AWARPS);
-            mbar_init(&sm.empty_a[s], 1);
-        }
-        for (int s = 0; s < G_BSTAGES; ++s) {
-            mbar_init(&sm.full_b[s], 1);
-            mbar_init(&sm.empty_b[s], 1);
+        for (int p = 0; p < G_PAIRS; ++p) {
+            mbar_init(&sm.full[p], G_AWARPS + 1);
+            mbar_init(&sm.empty[p], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.d_full[i], 1);
@@ -337,10 +343,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             // lane (g, c) writes 4 bytes at row 16 w + g + 8 (r & 1), 16-byte
             // chunk (2 st + (r >> 1)) ^ g, byte 4 c, for word st and byte r
             const uint32_t row0 = (uint32_t)((16 * warp + g4) * TC_ROW_BYTES) + 4u * c4;
-            auto process = [&](int kk, const uint4 &cw, uint32_t s01, uint32_t s23) -> bool {
-                const int s = kk % G_ASTAGES;
-                if (kk >= G_ASTAGES && !gwait_warp(&sm.empty_a[s], ((kk / G_ASTAGES) - 1) & 1, sm, flag, lane))
-                    return false;
+            auto fill = [&](int s, const uint4 &cw, uint32_t s01, uint32_t s23) {
                 const uint32_t abase = smem_u32(sm.a[s]) + row0;
                 const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
@@ -358,10 +361,19 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                         st_shared32(abase + off, v);
                     }
                 }
+            };
+            // super-chunk sci fills sub-stages 2 (sci % 2) and 2 (sci % 2) + 1:
+            // one wait, one fence and one arrive per super-chunk
+            auto process = [&](int sci, const uint4 &c0, const uint4 &c1, const uint4 &sw) -> bool {
+                const int p = sci % G_PAIRS;
+                if (sci >= G_PAIRS && !gwait_warp(&sm.empty[p], ((sci / G_PAIRS) - 1) & 1, sm, flag, lane))
+                    return false;
+                fill(2 * p, c0, sw.x, sw.y);
+                fill(2 * p + 1, c1, sw.z, sw.w);
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(&sm.full_a[s]);
+                    mbar_arrive(&sm.full[p]);
                 return true;
             };
             load(0, 0);
@@ -375,49 +387,55 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     if (sci < nsc && ok) {
                         const uint4 c0 = rc0[j], c1 = rc1[j], sw = rs[j];
                         load(j, sci + 3);                  // refill this slot
-                        ok = process(2 * sci, c0, sw.x, sw.y) && process(2 * sci + 1, c1, sw.z, sw.w);
+                        ok = process(sci, c0, c1, sw);
                     }
                 }
             }
         } else {
-            // bf16 rows: warp w copies rows 16 w .. 16 w + 15 (16 x 8 chunks of 16 bytes)
+            // bf16 rows: warp w copies rows 16 w .. 16 w + 15 (16 x 8 chunks of
+            // 16 bytes) of both chunks of a pair, one cp.async group per pair;
+            // a pair is signalled once the next one has been issued
             const int c8 = lane & 7;
-            int kk = 0;
-            for (; kk < stream_len; ++kk) {
-                const int s = kk % G_ASTAGES;
-                if (kk >= G_ASTAGES && !gwait_warp(&sm.empty_a[s], ((kk / G_ASTAGES) - 1) & 1, sm, flag, lane))
+            const int npairs = stream_len >> 1;
+            int pk = 0;
+            for (; pk < npairs; ++pk) {
+                const int p = pk % G_PAIRS;
+                if (pk >= G_PAIRS && !gwait_warp(&sm.empty[p], ((pk / G_PAIRS) - 1) & 1, sm, flag, lane))
                     break;
-                const Tile t = decode_tile(sm, a, tile_id(kk / nch));
-                const int ch = kk % nch;
+                const Tile t = decode_tile(sm, a, tile_id((2 * pk) / nch));
                 const __nv_bfloat16 *base = reinterpret_cast<const __nv_bfloat16 *>(a_base(t.g));
-                const uint32_t abase = smem_u32(sm.a[s]);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int R = 16 * warp + (lane >> 3) + 4 * i;
-                    int row;
-                    if (a.mode == GM_GATE_UP) {
-                        const int ii = R & 15, b = 8 * t.mt + (R >> 4);
-                        row = ii < 8 ? 8 * b + ii : I + 8 * b + (ii - 8);
-                    } else {
-                        row = 128 * t.mt + R;
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int ch = (2 * pk + h2) % nch;
+                    const uint32_t abase = smem_u32(sm.a[2 * p + h2]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int R = 16 * warp + (lane >> 3) + 4 * i;
+                        int row;
+                        if (a.mode == GM_GATE_UP) {
+                            const int ii = R & 15, b = 8 * t.mt + (R >> 4);
+                            row = ii < 8 ? 8 * b + ii : I + 8 * b + (ii - 8);
+                        } else {
+                            row = 128 * t.mt + R;
+                        }
+                        cp_async16(abase + sw128_offset(R, c8), base + (size_t)row * a.K + ch * TC_KCHUNK + 8 * c8,
+                                   16u);
                     }
-                    cp_async16(abase + sw128_offset(R, c8), base + (size_t)row * a.K + ch * TC_KCHUNK + 8 * c8, 16u);
                 }
                 cp_async_commit();
-                if (kk >= G_LAG) {
-                    cp_async_wait<G_LAG>();
+                if (pk >= 1) {
+                    cp_async_wait<1>();
                     fence_proxy_async();
                     __syncwarp();
                     if (lane == 0)
-                        mbar_arrive(&sm.full_a[(kk - G_LAG) % G_ASTAGES]);
+                        mbar_arrive(&sm.full[(pk - 1) % G_PAIRS]);
                 }
             }
             cp_async_wait<0>();
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0)
-                for (int k2 = max(0, kk - G_LAG); k2 < kk; ++k2)
-                    mbar_arrive(&sm.full_a[k2 % G_ASTAGES]);
+            if (lane == 0 && pk >= 1)
+                mbar_arrive(&sm.full[(pk - 1) % G_PAIRS]);
         }
     } else if (warp == G_BWARP) {
         // ------------------------------------------------------------ B producer
@@ -427,8 +445,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         // never stored
         int cur_tile = -1, npad = 0, row0 = 0;
         bool routed = false;
-        for (int kk = 0; kk < stream_len; ++kk) {
-            const int ti = kk / nch, ch = kk % nch;
+        const int npairs = stream_len >> 1;
+        for (int pk = 0; pk < npairs; ++pk) {
+            const int ti = (2 * pk) / nch, ch0 = (2 * pk) % nch;   // a pair never straddles two tiles
             if (ti != cur_tile) {
                 cur_tile = ti;
                 const Tile t = decode_tile(sm, a, tile_id(ti));
@@ -436,26 +455,28 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 routed = group_expert(a, t.g) >= 0;
                 row0 = (routed ? sm.goff[t.g] : 0) + t.n0;
             }
-            const int s = kk % G_BSTAGES;
-            if (kk >= G_BSTAGES && !gwait_warp(&sm.empty_b[s], ((kk / G_BSTAGES) - 1) & 1, sm, flag, lane))
+            const int p = pk % G_PAIRS;
+            if (pk >= G_PAIRS && !gwait_warp(&sm.empty[p], ((pk / G_PAIRS) - 1) & 1, sm, flag, lane))
                 break;
             if (lane == 0)
-                mbar_arrive_expect_tx(&sm.full_b[s], (uint32_t)(npad * TC_ROW_BYTES));
+                mbar_arrive_expect_tx(&sm.full[p], (uint32_t)(2 * npad * TC_ROW_BYTES));
             __syncwarp();
-            // 64-row boxes, then 16-row boxes for the rest (at most 3 + 3 copies)
-            const int n64 = npad >> 6, n16 = (npad & 63) >> 4;
-            if (lane < n64 + n16) {
-                const int r = lane < n64 ? 64 * lane : 64 * n64 + 16 * (lane - n64);
-                const CUtensorMap *map = lane < n64 ? (routed ? &map_routed64 : &map_shared64)
-                                                    : (routed ? &map_routed16 : &map_shared16);
-                tma_box(smem_u32(sm.b[s]) + (uint32_t)(r * TC_ROW_BYTES), map, ch * TC_KCHUNK, row0 + r, &sm.full_b[s]);
+            // per chunk 64-row boxes, then 16-row boxes for the rest (at most 3 + 3 copies)
+            const int n64 = npad >> 6, n16 = (npad & 63) >> 4, nb = n64 + n16;
+            if (lane < 2 * nb) {
+                const int h2 = lane >= nb ? 1 : 0, j = lane - h2 * nb;
+                const int r = j < n64 ? 64 * j : 64 * n64 + 16 * (j - n64);
+                const CUtensorMap *map = j < n64 ? (routed ? &map_routed64 : &map_shared64)
+                                                 : (routed ? &map_routed16 : &map_shared16);
+                tma_box(smem_u32(sm.b[2 * p + h2]) + (uint32_t)(r * TC_ROW_BYTES), map, (ch0 + h2) * TC_KCHUNK,
+                        row0 + r, &sm.full[p]);
             }
         }
     } else if (warp == G_MMA_WARP) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
             const uint32_t tbase = sm.tmem;
-            int kk = 0;
+            int pk = 0;                                // pairs of chunks so far
             bool ok = true;
             for (int ti = 0; ti < my_tiles && ok; ++ti) {
                 const Tile t = decode_tile(sm, a, tile_id(ti));
@@ -466,21 +487,22 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     break;
                 tc_fence_after();
                 const uint32_t d = tbase + (uint32_t)(ab * 256);
-                for (int ch = 0; ch < nch; ++ch, ++kk) {
-                    const int sa_ = kk % G_ASTAGES, sb_ = kk % G_BSTAGES;
-                    if (!gwait(&sm.full_a[sa_], (kk / G_ASTAGES) & 1, sm, flag) ||
-                        !gwait(&sm.full_b[sb_], (kk / G_BSTAGES) & 1, sm, flag)) {
+                for (int ch = 0; ch < nch; ch += 2, ++pk) {
+                    const int p = pk % G_PAIRS;
+                    if (!gwait(&sm.full[p], (pk / G_PAIRS) & 1, sm, flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t aa = smem_u32(sm.a[sa_]), bb = smem_u32(sm.b[sb_]);
 #pragma unroll
-                    for (int k16 = 0; k16 < 4; ++k16)
-                        tc_mma(d, sw128_desc(aa + 32 * k16), sw128_desc(bb + 32 * k16), idesc,
-                               (ch > 0 || k16 > 0) ? 1u : 0u);
-                    tc_commit(&sm.empty_a[sa_]);
-                    tc_commit(&sm.empty_b[sb_]);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const uint32_t aa = smem_u32(sm.a[2 * p + h2]), bb = smem_u32(sm.b[2 * p + h2]);
+#pragma unroll
+                        for (int k16 = 0; k16 < 4; ++k16)
+                            tc_mma(d, sw128_desc(aa + 32 * k16), sw128_desc(bb + 32 * k16), idesc,
+                                   (ch > 0 || h2 > 0 || k16 > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&sm.empty[p]);
                 }
                 if (ok)
                     tc_commit(&sm.d_full[ab]);
