@@ -23,10 +23,14 @@
 //  5. h rescale     (NVFP4 weights) every h row in place to f16 times a
 //                   power of two;
 //  6. down GEMM     routed experts: y * routing weight -> ybuf[token][choice];
-//  7. shared down   the shared expert's down projection, and the combine
-//                   out = sum over choices of ybuf (in choice order) + y_shared,
-//                   rounded once to bf16 (deterministic: no atomics).
-// Without a shared expert step 7 is a plain combine kernel.
+//  7. shared down   the shared expert's down projection -> ysh[token];
+//  8. combine       out = sum over choices of ybuf (in choice order) + ysh,
+//                   rounded once to bf16 (deterministic: no atomics), a
+//                   streaming kernel of 16-byte loads.
+// Without a shared expert step 7 is skipped.
+// Every GEMM epilogue fetches its tile's per-column factors (routing weight,
+// tensor scale, inverse power of two) into shared memory while the tile's
+// MMAs run, so its loop over columns makes no dependent global loads.
 //
 // NVFP4 operands enter the tensor cores as f16, like the decode path: a
 // weight is e2m1 x e4m3, exact in f16 (at most 6 significant bits, magnitude
@@ -94,6 +98,7 @@ struct GSmem {
     // tiles' bytes have landed, empty once the pair's MMAs have completed
     uint64_t full[G_PAIRS], empty[G_PAIRS];
     uint64_t d_full[2], d_empty[2];
+    alignas(16) float colf[2][G_NMAX];                 // per-column epilogue factor of the tile (by accumulator)
     uint32_t tmem;
     int abort;
     int n_groups;
@@ -517,25 +522,54 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         for (int ti = 0; ti < my_tiles; ++ti) {
             const Tile t = decode_tile(sm, a, tile_id(ti));
             const int ab = ti & 1;
+            const float ts = a_tscale(t.g);
+            const int e = group_expert(a, t.g);
+            // the tile's per-column factors (and ybuf rows), fetched into
+            // shared memory by the four epilogue warps while its MMAs run:
+            // ts times the column's inverse power of two, times its routing
+            // weight for the down projection
+            for (int c = R; c < t.nvalid; c += 128) {
+                float fc = ts;
+                if (a.mode == GM_GATE_UP) {
+                    if (a.xshift) {
+                        const int tok = (e >= 0) ? __ldg(a.list + sm.goff[t.g] + t.n0 + c) / TOPK : t.n0 + c;
+                        fc = ts * pow2f(-__ldg(a.xshift + tok));
+                    }
+                } else if (a.mode == GM_DOWN) {
+                    const int row = sm.goff[t.g] + t.n0 + c;
+                    fc = __ldg(a.topk_w + __ldg(a.list + row)) * ts;
+                    if (a.hshift_r)
+                        fc *= pow2f(-__ldg(a.hshift_r + row));
+                } else if (a.mode == GM_SHARED_DOWN) {
+                    if (a.hshift_s)
+                        fc = ts * pow2f(-__ldg(a.hshift_s + t.n0 + c));
+                }
+                sm.colf[ab][c] = fc;
+            }
+            // the four epilogue warps: tables written before any is read (the
+            // other buffer may still be in use by a warp on the previous tile)
+            asm volatile("bar.sync 1, 128;" ::: "memory");
             if (!gwait_warp(&sm.d_full[ab], (ti >> 1) & 1, sm, flag, lane))
                 break;
             tc_fence_after();
-            const float ts = a_tscale(t.g);
-            const int e = group_expert(a, t.g);
+            const float *colf = sm.colf[ab];
             for (int c0 = 0; c0 < t.npad; c0 += 32) {
                 float v[32];
                 tc_ld32(tbase + (uint32_t)(ab * 256 + c0), v);
-                // per-column factors, loaded by lane j for column c0 + j
-                const int colj = c0 + lane;
-                const bool okj = colj < t.nvalid;
+                // the block's 32 column factors in registers up front (eight
+                // broadcast loads), so no load sits between the stores below
+                float cf[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 q4 = reinterpret_cast<const float4 *>(colf + c0)[i];
+                    cf[4 * i] = q4.x;
+                    cf[4 * i + 1] = q4.y;
+                    cf[4 * i + 2] = q4.z;
+                    cf[4 * i + 3] = q4.w;
+                }
                 if (a.mode == GM_GATE_UP) {
                     // rows 16 bb + i: i < 8 gate, i >= 8 up of feature 8 (8 mt + bb) + (i & 7);
                     // column pair (2 m, 2 m + 1): gate lanes finish column 2 m, up lanes 2 m + 1
-                    float fj = ts;
-                    if (okj && a.xshift) {
-                        const int tok = (e >= 0) ? __ldg(a.list + sm.goff[t.g] + t.n0 + colj) / TOPK : t.n0 + colj;
-                        fj = ts * pow2f(-__ldg(a.xshift + tok));
-                    }
                     const int bb = R >> 4, ii = R & 15;
                     const bool up = ii >= 8;
                     const int f = 8 * (8 * t.mt + bb) + (ii & 7);
@@ -546,60 +580,22 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                         const float send = up ? v[2 * m] : v[2 * m + 1];
                         const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 8);
                         const int col = c0 + 2 * m + (up ? 1 : 0);
-                        const float fc = __shfl_sync(0xFFFFFFFFu, fj, 2 * m + (up ? 1 : 0));
-                        const float gv = (up ? recv : v[2 * m]) * fc;
-                        const float uv = (up ? v[2 * m + 1] : recv) * fc;
-                        if (col < t.nvalid)
+                        if (col < t.nvalid) {
+                            const float fc = up ? cf[2 * m + 1] : cf[2 * m];
+                            const float gv = (up ? recv : v[2 * m]) * fc;
+                            const float uv = (up ? v[2 * m + 1] : recv) * fc;
                             hrow[(size_t)col * I + f] = __float2bfloat16_rn(gv / (1.0f + __expf(-gv)) * uv);
+                        }
                     }
-                } else if (a.mode == GM_DOWN) {
-                    const int f = 128 * t.mt + R;
-                    int v6j = 0;
-                    float fj = 0.0f;
-                    if (okj) {
-                        const int row = sm.goff[t.g] + t.n0 + colj;
-                        v6j = __ldg(a.list + row);
-                        fj = __ldg(a.topk_w + v6j) * ts;
-                        if (a.hshift_r)
-                            fj *= pow2f(-__ldg(a.hshift_r + row));
-                    }
+                } else if (a.mode == GM_DOWN || a.mode == GM_SHARED_DOWN) {
+                    // routed: weighted rows of ybuf in list order; shared: its own rows (ysh)
+                    float *dst = (a.mode == GM_DOWN ? a.ybuf + (size_t)(sm.goff[t.g] + t.n0 + c0) * H
+                                                    : a.ysh + (size_t)(t.n0 + c0) * H) +
+                                 128 * t.mt + R;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int v6 = __shfl_sync(0xFFFFFFFFu, v6j, j);
-                        const float fc = __shfl_sync(0xFFFFFFFFu, fj, j);
+                    for (int j = 0; j < 32; ++j)
                         if (c0 + j < t.nvalid)
-                            a.ybuf[(size_t)v6 * H + f] = v[j] * fc;
-                    }
-                } else if (a.mode == GM_SHARED_DOWN) {
-                    const int f = 128 * t.mt + R;
-                    float fj = ts;
-                    if (okj && a.hshift_s)
-                        fj = ts * pow2f(-__ldg(a.hshift_s + t.n0 + colj));
-#pragma unroll
-                    for (int j0 = 0; j0 < 32; j0 += 8) {
-                        float y[8][TOPK];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int col = c0 + j0 + j;
-                            const float *yb = a.ybuf + (size_t)(t.n0 + col) * TOPK * H + f;
-#pragma unroll
-                            for (int i = 0; i < TOPK; ++i)
-                                y[j][i] = (col < t.nvalid) ? __ldcs(yb + (size_t)i * H) : 0.0f;
-                        }
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int col = c0 + j0 + j;
-                            const float fc = __shfl_sync(0xFFFFFFFFu, fj, j0 + j);
-                            if (col < t.nvalid) {
-                                float acc = 0.0f;
-#pragma unroll
-                                for (int i = 0; i < TOPK; ++i)
-                                    acc += y[j][i];
-                                acc += v[j0 + j] * fc;
-                                a.out[(size_t)(t.n0 + col) * H + f] = __float2bfloat16_rn(acc);
-                            }
-                        }
-                    }
+                            dst[(size_t)j * H] = v[j] * cf[j];
                 } else {
                     const int ee = 128 * t.mt + R;
 #pragma unroll
@@ -745,8 +741,8 @@ __global__ void __launch_bounds__(E) moe_grouped_scan_kernel(const int32_t *hist
 // copies token t's row of src (H 16-bit values) to xs[that list row].
 __global__ void __launch_bounds__(G_TOK_PER_CTA * TOPK) moe_grouped_scatter_kernel(const int32_t *idx, int T,
                                                                                  const int32_t *base, int32_t *list,
-                                                                                 const uint16_t *src, uint16_t *xs,
-                                                                                 uint32_t *flag)
+                                                                                 int32_t *inv, const uint16_t *src,
+                                                                                 uint16_t *xs, uint32_t *flag)
 {
     griddep_wait();
     griddep_launch();
@@ -771,6 +767,8 @@ __global__ void __launch_bounds__(G_TOK_PER_CTA * TOPK) moe_grouped_scatter_kern
         }
     }
     pos[k] = p;
+    if (k < n)
+        inv[v0 + k] = p;                               // the list row of (token, choice), -1 if invalid
     __syncthreads();
     // one warp per listed row: H values = 256 x 16 bytes
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -824,19 +822,48 @@ __global__ void __launch_bounds__(256) moe_grouped_hscale_kernel(uint16_t *h, in
     }
 }
 
-// out[t] = sum over choices of ybuf[t][i] (choice order), without a shared expert.
-__global__ void __launch_bounds__(256) moe_grouped_combine_kernel(const float *ybuf, int T, __nv_bfloat16 *out)
+// out[t] = sum over choices of the choice's ybuf row (choice order; ybuf is
+// in list order, inv[6 t + i] its row), then + ysh[t] (the shared expert's
+// down projection, when there is one), rounded once to bf16.  Four
+// consecutive features per thread (16-byte loads).
+__global__ void __launch_bounds__(256) moe_grouped_combine_kernel(const float *ybuf, const int32_t *inv,
+                                                                  const float *ysh, int T, __nv_bfloat16 *out)
 {
     griddep_wait();
     griddep_launch();
-    const size_t n = (size_t)T * H;
-    for (size_t o = (size_t)blockIdx.x * blockDim.x + threadIdx.x; o < n; o += (size_t)gridDim.x * blockDim.x) {
-        const size_t t = o / H, f = o % H;
-        float acc = 0.0f;
+    const size_t n4 = (size_t)T * (H / 4);
+    for (size_t o = (size_t)blockIdx.x * blockDim.x + threadIdx.x; o < n4; o += (size_t)gridDim.x * blockDim.x) {
+        const size_t t = o / (H / 4), f = 4 * (o % (H / 4));
+        int r[TOPK];
 #pragma unroll
         for (int i = 0; i < TOPK; ++i)
-            acc += __ldcg(ybuf + (t * TOPK + i) * H + f);
-        out[o] = __float2bfloat16_rn(acc);
+            r[i] = __ldg(inv + t * TOPK + i);
+        float4 y[TOPK + 1];
+#pragma unroll
+        for (int i = 0; i < TOPK; ++i)
+            y[i] = r[i] >= 0 ? __ldcs(reinterpret_cast<const float4 *>(ybuf + (size_t)r[i] * H + f))
+                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (ysh)
+            y[TOPK] = __ldcs(reinterpret_cast<const float4 *>(ysh + t * H + f));
+        float4 acc = y[0];
+#pragma unroll
+        for (int i = 1; i < TOPK; ++i) {
+            acc.x += y[i].x;
+            acc.y += y[i].y;
+            acc.z += y[i].z;
+            acc.w += y[i].w;
+        }
+        if (ysh) {
+            acc.x += y[TOPK].x;
+            acc.y += y[TOPK].y;
+            acc.z += y[TOPK].z;
+            acc.w += y[TOPK].w;
+        }
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t *>(&lo);
+        pk.y = *reinterpret_cast<uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(out + t * H + f) = pk;
     }
 }
 
@@ -865,6 +892,8 @@ GWsLayout gws_layout(int T)
     L.h_routed = o;  o = o + (size_t)T * TOPK * I * 2;          // h_shared follows directly
     L.h_shared = o;  o = align256(o + (size_t)T * I * 2);
     L.ybuf = o;      o = align256(o + (size_t)T * TOPK * H * 4);
+    L.ysh = o;       o = align256(o + (size_t)T * H * 4);
+    L.inv = o;       o = align256(o + (size_t)T * TOPK * 4);
     L.total = o;
     return L;
 }
@@ -1000,7 +1029,8 @@ cudaError_t launch_grouped_layer(const GroupedArgs &a0, int nsm, cudaStream_t st
             return e;
         const uint16_t *src = reinterpret_cast<const uint16_t *>(a.bf16w ? (const void *)a.x : (const void *)(ws + L.x16));
         uint16_t *xs = reinterpret_cast<uint16_t *>(ws + L.xs);
-        void *cargs[] = {&idx, &T, &base, &list, &src, &xs, &flag};
+        int32_t *inv = reinterpret_cast<int32_t *>(ws + L.inv);
+        void *cargs[] = {&idx, &T, &base, &list, &inv, &src, &xs, &flag};
         e = launch_ex((const void *)moe_grouped_scatter_kernel, dim3(nc), dim3(G_TOK_PER_CTA * TOPK), 0, st, cargs);
         if (e != cudaSuccess)
             return e;
@@ -1020,6 +1050,7 @@ cudaError_t launch_grouped_layer(const GroupedArgs &a0, int nsm, cudaStream_t st
     g.h_routed = reinterpret_cast<__nv_bfloat16 *>(ws + L.h_routed);
     g.h_shared = reinterpret_cast<__nv_bfloat16 *>(ws + L.h_shared);
     g.ybuf = reinterpret_cast<float *>(ws + L.ybuf);
+    g.ysh = reinterpret_cast<float *>(ws + L.ysh);
     g.out = a.out;
     int32_t *hshift = reinterpret_cast<int32_t *>(ws + L.hshift);
     if (f16) {
@@ -1062,12 +1093,15 @@ cudaError_t launch_grouped_layer(const GroupedArgs &a0, int nsm, cudaStream_t st
         return e;
     if (a.n_shared) {
         g.mode = GM_SHARED_DOWN;
-        return launch_gemm(g, nullptr, 0, ws + L.h_shared, (size_t)T, I, nsm, st);
+        if ((e = launch_gemm(g, nullptr, 0, ws + L.h_shared, (size_t)T, I, nsm, st)) != cudaSuccess)
+            return e;
     }
     const float *yb = g.ybuf;
+    const float *ys = a.n_shared ? g.ysh : nullptr;
     __nv_bfloat16 *out = a.out;
-    void *cargs[] = {&yb, &T, &out};
-    return launch_ex((const void *)moe_grouped_combine_kernel, dim3(nsm * 4), dim3(256), 0, st, cargs);
+    const int32_t *inv = reinterpret_cast<const int32_t *>(ws + L.inv);
+    void *cargs[] = {&yb, &inv, &ys, &T, &out};
+    return launch_ex((const void *)moe_grouped_combine_kernel, dim3(nsm * 8), dim3(256), 0, st, cargs);
 }
 
 }  // namespace moe

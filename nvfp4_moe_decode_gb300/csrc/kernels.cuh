@@ -198,7 +198,9 @@ struct GWsLayout {
     size_t hshift;     // i32[T * TOPK + T]: power of two of each h row (routed rows, then shared)
     size_t h_routed;   // [T * TOPK][I]: SiLU*up of list row r (bf16; f16 x 2^hshift after the rescale)
     size_t h_shared;   // [T][I], directly after h_routed
-    size_t ybuf;       // f32[T * TOPK][H]: weighted down output of (token, choice)
+    size_t ybuf;       // f32[T * TOPK][H]: weighted down output of (token, choice), in list order
+    size_t ysh;        // f32[T][H]: the shared expert's down output
+    size_t inv;        // i32[T][TOPK]: list row of (token, choice), -1 if invalid
     size_t total;
 };
 GWsLayout gws_layout(int T);
@@ -223,7 +225,8 @@ struct GArgs {
     const int32_t *counts, *offsets, *list;
     const float *topk_w;
     __nv_bfloat16 *h_routed, *h_shared;
-    float *ybuf;
+    float *ybuf;                    // [T * TOPK][H] weighted routed outputs, in list order
+    float *ysh;                     // [T][H] the shared expert's down projection
     __nv_bfloat16 *out;
     const int32_t *xshift;          // per token (f16 operands), or null
     const int32_t *hshift_r, *hshift_s; // per routed / shared h row (f16 operands), or null
