@@ -15,9 +15,10 @@
 //                   weights) the token in f16 times a power of two, x16;
 //  3. lists         a scan of the counts and a scatter: per expert, the
 //                   (token, choice) pairs v = 6 t + i that selected it, in
-//                   increasing v, and each listed token's row copied to
-//                   xs[list row] (the GEMM operand, x16 or x), so that every
-//                   GEMM reads consecutive rows;
+//                   increasing v (and the inverse map); then a gather copies
+//                   each listed token's row to xs[list row] (the GEMM
+//                   operand, x16 or x), so that every GEMM reads consecutive
+//                   rows;
 //  4. gate/up GEMM  for every routed expert its listed tokens, and for the
 //                   shared expert all tokens: SiLU(g) * u -> h (bf16);
 //  5. h rescale     (NVFP4 weights) every h row in place to f16 times a
@@ -737,17 +738,15 @@ __global__ void __launch_bounds__(E) moe_grouped_scan_kernel(const int32_t *hist
 
 // Expert lists, step 2 of 2: CTA c writes the pairs v = 6 t + i of its
 // tokens to list[base[c][e] + rank], rank = earlier pairs of the CTA that
-// chose the same expert, so every expert's rows are in increasing v; then
-// copies token t's row of src (H 16-bit values) to xs[that list row].
+// chose the same expert, so every expert's rows are in increasing v, and
+// inv[v] = that list row (-1 for an invalid selection).
 __global__ void __launch_bounds__(G_TOK_PER_CTA * TOPK) moe_grouped_scatter_kernel(const int32_t *idx, int T,
                                                                                  const int32_t *base, int32_t *list,
-                                                                                 int32_t *inv, const uint16_t *src,
-                                                                                 uint16_t *xs, uint32_t *flag)
+                                                                                 int32_t *inv, uint32_t *flag)
 {
     griddep_wait();
     griddep_launch();
     __shared__ int ex[G_TOK_PER_CTA * TOPK];
-    __shared__ int pos[G_TOK_PER_CTA * TOPK];
     const int n = min(G_TOK_PER_CTA, T - (int)blockIdx.x * G_TOK_PER_CTA) * TOPK;
     const int v0 = blockIdx.x * G_TOK_PER_CTA * TOPK;
     const int k = threadIdx.x;
@@ -766,21 +765,42 @@ __global__ void __launch_bounds__(G_TOK_PER_CTA * TOPK) moe_grouped_scatter_kern
             list[p] = v0 + k;
         }
     }
-    pos[k] = p;
     if (k < n)
         inv[v0 + k] = p;                               // the list row of (token, choice), -1 if invalid
-    __syncthreads();
-    // one warp per listed row: H values = 256 x 16 bytes
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int j = warp; j < n; j += blockDim.x >> 5) {
-        const int pj = pos[j];
-        if (pj < 0)
-            continue;
-        const uint4 *s4 = reinterpret_cast<const uint4 *>(src + (size_t)((v0 + j) / TOPK) * H);
-        uint4 *d4 = reinterpret_cast<uint4 *>(xs + (size_t)pj * H);
+}
+
+// xs[r] = src[list[r] / TOPK]: every listed (token, choice) row copied to its
+// list row, 16 bytes per thread and four copies in flight per thread.  Only
+// the offsets[E] listed rows are copied (fewer than T * TOPK when a selection
+// was invalid), and a token index outside [0, T) is skipped.
+__global__ void __launch_bounds__(256) moe_grouped_gather_kernel(const int32_t *list, const int32_t *offsets, int T,
+                                                                 const uint16_t *src, uint16_t *xs)
+{
+    griddep_wait();
+    griddep_launch();
+    constexpr int Q = H / 8;                           // 16-byte pieces per row
+    const int nrows = min(__ldg(offsets + E), T * TOPK);
+    const size_t n = (size_t)max(nrows, 0) * Q, stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t q0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q0 < n; q0 += 4 * stride) {
+        uint4 v[4];
+        size_t dq[4];
 #pragma unroll
-        for (int i = 0; i < H / 256; ++i)
-            d4[lane + 32 * i] = __ldg(s4 + lane + 32 * i);
+        for (int u = 0; u < 4; ++u) {
+            const size_t q = q0 + u * stride;
+            dq[u] = q;
+            if (q < n) {
+                const size_t r = q / Q, c = q % Q;
+                const int t = __ldg(list + r) / TOPK;
+                if ((unsigned)t < (unsigned)T)
+                    v[u] = __ldg(reinterpret_cast<const uint4 *>(src) + (size_t)t * Q + c);
+                else
+                    dq[u] = n;                         // skipped
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (dq[u] < n)
+                reinterpret_cast<uint4 *>(xs)[dq[u]] = v[u];
     }
 }
 
@@ -1030,8 +1050,12 @@ cudaError_t launch_grouped_layer(const GroupedArgs &a0, int nsm, cudaStream_t st
         const uint16_t *src = reinterpret_cast<const uint16_t *>(a.bf16w ? (const void *)a.x : (const void *)(ws + L.x16));
         uint16_t *xs = reinterpret_cast<uint16_t *>(ws + L.xs);
         int32_t *inv = reinterpret_cast<int32_t *>(ws + L.inv);
-        void *cargs[] = {&idx, &T, &base, &list, &inv, &src, &xs, &flag};
+        void *cargs[] = {&idx, &T, &base, &list, &inv, &flag};
         e = launch_ex((const void *)moe_grouped_scatter_kernel, dim3(nc), dim3(G_TOK_PER_CTA * TOPK), 0, st, cargs);
+        if (e != cudaSuccess)
+            return e;
+        void *gargs[] = {&list, &offsets, &T, &src, &xs};
+        e = launch_ex((const void *)moe_grouped_gather_kernel, dim3(nsm * 8), dim3(256), 0, st, gargs);
         if (e != cudaSuccess)
             return e;
     }

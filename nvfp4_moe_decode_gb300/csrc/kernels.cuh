@@ -176,7 +176,7 @@ cudaError_t launch_gemv(GemvArgs a, int sm_count, cudaStream_t stream);
 // Grouped path (T > MAXT): see grouped.cu.
 // ---------------------------------------------------------------------------
 constexpr int G_NMAX = 256;            // tokens per GEMM tile
-constexpr int G_TOK_PER_CTA = 128;     // tokens per CTA of the top-k / list kernels
+constexpr int G_TOK_PER_CTA = 32;      // tokens per CTA of the top-k / list kernels (one warp per token)
 constexpr int MAX_TOKENS = MOE_MAX_TOKENS;
 
 enum GMode { GM_ROUTER = 0, GM_GATE_UP = 1, GM_DOWN = 2, GM_SHARED_DOWN = 3 };
