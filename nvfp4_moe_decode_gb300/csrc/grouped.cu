@@ -576,17 +576,23 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     const int f = 8 * (8 * t.mt + bb) + (ii & 7);
                     __nv_bfloat16 *hrow = (e >= 0) ? a.h_routed + (size_t)(sm.goff[t.g] + t.n0) * I
                                                    : a.h_shared + (size_t)t.n0 * I;
+                    float hv[16];
 #pragma unroll
                     for (int m = 0; m < 16; ++m) {
+                        // branch-free, so the 16 chains interleave; padding
+                        // columns are computed and not stored
                         const float send = up ? v[2 * m] : v[2 * m + 1];
                         const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+                        const float fc = up ? cf[2 * m + 1] : cf[2 * m];
+                        const float gv = (up ? recv : v[2 * m]) * fc;
+                        const float uv = (up ? v[2 * m + 1] : recv) * fc;
+                        hv[m] = gv / (1.0f + __expf(-gv)) * uv;
+                    }
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
                         const int col = c0 + 2 * m + (up ? 1 : 0);
-                        if (col < t.nvalid) {
-                            const float fc = up ? cf[2 * m + 1] : cf[2 * m];
-                            const float gv = (up ? recv : v[2 * m]) * fc;
-                            const float uv = (up ? v[2 * m + 1] : recv) * fc;
-                            hrow[(size_t)col * I + f] = __float2bfloat16_rn(gv / (1.0f + __expf(-gv)) * uv);
-                        }
+                        if (col < t.nvalid)
+                            hrow[(size_t)col * I + f] = __float2bfloat16_rn(hv[m]);
                     }
                 } else if (a.mode == GM_DOWN || a.mode == GM_SHARED_DOWN) {
                     // routed: weighted rows of ybuf in list order; shared: its own rows (ysh)
@@ -688,52 +694,76 @@ __global__ void __launch_bounds__(1024) moe_grouped_topk_kernel(const float *log
         hist[(size_t)blockIdx.x * E + i] = h[i];
 }
 
-// Expert lists, step 1 of 2 (one CTA of E threads): thread e turns the
-// per-CTA counts hist[c][e] into the first list row of (c, e),
-// base[c][e] = offsets[e] + sum over c' < c of hist[c'][e], where offsets
-// is the exclusive prefix of the expert totals (counts).
-__global__ void __launch_bounds__(E) moe_grouped_scan_kernel(const int32_t *hist, int nc, int32_t *base,
-                                                           int32_t *counts, int32_t *offsets)
+// Expert lists, step 1 of 2 (one CTA, G_SCAN_PARTS threads per expert, each
+// over a quarter of the CTA rows): the per-CTA counts hist[c][e] become the
+// first list row of (c, e), base[c][e] = offsets[e] + sum over c' < c of
+// hist[c'][e], where offsets is the exclusive prefix of the expert totals
+// (counts): partial sums, then the totals and offsets, then each part writes
+// its rows from its starting value.
+constexpr int G_SCAN_PARTS = 4;                        // threads per expert in the scan
+
+__global__ void __launch_bounds__(E *G_SCAN_PARTS) moe_grouped_scan_kernel(const int32_t *hist, int nc,
+                                                                           int32_t *base, int32_t *counts,
+                                                                           int32_t *offsets)
 {
     griddep_wait();
     griddep_launch();
-    const int e = threadIdx.x;
-    int run = 0;
-    for (int c0 = 0; c0 < nc; c0 += 16) {
-        int hv[16];
+    const int e = threadIdx.x % E, part = threadIdx.x / E;
+    // rows [c_lo, c_hi) of hist for this (expert, part)
+    const int per = (nc + G_SCAN_PARTS - 1) / G_SCAN_PARTS;
+    const int c_lo = min(nc, part * per), c_hi = min(nc, c_lo + per);
+    auto sweep = [&](int run, bool store) {
+        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+            int hv[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            hv[j] = (c0 + j < nc) ? hist[(size_t)(c0 + j) * E + e] : 0;
+            for (int j = 0; j < 16; ++j)
+                hv[j] = (c0 + j < c_hi) ? hist[(size_t)(c0 + j) * E + e] : 0;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            if (c0 + j < nc)
-                base[(size_t)(c0 + j) * E + e] = run;
-            run += hv[j];
+            for (int j = 0; j < 16; ++j) {
+                if (store && c0 + j < c_hi)
+                    base[(size_t)(c0 + j) * E + e] = run;
+                run += hv[j];
+            }
         }
-    }
-    // exclusive prefix over experts (E = 256 totals, one warp-scan per 32)
-    const int lane = e & 31, warp = e >> 5;
-    int incl = run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o)
-            incl += v;
-    }
-    __shared__ int wtot[E / 32];
-    if (lane == 31)
-        wtot[warp] = incl;
+        return run;
+    };
+    __shared__ int psum[G_SCAN_PARTS][E];
+    __shared__ int off_s[E];
+    psum[part][e] = sweep(0, false);
     __syncthreads();
-    int before = 0;
-    for (int w2 = 0; w2 < warp; ++w2)
-        before += wtot[w2];
-    const int off = before + incl - run;
-    counts[e] = run;
-    offsets[e] = off;
-    if (e == E - 1)
-        offsets[E] = off + run;
-    for (int c = 0; c < nc; ++c)
-        base[(size_t)c * E + e] += off;
+    if (part == 0) {
+        int tot = 0;
+#pragma unroll
+        for (int q = 0; q < G_SCAN_PARTS; ++q)
+            tot += psum[q][e];
+        // exclusive prefix over experts (E = 256 totals, one warp-scan per 32)
+        const int lane = e & 31, warp = e >> 5;
+        int incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o)
+                incl += v;
+        }
+        __shared__ int wtot[E / 32];
+        if (lane == 31)
+            wtot[warp] = incl;
+        asm volatile("bar.sync 1, %0;" ::"n"(E) : "memory");   // the E threads of part 0
+        int before = 0;
+        for (int w2 = 0; w2 < warp; ++w2)
+            before += wtot[w2];
+        const int off = before + incl - tot;
+        counts[e] = tot;
+        offsets[e] = off;
+        if (e == E - 1)
+            offsets[E] = off + tot;
+        off_s[e] = off;
+    }
+    __syncthreads();
+    int start = off_s[e];
+    for (int q = 0; q < part; ++q)
+        start += psum[q][e];
+    sweep(start, true);
 }
 
 // Expert lists, step 2 of 2: CTA c writes the pairs v = 6 t + i of its
@@ -770,7 +800,7 @@ __global__ void __launch_bounds__(G_TOK_PER_CTA * TOPK) moe_grouped_scatter_kern
 }
 
 // xs[r] = src[list[r] / TOPK]: every listed (token, choice) row copied to its
-// list row, 16 bytes per thread and four copies in flight per thread.  Only
+// list row, 16 bytes per thread and eight copies in flight per thread.  Only
 // the offsets[E] listed rows are copied (fewer than T * TOPK when a selection
 // was invalid), and a token index outside [0, T) is skipped.
 __global__ void __launch_bounds__(256) moe_grouped_gather_kernel(const int32_t *list, const int32_t *offsets, int T,
@@ -781,11 +811,11 @@ __global__ void __launch_bounds__(256) moe_grouped_gather_kernel(const int32_t *
     constexpr int Q = H / 8;                           // 16-byte pieces per row
     const int nrows = min(__ldg(offsets + E), T * TOPK);
     const size_t n = (size_t)max(nrows, 0) * Q, stride = (size_t)gridDim.x * blockDim.x;
-    for (size_t q0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q0 < n; q0 += 4 * stride) {
-        uint4 v[4];
-        size_t dq[4];
+    for (size_t q0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q0 < n; q0 += 8 * stride) {
+        uint4 v[8];
+        size_t dq[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 8; ++u) {
             const size_t q = q0 + u * stride;
             dq[u] = q;
             if (q < n) {
@@ -798,9 +828,9 @@ __global__ void __launch_bounds__(256) moe_grouped_gather_kernel(const int32_t *
             }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < 8; ++u)
             if (dq[u] < n)
-                reinterpret_cast<uint4 *>(xs)[dq[u]] = v[u];
+                __stcs(reinterpret_cast<uint4 *>(xs) + dq[u], v[u]);
     }
 }
 
@@ -1044,7 +1074,7 @@ cudaError_t launch_grouped_layer(const GroupedArgs &a0, int nsm, cudaStream_t st
     int nc = (a.T + G_TOK_PER_CTA - 1) / G_TOK_PER_CTA;
     {
         void *sargs[] = {&hist, &nc, &base, &counts, &offsets};
-        e = launch_ex((const void *)moe_grouped_scan_kernel, dim3(1), dim3(E), 0, st, sargs);
+        e = launch_ex((const void *)moe_grouped_scan_kernel, dim3(1), dim3(E * G_SCAN_PARTS), 0, st, sargs);
         if (e != cudaSuccess)
             return e;
         const uint16_t *src = reinterpret_cast<const uint16_t *>(a.bf16w ? (const void *)a.x : (const void *)(ws + L.x16));
