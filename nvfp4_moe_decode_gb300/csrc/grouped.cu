@@ -631,7 +631,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 // One warp per token: top-k of the fp32 logits, renormalised weights; CTA
 // c (G_TOK_PER_CTA tokens) counts its selections per expert into hist[c][E];
 // with x16 given, the token row is also written as f16 times 2^xshift[t].
-__global__ void __launch_bounds__(1024) moe_grouped_topk_kernel(const float *logits, int T, int32_t *idx, float *w,
+constexpr int G_TOPK_WARPS = 16;                       // warps per top-k CTA (two tokens each)
+
+__global__ void __launch_bounds__(G_TOPK_WARPS * 32) moe_grouped_topk_kernel(const float *logits, int T, int32_t *idx, float *w,
                                                              int32_t *hist, const __nv_bfloat16 *x, __half *x16,
                                                              int32_t *xshift, uint32_t *flag)
 {
@@ -642,8 +644,8 @@ __global__ void __launch_bounds__(1024) moe_grouped_topk_kernel(const float *log
     for (int i = threadIdx.x; i < E; i += blockDim.x)
         h[i] = 0;
     __syncthreads();
-    for (int k = 0; k < G_TOK_PER_CTA / 32; ++k) {
-        const int t = blockIdx.x * G_TOK_PER_CTA + k * 32 + warp;
+    for (int k = 0; k < G_TOK_PER_CTA / G_TOPK_WARPS; ++k) {
+        const int t = blockIdx.x * G_TOK_PER_CTA + k * G_TOPK_WARPS + warp;
         if (t >= T)
             break;
         int ex;
@@ -694,44 +696,54 @@ __global__ void __launch_bounds__(1024) moe_grouped_topk_kernel(const float *log
         hist[(size_t)blockIdx.x * E + i] = h[i];
 }
 
-// Expert lists, step 1 of 2 (one CTA, G_SCAN_PARTS threads per expert, each
-// over a quarter of the CTA rows): the per-CTA counts hist[c][e] become the
+// Expert lists, step 1 of 2 (one CTA; a thread takes four experts over one
+// of G_SCAN_PARTS ranges of the CTA rows): the per-CTA counts hist[c][e] become the
 // first list row of (c, e), base[c][e] = offsets[e] + sum over c' < c of
 // hist[c'][e], where offsets is the exclusive prefix of the expert totals
 // (counts): partial sums, then the totals and offsets, then each part writes
 // its rows from its starting value.
-constexpr int G_SCAN_PARTS = 4;                        // threads per expert in the scan
+constexpr int G_SCAN_PARTS = 16;                       // row ranges of the scan (4 experts per thread)
 
-__global__ void __launch_bounds__(E *G_SCAN_PARTS) moe_grouped_scan_kernel(const int32_t *hist, int nc,
-                                                                           int32_t *base, int32_t *counts,
-                                                                           int32_t *offsets)
+__global__ void __launch_bounds__(E / 4 * G_SCAN_PARTS) moe_grouped_scan_kernel(const int32_t *hist, int nc,
+                                                                                int32_t *base, int32_t *counts,
+                                                                                int32_t *offsets)
 {
     griddep_wait();
     griddep_launch();
-    const int e = threadIdx.x % E, part = threadIdx.x / E;
-    // rows [c_lo, c_hi) of hist for this (expert, part)
+    const int g4 = threadIdx.x % (E / 4), part = threadIdx.x / (E / 4);   // experts 4 g4 .. 4 g4 + 3
     const int per = (nc + G_SCAN_PARTS - 1) / G_SCAN_PARTS;
     const int c_lo = min(nc, part * per), c_hi = min(nc, c_lo + per);
-    auto sweep = [&](int run, bool store) {
-        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-            int hv[16];
+    auto sweep = [&](int4 run, bool store) {
+        for (int c0 = c_lo; c0 < c_hi; c0 += 8) {
+            int4 hv[8];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                hv[j] = (c0 + j < c_hi) ? hist[(size_t)(c0 + j) * E + e] : 0;
+            for (int j = 0; j < 8; ++j)
+                hv[j] = (c0 + j < c_hi) ? __ldcg(reinterpret_cast<const int4 *>(hist + (size_t)(c0 + j) * E) + g4)
+                                        : make_int4(0, 0, 0, 0);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < 8; ++j) {
                 if (store && c0 + j < c_hi)
-                    base[(size_t)(c0 + j) * E + e] = run;
-                run += hv[j];
+                    reinterpret_cast<int4 *>(base + (size_t)(c0 + j) * E)[g4] = run;
+                run.x += hv[j].x;
+                run.y += hv[j].y;
+                run.z += hv[j].z;
+                run.w += hv[j].w;
             }
         }
         return run;
     };
     __shared__ int psum[G_SCAN_PARTS][E];
     __shared__ int off_s[E];
-    psum[part][e] = sweep(0, false);
+    {
+        const int4 r = sweep(make_int4(0, 0, 0, 0), false);
+        psum[part][4 * g4] = r.x;
+        psum[part][4 * g4 + 1] = r.y;
+        psum[part][4 * g4 + 2] = r.z;
+        psum[part][4 * g4 + 3] = r.w;
+    }
     __syncthreads();
-    if (part == 0) {
+    if (threadIdx.x < E) {
+        const int e = threadIdx.x;
         int tot = 0;
 #pragma unroll
         for (int q = 0; q < G_SCAN_PARTS; ++q)
@@ -748,7 +760,7 @@ __global__ void __launch_bounds__(E *G_SCAN_PARTS) moe_grouped_scan_kernel(const
         __shared__ int wtot[E / 32];
         if (lane == 31)
             wtot[warp] = incl;
-        asm volatile("bar.sync 1, %0;" ::"n"(E) : "memory");   // the E threads of part 0
+        asm volatile("bar.sync 1, %0;" ::"n"(E) : "memory");   // the first E threads
         int before = 0;
         for (int w2 = 0; w2 < warp; ++w2)
             before += wtot[w2];
@@ -760,9 +772,13 @@ __global__ void __launch_bounds__(E *G_SCAN_PARTS) moe_grouped_scan_kernel(const
         off_s[e] = off;
     }
     __syncthreads();
-    int start = off_s[e];
-    for (int q = 0; q < part; ++q)
-        start += psum[q][e];
+    int4 start = make_int4(off_s[4 * g4], off_s[4 * g4 + 1], off_s[4 * g4 + 2], off_s[4 * g4 + 3]);
+    for (int q = 0; q < part; ++q) {
+        start.x += psum[q][4 * g4];
+        start.y += psum[q][4 * g4 + 1];
+        start.z += psum[q][4 * g4 + 2];
+        start.w += psum[q][4 * g4 + 3];
+    }
     sweep(start, true);
 }
 
@@ -1050,7 +1066,7 @@ cudaError_t launch_grouped_route(const GroupedArgs &a, int nsm, cudaStream_t st)
     int32_t *xshift = reinterpret_cast<int32_t *>(ws + L.xshift);
     uint32_t *flag = g.flag;
     void *targs[] = {&logits, &T, &idx, &w, &hist, &x, &x16, &xshift, &flag};
-    return launch_ex((const void *)moe_grouped_topk_kernel, dim3((a.T + G_TOK_PER_CTA - 1) / G_TOK_PER_CTA), dim3(1024),
+    return launch_ex((const void *)moe_grouped_topk_kernel, dim3((a.T + G_TOK_PER_CTA - 1) / G_TOK_PER_CTA), dim3(G_TOPK_WARPS * 32),
                      0, st, targs);
 }
 
@@ -1074,7 +1090,7 @@ cudaError_t launch_grouped_layer(const GroupedArgs &a0, int nsm, cudaStream_t st
     int nc = (a.T + G_TOK_PER_CTA - 1) / G_TOK_PER_CTA;
     {
         void *sargs[] = {&hist, &nc, &base, &counts, &offsets};
-        e = launch_ex((const void *)moe_grouped_scan_kernel, dim3(1), dim3(E * G_SCAN_PARTS), 0, st, sargs);
+        e = launch_ex((const void *)moe_grouped_scan_kernel, dim3(1), dim3(E / 4 * G_SCAN_PARTS), 0, st, sargs);
         if (e != cudaSuccess)
             return e;
         const uint16_t *src = reinterpret_cast<const uint16_t *>(a.bf16w ? (const void *)a.x : (const void *)(ws + L.x16));
