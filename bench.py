@@ -15,8 +15,9 @@ rotation are far larger than the 126 MB L2): step k runs layer k mod L.
 (x <- x + MoE_l(RMSNorm(x)), one moe_stack_forward per step; the stack is far
 larger than L2, so it runs cold without rotation).
 
-9..160 tokens run the decode kernel on chunks of at most 8 tokens (bytes
-summed over the chunks).  Above 160 tokens the grouped tensor-core path runs;
+9..88 tokens (BF16 weights: 9..56) run the decode kernel on chunks of at
+most 8 tokens (bytes summed over the chunks).  Above that the grouped
+tensor-core path runs;
 the line then reports the layer's dense-equivalent TFLOP/s (router + 7 expert
 MLPs per token, padding excluded) against the measured bf16 tensor peak.
 --dense times the dense NVFP4 GEMV (moe_dense_gemv_nvfp4) instead.
@@ -326,7 +327,7 @@ def main():
         if rank == 0:
             print(json.dumps(line), flush=True)
         return
-    if T > 160:
+    if T > chunk_limit(WT):
         line = measure_grouped(args, T, WT, world, dev, True, K, W)
     else:
         line = measure_decode(args, T, WT, L, world, dev, True, K, W)
@@ -401,14 +402,20 @@ def timed_replays(stream, graphs, local: int):
     return e0.elapsed_time(e1), clk
 
 
+def chunk_limit(WT: str) -> int:
+    """The largest T the library runs as chunks of the decode kernel."""
+    import nvfp4_moe_decode_gb300 as m
+    return m.MAX_CHUNKED_T_BF16 if WT == "bf16" else m.MAX_CHUNKED_T
+
+
 def chunks_of(T: int):
-    """The library's balanced chunks of at most 8 tokens (T <= 160)."""
+    """The library's balanced chunks of at most 8 tokens (T <= chunk_limit)."""
     n = (T + 7) // 8
     return [(T * c // n, T * (c + 1) // n) for c in range(n)]
 
 
 def measure_decode(args, T: int, WT: str, L: int, world: int, dev, with_e2e: bool, K: int, W: int) -> dict:
-    """One decode-path layer (T <= 8, or up to 160 tokens in chunks of at
+    """One decode-path layer (T <= 8, or up to chunk_limit tokens in chunks of at
     most 8) per step, rotating over L resident layers.  The bytes of a step
     add up the chunks: each reads the router, its own selected and the
     shared experts, its x and out."""

@@ -34,7 +34,8 @@
  * 2, of either weight type, for 1..MOE_MAX_DECODE_T tokens), and
  * 1 <= T <= MOE_MAX_TOKENS tokens per call (the decode kernel up to
  * MOE_MAX_DECODE_T tokens, on chunks of at most MOE_MAX_DECODE_T tokens up to
- * MOE_MAX_CHUNKED_T, the grouped tensor-core path above; the stack and
+ * MOE_MAX_CHUNKED_T (BF16 weights: MOE_MAX_CHUNKED_T_BF16), the grouped
+ * tensor-core path above; the stack and
  * pre-norm calls take 1..MOE_MAX_DECODE_T).
  *
  * Conventions for every entry point:
@@ -102,7 +103,8 @@ enum {
 #define MOE_EXPERTS 256
 #define MOE_TOPK 6
 #define MOE_MAX_DECODE_T 8
-#define MOE_MAX_CHUNKED_T 160  /* largest T of moe_layer_forward's chunked decode path */
+#define MOE_MAX_CHUNKED_T 88        /* largest T of moe_layer_forward's chunked decode path (NVFP4 weights) */
+#define MOE_MAX_CHUNKED_T_BF16 56   /* the same for BF16 weights */
 #define MOE_MAX_TOKENS 65536   /* largest T of moe_route / moe_layer_forward */
 
 /*
@@ -178,10 +180,10 @@ moe_status moe_dequant_nvfp4(const void *packed, int N, int K, int kind, float t
 /* Workspace bytes for moe_route / moe_layer_forward with T tokens (0 unless
  * 1 <= T <= MOE_MAX_TOKENS).  The workspace holds routing results, the
  * SiLU*up activations, combine partials, arrival counters and the device
- * flag; up to MOE_MAX_CHUNKED_T tokens also every chunk's routing; above
- * MOE_MAX_DECODE_T tokens also the grouped path's expert lists, the tokens'
- * rows sorted by expert and the per-(token, choice) down outputs (about
- * 72 KB per token; the grouped router of moe_route uses them at any T above
+ * flag; above MOE_MAX_DECODE_T tokens also the routing of every token
+ * (either path), the grouped path's expert lists, the tokens' rows sorted
+ * by expert and the per-(token, choice) down outputs (about 93 KB per token;
+ * the grouped router of moe_route uses them at any T above
  * MOE_MAX_DECODE_T). */
 size_t moe_workspace_bytes(int T);
 
@@ -245,8 +247,9 @@ moe_status moe_route(const void *x, const void *router_w, int T, int n_experts, 
  *  idx:    device int32 [T][top_k], selection order (best first), or NULL.
  *  w:      device float [T][top_k], renormalised weights, or NULL.
  *  logits: device float [T][E] fp32 router logits, or NULL.
- *  T <= MOE_MAX_CHUNKED_T: logits are fp32 sums of exact bf16*bf16 products
- *  along a fixed tree of depth 15 (the decode kernel).  Larger T: the
+ *  Where the decode kernel ran (T up to MOE_MAX_CHUNKED_T, or
+ *  MOE_MAX_CHUNKED_T_BF16 for BF16 weights): logits are fp32 sums of exact
+ *  bf16*bf16 products along a fixed tree of depth 15.  Larger T: the
  *  grouped path's router GEMM (see moe_route).
  * At least one output must be non-NULL.  Enqueued device-to-device copies;
  * the result is undefined if no layer call with this T preceded it.
@@ -267,14 +270,15 @@ moe_status moe_read_routing(const void *workspace, size_t workspace_bytes, int T
 /*
  * out = MoE(x) for 1 <= T <= MOE_MAX_TOKENS tokens (see the top of this
  * header).
- * From MOE_MAX_DECODE_T + 1 to MOE_MAX_CHUNKED_T tokens the decode kernel
- * below runs on ceil(T / MOE_MAX_DECODE_T) balanced chunks of consecutive
- * tokens, one launch per chunk (each token's output depends only on that
- * token; a chunk reads the weights of its own selected experts).  On GB300
- * this beats the grouped path up to about 160 tokens (measured: 175 us for
- * the grouped path at 9 tokens, 474 us at 64; the decode kernel 30 us per
- * 8 tokens).
- * Above MOE_MAX_CHUNKED_T tokens the grouped path runs instead [FLINT,
+ * From MOE_MAX_DECODE_T + 1 to MOE_MAX_CHUNKED_T tokens (NVFP4 weights;
+ * MOE_MAX_CHUNKED_T_BF16 for BF16) the decode kernel below runs on
+ * ceil(T / MOE_MAX_DECODE_T) balanced chunks of consecutive tokens, one
+ * launch per chunk (each token's output depends only on that token; a chunk
+ * reads the weights of its own selected experts).  On GB300 this beats the
+ * grouped path up to those sizes (measured, NVFP4: the grouped path 122 us
+ * at 9 tokens, 341 at 88, 346 at 96; the decode kernel about 30 us per 8
+ * tokens).
+ * Above those sizes the grouped path runs instead [FLINT,
  * "From 1,096 kernels to 346": the same packed layout serves the grouped
  * GEMMs of large batches]: a router GEMM, top-k, per-expert token lists in
  * token order, then tcgen05 tensor-core GEMMs per expert (weights dequantised

@@ -39,7 +39,8 @@ INTER = 512
 EXPERTS = 256
 TOPK = 6
 MAX_DECODE_T = 8
-MAX_CHUNKED_T = 160
+MAX_CHUNKED_T = 88           # NVFP4 weights
+MAX_CHUNKED_T_BF16 = 56
 MAX_TOKENS = 65536
 
 # Exported symbols (kept in step with include/nvfp4moe.h; a CPU test checks).

@@ -127,7 +127,7 @@ size_t moe_workspace_bytes(int T)
     if (T <= MAXT)
         return ws_layout().total;
     const size_t g = gws_layout(T).total;   // moe_route above MAXT tokens
-    const size_t d = T <= CHUNK_MAX_T ? chunk_route_layout(T).total : ws_layout().total;
+    const size_t d = chunk_route_layout(T).total;   // the chunked decode path's copy-out
     return g > d ? g : d;
 }
 
@@ -188,18 +188,13 @@ moe_status moe_read_routing(const void *workspace, size_t workspace_bytes, int T
         o_w = L.topk_w;
         o_lg = L.tlogits;
         lg_pitch = 8;
-    } else if (T <= CHUNK_MAX_T) {
-        // the decode kernel's chunks wrote their routing here
+    } else {
+        // the decode kernel's chunks and the grouped path write their routing
+        // at the same offsets
         const ChunkRouteLayout C = chunk_route_layout(T);
         o_idx = C.idx;
         o_w = C.w;
         o_lg = C.logits;
-        lg_pitch = 4;
-    } else {
-        const GWsLayout L = gws_layout(T);
-        o_idx = L.idx;
-        o_w = L.w;
-        o_lg = L.logits;
         lg_pitch = 4;
     }
     cudaError_t e = cudaSuccess;
@@ -406,7 +401,7 @@ static moe_status launch_layer_on_all_sms(const LayerArgs &la, cudaStream_t st, 
 
 }  // extern "C"
 
-// MAXT < T <= CHUNK_MAX_T: the decode kernel on ceil(T / MAXT) balanced
+// MAXT < T <= chunk_max_t(weight type): the decode kernel on ceil(T / MAXT) balanced
 // chunks (each token's output depends only on that token), every chunk's
 // routing copied out for moe_read_routing.
 static moe_status layer_forward_chunked(const void *x, const void *router_w, const moe_expert_bank *routed,
@@ -460,7 +455,7 @@ moe_status moe::layer_forward(const void *x, const void *router_w, const moe_exp
     const int nsm = sm_count();
     if (nsm <= 0)
         return MOE_ERR_CUDA;
-    if (T > MAXT && T <= CHUNK_MAX_T) {
+    if (T > MAXT && T <= chunk_max_t(routed->wtype)) {
         if (!disjoint(out, x, (size_t)T * H * 2))
             return MOE_ERR_INVALID_ARG;
         return layer_forward_chunked(x, router_w, routed, shared, out, T, workspace, (cudaStream_t)stream);

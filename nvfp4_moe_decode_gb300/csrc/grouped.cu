@@ -941,11 +941,15 @@ GWsLayout gws_layout(int T)
 {
     const size_t nc = (size_t)(T + G_TOK_PER_CTA - 1) / G_TOK_PER_CTA;
     GWsLayout L;
-    size_t o = 0;
-    L.ctrl = o;      o = align256(o + 64 * 4);
-    L.logits = o;    o = align256(o + (size_t)T * E * 4);
-    L.idx = o;       o = align256(o + (size_t)T * TOPK * 4);
-    L.w = o;         o = align256(o + (size_t)T * TOPK * 4);
+    // ctrl is the decode workspace's flag word; the routing (idx, w, logits)
+    // sits where the chunked decode path copies its routing out, after the
+    // decode workspace, so moe_read_routing reads one place for either path
+    const ChunkRouteLayout C = chunk_route_layout(T);
+    L.ctrl = 0;
+    L.idx = C.idx;
+    L.w = C.w;
+    L.logits = C.logits;
+    size_t o = C.total;
     L.counts = o;    o = align256(o + (size_t)E * 4);
     L.offsets = o;   o = align256(o + (size_t)(E + 1) * 4);
     L.list = o;      o = align256(o + (size_t)T * TOPK * 4);

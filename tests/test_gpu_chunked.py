@@ -1,4 +1,5 @@
-"""Mid-size batches (MOE_MAX_DECODE_T < T <= 160): the decode kernel on
+"""Mid-size batches (MOE_MAX_DECODE_T < T <= MOE_MAX_CHUNKED_T, 88 tokens;
+BF16 weights up to 56): the decode kernel on
 balanced chunks of at most 8 tokens, against the fp64 oracle: every token's
 routing read back from the workspace (the decode router's certified bound,
 indices bit-exact on certain tokens) and the outputs."""
@@ -35,15 +36,17 @@ def _check(li, out, ws, tol):
     assert hp.within_tol(got[same], ref[same], tol), hp.describe_err(got[same], ref[same])
 
 
-@pytest.mark.parametrize("T", [9, 13, 64, 160])
+@pytest.mark.parametrize("T", [9, 13, 64, 88])
 def test_chunked_layer_nvfp4(cuda_dev, T):
     li = synth.make_layer(90 + T, T, device=cuda_dev)
     out, ws = _run(PackedLayer.from_inputs(li), li.x, cuda_dev)
     _check(li, out, ws, hp.TOL_NVFP4)
 
 
-def test_chunked_layer_bf16(cuda_dev):
-    li = synth.make_layer(91, 24, wtype=synth.BF16, device=cuda_dev)
+@pytest.mark.parametrize("T", [24, 56])
+def test_chunked_layer_bf16(cuda_dev, T):
+    """BF16 weights up to the largest size of their chunked range (56)."""
+    li = synth.make_layer(91 + T, T, wtype=synth.BF16, device=cuda_dev)
     out, ws = _run(Bf16Layer.from_inputs(li), li.x, cuda_dev)
     _check(li, out, ws, hp.TOL_BF16)
 

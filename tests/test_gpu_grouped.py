@@ -1,4 +1,5 @@
-"""The grouped path (T above the decode kernel's chunked range, 160 tokens;
+"""The grouped path (T above the decode kernel's chunked range, 88 tokens for
+NVFP4 weights and 56 for BF16;
 moe_route above MOE_MAX_DECODE_T): router GEMM, top-k, expert lists and the
 tcgen05 grouped GEMMs, against the fp64 oracle."""
 import numpy as np
@@ -75,8 +76,9 @@ def _check(li, out, ws, tol, tokens=None):
     assert hp.within_tol(got[keep], ref[keep], tol), hp.describe_err(got[keep], ref[keep])
 
 
-@pytest.mark.parametrize("T", [161, 300])
+@pytest.mark.parametrize("T", [89, 161, 300])
 def test_grouped_layer_small(cuda_dev, T):
+    """From the first size above the chunked range (89 tokens) up."""
     li = synth.make_layer(70 + T, T, device=cuda_dev)
     pl = PackedLayer.from_inputs(li)
     out, flag, ws = _forward(pl, li.x, cuda_dev)
@@ -101,9 +103,10 @@ def test_grouped_layer_8192_sampled(cuda_dev):
     _check(li, out, ws, hp.TOL_NVFP4, toks)
 
 
-def test_grouped_bf16_weights(cuda_dev):
-    T = 200
-    li = synth.make_layer(80, T, wtype=synth.BF16, device=cuda_dev)
+@pytest.mark.parametrize("T", [57, 200])
+def test_grouped_bf16_weights(cuda_dev, T):
+    """BF16 weights, from the first size above their chunked range (57)."""
+    li = synth.make_layer(80 + T, T, wtype=synth.BF16, device=cuda_dev)
     bl = Bf16Layer.from_inputs(li)
     out, flag, ws = _forward(bl, li.x, cuda_dev)
     assert flag == 0
