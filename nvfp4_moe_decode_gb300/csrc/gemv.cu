@@ -40,7 +40,7 @@ constexpr int GSTG = 2 * SC_BYTES;      // ring slot: one NVFP4 stage (a BF16 st
 
 template <int RW>
 struct GSmem {
-    uint8_t ring[RW][GW][GSTG];
+    uint8_t ring[GW][RW][GSTG];         // per warp RW stage slots, contiguous (a unit fills 1 or 2 of them)
     float4 red[2][GW][32];              // a round's partials (round r uses r % 2)
     uint64_t full[GW][RW];
     uint64_t pfull[2];                  // all 16 warps stored their round-r partials
@@ -78,9 +78,14 @@ __global__ void __launch_bounds__(GNT, 1) dense_gemv_kernel(GemvArgs a)
     const int rounds = (b1 - b0 + G - 1) / G;
     const int S = BW ? K / 64 : K / 256;      // stages per band
     const uint8_t *w = a.w + (size_t)m * a.w_mat_stride;
+    // NVFP4 stages move in units of up to UNIT adjacent stages of a band (one
+    // bulk copy each): an SM completes only ~10 bulk copies per µs whatever
+    // their size, so 4,608-byte copies stream about twice as fast as 2,304
+    constexpr int UNIT = (!BW && RW >= 4) ? 2 : 1;
+    constexpr int NU = RW / UNIT;             // unit slots per warp
 
     if (lane == 0 && warp < GW) {
-        for (int s = 0; s < RW; ++s)
+        for (int s = 0; s < NU; ++s)
             mbar_init(&sm.full[warp][s], BW ? 32 : 1);   // BF16: one cp.async arrival per lane
     }
     if (threadIdx.x < 2) {
@@ -99,13 +104,16 @@ __global__ void __launch_bounds__(GNT, 1) dense_gemv_kernel(GemvArgs a)
     const int g = warp / Q, q = warp % Q;
     const int s0 = S * q / Q, s1 = S * (q + 1) / Q, per = s1 - s0;
     const int my_rounds = warp < GW && b1 - b0 > g ? (b1 - b0 - g + G - 1) / G : 0;
-    const int n_stages = my_rounds * per;
+    const int upr = (per + UNIT - 1) / UNIT;  // units per round
+    const int n_units = my_rounds * upr;
 
+    // unit i: round i / upr, stages s0 + UNIT (i % upr) .. (at most UNIT, within the round)
     auto issue_stage = [&](int rs, int i) {
-        const int r = i / per, s = s0 + i % per;
+        const int r = i / upr, s = s0 + UNIT * (i % upr);
+        const int nst = min(UNIT, s1 - s);
         const int band = b0 + G * r + g;
         uint64_t *bar = &sm.full[warp][rs];
-        uint8_t *slot = sm.ring[rs][warp];
+        uint8_t *slot = sm.ring[warp][UNIT * rs];
         if (BW) {
             // rows of the band (GATE_UP: 8 gate rows 8 band.. and the matching
             // up rows), columns 64 s ..; lane 2 rr + h copies bytes [64 h, 64 h
@@ -123,17 +131,17 @@ __global__ void __launch_bounds__(GNT, 1) dense_gemv_kernel(GemvArgs a)
         }
         if (lane != 0)
             return;
-        mbar_arrive_expect_tx(bar, GSTG);
-        bulk_g2s(slot, w + (size_t)band * band_bytes(K) + (size_t)s * GSTG, GSTG, bar);
+        mbar_arrive_expect_tx(bar, (uint32_t)(nst * GSTG));
+        bulk_g2s(slot, w + (size_t)band * band_bytes(K) + (size_t)s * GSTG, (uint32_t)(nst * GSTG), bar);
     };
-    int ic = 0, ii = 0;
+    int ic = 0, ii = 0;                        // units consumed / issued
     auto issue_upto = [&](int depth) {
-        while (ii < n_stages && ii < ic + depth) {
-            issue_stage(ii % RW, ii);
+        while (ii < n_units && ii < ic + depth) {
+            issue_stage(ii % NU, ii);
             ++ii;
         }
     };
-    auto issue_ahead = [&]() { issue_upto(RW); };
+    auto issue_ahead = [&]() { issue_upto(NU); };
     if (warp < GW)
         issue_upto(PRE);
 
@@ -287,15 +295,18 @@ __global__ void __launch_bounds__(GNT, 1) dense_gemv_kernel(GemvArgs a)
         if (r < my_rounds) {
 #pragma unroll 1
             for (int s = s0; s < s1; ++s) {
-                const int rs = ic % RW;
-                mbar_wait_bounded(&sm.full[warp][rs], (ic / RW) & 1, flag);
+                const int rs = ic % NU, off = (s - s0) % UNIT;
+                if (off == 0)
+                    mbar_wait_bounded(&sm.full[warp][rs], (ic / NU) & 1, flag);
                 if (BW)
-                    bf16_stage_xs(sm.ring[rs][warp], sm.xs, rpw, 4 * s, lane, acc);
+                    bf16_stage_xs(sm.ring[warp][UNIT * rs + off], sm.xs, rpw, 4 * s, lane, acc);
                 else
-                    mma_stage_xs(sm.ring[rs][warp], sm.xs, rpw, 16 * s, lane, acc);
-                __syncwarp();
-                ++ic;
-                issue_ahead();
+                    mma_stage_xs(sm.ring[warp][UNIT * rs + off], sm.xs, rpw, 16 * s, lane, acc);
+                if (off == UNIT - 1 || s == s1 - 1) {   // the unit's last stage: free its slot
+                    __syncwarp();
+                    ++ic;
+                    issue_ahead();
+                }
             }
         }
         // every warp reports every round (an idle one with zeros), so the
@@ -327,15 +338,17 @@ PerDevice g_gemv_attr[4];
 
 }  // namespace
 
-// Warps per band: the power of two Q <= 16 that minimises rounds x stages per
-// warp (ties: more bands at once, i.e. fewer rounds).
-int gemv_warps_per_band(int bands_per_cta, int stages)
+// Warps per band: the power of two Q <= 16 that minimises a warp's stage
+// steps plus its bulk copies (units of `unit` stages), both about 0.1 µs on
+// GB300 (ties: more bands at once, i.e. fewer rounds).
+int gemv_warps_per_band(int bands_per_cta, int stages, int unit)
 {
     int best_q = 16;
     long best = -1;
     for (int qq = 16; qq >= 1; qq >>= 1) {
         const int gq = 16 / qq;
-        const long cost = (long)((bands_per_cta + gq - 1) / gq) * ((stages + qq - 1) / qq);
+        const long per = (stages + qq - 1) / qq;
+        const long cost = (long)((bands_per_cta + gq - 1) / gq) * (per + (per + unit - 1) / unit);
         if (best < 0 || cost <= best) {
             best = cost;
             best_q = qq;
@@ -361,7 +374,7 @@ cudaError_t launch_gemv(GemvArgs a, int sm_count, cudaStream_t stream)
         cpm = nbm;
     a.ctas_per_mat = cpm;
     const int stages = bw ? a.K / 64 : a.K / 256;
-    a.q = gemv_warps_per_band((nbm + cpm - 1) / cpm, stages);
+    a.q = gemv_warps_per_band((nbm + cpm - 1) / cpm, stages, (!bw && rw4) ? 2 : 1);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(cpm * a.n_mat));

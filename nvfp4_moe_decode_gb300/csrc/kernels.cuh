@@ -171,7 +171,7 @@ struct GemvArgs {
 };
 
 // Warps per band for a CTA holding `bands_per_cta` bands of `stages` stages.
-int gemv_warps_per_band(int bands_per_cta, int stages);
+int gemv_warps_per_band(int bands_per_cta, int stages, int unit);
 // cuTensorMapEncodeTiled (null if the driver does not provide it).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 cudaError_t launch_gemv(GemvArgs a, int sm_count, cudaStream_t stream);
