@@ -44,10 +44,14 @@
 //         until every one carries the tag, scale each token by a power of two
 //         into f16 fragments once for the whole CTA, and count themselves
 //         done; each down partial goes out as tagged fp32 words;
-//     every compute warp streams its own stages (2304-byte pieces of its
-//     bands) through its ring of bulk copies, ahead across all of its bands,
-//     gate/up first: slots complete in order on every CTA, so by the time a
-//     warp reaches its down bands their h is normally ready;
+//     NVFP4 gate/up bands arrive whole (one 18,432-byte bulk copy each) in
+//     four band slots per parity group; each warp reads its slice there, and
+//     the eighth warp done with a slot refills it with the group's next band.
+//     Every compute warp streams its own down bands (4,608-byte copies)
+//     through a ring that takes its share of its group's band slots once
+//     their last bands are read (BF16: every stage through the warp's own
+//     ring).  Slots complete in order on every CTA, so by the time a warp
+//     reaches its down bands their h is normally ready;
 //  5. CTA b < 128 writes out rows 16 b .. 16 b + 15: its compute warps read
 //     every slot's tagged partials of the band, each warp summing every 16th
 //     slot in order, then warp 0 adds the 16 sums in warp order and the
@@ -72,7 +76,8 @@ constexpr int EP_WARP = FW;            // warps 16, 17: gate/up epilogues (band 
 constexpr int HW_WARP = FW + 2;        // warps 18, 19: h fragments of the CTA's down slots (half of the steps each)
 constexpr int NHB = 3;                 // h buffers: the two range slots and the last slot
 constexpr int NT = FT + 128;           // threads per CTA (20 warps: a multiple of 4 keeps 96 registers a thread)
-constexpr int RW = 4;                  // ring stages per compute warp
+constexpr int RW = 4;                  // ring stages per compute warp (BF16)
+constexpr int GBS = 4;                 // NVFP4: whole-band gate/up slots per band-parity group
 constexpr int STG = 2 * SC_BYTES;      // 2304 bytes: two NVFP4 super-chunks (a BF16 stage uses 2048)
 constexpr int GQ = 8;                  // 256-column slices of a gate/up band
 constexpr int NB = 8;                  // gate/up reduction buffers (band k uses k % NB)
@@ -86,7 +91,20 @@ constexpr int HBUF = HS * 32 * 8;      // one slot's h as B fragments [step][lan
 // last slot).
 
 struct FSmem {
-    uint8_t ring[FW][RW][STG];         // per-warp stage rings; phase 2: warps 8..15's hold x (and delta)
+    // Stage memory.  BF16: per-warp rings of RW stages.  NVFP4: gate/up bands
+    // move whole (one 18,432-byte copy per band: an SM completes only ~10
+    // bulk copies per us whatever their size, so eight 2,304-byte slices
+    // per band would cap the stream near 3.5 TB/s), into GBS slots per
+    // band-parity group, and each warp reads its slice there; once its
+    // group's gate/up bands are done, warp q's ring of RW down stages is
+    // bytes [q, q + 1) * RW * STG of the group's slots.  Phase 2 stages x
+    // (and delta) in the second half, which the unit phase writes first.
+    union {
+        uint8_t ring[FW][RW][STG];
+        struct {
+            uint8_t gband[2][GBS][W13_BAND_BYTES];
+        } nv;
+    };
     union {
         RouterRed rred;                // phase 2: the router's partial sums
         struct {
@@ -95,6 +113,9 @@ struct FSmem {
         } u;
     };
     uint64_t full[FW][RW];
+    uint64_t gfull[2][GBS];            // NVFP4: a gate/up band slot holds its band
+    uint32_t gdone[2][GBS];            // NVFP4: warps done with the slot's band (the eighth refills it)
+    uint32_t sfree[2][GBS];            // NVFP4: the slot's last band has been read (down rings may use it)
     uint64_t xbar;
     int32_t sel[MAXT][TOPK];
     float selw[MAXT][TOPK];
@@ -257,6 +278,8 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
 {
     static_assert(sizeof(RouterRed) <= sizeof(FSmem::u), "router partials fit the unit-phase buffers");
     static_assert((size_t)2 * MAXT * XPITCH <= sizeof(FSmem::ring) / 2, "x and delta fit the rings of warps 8..15");
+    static_assert(sizeof(FSmem::nv) == sizeof(FSmem::ring) && GBS * W13_BAND_BYTES == (size_t)GQ * RW * STG,
+                  "NVFP4: a group's band slots hold its eight warps' down rings");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     FSmem &sm = *reinterpret_cast<FSmem *>(smem_raw);
 
@@ -281,6 +304,12 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         mbar_init(&sm.pfull[threadIdx.x], GQ);   // the band's eight K partials are in
         mbar_init(&sm.pempty[threadIdx.x], 1);   // the epilogue warp has read them
     }
+    if (threadIdx.x < 2 * GBS) {
+        mbar_init(&sm.gfull[threadIdx.x / GBS][threadIdx.x % GBS], 1);
+        sm.gdone[threadIdx.x / GBS][threadIdx.x % GBS] = 0u;
+    }
+    if (threadIdx.x < 2 * GBS)
+        sm.sfree[threadIdx.x / GBS][threadIdx.x % GBS] = 0u;
     if (threadIdx.x == 0)
         mbar_init(&sm.xbar, 1);
     if (lane == 0 && warp <= FW)
@@ -304,13 +333,13 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
 
     // ---- phase 1: work that needs nothing from the preceding kernel ----
     // CTA c's first gate/up band is band c of slot 0: the shared expert when
-    // there is one.  Its parity-0 warps take their slices of it now (NVFP4;
-    // the slot table is not built yet, so the address is computed directly).
-    const bool pre_shared = !BW && warp < FW && par == 0 && a.n_shared > 0 && cta < W13_BANDS;
-    if (pre_shared && lane == 0) {
-        uint64_t *bar = &sm.full[warp][0];
-        mbar_arrive_expect_tx(bar, STG);
-        bulk_g2s(sm.ring[warp][0], a.s_w13 + (size_t)cta * W13_BAND_BYTES + (size_t)q * STG, STG, bar);
+    // there is one.  Its copy into band slot 0 of parity group 0 starts now
+    // (NVFP4; the slot table is not built yet, so the address is computed
+    // directly).
+    const bool pre_shared = !BW && a.n_shared > 0 && cta < W13_BANDS;
+    if (pre_shared && threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&sm.gfull[0][0], W13_BAND_BYTES);
+        bulk_g2s(sm.nv.gband[0][0], a.s_w13 + (size_t)cta * W13_BAND_BYTES, W13_BAND_BYTES, &sm.gfull[0][0]);
     }
     // every expert's tensor scales (NVFP4), for the slot table built later
     if (!BW) {
@@ -849,13 +878,20 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
         const int n_dnb = n_dn_cta > jp ? (n_dn_cta - jp + jstride - 1) / jstride : 0;
         constexpr int SPG = BW ? 4 : 1;   // stages per gate/up slice
         constexpr int SPD = BW ? 4 : 2;   // stages per down band (BF16: per half band)
-        const int n_stages = n_gub * SPG + n_dnb * SPD;
+        constexpr int RWX = RW;            // the warp's ring stages
+        // the warp's own ring carries its gate/up slices (BF16) and its down
+        // bands; NVFP4 gate/up bands come whole through the group's band slots
+        const int n_gu_ring = BW ? n_gub * SPG : 0;
+        const int n_stages = n_gu_ring + n_dnb * SPD;
+        auto wring = [&](int rs) -> uint8_t * {
+            return BW ? sm.ring[warp][rs] : &sm.nv.gband[par][0][0] + (size_t)(q * RW + rs) * STG;
+        };
 
         // stage i of this warp into ring slot rs
         auto issue_stage = [&](int rs, int i) {
             uint64_t *bar = &sm.full[warp][rs];
             const uint8_t *src;
-            if (i < n_gub * SPG) {
+            if (i < n_gu_ring) {
                 const int k = par + 2 * (i / SPG), sub = i % SPG;
                 const int gb = cta + G * k, slot = gb / W13_BANDS, band = gb % W13_BANDS;
                 if (BW) {
@@ -869,7 +905,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                     src = bank13(slot) + (size_t)band * W13_BAND_BYTES + (size_t)q * STG;
                 }
             } else {
-                const int d = i - n_gub * SPG;
+                const int d = i - n_gu_ring;
                 const int j = jp + jstride * (d / SPD), sub = d % SPD + SPD * dh;
                 int slot, band, hb;
                 dn_band(j, slot, band, hb);
@@ -882,7 +918,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             }
             if (BW) {
                 const int r = lane >> 1, h = lane & 1;
-                uint8_t *dst = sm.ring[warp][rs] + r * 128;
+                uint8_t *dst = wring(rs) + r * 128;
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     cp_async_cg16(dst + 16 * ((4 * h + u) ^ (4 * (r & 1))), src + 16 * u);
@@ -892,15 +928,15 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             if (lane != 0)
                 return;
             mbar_arrive_expect_tx(bar, STG);
-            bulk_g2s(sm.ring[warp][rs], src, STG, bar);
+            bulk_g2s(wring(rs), src, STG, bar);
         };
         int ic = 0;                                  // next stage to consume
-        int ii = pre_shared ? 1 : 0;                 // next stage to issue
+        int ii = 0;                                  // next stage to issue
         auto issue_ahead = [&]() {
-            while (ii < n_stages && ii < ic + RW) {
-                const int rs = ii % RW;
-                const int d = ii - n_gub * SPG;
-                if (!BW && d >= 0 && (d & 1) == 0 && rs + 1 < RW && ii + 1 < ic + RW) {
+            while (ii < n_stages && ii < ic + RWX) {
+                const int rs = ii % RWX;
+                const int d = ii - n_gu_ring;
+                if (!BW && d >= 0 && (d & 1) == 0 && rs + 1 < RWX && ii + 1 < ic + RWX) {
                     // both stages of an NVFP4 down band into adjacent slots by
                     // one copy; the second slot's barrier completes at once
                     // (its data is covered by the first slot's)
@@ -908,7 +944,7 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                         int slot, band, hb;
                         dn_band(jp + jstride * (d >> 1), slot, band, hb);
                         mbar_arrive_expect_tx(&sm.full[warp][rs], 2 * STG);
-                        bulk_g2s(sm.ring[warp][rs], bank2(slot) + (size_t)band * W2_BAND_BYTES, 2 * STG,
+                        bulk_g2s(wring(rs), bank2(slot) + (size_t)band * W2_BAND_BYTES, 2 * STG,
                                  &sm.full[warp][rs]);
                         mbar_arrive(&sm.full[warp][rs + 1]);
                     }
@@ -920,17 +956,34 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             }
         };
         auto wait_stage = [&]() -> const uint8_t * {
-            const int rs = ic % RW;
-            mbar_wait_bounded(&sm.full[warp][rs], (ic / RW) & 1, flag);
-            return sm.ring[warp][rs];
+            const int rs = ic % RWX;
+            mbar_wait_bounded(&sm.full[warp][rs], (ic / RWX) & 1, flag);
+            return wring(rs);
         };
         auto next_stage = [&]() {
             __syncwarp();
             ++ic;
             issue_ahead();
         };
-        issue_ahead();
+        if (BW)
+            issue_ahead();
         const int g = lane >> 2, c = lane & 3;
+
+        // NVFP4: band bi of this parity group (CTA band par + 2 bi) into the
+        // group's slot bi % GBS, one copy of the whole band
+        auto issue_band = [&](int bi) {
+            const int k = par + 2 * bi;
+            const int gb = cta + G * k, slot = gb / W13_BANDS, band = gb % W13_BANDS;
+            uint64_t *bar = &sm.gfull[par][bi % GBS];
+            mbar_arrive_expect_tx(bar, W13_BAND_BYTES);
+            bulk_g2s(sm.nv.gband[par][bi % GBS], bank13(slot) + (size_t)band * W13_BAND_BYTES, W13_BAND_BYTES, bar);
+        };
+        if (!BW && q == 0 && lane == 0) {
+            // the group's first GBS bands (group 0's first: already in flight
+            // when it is the shared expert's)
+            for (int bi = (par == 0 && pre_shared) ? 1 : 0; bi < GBS && bi < n_gub; ++bi)
+                issue_band(bi);
+        }
 
         // ---- gate/up slices ----
 #pragma unroll 1
@@ -947,8 +1000,24 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
                 bf16_stage_r<3>(wait_stage(), xf, lane, acc);
                 next_stage();
             } else {
-                mma_stage_r(wait_stage(), xf, lane, acc);
-                next_stage();
+                // slice q of the band in slot bi % GBS; the eighth warp done
+                // with the slot refills it with the group's band bi + GBS (its
+                // reads are ordered before the copy by the fence and the count)
+                const int sl = bi % GBS;
+                mbar_wait_bounded(&sm.gfull[par][sl], (uint32_t)(bi / GBS) & 1u, flag);
+                mma_stage_r(sm.nv.gband[par][sl] + (size_t)q * STG, xf, lane, acc);
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence_block();
+                    if (atomicAdd(&sm.gdone[par][sl], 1u) == GQ - 1) {
+                        sm.gdone[par][sl] = 0u;
+                        __threadfence_block();
+                        if (bi + GBS < n_gub)
+                            issue_band(bi + GBS);
+                        else
+                            st_release_cta(&sm.sfree[par][sl], 1u);   // the slot's last band is read
+                    }
+                }
             }
             // the band's eight K partials meet in buffer k % NB (its previous
             // use, band k - NB, must have been read by the epilogue warp)
@@ -959,6 +1028,17 @@ __global__ void __launch_bounds__(NT, 1) moe_layer_kernel(LayerArgs a)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&sm.pfull[b]);
+        }
+
+        if (!BW) {
+            // the warp's down ring lives in band slot q / 2 of its group: wait
+            // until the slot's last band has been read by all eight warps (a
+            // slot the group never used is free)
+            const int ds = q * RW * STG / (int)W13_BAND_BYTES;
+            if (lane == 0 && ds < n_gub)
+                smem_wait_geq(&sm.sfree[par][ds], 1u, flag);
+            __syncwarp();
+            issue_ahead();
         }
 
         // ---- down bands ----
