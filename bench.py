@@ -69,10 +69,10 @@ def layer_bytes(T: int, n_distinct: int, n_shared: int = 1, wtype: str = "nvfp4"
 NCU_TRAFFIC = {
     # DRAM bytes read + written per algorithmic byte of the decode kernel at
     # T = 8, from one ncu capture of two launches (layers with 46 and 42
-    # distinct experts: 168,355,328 bytes against 161,480,704), valid while
+    # distinct experts: 168,418,304 bytes against 161,480,704), valid while
     # the kernel's sources hash to this value
-    "sources_sha256": "70e5d90fe03076f7678d28234abb2a378119a4458f0438171b81b51079cf93e6",
-    "per_algorithmic_byte": 168_355_328 / 161_480_704,
+    "sources_sha256": "e4728cf4b97467716ce9734e60dd6010695bf7df396f66a7804e0bdfd19a8a4f",
+    "per_algorithmic_byte": 168_418_304 / 161_480_704,
 }
 KERNEL_SOURCES = ("layer.cu", "stage.cuh", "common.cuh", "kernels.cuh", "topk.cuh")
 
