@@ -297,7 +297,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const int nch = a.K / TC_KCHUNK;
     const int my_tiles = (int)blockIdx.x < total_tiles ? (total_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int stream_len = my_tiles * nch;          // chunks this CTA streams
-    auto tile_id = [&](int ti) { return (int)blockIdx.x + ti * (int)gridDim.x; };
+    // gate/up walks the tiles from the last expert down: the gather wrote
+    // the sorted rows in list order, so its last rows are still in L2 when
+    // the GEMM starts (measured: 670 -> 664 us per layer at T = 8192)
+    auto tile_id = [&](int ti) {
+        const int id = (int)blockIdx.x + ti * (int)gridDim.x;
+        return a.mode == GM_GATE_UP ? total_tiles - 1 - id : id;
+    };
     uint32_t *flag = a.flag;
 
     // A-operand base of group g (bytes): packed NVFP4 or bf16 rows of one matrix
