@@ -27,6 +27,21 @@ def test_header_declares_the_binding_exports():
     assert declared_functions() == set(m.EXPORTS)
 
 
+def header_defines():
+    text = open(os.path.join(ROOT, "include", "nvfp4moe.h")).read()
+    return {mt.group(1): int(mt.group(2)) for mt in re.finditer(r"#define (MOE_[A-Z0-9_]+) (\d+)u?\b", text)}
+
+
+def test_binding_constants_match_the_header():
+    d = header_defines()
+    assert d["MOE_HIDDEN"] == m.HIDDEN and d["MOE_INTER"] == m.INTER
+    assert d["MOE_MAX_DECODE_T"] == m.MAX_DECODE_T and d["MOE_MAX_TOKENS"] == m.MAX_TOKENS
+    assert d["MOE_MAX_CHUNKED_T"] == m.MAX_CHUNKED_T
+    assert d["MOE_MAX_CHUNKED_T_BF16"] == m.MAX_CHUNKED_T_BF16
+    assert d["MOE_STATIC_SCRATCH_BYTES"] == m.MOE_STATIC_SCRATCH_BYTES
+    assert m.MAX_DECODE_T < m.MAX_CHUNKED_T_BF16 <= m.MAX_CHUNKED_T
+
+
 def test_library_exports_every_declared_symbol(moe_lib):
     for name in declared_functions():
         assert hasattr(moe_lib, name), name
