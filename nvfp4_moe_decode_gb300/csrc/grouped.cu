@@ -23,11 +23,11 @@
 //                   shared expert all tokens: SiLU(g) * u -> h (bf16);
 //  5. h rescale     (NVFP4 weights) every h row in place to f16 times a
 //                   power of two;
-//  6. down GEMM     routed experts: y * routing weight -> ybuf[token][choice];
+//  6. down GEMM     routed experts: y * routing weight -> ybuf[list row];
 //  7. shared down   the shared expert's down projection -> ysh[token];
-//  8. combine       out = sum over choices of ybuf (in choice order) + ysh,
-//                   rounded once to bf16 (deterministic: no atomics), a
-//                   streaming kernel of 16-byte loads.
+//  8. combine       out = sum over choices of ybuf[inverse map] (in choice
+//                   order) + ysh, rounded once to bf16 (deterministic: no
+//                   atomics), a streaming kernel of 16-byte loads.
 // Without a shared expert step 7 is skipped.
 // Every GEMM epilogue fetches its tile's per-column factors (routing weight,
 // tensor scale, inverse power of two) into shared memory while the tile's
@@ -51,10 +51,13 @@
 //               into the 128B-swizzled K-major A stage (bf16 rows are copied
 //               there with cp.async instead);
 //   warp 8      B producer: the tile's token rows, consecutive rows of xs,
-//               x16, h or x, by 16-row TMA tiles;
-//   warp 10     TMEM allocation and the MMA issue (one thread, 4 MMAs of
-//               K = 16 per 64-column chunk, one commit to the stage's empty
-//               barrier, and one to the accumulator's full barrier per tile);
+//               x16, h or x, by 64- and 16-row TMA boxes;
+//   warp 10     TMEM allocation and the MMA issue (one thread, 8 MMAs of
+//               K = 16 per pair of 64-column chunks, one commit to the pair's
+//               empty barrier, and one to the accumulator's full barrier per
+//               tile);
+//   warps 12-15 epilogue: tcgen05.ld of the accumulator (two 256-column
+//               buffers, so a tile's epilogue overlaps the next tile's MMAs).
 // Synchronisation is per pair of chunks (128 columns of K; every K here is a
 // multiple of 128): the A and B tiles of both chunks share one full/empty
 // barrier pair.  On GB300 an mbarrier wait costs ~200 cycles even when the
@@ -63,8 +66,6 @@
 // commits 0.55 us), so every role makes one wait and one signal per 128
 // columns: the MMA thread 8 MMAs per wait and commit, the A warps one fence
 // and arrive per super-chunk, the B producer one expect-tx for both chunks.
-//   warps 12-15 epilogue: tcgen05.ld of the accumulator (two 256-column
-//               buffers, so a tile's epilogue overlaps the next tile's MMAs).
 // Every wait is bounded: a wait that runs out sets MOE_FLAG_WAIT_TIMEOUT
 // and makes the CTA skip the rest of its work.
 #include <cudaTypedefs.h>
