@@ -103,6 +103,35 @@ def test_grouped_layer_8192_sampled(cuda_dev):
     _check(li, out, ws, hp.TOL_NVFP4, toks)
 
 
+def test_grouped_layer_max_tokens(cuda_dev):
+    """The largest batch, MOE_MAX_TOKENS = 65,536 tokens (a 6.2 GB workspace):
+    every output finite, every token's own routing valid (six distinct
+    experts, positive weights that sum to 1), and 128 tokens (first, last and
+    random ones) against the oracle: their routing (indices bit-exact where
+    certain) and their outputs."""
+    T = m.MAX_TOKENS
+    li = synth.make_layer(65, T, device=cuda_dev)
+    pl = PackedLayer.from_inputs(li)
+    out, flag, ws = _forward(pl, li.x, cuda_dev)
+    assert flag == 0
+    assert torch.isfinite(out.float()).all()
+    gidx, gw, glg = hp.read_routing(ws, T)
+    srt = np.sort(gidx, axis=1)
+    assert srt.min() >= 0 and srt.max() < 256 and np.all(srt[:, 1:] != srt[:, :-1])
+    assert np.all(gw > 0) and np.all(np.abs(gw.sum(axis=1) - 1.0) <= 1e-5)
+    rng = np.random.default_rng(T)
+    toks = sorted(set([0, 1, T - 1] + rng.choice(np.arange(2, T - 1), 125, replace=False).tolist()))
+    assert len(toks) == 128
+    xb, wb = hp.bits16(li.x)[toks], hp.bits16(li.router_w)
+    _, near, same = hp.check_gpu_routing(xb, wb, gidx[toks], gw[toks], glg[toks], hp.GEMM_DEPTH, 1e-5)
+    assert len(near) <= 4, f"{len(near)} near-tie tokens of 128"
+    ref, _, _, _, _ = hp.oracle_layer(li, tokens=toks)
+    got = hp.to_f64(out)[toks]
+    keep = sorted(same)
+    assert len(keep) >= len(toks) - len(near)
+    assert hp.within_tol(got[keep], ref[keep], hp.TOL_NVFP4), hp.describe_err(got[keep], ref[keep])
+
+
 @pytest.mark.parametrize("T", [57, 200])
 def test_grouped_bf16_weights(cuda_dev, T):
     """BF16 weights, from the first size above their chunked range (57)."""
