@@ -132,6 +132,25 @@ def test_grouped_layer_max_tokens(cuda_dev):
     assert hp.within_tol(got[keep], ref[keep], hp.TOL_NVFP4), hp.describe_err(got[keep], ref[keep])
 
 
+def test_grouped_zero_tokens_route_by_index(cuda_dev):
+    """The grouped path with all-zero tokens among the others: experts 0..5
+    in that order (a tie goes to the lower index), weights 1/6, and output
+    rows exactly 0; the other tokens against the oracle."""
+    T = 100
+    li = synth.make_layer(430, T, device=cuda_dev)
+    zeros = [0, 50, 99]
+    li.x[zeros] = 0
+    pl = PackedLayer.from_inputs(li)
+    out, flag, ws = _forward(pl, li.x, cuda_dev)
+    assert flag == 0
+    gidx, gw, _ = hp.read_routing(ws, T)
+    for t in zeros:
+        assert gidx[t].tolist() == [0, 1, 2, 3, 4, 5]
+        assert np.all(np.abs(gw[t] - 1.0 / 6.0) <= 1e-7)
+        assert torch.count_nonzero(out[t].float()) == 0
+    _check(li, out, ws, hp.TOL_NVFP4)
+
+
 @pytest.mark.parametrize("T", [57, 200])
 def test_grouped_bf16_weights(cuda_dev, T):
     """BF16 weights, from the first size above their chunked range (57)."""

@@ -108,6 +108,25 @@ def test_layer_without_shared_expert(cuda_dev):
     _check(li.x, li_ns, out, ws)
 
 
+@pytest.mark.parametrize("T,zeros", [(8, [0, 5]), (3, [1])])
+def test_layer_zero_tokens_route_by_index(cuda_dev, T, zeros):
+    """Tokens whose activations are all zero: every logit is exactly 0, so
+    the six selected experts are 0..5 in that order (a tie goes to the lower
+    index), each weighted 1/6, and the output row is exactly 0 (every expert
+    FFN maps 0 to 0).  The other tokens as usual."""
+    li = synth.make_layer(420 + T, T, device=cuda_dev)
+    li.x[zeros] = 0
+    pl = PackedLayer.from_inputs(li)
+    out, flag, ws = _forward(pl, li.x, cuda_dev)
+    assert flag == 0
+    gidx, gw, _ = hp.read_routing(ws, T)
+    for t in zeros:
+        assert gidx[t].tolist() == [0, 1, 2, 3, 4, 5]
+        assert np.all(np.abs(gw[t] - 1.0 / 6.0) <= 1e-7)
+        assert torch.count_nonzero(out[t].float()) == 0
+    hp.check_decode_layer(li, li.x, out, ws, hp.TOL_NVFP4, max_near=len(zeros) + 1)
+
+
 def test_layer_zero_scales_give_zero(cuda_dev):
     li = synth.make_layer(9, 2, device=cuda_dev)
     li.scales2.zero_()
