@@ -151,6 +151,24 @@ def test_grouped_zero_tokens_route_by_index(cuda_dev):
     _check(li, out, ws, hp.TOL_NVFP4)
 
 
+def test_grouped_nonfinite_router_weight_sets_flag(cuda_dev):
+    """The grouped path with a NaN router weight (expert 17's logit NaN for
+    every token): the flag is set, expert 17 is never selected, and every
+    output is finite."""
+    T = 100
+    li = synth.make_layer(441, T, device=cuda_dev)
+    li.router_w[17, 3] = float("nan")
+    pl = PackedLayer.from_inputs(li)
+    out, flag, ws = _forward(pl, li.x, cuda_dev)
+    assert flag & m.MOE_FLAG_NONFINITE_LOGIT
+    gidx, gw, _ = hp.read_routing(ws, T)
+    assert not np.any(gidx == 17)
+    srt = np.sort(gidx, axis=1)
+    assert np.all(srt[:, 1:] != srt[:, :-1]) and srt.min() >= 0 and srt.max() < 256
+    assert np.all(gw > 0) and np.all(np.abs(gw.sum(axis=1) - 1.0) <= 1e-5)
+    assert torch.isfinite(out.float()).all()
+
+
 @pytest.mark.parametrize("T", [57, 200])
 def test_grouped_bf16_weights(cuda_dev, T):
     """BF16 weights, from the first size above their chunked range (57)."""

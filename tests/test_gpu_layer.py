@@ -127,6 +127,23 @@ def test_layer_zero_tokens_route_by_index(cuda_dev, T, zeros):
     hp.check_decode_layer(li, li.x, out, ws, hp.TOL_NVFP4, max_near=len(zeros) + 1)
 
 
+def test_layer_nonfinite_router_weight_sets_flag(cuda_dev):
+    """A NaN router weight makes expert 17's logit NaN for every token: the
+    layer reports MOE_FLAG_NONFINITE_LOGIT, ranks the NaN last (17 is never
+    selected) and still produces finite outputs."""
+    T = 4
+    li = synth.make_layer(440, T, device=cuda_dev)
+    li.router_w[17, 3] = float("nan")
+    pl = PackedLayer.from_inputs(li)
+    out, flag, ws = _forward(pl, li.x, cuda_dev)
+    assert flag & m.MOE_FLAG_NONFINITE_LOGIT
+    gidx, gw, _ = hp.read_routing(ws, T)
+    for t in range(T):
+        assert 17 not in gidx[t].tolist() and len(set(gidx[t].tolist())) == 6
+        assert np.all(gw[t] > 0) and abs(gw[t].sum() - 1.0) <= 1e-5
+    assert torch.isfinite(out.float()).all()
+
+
 def test_layer_zero_scales_give_zero(cuda_dev):
     li = synth.make_layer(9, 2, device=cuda_dev)
     li.scales2.zero_()
